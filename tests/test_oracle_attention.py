@@ -1,0 +1,121 @@
+"""Pins of the oracle's decode attention and bit-budget helpers (CPU only)."""
+import math
+
+import numpy as np
+import pytest
+from scipy import special
+
+import oracle
+from bit_kv_cache_10_gb300 import synth
+
+
+def _cache(b, hk, length, kb, vb, k_fp16=False, hot=0, seed=0, scaled=True, cap=None):
+    d = 128
+    sk = synth.channel_scales(seed, 4, hk, d) if scaled else None
+    sv = synth.channel_scales(seed, 5, hk, d) if scaled else None
+    k = synth.kv_fp16(seed, 1, b, hk, length, d, sk)
+    v = synth.kv_fp16(seed, 2, b, hk, length, d, sv)
+    lens = np.full(b, length)
+    c = oracle.build_cache(k, v, lens, cap or length, kb, vb, seed=seed, k_fp16=k_fp16, hot_window=hot)
+    return c, k, v, lens
+
+
+def test_single_token_returns_its_value():
+    c, _, _, lens = _cache(1, 1, 1, 4, 4)
+    q = synth.queries_fp16(0, 1, 1, 128)
+    _, v = oracle.dequantized_kv(c, 0, 0, 1)
+    np.testing.assert_allclose(oracle.decode_attention(c, q, lens)[0, 0], v[0], rtol=1e-14)
+
+
+def test_zero_query_is_mean_of_values():
+    c, _, _, lens = _cache(1, 1, 37, 3, 4)
+    q = np.zeros((1, 1, 128), np.float16)
+    _, v = oracle.dequantized_kv(c, 0, 0, 37)
+    np.testing.assert_allclose(oracle.decode_attention(c, q, lens)[0, 0], v.mean(axis=0), rtol=1e-12, atol=1e-13)
+
+
+def test_identical_keys_give_uniform_weights():
+    d = 128
+    k = np.tile(synth.kv_fp16(4, 1, 1, 1, 1, d), (1, 1, 20, 1))
+    v = synth.kv_fp16(4, 2, 1, 1, 20, d)
+    c = oracle.build_cache(k, v, [20], 20, 4, 4)
+    q = synth.queries_fp16(4, 1, 1, d)
+    _, vh = oracle.dequantized_kv(c, 0, 0, 20)
+    np.testing.assert_allclose(oracle.decode_attention(c, q, [20])[0, 0], vh.mean(axis=0), rtol=1e-12, atol=1e-13)
+
+
+def test_fp16_keys_reduce_to_textbook_softmax_attention():
+    c, k, _, lens = _cache(1, 2, 50, 16, 4, k_fp16=True)
+    q = synth.queries_fp16(0, 1, 8, 128)
+    out = oracle.decode_attention(c, q, lens)
+    for hq in range(8):
+        h = hq // 4
+        _, vh = oracle.dequantized_kv(c, 0, h, 50)
+        kf = k[0, h].astype(np.float64)
+        p = special.softmax(kf @ q[0, hq].astype(np.float64) / math.sqrt(128))
+        np.testing.assert_allclose(out[0, hq], p @ vh, rtol=1e-11, atol=1e-12)
+
+
+def test_gqa_groups_are_contiguous():
+    c, _, _, lens = _cache(1, 2, 40, 3, 4)
+    q = np.tile(synth.queries_fp16(1, 1, 1, 128), (1, 4, 1))
+    out = oracle.decode_attention(c, q, lens)
+    np.testing.assert_array_equal(out[0, 0], out[0, 1])
+    np.testing.assert_array_equal(out[0, 2], out[0, 3])
+    assert np.abs(out[0, 1] - out[0, 2]).max() > 1e-3
+
+
+@pytest.mark.parametrize("hot", [0, 16])
+def test_rotated_domain_identity(hot):
+    c, _, _, lens = _cache(2, 2, 100, 3, 4, hot=hot)
+    q = synth.queries_fp16(0, 2, 8, 128)
+    dense = oracle.decode_attention(c, q, lens)
+    for b, hq in [(0, 0), (1, 5), (1, 7)]:
+        np.testing.assert_allclose(oracle.decode_attention_rotated(c, q, lens, b, hq), dense[b, hq],
+                                   rtol=1e-11, atol=1e-12)
+
+
+def test_hot_window_reads_raw_fp16_values():
+    d, length, hot = 128, 30, 8
+    c, k, v, lens = _cache(1, 1, length, 3, 4, hot=hot)
+    q = synth.queries_fp16(2, 1, 1, d)
+    kd, vd = oracle.dequantized_kv(c, 0, 0, length)
+    np.testing.assert_array_equal(vd[length - hot:], v[0, 0, length - hot:].astype(np.float64))
+    full = oracle.build_cache(k, v, lens, length, 3, 4)
+    _, v_cold = oracle.dequantized_kv(full, 0, 0, length)
+    np.testing.assert_array_equal(vd[:length - hot], v_cold[:length - hot])
+    p = special.softmax(kd @ q[0, 0].astype(np.float64) / math.sqrt(d))
+    np.testing.assert_allclose(oracle.decode_attention(c, q, lens)[0, 0], p @ vd, rtol=1e-12, atol=1e-12)
+    # ring slots: position p sits in slot p mod W
+    for p_ in range(length - hot, length):
+        np.testing.assert_array_equal(c.v_hot[0, 0, p_ % hot], v[0, 0, p_])
+
+
+def test_hot_window_longer_than_sequence():
+    c, _, v, lens = _cache(1, 1, 5, 3, 4, hot=8, cap=16)
+    _, vd = oracle.dequantized_kv(c, 0, 0, 5)
+    np.testing.assert_array_equal(vd, v[0, 0, :5].astype(np.float64))
+
+
+def test_empty_sequence_gives_zero_output():
+    c, _, _, _ = _cache(1, 1, 4, 3, 4)
+    q = synth.queries_fp16(0, 1, 1, 128)
+    assert np.all(oracle.decode_attention(c, q, [0])[0, 0] == 0)
+
+
+def test_split_bits():
+    assert oracle.split_bits(3.5) == (3, 4)
+    assert oracle.split_bits(4) == (4, 4)
+    assert oracle.split_bits(2.5) == (2, 3)
+    assert oracle.split_bits(4.2) == (4, 5)
+
+
+def test_turboquant_enabled_truth_table():
+    assert oracle.turboquant_enabled(None) is False
+    assert oracle.turboquant_enabled(None, "turboquant") is False
+    assert oracle.turboquant_enabled(4, "turboquant") is True
+    assert oracle.turboquant_enabled(3.5) is True
+    assert oracle.turboquant_enabled(4) is False
+    assert oracle.turboquant_enabled(4.0000001) is False
+    assert oracle.turboquant_enabled(4.2) is True
+    assert oracle.turboquant_enabled(2, "uniform") is False
