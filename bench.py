@@ -1,0 +1,478 @@
+#!/usr/bin/env python3
+"""Benchmark of the TurboQuant packed-KV hot path on GB300.
+
+Workload (the long-context 3.5-bit decode): batch 4, 32 query / 8 KV heads,
+head_dim 128, context lengths drawn uniform in [65536, 131072] per sequence,
+K 3-bit packed at every position, V 4-bit packed with the newest 256 tokens
+kept as an fp16 ring.  One step is one pass of the whole hot path for a
+decode step: append one new token per sequence (quantize K and V of all
+heads, quantizing the V token that leaves the ring) and decode attention of
+every query head over the whole cache (query rotation, split-K scoring with
+online softmax and V accumulation, merge and inverse rotation).  Lengths grow
+by one per step; the cache has head-room for the steps.
+
+Reported: decode-attention algorithmic HBM GB/s (packed K+V+norms, hot fp16 V,
+q, out per step) over the timed steps, its fraction of the measured HBM peak,
+quantize throughput (Mtokens/s) on the batch 16 x 8192-token x 8-head
+append at 3.5 bits, an end-to-end number through the public API with host
+buffers, and the CPU oracle on a bounded sample.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from bit_kv_cache_10_gb300 import synth  # noqa: E402
+
+METRIC = "packed-KV decode-attn HBM GB/s (% roofline) & quantize Mtokens/s, 1 GB300"
+SEED = 5
+B, HQ, HKV, D, W = 4, 32, 8, 128, 256
+KB, VB = 3, 4
+LO, HI = 65536, 131072
+QB, QT = 16, 8192  # quantize workload: batch x new tokens (8 KV heads)
+FALLBACK_HBM_GBS = 6800.0
+
+
+def decode_bytes(lens) -> int:
+    """Algorithmic bytes of one decode step: packed K + norms at every
+    position, packed V + norms on the cold part, fp16 V on the hot part,
+    the fp16 queries and the float32 outputs."""
+    total = 0
+    for L in lens:
+        L = int(L)
+        hot = min(W, L)
+        total += HKV * (L * (D * KB // 8 + 4) + (L - hot) * (D * VB // 8 + 4) + hot * D * 2)
+    return total + len(lens) * HQ * D * (2 + 4)
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as fh:
+            return float(json.load(fh)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profile_traffic():
+    """dram bytes per decode launch from the committed ncu summary, if it was
+    taken on the current decode kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "decode_long_context.md")
+    src = os.path.join(ROOT, "bit_kv_cache_10_gb300", "csrc", "tq_decode.cu")
+    try:
+        text = open(path).read()
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        m = re.search(r"traffic_bytes_per_step:\s*([0-9]+)", text)
+        s = re.search(r"decode_source_sha256_16:\s*([0-9a-f]+)", text)
+        if m and s and s.group(1) == sha:
+            return int(m.group(1))
+    except OSError:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = os.path.join("/tmp", "tq_clocks_%d_%d.csv" % (os.getpid(), gpu_index))
+
+    def start(self):
+        try:
+            self.fh = open(self.out, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self) -> list:
+        if self.proc is None:
+            return []
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        for line in open(self.out):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+                except ValueError:
+                    pass
+        os.unlink(self.out)
+        return rows
+
+    @staticmethod
+    def summarize(rows, source):
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "source": source}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[2]) if v.lower() == "active"})
+        return {"sm_mhz": float(np.median([r[0] for r in rows])), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows), "source": source}
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle (reference arm and cpu_baseline)
+# ----------------------------------------------------------------------------
+
+_ROWS: dict = {}
+
+
+def _oracle_row_cache(lens, b, h, n_tokens):
+    """The oracle's view of one (batch, KV head) row of the bench cache,
+    restricted to its first n_tokens positions (a bounded sample; the row
+    generators are prefix-consistent, so this equals a slice of the full row)."""
+    import oracle
+    key = (b, h, n_tokens)
+    if key not in _ROWS:
+        if len(_ROWS) > 64:
+            _ROWS.clear()
+        kw, kn = synth.packed_row(SEED, synth.STREAM_CODES_K, b, h, n_tokens, D * KB // 32, 12.0)
+        vw, vn = synth.packed_row(SEED, synth.STREAM_CODES_V, b, h, n_tokens, D * VB // 32, 30.0)
+        ring = synth.kv_fp16(SEED, synth.STREAM_V, B, HKV, W, D,
+                             synth.channel_scales(SEED, synth.STREAM_SCALE_V, HKV, D))[b:b + 1, h:h + 1]
+        _ROWS[key] = oracle.PackedCache(0, 0, D, KB, VB, kw[None, None], kn[None, None], None, vw[None, None],
+                                        vn[None, None], W, ring)
+    return _ROWS[key]
+
+
+def oracle_sample_step(lens, q16, b, h, n_tokens):
+    """Oracle decode of the G query heads of one (b, h) row over its first
+    n_tokens positions; returns (seconds, algorithmic bytes)."""
+    import oracle
+    c = _oracle_row_cache(lens, b, h, n_tokens)
+    g = HQ // HKV
+    t0 = time.perf_counter()
+    k, v = oracle.dequantized_kv(c, 0, 0, n_tokens)
+    for j in range(g):
+        oracle.attention_one(q16[b, h * g + j].astype(np.float64), k, v)
+    dt = time.perf_counter() - t0
+    hot = min(W, n_tokens)
+    nbytes = n_tokens * (D * KB // 8 + 4) + (n_tokens - hot) * (D * VB // 8 + 4) + hot * D * 2 + g * D * 6
+    return dt, nbytes
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(lens, q16, budget_s=12.0):
+    total_t, total_b, rows, row = 0.0, 0, 0, 0
+    while total_t < budget_s and rows < 2 * B * HKV:
+        b, h = row % B, (row // B) % HKV
+        dt, nb = oracle_sample_step(lens, q16, b, h, int(lens[b]))
+        total_t += dt
+        total_b += nb
+        rows += 1
+        row += 1
+    return {"value": total_b / total_t / 1e9, "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": "%d (batch, KV head) rows of the workload at full context (%.2f GB of algorithmic bytes), "
+                      "numpy float64 dequantize + softmax attention for the 4 query heads of each row" % (rows, total_b / 1e9)}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    lens = synth.seq_lengths(SEED, B, LO, HI)
+    q16 = synth.queries_fp16(SEED, B, HQ, D)
+    # size each step so that the whole run stays within a few minutes
+    dt_cal, nb_cal = oracle_sample_step(lens, q16, 0, 0, 4096)
+    rate = nb_cal / dt_cal
+    per_step_bytes = max(200_000.0, min(rate * 120.0 / max(1, args.steps + args.warmup), 5e8))
+    bytes_per_token = (D * KB // 8 + 4) + (D * VB // 8 + 4)
+    n_tok = int(max(512, min(HI, per_step_bytes / bytes_per_token)))
+    for s in range(args.warmup):
+        oracle_sample_step(lens, q16, s % B, (s // B) % HKV, min(n_tok, int(lens[s % B])))
+    tt, tb = 0.0, 0
+    for s in range(args.steps):
+        b, h = s % B, (s // B) % HKV
+        dt, nb = oracle_sample_step(lens, q16, b, h, min(n_tok, int(lens[b])))
+        tt += dt
+        tb += nb
+    value = tb / tt / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": tt / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "long-context 3.5-bit decode (K3 packed, V4 cold + 256 fp16 hot), B4, 32q/8kv, "
+                               "d128, L~U[65536,131072]; each step: one (batch, KV head) row, first %d positions" % n_tok},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "kind": "oracle", "cores": cpu_cores(),
+                         "sample": "per step one (batch, KV head) row of the decode workload, first %d context "
+                                   "positions, float64 dequantize + attention for its 4 query heads" % n_tok},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+
+def build_decode_cache(torch, cap):
+    from bit_kv_cache_10_gb300.cache import TurboQuantKVCache
+    lens = synth.seq_lengths(SEED, B, LO, HI)
+    tc = TurboQuantKVCache(B, HKV, HQ, cap, bits=(KB, VB), hot_window=W)
+    for b in range(B):
+        L = int(lens[b])
+        for h in range(HKV):
+            kw, kn = synth.packed_row(SEED, synth.STREAM_CODES_K, b, h, L, D * KB // 32, 12.0)
+            vw, vn = synth.packed_row(SEED, synth.STREAM_CODES_V, b, h, L, D * VB // 32, 30.0)
+            tc.k_cache[b, h, :L].copy_(torch.from_numpy(kw.view(np.int32)))
+            tc.k_norms[b, h, :L].copy_(torch.from_numpy(kn))
+            tc.v_cache[b, h, :L].copy_(torch.from_numpy(vw.view(np.int32)))
+            tc.v_norms[b, h, :L].copy_(torch.from_numpy(vn))
+    ring = synth.kv_fp16(SEED, synth.STREAM_V, B, HKV, W, D, synth.channel_scales(SEED, synth.STREAM_SCALE_V, HKV, D))
+    tc.v_hot.copy_(torch.from_numpy(ring))
+    torch.cuda.synchronize()
+    return tc, lens
+
+
+def step_inputs(n_steps):
+    """Per-step new K/V tokens [S, B, Hkv, 1, D] and queries [S, B, Hq, D], fp16."""
+    g = synth.rng(SEED + 1, synth.STREAM_Q)
+    q = g.standard_normal((n_steps, B, HQ, D), dtype=np.float32).astype(np.float16)
+    sk = synth.channel_scales(SEED, synth.STREAM_SCALE_K, HKV, D).astype(np.float32)
+    sv = synth.channel_scales(SEED, synth.STREAM_SCALE_V, HKV, D).astype(np.float32)
+    gk = synth.rng(SEED + 1, synth.STREAM_K)
+    gv = synth.rng(SEED + 1, synth.STREAM_V)
+    k = (gk.standard_normal((n_steps, B, HKV, 1, D), dtype=np.float32) * sk[None, None, :, None, :]).astype(np.float16)
+    v = (gv.standard_normal((n_steps, B, HKV, 1, D), dtype=np.float32) * sv[None, None, :, None, :]).astype(np.float16)
+    return k, v, q
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+    from bit_kv_cache_10_gb300 import build as tq_build
+    from bit_kv_cache_10_gb300.cache import TurboQuantKVCache
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    if rank == 0:
+        tq_build.build()
+    if world > 1:
+        dist.barrier()
+    from bit_kv_cache_10_gb300 import native
+    native.lib()
+
+    e2e_steps, e2e_warm = max(3, min(args.steps, 500)), 3
+    probe_steps = 10000
+    total_steps = args.warmup + args.steps + e2e_warm + e2e_steps + probe_steps
+    cap = HI + total_steps + 64
+    tc, lens0 = build_decode_cache(torch, cap)
+    kn, vn, qn = step_inputs(total_steps)
+    k_dev = torch.from_numpy(kn).cuda()
+    v_dev = torch.from_numpy(vn).cuda()
+    q_dev = torch.from_numpy(qn).cuda()
+    starts = torch.from_numpy((lens0[None, :] + np.arange(total_steps)[:, None]).astype(np.int32)).cuda()
+    seqs = starts + 1
+    max_len = HI + total_steps
+    out = torch.empty(B, HQ, D, dtype=torch.float32, device="cuda")
+    ws = torch.empty(tc.workspace_bytes(max_len), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(s):
+        tc.append(k_dev[s], v_dev[s], starts[s])
+        tc.decode(q_dev[s], seqs[s], max_len, out=out, workspace=ws)
+
+    for s in range(args.warmup):
+        step(s)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.15)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps + 2)]
+    torch.cuda.synchronize()
+    ev[0].record(stream)
+    for i in range(args.steps):
+        s = args.warmup + i
+        tc.append(k_dev[s], v_dev[s], starts[s])
+        ev[2 * i + 1].record(stream)
+        tc.decode(q_dev[s], seqs[s], max_len, out=out, workspace=ws)
+        ev[2 * i + 2].record(stream)
+    ev[-1].record(stream)
+    torch.cuda.synchronize()
+    clock_rows = sampler.stop()
+    total_ms = ev[0].elapsed_time(ev[-1])
+    decode_ms = [ev[2 * i + 1].elapsed_time(ev[2 * i + 2]) for i in range(args.steps)]
+    status = tc.device_status()
+    if status != 0:
+        raise RuntimeError("device status %#x during the benchmark" % status)
+    step_bytes = [decode_bytes(lens0 + args.warmup + i + 1) for i in range(args.steps)]
+    if world > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = world * sum(step_bytes) / (total_ms * 1e-3) / 1e9
+    s0 = args.warmup + args.steps
+
+    clocks = ClockSampler.summarize(clock_rows, "timed region")
+    if clocks["samples"] < 3:  # timed region too short for nvidia-smi: sample a longer run of the same step
+        sampler = ClockSampler(torch.cuda.current_device())
+        sampler.start()
+        time.sleep(0.15)
+        for i in range(probe_steps):
+            step(total_steps - probe_steps + i)
+        torch.cuda.synchronize()
+        clocks = ClockSampler.summarize(sampler.stop(), "%d further steps right after the timed region "
+                                                        "(the timed region was shorter than the sampling period)"
+                                        % probe_steps)
+
+    # end to end through the public API with host buffers
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+    h_k, h_v, h_q = pin(kn), pin(vn), pin(qn)
+    h_start = pin((lens0[None, :] + np.arange(total_steps)[:, None]).astype(np.int32))
+    h_out = torch.empty(B, HQ, D, dtype=torch.float32).pin_memory()
+    d_k = torch.empty_like(k_dev[0])
+    d_v = torch.empty_like(v_dev[0])
+    d_q = torch.empty_like(q_dev[0])
+    d_start = torch.empty(B, dtype=torch.int32, device="cuda")
+    d_seq = torch.empty(B, dtype=torch.int32, device="cuda")
+
+    def e2e_step(s):
+        d_k.copy_(h_k[s], non_blocking=True)
+        d_v.copy_(h_v[s], non_blocking=True)
+        d_q.copy_(h_q[s], non_blocking=True)
+        d_start.copy_(h_start[s], non_blocking=True)
+        torch.add(d_start, 1, out=d_seq)
+        tc.append(d_k, d_v, d_start)
+        tc.decode(d_q, d_seq, max_len, out=out, workspace=ws)
+        h_out.copy_(out, non_blocking=True)
+
+    for i in range(e2e_warm):
+        e2e_step(s0 + i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(e2e_steps):
+        e2e_step(s0 + e2e_warm + i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    e2e_bytes = sum(decode_bytes(lens0 + s0 + e2e_warm + i + 1) for i in range(e2e_steps))
+    h2d = kn[0].nbytes + vn[0].nbytes + qn[0].nbytes + B * 4
+    d2h = B * HQ * D * 4
+
+    # quantize throughput: batch 16 x 8192 new tokens x 8 KV heads at 3.5 bits (K3 / V4)
+    del k_dev, v_dev
+    gq = synth.rng(SEED + 2, synth.STREAM_K)
+    qsk = torch.from_numpy(synth.channel_scales(SEED + 2, synth.STREAM_SCALE_K, HKV, D).astype(np.float32)).cuda()
+    qsv = torch.from_numpy(synth.channel_scales(SEED + 2, synth.STREAM_SCALE_V, HKV, D).astype(np.float32)).cuda()
+    kq = torch.empty(QB, HKV, QT, D, dtype=torch.float16, device="cuda")
+    vq = torch.empty_like(kq)
+    for b in range(QB):  # drawn on the host in slices to bound host memory
+        kq[b].copy_((torch.from_numpy(gq.standard_normal((HKV, QT, D), dtype=np.float32)).cuda()
+                     * qsk[:, None, :]).half())
+        vq[b].copy_((torch.from_numpy(gq.standard_normal((HKV, QT, D), dtype=np.float32)).cuda()
+                     * qsv[:, None, :]).half())
+    qc = TurboQuantKVCache(QB, HKV, HKV * 4, QT, bits=(KB, VB))
+    zero = torch.zeros(QB, dtype=torch.int32, device="cuda")
+    for _ in range(3):
+        qc.append(kq, vq, zero)
+    torch.cuda.synchronize()
+    reps = 10
+    qe = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+    qe[0].record(stream)
+    for i in range(reps):
+        qc.append(kq, vq, zero)
+        qe[i + 1].record(stream)
+    torch.cuda.synchronize()
+    q_ms = [qe[i].elapsed_time(qe[i + 1]) for i in range(reps)]
+    q_avg = float(np.mean(q_ms))
+    q_tokens = QB * QT
+    q_bytes = 2 * QB * HKV * QT * D * 2 + QB * HKV * QT * ((D * KB // 8 + 4) + (D * VB // 8 + 4))
+    if qc.device_status() != 0:
+        raise RuntimeError("device status set by the quantize benchmark")
+
+    peak, peak_kind = measured_peak()
+    dec_avg_ms = float(np.mean(decode_ms))
+    dec_bytes = float(np.mean(step_bytes))
+    achieved = dec_bytes / (dec_avg_ms * 1e-3) / 1e9
+    traffic = profile_traffic()
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {
+            "workload": "long-context 3.5-bit decode: B4, 32q/8kv heads, d128, L~U[65536,131072] (+1 per step), "
+                        "K 3-bit packed, V 4-bit packed + 256-token fp16 hot window; step = append 1 token per "
+                        "sequence (quantize + ring evict) + decode attention of all query heads",
+            "mean_context": float(np.mean(lens0) + args.warmup + args.steps / 2),
+            "l2": "inputs larger than L2: %.0f MB of packed cache read per step" % (dec_bytes / 1e6),
+            "parallelism": "replicas" if world > 1 else "single GPU",
+        },
+        "roofline": {"bound": "hbm", "kernel": "decode attention (split-K kernel + merge kernel, one call)",
+                     "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": dec_bytes, "avg_launch_ms": dec_avg_ms},
+        "quantize": {"value": q_tokens / (q_avg * 1e-3) / 1e6, "unit": "Mtokens/s",
+                     "token": "one (batch, position) with all 8 KV heads, K and V",
+                     "token_heads_per_s": q_tokens * HKV / (q_avg * 1e-3),
+                     "workload": "batch 16 x 8192 new tokens x 8 KV heads, K 3-bit / V 4-bit, lognormal channels",
+                     "ms": q_avg, "hbm_gbs": q_bytes / (q_avg * 1e-3) / 1e9,
+                     "frac": q_bytes / (q_avg * 1e-3) / 1e9 / peak},
+        "e2e": {"value": world * e2e_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "clocks": clocks,
+        "gpu_launches": args.steps * 4,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(lens0, synth.queries_fp16(SEED, B, HQ, D))
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle timing")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)  # timing rule: at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,119 @@
+"""Torch-facing wrapper of the C ABI: a packed KV cache whose buffers are torch
+tensors on one CUDA device.  Argument marshalling only -- every step of the
+quantize, decode and dequantize paths runs in the CUDA library.
+
+Shapes follow the ``TurboQuantKVCache`` of the MLX-VLM deep-dive ("The
+TurboQuantKVCache Class"): packed uint32 words per token plus a float32 norm,
+with the (batch, KV head, position) shape kept so that slices stay cheap.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import native as N
+
+
+def _stream_handle(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+class TurboQuantKVCache:
+    """Packed K/V cache of one attention layer.
+
+    ``bits`` may be fractional (K gets floor, V gets ceil) or a (k_bits,
+    v_bits) pair; ``k_fp16=True`` keeps K in fp16 (the asym modes);
+    ``hot_window`` > 0 keeps the newest V tokens in an fp16 ring.
+    """
+
+    def __init__(self, batch: int, num_kv_heads: int, num_q_heads: int, capacity: int, bits=3.5,
+                 head_dim: int = 128, k_fp16: bool = False, hot_window: int = 0, seed: int = 0, layer: int = 0,
+                 device="cuda"):
+        if isinstance(bits, tuple):
+            k_bits, v_bits = bits
+        else:
+            k_bits, v_bits = N.tq_split_bits(float(bits))
+        self.device = torch.device(device)
+        self.desc = N.tq_cache_desc_init(batch, num_kv_heads, num_q_heads, head_dim, capacity,
+                                         N.TQ_K_FP16 if k_fp16 else N.TQ_K_PACKED, 0 if k_fp16 else k_bits, v_bits,
+                                         hot_window, seed, layer)
+        d = self.desc
+        self.batch, self.num_kv_heads, self.num_q_heads = batch, num_kv_heads, num_q_heads
+        self.head_dim, self.capacity, self.hot_window = head_dim, capacity, hot_window
+        self.k_bits = 16 if k_fp16 else k_bits
+        self.v_bits = v_bits
+        shape = (batch, num_kv_heads, capacity)
+        if k_fp16:
+            self.k_cache = torch.zeros(*shape, head_dim, dtype=torch.float16, device=self.device)
+            self.k_norms = None
+        else:
+            self.k_cache = torch.zeros(*shape, head_dim * k_bits // 32, dtype=torch.int32, device=self.device)
+            self.k_norms = torch.zeros(*shape, dtype=torch.float32, device=self.device)
+        self.v_cache = torch.zeros(*shape, head_dim * v_bits // 32, dtype=torch.int32, device=self.device)
+        self.v_norms = torch.zeros(*shape, dtype=torch.float32, device=self.device)
+        self.v_hot = (torch.zeros(batch, num_kv_heads, hot_window, head_dim, dtype=torch.float16, device=self.device)
+                      if hot_window > 0 else None)
+        self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
+        d.k_cache = self.k_cache.data_ptr()
+        d.k_norms = self.k_norms.data_ptr() if self.k_norms is not None else None
+        d.v_cache = self.v_cache.data_ptr()
+        d.v_norms = self.v_norms.data_ptr()
+        d.v_hot = self.v_hot.data_ptr() if self.v_hot is not None else None
+        d.d_status = self.status.data_ptr()
+        self._workspace = None
+
+    # -- update ---------------------------------------------------------------
+    def append(self, k: torch.Tensor, v: torch.Tensor, start_pos: torch.Tensor,
+               num_new: torch.Tensor | None = None) -> None:
+        """Quantize and store fp16 K/V [B, Hkv, n_new, d] at positions start_pos[b] + t.
+
+        ``k`` and ``v`` must have the same strides with a contiguous last
+        dimension; ``start_pos`` is an int32 device tensor [B]; the optional
+        int32 ``num_new`` [B] limits sequence b to its first num_new[b] rows."""
+        if k.dtype != torch.float16 or v.dtype != torch.float16 or k.shape != v.shape or k.stride() != v.stride():
+            raise ValueError("k and v must be fp16 tensors of equal shape and strides")
+        if k.dim() != 4 or k.stride(3) != 1 or k.device != self.device:
+            raise ValueError("k/v must be [B, Hkv, n_new, d] on the cache device with contiguous d")
+        if start_pos.dtype != torch.int32 or start_pos.device != self.device or not start_pos.is_contiguous():
+            raise ValueError("start_pos must be a contiguous int32 tensor on the cache device")
+        if num_new is not None and (num_new.dtype != torch.int32 or num_new.device != self.device
+                                    or not num_new.is_contiguous()):
+            raise ValueError("num_new must be a contiguous int32 tensor on the cache device")
+        N.tq_quantize_append(self.desc, k.data_ptr(), v.data_ptr(), k.stride(0), k.stride(1), k.stride(2),
+                             k.shape[2], start_pos.data_ptr(), num_new.data_ptr() if num_new is not None else None,
+                             _stream_handle(self.device))
+
+    # -- decode ---------------------------------------------------------------
+    def workspace_bytes(self, max_seq_len: int) -> int:
+        return N.tq_decode_workspace_bytes(self.desc, max_seq_len)
+
+    def decode(self, q: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int, out: torch.Tensor | None = None,
+               workspace: torch.Tensor | None = None) -> torch.Tensor:
+        """Attention of fp16 queries [B, Hq, d] over the cache; returns float32 [B, Hq, d]."""
+        if q.dtype != torch.float16 or not q.is_contiguous() or q.shape != (self.batch, self.num_q_heads, self.head_dim):
+            raise ValueError("q must be a contiguous fp16 tensor [B, Hq, d]")
+        if seq_lens.dtype != torch.int32 or seq_lens.device != self.device or not seq_lens.is_contiguous():
+            raise ValueError("seq_lens must be a contiguous int32 tensor on the cache device")
+        if out is None:
+            out = torch.empty(self.batch, self.num_q_heads, self.head_dim, dtype=torch.float32, device=self.device)
+        need = self.workspace_bytes(max_seq_len)
+        if workspace is None:
+            if self._workspace is None or self._workspace.numel() < need:
+                self._workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=self.device)
+            workspace = self._workspace
+        N.tq_decode_attention(self.desc, q.data_ptr(), seq_lens.data_ptr(), max_seq_len, out.data_ptr(),
+                              workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                              _stream_handle(self.device))
+        return out
+
+    # -- inspection -------------------------------------------------------------
+    def dequantize(self, which: int, b: int, seq_len: int, token_start: int, n_tokens: int) -> torch.Tensor:
+        """float32 [Hkv, n_tokens, d] of positions [token_start, token_start + n_tokens) of sequence b."""
+        out = torch.empty(self.num_kv_heads, max(n_tokens, 1), self.head_dim, dtype=torch.float32,
+                          device=self.device)
+        N.tq_dequantize(self.desc, which, b, seq_len, token_start, n_tokens, out.data_ptr(),
+                        _stream_handle(self.device))
+        return out[:, :n_tokens]
+
+    def device_status(self) -> int:
+        """OR of the TQ_DEV_ERR_* bits raised by the kernels so far (synchronizes)."""
+        return int(self.status.item())

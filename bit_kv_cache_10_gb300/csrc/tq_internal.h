@@ -1,0 +1,37 @@
+// Internal declarations shared by the library's translation units (not part of the C ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "tq.h"
+
+namespace tq {
+
+constexpr int kHeadDim = 128;     // the kernels are written for d = 128
+constexpr int kMinBits = 2;       // GPU path: 2..4 bits per coordinate ([MLX-VLM CLI guide] FAQ
+constexpr int kMaxBits = 4;       // "What bit widths does TurboQuant support?")
+constexpr int kMaxGroup = 4;      // query heads per KV head handled by the decode kernels
+constexpr int kDecodeChunk = 1024;  // context tokens per split-K chunk
+
+// Words of one packed token vector.
+inline int words_per_token(int head_dim, int bits) { return head_dim * bits / 32; }
+
+// Host validation of a descriptor: shapes, modes and codebooks only, then
+// additionally the buffer pointers (non-NULL where the mode needs them, 16-byte aligned).
+tq_status validate_shape(const tq_cache_desc* d);
+tq_status validate_desc(const tq_cache_desc* d);
+
+// Number of split-K chunks covering max_seq_len tokens (cold part) and the
+// number of partial slots per (batch, query head), including the hot-window slot.
+int decode_num_chunks(const tq_cache_desc* d, int max_seq_len);
+int decode_num_slots(const tq_cache_desc* d, int max_seq_len);
+
+// Bucket scale of the threshold lookup table used by the quantize kernel: the
+// smallest power of two A for which every bucket RN(y*A) holds at most one
+// float32 threshold.  Returns 0 if none up to 4096.
+int quant_lut_scale(const float* thresholds, int n_thresholds);
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace tq

@@ -92,3 +92,20 @@ def random_norms(seed: int, stream: int, shape: tuple, median: float = 30.0,
     """Positive float32 norms, lognormal around ``median`` (spread ``sigma``)."""
     g = rng(seed, stream)
     return (median * np.exp(sigma * g.standard_normal(shape))).astype(np.float32)
+
+
+def row_rng(seed: int, stream: int, b: int, h: int) -> np.random.Generator:
+    """PCG64 generator of one (batch, KV head) row of a stream, so that a
+    sampled row can be drawn without drawing the whole cache."""
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence([int(seed), int(stream), int(b), int(h)])))
+
+
+def packed_row(seed: int, stream: int, b: int, h: int, tokens: int, words_per_token: int,
+               norm_median: float, norm_sigma: float = 0.3):
+    """Random packed words uint32 [tokens, words_per_token] and lognormal
+    float32 norms [tokens] of one cache row: every bit pattern is a valid
+    packed record, so uniform random words stand in for a filled cache."""
+    words = row_rng(seed, stream, b, h).integers(0, 2 ** 32, size=(tokens, words_per_token), dtype=np.uint32)
+    g = row_rng(seed, stream + 1000, b, h)  # separate stream: a shorter draw is a prefix of a longer one
+    norms = (norm_median * np.exp(norm_sigma * g.standard_normal(tokens))).astype(np.float32)
+    return words, norms

@@ -1,0 +1,306 @@
+/*
+ * tq.h -- C ABI of the TurboQuant packed KV-cache library (GB300, sm_103a).
+ *
+ * The library implements the data-parallel hot path of TurboQuant KV-cache
+ * quantization as the pages below describe it, in hand-written CUDA:
+ *
+ *   [MLX-VLM deep-dive]  "TurboQuant KV Cache Quantization in MLX-VLM: Low-Bit
+ *                         Compression for Efficient Generation"
+ *   [MLX-VLM CLI guide]  "How to Use TurboQuant with the MLX-VLM CLI:
+ *                         KV-Cache Compression Guide"
+ *   [mlxcel doc]         "TurboQuant KV cache" (mlxcel docs/turbo-kv-cache.md)
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Ownership.   The caller allocates every device buffer (cache, queries,
+ *              outputs, workspace) and keeps it alive while work that uses it
+ *              is queued.  The library allocates no device memory, keeps no
+ *              global state, and may be called from several host threads.
+ * Asynchrony.  Functions taking a stream enqueue kernels on it and return at
+ *              once; results are ready when the stream is.  A NULL stream is
+ *              the legacy default stream.  The host-only helpers are
+ *              synchronous and need no GPU.
+ * Errors.      Argument errors are found on the host and returned before any
+ *              launch (nothing is enqueued).  A failed launch returns
+ *              TQ_ERR_CUDA.  Errors that only the device can see (a start
+ *              position or a sequence length outside the cache) set bits of
+ *              the optional device status word `d_status` (atomic OR) and the
+ *              offending sequence is skipped; kernels never trap and never
+ *              spin-wait.
+ * Layouts.     All index arithmetic is row-major.  "[B, Hkv, cap, W]" means a
+ *              contiguous array with W fastest.  Device pointers must be
+ *              16-byte aligned (cudaMalloc and torch give 256 bytes).
+ */
+#ifndef TQ_H_
+#define TQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t (declared here so that the header needs no CUDA headers). */
+typedef struct CUstream_st *tq_stream_t;
+
+typedef enum tq_status {
+  TQ_OK = 0,
+  TQ_ERR_INVALID_ARG = -1, /* null pointer, bad shape, misaligned pointer or stride */
+  TQ_ERR_UNSUPPORTED = -2, /* valid request outside what the kernels implement
+                              (head_dim not a power of two, bits outside 2..4, ...) */
+  TQ_ERR_CAPACITY = -3,    /* a host-visible size exceeds the cache capacity */
+  TQ_ERR_WORKSPACE = -4,   /* workspace pointer missing, misaligned or too small */
+  TQ_ERR_CUDA = -5,        /* a CUDA runtime call or launch failed */
+  TQ_ERR_DEVICE = -6       /* reserved: device-side error reported through d_status */
+} tq_status;
+
+/* Bits of the device status word (OR-ed together by the kernels). */
+#define TQ_DEV_ERR_APPEND_RANGE 0x1u /* start_pos < 0, bad per-sequence count, or past capacity */
+#define TQ_DEV_ERR_SEQ_LEN 0x2u      /* seq_len < 0 or seq_len > capacity (or > max_seq_len) */
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *tq_status_string(tq_status status);
+
+/* ------------------------------------------------------------------------ */
+/* Codebook                                                                   */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Lloyd-Max scalar codebook for one coordinate of a randomly rotated unit
+ * vector in R^d, whose density is f_d(x) = C_d (1 - x^2)^((d-3)/2) on [-1, 1]
+ * ([MLX-VLM deep-dive] "How TurboQuant KV Cache Quantization Works": a
+ * Beta-PDF-based Lloyd-Max quantizer; [MLX-VLM CLI guide] "What Is
+ * TurboQuant?": the codebook generator).  2^bits reconstruction levels in
+ * ascending order; thresholds are the midpoints of neighbouring levels.
+ * The kernels use the float32 fields; the float64 fields record the fixed
+ * point before rounding.
+ */
+typedef struct tq_codebook {
+  int32_t head_dim;
+  int32_t bits;               /* 1..4 */
+  float centroids[16];        /* first 2^bits used, ascending */
+  float thresholds[15];       /* first 2^bits - 1 used: (c[k] + c[k+1]) / 2 */
+  double centroids_f64[16];
+  double thresholds_f64[15];
+  double mse_per_coord;       /* E[(x - c(x))^2] under f_d */
+  int32_t iterations;         /* Lloyd iterations taken */
+} tq_codebook;
+
+/*
+ * Build the codebook for (head_dim, bits).  Host only, synchronous, needs no
+ * GPU; takes up to about a second for bits = 4.  Lloyd's two conditions are
+ * iterated with cell integrals by composite Gauss-Legendre quadrature until
+ * no level moves by more than 1e-15.
+ *   head_dim  3 .. 65536 (the density needs d >= 3)
+ *   bits      1 .. 4
+ *   out       written on success
+ * Returns TQ_ERR_INVALID_ARG for a NULL `out`, TQ_ERR_UNSUPPORTED for values
+ * outside the ranges above.
+ */
+tq_status tq_build_codebook(int32_t head_dim, int32_t bits, tq_codebook *out);
+
+/*
+ * Fractional bit budget split: K gets floor(bits), V gets ceil(bits)
+ * ([MLX-VLM deep-dive] "Quantization Codecs and Bit Splitting").
+ * bits must be finite and in (0, 16]; both outputs must be non-NULL.
+ */
+tq_status tq_split_bits(double bits, int32_t *k_bits, int32_t *v_bits);
+
+/*
+ * Whether the TurboQuant scheme is selected ([MLX-VLM CLI guide] "Activation
+ * Logic and CLI Integration"): 0 when no bit width is given (has_bits == 0);
+ * 1 when the scheme is explicitly "turboquant"; otherwise 1 exactly when
+ * `bits` is more than 1e-6 away from the nearest integer.
+ */
+int32_t tq_turboquant_enabled(double bits, int32_t has_bits, int32_t scheme_is_turboquant);
+
+/*
+ * The library's rotation signs for one KV head: out[i] = +1 or -1, i < head_dim.
+ * s_i = -1 when bit 63 of SplitMix64's first output from state
+ * seed + (layer << 32 | head << 16 | i) is set ([MLX-VLM deep-dive] "How
+ * TurboQuant KV Cache Quantization Works" names a deterministic random
+ * rotation but no generator; this reading fixes one).  Host only.
+ * layer in [0, 2^31), head in [0, 2^16), head_dim in [1, 2^16].
+ */
+tq_status tq_rotation_signs(uint64_t seed, int32_t layer, int32_t head, int32_t head_dim, int8_t *out);
+
+/* ------------------------------------------------------------------------ */
+/* Cache descriptor                                                           */
+/* ------------------------------------------------------------------------ */
+
+enum { TQ_K_PACKED = 0, /* K quantized like V (symmetric turbo modes) */
+       TQ_K_FP16 = 1    /* K kept fp16, V packed (the "asym" modes of [mlxcel doc] "Available modes") */ };
+
+/*
+ * Describes one layer's KV cache.  All pointers are caller-owned device
+ * buffers; sizes follow from the shape fields (see tq_cache_buffer_bytes).
+ *
+ *   k_cache  TQ_K_PACKED: uint32 [B, Hkv, cap, head_dim*k_bits/32] packed codes
+ *            TQ_K_FP16:   fp16   [B, Hkv, cap, head_dim]
+ *   k_norms  float [B, Hkv, cap] per-token K norms (TQ_K_PACKED only)
+ *   v_cache  uint32 [B, Hkv, cap, head_dim*v_bits/32] packed V codes
+ *   v_norms  float [B, Hkv, cap]
+ *   v_hot    fp16 [B, Hkv, hot_window, head_dim] ring of the newest V tokens
+ *            (hot_window > 0 only): position p lives in slot p mod hot_window
+ *            ([mlxcel doc] "Available modes", turbo4-delegated: recent V in
+ *            fp16, the cold tail packed)
+ *   d_status optional device uint32 status word (may be NULL)
+ *
+ * Packed layout: code i of a token occupies bits [i*b, i*b+b) of that
+ * token's bitstream, stream bit j is bit (j mod 32) of word j/32, codes may
+ * straddle words ([MLX-VLM deep-dive] "The TurboQuantKVCache Class" and
+ * "Manual Cache Operations": packed uint32 buffers, several codes per word).
+ * The per-token norm is the correctly rounded float32 of the exact norm.
+ *
+ * GQA: query head hq reads KV head hq / (num_q_heads / num_kv_heads).
+ */
+typedef struct tq_cache_desc {
+  int32_t batch;         /* B >= 1 */
+  int32_t num_kv_heads;  /* Hkv >= 1 */
+  int32_t num_q_heads;   /* Hq, a multiple of Hkv */
+  int32_t head_dim;      /* d; the kernels implement d = 128 */
+  int32_t capacity;      /* cap >= 1 tokens per (sequence, KV head) */
+  int32_t k_mode;        /* TQ_K_PACKED or TQ_K_FP16 */
+  int32_t k_bits;        /* 2..4 when K is packed (ignored for TQ_K_FP16) */
+  int32_t v_bits;        /* 2..4 */
+  int32_t hot_window;    /* 0 = none; else 1..cap fp16 V ring length */
+  int32_t layer;         /* rotation-sign stream, [0, 2^31) */
+  uint64_t seed;         /* rotation-sign seed */
+  tq_codebook k_cb;      /* built for (head_dim, k_bits) when K is packed */
+  tq_codebook v_cb;      /* built for (head_dim, v_bits) */
+  void *k_cache;
+  float *k_norms;
+  void *v_cache;
+  float *v_norms;
+  void *v_hot;
+  uint32_t *d_status;
+} tq_cache_desc;
+
+/*
+ * Fill the shape and mode fields of `desc`, build both codebooks (host, as
+ * tq_build_codebook) and set every pointer to NULL.  The caller then sets
+ * the buffer pointers.  Validates like the launch entry points.
+ */
+tq_status tq_cache_desc_init(tq_cache_desc *desc, int32_t batch, int32_t num_kv_heads, int32_t num_q_heads,
+                             int32_t head_dim, int32_t capacity, int32_t k_mode, int32_t k_bits,
+                             int32_t v_bits, int32_t hot_window, uint64_t seed, int32_t layer);
+
+/*
+ * Bytes of each buffer the descriptor needs (0 for a buffer the mode does
+ * not use).  Any output pointer may be NULL.  Host only.
+ */
+tq_status tq_cache_buffer_bytes(const tq_cache_desc *desc, size_t *k_cache_bytes, size_t *k_norms_bytes,
+                                size_t *v_cache_bytes, size_t *v_norms_bytes, size_t *v_hot_bytes);
+
+/* ------------------------------------------------------------------------ */
+/* Quantize / append                                                          */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Append n_new fp16 token vectors of K and of V to every (sequence, KV head)
+ * of the cache, at positions [start_b, start_b + n_new) of sequence b, with
+ * start_b = d_start_pos[b] (device int32 [B]).  This is the update step of
+ * [MLX-VLM deep-dive] "Manual Cache Operations" (update_and_fetch) and, with
+ * start 0, the bulk conversion of an existing fp16 cache.
+ *
+ * Each packed vector x gets its norm n = ||x|| (correctly rounded float32)
+ * and codes of y = R (x / n), R = (1/sqrt(d)) H diag(s): the sign flip, a
+ * fast Walsh-Hadamard transform and the 1/sqrt(d) scale ([MLX-VLM
+ * deep-dive] "How TurboQuant KV Cache Quantization Works"); code_i is the
+ * number of float32 thresholds t_k <= y_i, i.e. the nearest level with ties
+ * going up.  K and V of all heads are processed by one launch
+ * ([MLX-VLM deep-dive] "Fused vs. Separate Quantization Paths").
+ *
+ *   k_new, v_new  fp16 device arrays viewed as [B, Hkv, n_new, head_dim] with
+ *                 the given element strides (stride over batch, head, token;
+ *                 the last dimension is contiguous).  Both use the same
+ *                 strides; strides and base pointers must be multiples of 8
+ *                 elements / 16 bytes.
+ *   n_new         >= 0 (0 is a no-op)
+ *   d_start_pos   device int32 [B]: number of tokens already stored for each
+ *                 sequence (appends must continue a sequence)
+ *   d_num_new     optional device int32 [B] (NULL = n_new for every
+ *                 sequence): sequence b appends its first d_num_new[b] <=
+ *                 n_new rows, so that sequences of different lengths can be
+ *                 filled in one launch (ragged prefill)
+ *   stream        CUDA stream
+ *
+ * TQ_K_FP16: K rows are copied into the fp16 K cache.
+ * hot_window W > 0: after the call positions [end - W, end) of V (end =
+ * start + n_new) are in the fp16 ring and [0, end - W) are packed; V tokens
+ * that leave the ring are quantized before their slot is reused (one extra
+ * launch, before the append launch, on the same stream).
+ *
+ * A start position < 0, a count outside [0, n_new] or start + count >
+ * capacity sets TQ_DEV_ERR_APPEND_RANGE in d_status and skips that sequence.
+ */
+tq_status tq_quantize_append(const tq_cache_desc *desc, const void *k_new, const void *v_new, int64_t stride_b,
+                             int64_t stride_h, int64_t stride_t, int32_t n_new, const int32_t *d_start_pos,
+                             const int32_t *d_num_new, tq_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Decode attention                                                           */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Workspace bytes tq_decode_attention needs for this descriptor when no
+ * sequence is longer than max_seq_len (>= 0).  Host only; 0 on bad input.
+ */
+size_t tq_decode_workspace_bytes(const tq_cache_desc *desc, int32_t max_seq_len);
+
+/*
+ * One decode step of attention for every query head, reading the packed
+ * cache directly ([MLX-VLM deep-dive] "How TurboQuant KV Cache Quantization
+ * Works": scores from the compressed form; [MLX-VLM CLI guide] "What Is
+ * TurboQuant?": fused scoring kernels with query-head repeat):
+ *
+ *   out[b, hq] = sum_j softmax_j(q.k_j / sqrt(d)) v_j,   j < seq_len_b
+ *
+ * with k_j, v_j the dequantized tokens n_j R^T c[codes_j] (or the raw fp16 K
+ * in TQ_K_FP16 mode, and the raw fp16 V of the hot ring for the newest
+ * min(W, L) positions).  The query is rotated once, scores are
+ * n_j * sum_i (R q)_i c[code_ji], the softmax runs online over split-K
+ * chunks of the context, V is accumulated in the rotated domain and rotated
+ * back once per output by a reduction kernel.
+ *
+ *   q            fp16 device [B, Hq, head_dim] (contiguous)
+ *   d_seq_lens   device int32 [B], each in [0, min(capacity, max_seq_len)]
+ *   max_seq_len  host upper bound of the lengths (sizes the split grid)
+ *   out          float32 device [B, Hq, head_dim]; zeros for an empty sequence
+ *   workspace    device scratch of >= tq_decode_workspace_bytes(desc,
+ *                max_seq_len) bytes, 16-byte aligned; contents are
+ *                overwritten, nothing needs clearing
+ *
+ * Launches two kernels on `stream`.  A length outside [0, capacity] or above
+ * max_seq_len sets TQ_DEV_ERR_SEQ_LEN and that sequence's output is zero.
+ */
+tq_status tq_decode_attention(const tq_cache_desc *desc, const void *q, const int32_t *d_seq_lens,
+                              int32_t max_seq_len, float *out, void *workspace, size_t workspace_bytes,
+                              tq_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Dequantize                                                                 */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Dequantize positions [token_start, token_start + n_tokens) of sequence b
+ * for all KV heads: x_hat = n R^T c[codes] as float32 ([MLX-VLM deep-dive]
+ * FAQ "Where is the dequantization logic implemented?").  which = 0 reads
+ * K, 1 reads V.  For V with a hot window, positions >= seq_len - min(W,
+ * seq_len) return the fp16 ring value; seq_len is the host-known length of
+ * sequence b (only used for that split).  TQ_K_FP16 K returns the stored
+ * fp16 values.
+ *
+ *   out  float32 device [Hkv, n_tokens, head_dim]
+ * Requires 0 <= token_start, token_start + n_tokens <= capacity and
+ * token_start + n_tokens <= seq_len when a hot window is used.
+ */
+tq_status tq_dequantize(const tq_cache_desc *desc, int32_t which, int32_t b, int32_t seq_len,
+                        int32_t token_start, int32_t n_tokens, float *out, tq_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TQ_H_ */

@@ -1,0 +1,33 @@
+/*
+ * tq_debug.h -- verification hooks of the TurboQuant library.
+ *
+ * These entry points run the host build of the kernels' per-vector
+ * arithmetic (the same source file, compiled for the CPU with IEEE float32
+ * round-to-nearest and no contraction), so that the exact-norm rounding, the
+ * rotation and the bucketed threshold lookup can be checked on a machine
+ * without a GPU.  No product entry point of tq.h calls them, and they are
+ * not a fallback: they only exist to test the device code path.
+ */
+#ifndef TQ_DEBUG_H_
+#define TQ_DEBUG_H_
+
+#include "tq.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * Quantize n_rows fp16 vectors of length 128 (host memory, `rows` holds the
+ * raw fp16 bit patterns, row-major) with the codebook `cb` (head_dim 128,
+ * bits 2..4) and the rotation signs of (seed, layer, head).  Writes
+ * n_rows * bits * 4 packed words and n_rows norms (host memory).
+ */
+tq_status tq_debug_quantize_rows_host(const tq_codebook *cb, uint64_t seed, int32_t layer, int32_t head,
+                                      const uint16_t *rows, int32_t n_rows, uint32_t *words, float *norms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TQ_DEBUG_H_ */
