@@ -33,6 +33,8 @@ class TurboQuantKVCache:
         else:
             k_bits, v_bits = N.tq_split_bits(float(bits))
         self.device = torch.device(device)
+        if self.device.type == "cuda" and self.device.index is None:
+            self.device = torch.device("cuda", torch.cuda.current_device())
         self.desc = N.tq_cache_desc_init(batch, num_kv_heads, num_q_heads, head_dim, capacity,
                                          N.TQ_K_FP16 if k_fp16 else N.TQ_K_PACKED, 0 if k_fp16 else k_bits, v_bits,
                                          hot_window, seed, layer)
