@@ -73,6 +73,7 @@ def rotation_signs(seed: int, layer: int, head: int, d: int) -> np.ndarray:
     the first SplitMix64 output from state ``seed + (layer<<32 | h<<16 | i)``
     is set, else +1.  K and V of one head share the signs.
     """
+    seed, layer, head, d = int(seed), int(layer), int(head), int(d)  # plain Python integers (no numpy overflow)
     if not (0 <= head < 1 << 16 and 0 <= d <= 1 << 16 and 0 <= layer < 1 << 31):
         raise ValueError("head, d or layer out of range")
     out = np.empty(d, dtype=np.int8)

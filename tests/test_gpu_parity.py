@@ -209,7 +209,7 @@ def test_quantize_full_size(bits):
         gw = (tc.k_cache if which == 0 else tc.v_cache).cpu().numpy().view(np.uint32)
         gn = (tc.k_norms if which == 0 else tc.v_norms).cpu().numpy()
         # two full (batch, head) rows and 4096 random token vectors
-        sel = [(0, 0), (B - 1, HK - 1)] + [tuple(t) for t in zip(rng.integers(0, B, 8), rng.integers(0, HK, 8))]
+        sel = [(0, 0), (B - 1, HK - 1)] + [(int(b), int(h)) for b, h in zip(rng.integers(0, B, 8), rng.integers(0, HK, 8))]
         for b, h in sel[:2]:
             ref_w, ref_n, ys = quantize_reference(x[b:b + 1, h:h + 1], 0, 0, nb, heads=[h])
             np.testing.assert_array_equal(gn[b, h], ref_n[0, 0])
