@@ -13,7 +13,7 @@ import oracle
 from bit_kv_cache_10_gb300 import native as N
 from bit_kv_cache_10_gb300 import synth
 
-from helpers import assert_attention_close, compare_packed
+from helpers import assert_attention_close, assert_code_rate, compare_packed
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -80,13 +80,14 @@ def check_quantized(tc, x16, which, bits, lengths, seed=0, layer=0, what=""):
     gw = (tc.k_cache if which == 0 else tc.v_cache).cpu().numpy().view(np.uint32)
     gn = (tc.k_norms if which == 0 else tc.v_norms).cpu().numpy()
     thr = oracle.codebook(D, bits).thresholds32
-    total_mism = 0
+    total_mism, total_codes = 0, 0
     for b in range(x16.shape[0]):
         L = int(lengths[b])
         np.testing.assert_array_equal(gn[b, :, :L], ref_n[b, :, :L], err_msg=what + " norms")
-        m, _ = compare_packed(gw[b, :, :L].reshape(-1, gw.shape[-1]), ref_w[b, :, :L].reshape(-1, ref_w.shape[-1]),
-                              ys[b, :, :L].reshape(-1, D), bits, thr, what)
-        total_mism += m
+        m, c = compare_packed(gw[b, :, :L].reshape(-1, gw.shape[-1]), ref_w[b, :, :L].reshape(-1, ref_w.shape[-1]),
+                              ys[b, :, :L].reshape(-1, D), bits, thr, what, check_rate=False)
+        total_mism, total_codes = total_mism + m, total_codes + c
+    assert_code_rate(total_mism, total_codes, what)
     return total_mism
 
 
@@ -205,21 +206,25 @@ def test_quantize_full_size(bits):
     assert tc.device_status() == 0
     kb, vb = bits
     rng = np.random.default_rng(sum(bits))
+    n_mism, n_codes = 0, 0
     for which, x, nb in ((0, k, kb), (1, v, vb)):
         gw = (tc.k_cache if which == 0 else tc.v_cache).cpu().numpy().view(np.uint32)
         gn = (tc.k_norms if which == 0 else tc.v_norms).cpu().numpy()
-        # two full (batch, head) rows and 4096 random token vectors
+        thr = oracle.codebook(D, nb).thresholds32
+        # two full (batch, head) rows and 8 x 512 random token vectors
         sel = [(0, 0), (B - 1, HK - 1)] + [(int(b), int(h)) for b, h in zip(rng.integers(0, B, 8), rng.integers(0, HK, 8))]
         for b, h in sel[:2]:
             ref_w, ref_n, ys = quantize_reference(x[b:b + 1, h:h + 1], 0, 0, nb, heads=[h])
             np.testing.assert_array_equal(gn[b, h], ref_n[0, 0])
-            compare_packed(gw[b, h], ref_w[0, 0], ys[0, 0], nb, oracle.codebook(D, nb).thresholds32, "full row")
+            m, c = compare_packed(gw[b, h], ref_w[0, 0], ys[0, 0], nb, thr, "full row", check_rate=False)
+            n_mism, n_codes = n_mism + m, n_codes + c
         for b, h in sel[2:]:
             t_idx = rng.choice(T, 512, replace=False)
-            c, n, y = oracle.quantize_rows(x[b, h, t_idx], oracle.rotation(0, 0, h, D), oracle.codebook(D, nb))
+            c_, n, y = oracle.quantize_rows(x[b, h, t_idx], oracle.rotation(0, 0, h, D), oracle.codebook(D, nb))
             np.testing.assert_array_equal(gn[b, h, t_idx], n)
-            compare_packed(gw[b, h, t_idx], oracle.pack(c, nb), y, nb, oracle.codebook(D, nb).thresholds32,
-                           "sampled rows")
+            m, c = compare_packed(gw[b, h, t_idx], oracle.pack(c_, nb), y, nb, thr, "sampled rows", check_rate=False)
+            n_mism, n_codes = n_mism + m, n_codes + c
+    assert_code_rate(n_mism, n_codes, "quantize %s" % (bits,))
 
 
 # --------------------------------------------------------------------------
