@@ -21,6 +21,7 @@
 // of the chunks, one inverse rotation D_h H / sqrt(d) of the cold sum, the
 // hot sum added in the original domain, division by the softmax mass.
 #include <cstring>
+#include <mutex>
 
 #include "tq_device.cuh"
 #include "tq_internal.h"
@@ -566,4 +567,47 @@ extern "C" tq_status tq_decode_attention(const tq_cache_desc* d, const void* q, 
   if (st != TQ_OK) return st;
   decode_merge_kernel<<<dim3(d->num_q_heads, d->batch), D, 0, s>>>(p);
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------
+// Decode without a caller workspace: the split-K partials live in a fixed
+// device array of this file, for callers that cannot allocate device memory.
+// ---------------------------------------------------------------------------
+namespace {
+
+static __device__ __align__(256) unsigned char g_no_alloc_scratch[TQ_NO_ALLOC_WORKSPACE_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+void* g_scratch_address[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device.  In host code the
+// array's name only stands in for the symbol, so the address is looked up once
+// per device with that device current.
+tq_status no_alloc_scratch(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return TQ_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return TQ_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (g_scratch_address[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_no_alloc_scratch) != cudaSuccess || p == nullptr) return TQ_ERR_CUDA;
+    g_scratch_address[dev] = p;
+  }
+  *out = g_scratch_address[dev];
+  return TQ_OK;
+}
+
+}  // namespace
+
+extern "C" tq_status tq_decode_attention_no_alloc(const tq_cache_desc* d, const void* q, const int32_t* d_seq_lens,
+                                                  int32_t max_seq_len, float* out, tq_stream_t stream) {
+  const tq_status vs = tq::validate_desc(d);
+  if (vs != TQ_OK) return vs;
+  if (max_seq_len < 0) return TQ_ERR_INVALID_ARG;
+  if (tq_decode_workspace_bytes(d, max_seq_len) > TQ_NO_ALLOC_WORKSPACE_BYTES) return TQ_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  const tq_status st = no_alloc_scratch(&scratch);
+  if (st != TQ_OK) return st;
+  return tq_decode_attention(d, q, d_seq_lens, max_seq_len, out, scratch, TQ_NO_ALLOC_WORKSPACE_BYTES, stream);
 }

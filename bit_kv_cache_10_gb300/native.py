@@ -30,8 +30,9 @@ TQ_DEV_ERR_SEQ_LEN = 0x2
 EXPORTED = (
     "tq_status_string", "tq_build_codebook", "tq_split_bits", "tq_turboquant_enabled", "tq_rotation_signs",
     "tq_cache_desc_init", "tq_cache_buffer_bytes", "tq_quantize_append", "tq_decode_workspace_bytes",
-    "tq_decode_attention", "tq_dequantize", "tq_debug_quantize_rows_host",
+    "tq_decode_attention", "tq_dequantize", "tq_debug_quantize_rows_host", "tq_decode_attention_no_alloc",
 )
+TQ_NO_ALLOC_WORKSPACE_BYTES = 16 << 20
 
 
 class TQCodebook(ctypes.Structure):
@@ -92,6 +93,9 @@ def lib() -> ctypes.CDLL:
         L.tq_decode_attention.restype = c_int32
         L.tq_decode_attention.argtypes = [POINTER(TQCacheDesc), c_void_p, c_void_p, c_int32, c_void_p, c_void_p,
                                           c_size_t, c_void_p]
+        L.tq_decode_attention_no_alloc.restype = c_int32
+        L.tq_decode_attention_no_alloc.argtypes = [POINTER(TQCacheDesc), c_void_p, c_void_p, c_int32, c_void_p,
+                                                   c_void_p]
         L.tq_dequantize.restype = c_int32
         L.tq_dequantize.argtypes = [POINTER(TQCacheDesc), c_int32, c_int32, c_int32, c_int32, c_int32, c_void_p,
                                     c_void_p]
@@ -161,6 +165,12 @@ def tq_decode_workspace_bytes(desc, max_seq_len: int) -> int:
 def tq_decode_attention(desc, q_ptr, d_seq_lens_ptr, max_seq_len, out_ptr, ws_ptr, ws_bytes, stream):
     _check(lib().tq_decode_attention(ctypes.byref(desc), q_ptr, d_seq_lens_ptr, max_seq_len, out_ptr, ws_ptr,
                                      ws_bytes, stream), "tq_decode_attention")
+
+
+def tq_decode_attention_no_alloc(desc, q_ptr, d_seq_lens_ptr, max_seq_len, out_ptr, stream):
+    """Decode attention with the library's fixed device scratch (no workspace argument)."""
+    _check(lib().tq_decode_attention_no_alloc(ctypes.byref(desc), q_ptr, d_seq_lens_ptr, max_seq_len, out_ptr,
+                                              stream), "tq_decode_attention_no_alloc")
 
 
 def tq_dequantize(desc, which, b, seq_len, token_start, n_tokens, out_ptr, stream):

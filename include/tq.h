@@ -279,6 +279,33 @@ tq_status tq_decode_attention(const tq_cache_desc *desc, const void *q, const in
                               int32_t max_seq_len, float *out, void *workspace, size_t workspace_bytes,
                               tq_stream_t stream);
 
+/*
+ * Decode attention for callers that cannot allocate device memory.  The pages
+ * have no counterpart of this entry point; it exists for hosts that hand a
+ * library only input and output pointers (plugin interfaces with no scratch
+ * allocator, runtimes whose memory pool owns all of the GPU's memory, serving
+ * loops that must not call cudaMalloc because it can synchronize the device
+ * and fail under a full pool).  It computes exactly what tq_decode_attention
+ * computes, with the same arguments minus the workspace: the split-K partials
+ * go to a scratch array of TQ_NO_ALLOC_WORKSPACE_BYTES that the library holds
+ * in device memory on every GPU where it is loaded, until the process exits.
+ *
+ *   Limit      the call needs tq_decode_workspace_bytes(desc, max_seq_len) <=
+ *              TQ_NO_ALLOC_WORKSPACE_BYTES; a larger request returns
+ *              TQ_ERR_WORKSPACE before any launch.
+ *   Device     the current device.  The first call on a device looks up the
+ *              scratch array's device address (a runtime call, made once per
+ *              device); make that first call before any stream capture.
+ *   Sharing    every call uses the same array and leaves its contents behind;
+ *              nothing in it needs to start at zero.  Calls whose kernels can
+ *              overlap on the GPU (different streams, no ordering between
+ *              them) race on the array and give wrong results: order them.
+ * No cudaMalloc, cudaFree or other allocating call is made.
+ */
+#define TQ_NO_ALLOC_WORKSPACE_BYTES ((size_t)16 << 20)
+tq_status tq_decode_attention_no_alloc(const tq_cache_desc *desc, const void *q, const int32_t *d_seq_lens,
+                                       int32_t max_seq_len, float *out, tq_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Dequantize                                                                 */
 /* ------------------------------------------------------------------------ */
