@@ -460,6 +460,47 @@ def run_gpu(args):
     return 0
 
 
+def run_profile(args):
+    """Only the decode step or only the quantize append, at the bench shapes
+    (quantize batch reduced to --profile-batch), for profiler captures."""
+    import torch
+    from bit_kv_cache_10_gb300 import build as tq_build
+    from bit_kv_cache_10_gb300.cache import TurboQuantKVCache
+    tq_build.build()
+    total = args.warmup + args.steps
+    if args.profile == "decode":
+        tc, lens0 = build_decode_cache(torch, HI + total + 64)
+        kn, vn, qn = step_inputs(total)
+        k_dev, v_dev, q_dev = (torch.from_numpy(a).cuda() for a in (kn, vn, qn))
+        starts = torch.from_numpy((lens0[None, :] + np.arange(total)[:, None]).astype(np.int32)).cuda()
+        seqs = starts + 1
+        max_len = HI + total
+        out = torch.empty(B, HQ, D, dtype=torch.float32, device="cuda")
+        ws = torch.empty(tc.workspace_bytes(max_len), dtype=torch.uint8, device="cuda")
+        t0 = None
+        for s in range(total):
+            if s == args.warmup:
+                torch.cuda.synchronize()
+                t0 = time.perf_counter()
+            tc.append(k_dev[s], v_dev[s], starts[s])
+            tc.decode(q_dev[s], seqs[s], max_len, out=out, workspace=ws)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile": "decode", "steps": args.steps, "wall_ms_per_step":
+                          (time.perf_counter() - t0) * 1e3 / max(1, args.steps), "status": tc.device_status()}))
+    else:
+        qb = args.profile_batch
+        g = synth.rng(SEED + 2, synth.STREAM_K)
+        kq = torch.from_numpy(g.standard_normal((qb, HKV, QT, D), dtype=np.float32).astype(np.float16)).cuda()
+        vq = torch.from_numpy(g.standard_normal((qb, HKV, QT, D), dtype=np.float32).astype(np.float16)).cuda()
+        qc = TurboQuantKVCache(qb, HKV, HKV * 4, QT, bits=(KB, VB))
+        zero = torch.zeros(qb, dtype=torch.int32, device="cuda")
+        for s in range(total):
+            qc.append(kq, vq, zero)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile": "quantize", "batch": qb, "steps": total, "status": qc.device_status()}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -467,10 +508,15 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle timing")
+    ap.add_argument("--profile", choices=["decode", "quantize"],
+                    help="run only warm-up + timed steps of one part (for ncu captures); prints a short line")
+    ap.add_argument("--profile-batch", type=int, default=4, help="batch of the quantize part in --profile mode")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # timing rule: at least 3 untimed warm-up steps
     if args.impl == "reference":
         return run_reference(args)
+    if args.profile:
+        return run_profile(args)
     return run_gpu(args)
 
 
