@@ -248,14 +248,13 @@ tq_status validate_desc(const tq_cache_desc* d) {
   return TQ_OK;
 }
 
-int decode_num_chunks(const tq_cache_desc* d, int max_seq_len) {
-  if (max_seq_len <= 0) return 0;
-  return (max_seq_len + kDecodeChunk - 1) / kDecodeChunk;
+size_t decode_workspace_slots(const tq_cache_desc* d) {
+  return static_cast<size_t>(kMaxDecodeCtas) + 2 * static_cast<size_t>(d->batch) * d->num_kv_heads;
 }
 
-int decode_num_slots(const tq_cache_desc* d, int max_seq_len) {
-  if (max_seq_len <= 0) return 0;
-  return decode_num_chunks(d, max_seq_len) + (d->hot_window > 0 ? 1 : 0);
+size_t decode_workspace_bytes(const tq_cache_desc* d) {
+  const size_t g = static_cast<size_t>(d->num_q_heads / d->num_kv_heads);
+  return decode_workspace_slots(d) * g * (kHeadDim + 2) * sizeof(float);
 }
 
 int quant_lut_scale(const float* t, int n) {

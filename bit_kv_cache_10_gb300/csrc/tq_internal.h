@@ -12,7 +12,8 @@ constexpr int kHeadDim = 128;     // the kernels are written for d = 128
 constexpr int kMinBits = 2;       // GPU path: 2..4 bits per coordinate ([MLX-VLM CLI guide] FAQ
 constexpr int kMaxBits = 4;       // "What bit widths does TurboQuant support?")
 constexpr int kMaxGroup = 4;      // query heads per KV head handled by the decode kernels
-constexpr int kDecodeChunk = 1024;  // context tokens per split-K chunk
+constexpr int kMaxDecodeCtas = 512;   // largest split-K grid (one CTA per SM)
+constexpr int kMaxDecodeBatch = 512;  // sequences per decode call (per-sequence tile prefix in shared memory)
 
 // Words of one packed token vector.
 inline int words_per_token(int head_dim, int bits) { return head_dim * bits / 32; }
@@ -22,10 +23,11 @@ inline int words_per_token(int head_dim, int bits) { return head_dim * bits / 32
 tq_status validate_shape(const tq_cache_desc* d);
 tq_status validate_desc(const tq_cache_desc* d);
 
-// Number of split-K chunks covering max_seq_len tokens (cold part) and the
-// number of partial slots per (batch, query head), including the hot-window slot.
-int decode_num_chunks(const tq_cache_desc* d, int max_seq_len);
-int decode_num_slots(const tq_cache_desc* d, int max_seq_len);
+// Decode workspace: one partial (G heads x (d accumulators + max + sum)) per
+// (split-K CTA, row) pair, at slot CTA + row; rows are the cold and hot rows of
+// every (sequence, KV head), so kMaxDecodeCtas + 2 B Hkv slots always suffice.
+size_t decode_workspace_slots(const tq_cache_desc* d);
+size_t decode_workspace_bytes(const tq_cache_desc* d);
 
 // Bucket scale of the threshold lookup table used by the quantize kernel: the
 // smallest power of two A for which every bucket RN(y*A) holds at most one

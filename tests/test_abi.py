@@ -128,8 +128,9 @@ def test_entry_points_reject_bad_arguments_before_launch():
 
 def test_workspace_and_buffer_sizes():
     d = N.tq_cache_desc_init(4, 8, 32, 128, 131072, N.TQ_K_PACKED, 3, 4, hot_window=256)
-    chunks = math.ceil(131072 / 1024)
-    assert N.tq_decode_workspace_bytes(d, 131072) == 4 * 32 * (chunks + 1) * 130 * 4
+    # one partial of 4 query heads per (split-K CTA, row) pair: 512 CTAs + cold and hot rows of 4 x 8 (b, h)
+    assert N.tq_decode_workspace_bytes(d, 131072) == (512 + 2 * 4 * 8) * 4 * 130 * 4
+    assert N.tq_decode_workspace_bytes(d, 7) == N.tq_decode_workspace_bytes(d, 131072)
     assert N.tq_decode_workspace_bytes(d, 0) == 0
     sizes = N.tq_cache_buffer_bytes(d)
     rows = 4 * 8 * 131072

@@ -73,8 +73,8 @@ def test_no_alloc_decode_matches_workspace_decode_on_consecutive_calls():
 
 
 def test_no_alloc_decode_rejects_requests_beyond_its_scratch():
-    # 4 x 32 query heads over 1M tokens need more than the fixed scratch: refused before any launch
-    B, HK, HQ, CAP = 4, 8, 32, 1 << 20
+    # 512 sequences x 8 KV heads need more partial slots than the fixed scratch holds: refused before any launch
+    B, HK, HQ, CAP = 512, 8, 32, 64
     d = N.tq_cache_desc_init(B, HK, HQ, D, CAP, N.TQ_K_PACKED, 3, 4)
     assert N.tq_decode_workspace_bytes(d, CAP) > N.TQ_NO_ALLOC_WORKSPACE_BYTES
     fake = 1 << 20
