@@ -166,9 +166,9 @@ __device__ __forceinline__ TileInfo tile_info(const DecodeParams& p, const long 
   ti.b = lo;
   const SeqTiles s = seq_tiles(p, lo);
   const int per_h = s.tc + s.th;
-  const long long rem = t - prefix[lo];
-  ti.h = static_cast<int>(rem / per_h);
-  const int x = static_cast<int>(rem - static_cast<long long>(ti.h) * per_h);
+  const int rem = static_cast<int>(t - prefix[lo]);  // < Hkv * per_h < 2^31 (checked on the host)
+  ti.h = rem / per_h;
+  const int x = rem - ti.h * per_h;
   const long long hbase = prefix[lo] + static_cast<long long>(ti.h) * per_h;
   if (x < s.tc) {
     ti.hot = 0;
@@ -200,7 +200,8 @@ struct Cfg {
   static constexpr int kVTab = (1 << (2 * VB)) * kCopies * 8;
   static constexpr int kWts = 36 * 32;  // per warp: (w, w) x 4 heads per token, one pad row per 8 tokens
   static constexpr int kFixed = kKTab + kVTab + kWarps * kWts + 4 * D * 4 /* q' */ + 4 * D * 4 /* combine */ +
-                                kWarps * 4 * 2 * 4 /* warp (m, l) */ + (kMaxDecodeBatch + 1) * 8 + 34 * 8;
+                                kWarps * 4 * 2 * 4 /* warp (m, l) */ + kWarps * 4 * 16 /* tile descriptors */ +
+                                (kMaxDecodeBatch + 1) * 8 + 34 * 8;
   static constexpr int kStages = kFixed + kWarps * 4 * kBuf <= kSmemBudget   ? 4
                                  : kFixed + kWarps * 3 * kBuf <= kSmemBudget ? 3
                                                                              : 2;
@@ -208,29 +209,42 @@ struct Cfg {
   static_assert(kSmem <= kSmemBudget, "shared memory budget");
 };
 
-// Lane window of 16*BITS code bits starting at bit 16*BITS*r of a token record.
+// Lane window of 16*BITS code bits starting at bit 16*BITS*r of a token
+// record, as two 32-bit words (bits 0..31 and 32..63 of the window).
+struct Win {
+  uint32_t lo, hi;
+};
 template <int BITS>
-__device__ __forceinline__ uint64_t code_window(const uint8_t* rec, int r) {
+__device__ __forceinline__ Win code_window(const uint8_t* rec, int r) {
   if constexpr (BITS == 4) {
     const uint2 w = *reinterpret_cast<const uint2*>(rec + 8 * r);
-    return (static_cast<uint64_t>(w.y) << 32) | w.x;
+    return Win{w.x, w.y};
   } else if constexpr (BITS == 2) {
-    return *reinterpret_cast<const uint32_t*>(rec + 4 * r);
+    return Win{*reinterpret_cast<const uint32_t*>(rec + 4 * r), 0u};
   } else {
     const uint32_t* wd = reinterpret_cast<const uint32_t*>(rec) + ((3 * r) >> 1);
-    const uint64_t v = (static_cast<uint64_t>(wd[1]) << 32) | wd[0];
-    return v >> ((r & 1) * 16);
+    const uint32_t w0 = wd[0], w1 = wd[1];
+    const uint32_t sh = (r & 1) * 16;
+    return Win{__funnelshift_r(w0, w1, sh), w1 >> sh};
   }
 }
 
-// Byte offset, inside a pair table, of the entry of code pair k of a window:
-// entry e = two codes, 16 copies x 8 bytes per entry, this lane's copy.
+// Byte offset, inside a pair table, of the entry of code pair K of a window
+// (entry = two codes; 16 copies x 8 bytes per entry; this lane's copy): the
+// field is shifted to bit 7 with one 32-bit (funnel) shift, then masked.
 template <int BITS, int K>
-__device__ __forceinline__ uint32_t pair_offset(uint64_t win, uint32_t copy8) {
-  constexpr int kS = 2 * BITS * K - 7;
-  const uint32_t x = kS >= 0 ? static_cast<uint32_t>(win >> (kS >= 0 ? kS : 0))
-                             : static_cast<uint32_t>(win << (kS < 0 ? -kS : 0));
-  return (x & (((1u << (2 * BITS)) - 1u) << 7)) | copy8;
+__device__ __forceinline__ uint32_t pair_offset(const Win& w, uint32_t copy8) {
+  constexpr int kP = 2 * BITS * K;   // first bit of the field in the window
+  constexpr int kW = 2 * BITS;       // field width
+  uint32_t v;
+  if constexpr (kP + kW <= 32) {
+    v = kP >= 7 ? (w.lo >> (kP >= 7 ? kP - 7 : 0)) : (w.lo << (kP < 7 ? 7 - kP : 0));
+  } else if constexpr (kP >= 32) {
+    v = kP - 32 >= 7 ? (w.hi >> (kP - 32 >= 7 ? kP - 39 : 0)) : (w.hi << (kP - 32 < 7 ? 39 - kP : 0));
+  } else {
+    v = __funnelshift_r(w.lo, w.hi, kP - 7);
+  }
+  return (v & (((1u << kW) - 1u) << 7)) | copy8;
 }
 
 template <int KB, int VB>
@@ -263,7 +277,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
   float* qs = reinterpret_cast<float*>(wts_all + kWarps * C::kWts);
   float* comb = qs + 4 * D;
   float* wml = comb + 4 * D;                    // [warp][head][2]
-  long long* prefix = reinterpret_cast<long long*>(wml + kWarps * 4 * 2);
+  int4* descs_all = reinterpret_cast<int4*>(wml + kWarps * 4 * 2);  // [warp][stage] tile descriptors
+  long long* prefix = reinterpret_cast<long long*>(descs_all + kWarps * 4);
   long long* scan = prefix + kMaxDecodeBatch + 1;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -301,17 +316,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
 
   uint8_t* wbuf = stages + warp * S * C::kBuf;
   uint8_t* wts = wts_all + warp * C::kWts;
-  const long long my_n = (t1 - t0 - warp + kWarps - 1) / kWarps;  // this warp's tiles: t0 + warp + 8 j
-  long long j_issue = 0, j = 0;
-#pragma unroll
-  for (int s = 0; s < S - 1; ++s) {
+  int4* descs = descs_all + warp * 4;
+  const int my_n = static_cast<int>((t1 - t0 - warp + kWarps - 1) / kWarps);  // tiles t0 + warp + 8 j
+  int j_issue = 0, j = 0;
+  // stage tile j_issue and record its descriptor {b, h | hot << 16, t_begin, n_valid}
+  auto issue = [&]() {
     if (j_issue < my_n) {
-      const TileInfo ti = tile_info(p, prefix, t0 + warp + kWarps * j_issue);
+      const TileInfo ti = tile_info(p, prefix, t0 + warp + static_cast<long long>(kWarps) * j_issue);
       stage_tile<KB, VB>(p, ti, wbuf + (j_issue % S) * C::kBuf, lane);
+      if (lane == 0) descs[j_issue % S] = make_int4(ti.b, ti.h | (ti.hot << 16), ti.t_begin, ti.n_valid);
     }
     cp_async_commit();
     ++j_issue;
-  }
+  };
+#pragma unroll
+  for (int s = 0; s < S - 1; ++s) issue();
 
   float2 qr[G][8];
   int cur_b = -1, cur_h = -1;
@@ -367,17 +386,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
       for (int k = 0; k < 8; ++k) acc[jj][k] = make_float2(0.0f, 0.0f);
     }
 
-    while (j < my_n && t0 + warp + kWarps * j < seg_end) {
-      if (j_issue < my_n) {
-        const TileInfo tn = tile_info(p, prefix, t0 + warp + kWarps * j_issue);
-        stage_tile<KB, VB>(p, tn, wbuf + (j_issue % S) * C::kBuf, lane);
-      }
-      cp_async_commit();
-      ++j_issue;
+    while (j < my_n && t0 + warp + static_cast<long long>(kWarps) * j < seg_end) {
+      issue();
       cp_async_wait<S - 1>();
       __syncwarp();
 
-      const TileInfo ti = tile_info(p, prefix, t0 + warp + kWarps * j);
+      const int4 dsc = descs[j % S];
+      TileInfo ti;
+      ti.b = dsc.x;
+      ti.h = dsc.y & 0xFFFF;
+      ti.hot = dsc.y >> 16;
+      ti.t_begin = dsc.z;
+      ti.n_valid = dsc.w;
       const uint8_t* tb = wbuf + (j % S) * C::kBuf;
       const bool hot = ti.hot != 0;
 
@@ -404,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
           }
         } else {
           constexpr int KBB = C::kFp16K ? 2 : KB;
-          const uint64_t win = code_window<KBB>(tb + tau * C::kKRow, r);
+          const Win win = code_window<KBB>(tb + tau * C::kKRow, r);
           float2 cp[8];
           cp[0] = *reinterpret_cast<const float2*>(ktab + pair_offset<KBB, 0>(win, copy8));
           cp[1] = *reinterpret_cast<const float2*>(ktab + pair_offset<KBB, 1>(win, copy8));
@@ -517,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
           for (int jj = 0; jj < G; ++jj) w2[jj] = wr[jj];
         }
         if (!hot) {
-          const uint64_t win = code_window<VB>(tb + C::kKTile + C::kKNorm + tau * C::kVRow, r);
+          const Win win = code_window<VB>(tb + C::kKTile + C::kKNorm + tau * C::kVRow, r);
           float2 cv[8];
           cv[0] = *reinterpret_cast<const float2*>(vtab + pair_offset<VB, 0>(win, copy8));
           cv[1] = *reinterpret_cast<const float2*>(vtab + pair_offset<VB, 1>(win, copy8));
@@ -735,6 +755,8 @@ extern "C" tq_status tq_decode_attention(const tq_cache_desc* d, const void* q, 
   if (q == nullptr || d_seq_lens == nullptr || out == nullptr || max_seq_len < 0) return TQ_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(out)) return TQ_ERR_INVALID_ARG;
   if (d->batch > kMaxDecodeBatch) return TQ_ERR_UNSUPPORTED;
+  if (static_cast<long long>(d->num_kv_heads) * (d->capacity / 32 + d->hot_window / 32 + 2) >= (1ll << 31))
+    return TQ_ERR_UNSUPPORTED;  // tiles of one sequence must fit in 32 bits
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const size_t out_bytes = static_cast<size_t>(d->batch) * d->num_q_heads * D * sizeof(float);
   if (max_seq_len == 0) return cudaMemsetAsync(out, 0, out_bytes, s) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
