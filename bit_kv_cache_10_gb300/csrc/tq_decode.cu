@@ -4,26 +4,28 @@
 // Work list.  Every (sequence b, KV head h) has a cold row (the packed
 // positions [0, L - min(W, L))) and, with a hot window, a hot row (the newest
 // min(W, L) positions, whose V is read from the fp16 ring).  Rows are cut into
-// 32-token tiles and listed in (b, h, cold/hot) order; the list is split into
+// 16-token tiles and listed in (b, h, cold/hot) order; the list is split into
 // one contiguous, equal range per CTA, so that every SM gets the same number
 // of tiles whatever the lengths are.
 //
-// Split kernel: one CTA of 8 warps per SM.  The codebook pair tables are built
-// once per CTA in shared memory (16 copies, one per lane of a half-warp, so the
-// data-dependent lookups are bank-conflict free).  Warp w takes tiles
-// t0 + w, t0 + w + 8, ... of the CTA's range and streams them through a 3-4
-// stage cp.async ring that runs across row boundaries.  Inside a warp 8 lanes
-// share a token and each owns 16 coordinates; 4 tokens are in flight per step
+// Split kernel: one CTA of 16 warps per SM (128 registers per thread).  The
+// codebook pair tables are built once per CTA in shared memory (16 copies, one
+// per lane of a half-warp, so the data-dependent lookups are bank-conflict
+// free), at a base aligned to the table size so that a lookup address is one
+// PRMT (4-bit codes) or one shift and one masked OR.  Warp w takes tiles
+// t0 + w, t0 + w + 16, ... of the CTA's range and streams them through a 3-4
+// stage cp.async ring that runs across row boundaries.  Inside a warp 16 lanes
+// share a token and each owns 8 coordinates; 2 tokens are in flight per step
 // and 8 steps cover the tile:
-//   score:   partial sum_i q'[h][i] c[code_i] over the lane's 16 coordinates
+//   score:   partial sum_i q'[h][i] c[code_i] over the lane's 8 coordinates
 //            for the G query heads of the group, with the two codes of a
 //            coordinate pair looked up at once in a (c_a, c_b) table; a
-//            transposing butterfly over the 8 lanes leaves lane l with the
-//            full scores of token l;
+//            transposing butterfly over the 16 lanes leaves each lane with
+//            the full scores of one token for half of the heads;
 //   softmax: online, per 8-token group, in base 2 (log2 e is folded into q');
 //   V:       acc[h][i] += p_h n_V c[code_i] in the rotated domain (cold rows)
 //            or += p_h v_i with the raw fp16 V (hot rows, original domain).
-// When the CTA leaves a row it combines its 8 warps and writes one partial
+// When the CTA leaves a row it combines its warps and writes one partial
 // (acc, max, sum) to workspace slot (CTA index + row index): these slots are
 // distinct for all (CTA, row) pairs because both indices only grow along the
 // tile list.  All arithmetic is float32 (packed pairs where possible).
@@ -41,9 +43,9 @@
 namespace tq {
 namespace {
 
-constexpr int kWarps = 8;
+constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
-constexpr int kTile = 32;
+constexpr int kTile = 16;
 constexpr int kCopies = 16;                 // pair-table copies (one per lane of a half-warp)
 constexpr int kSmemBudget = 227 * 1024;
 
@@ -190,61 +192,77 @@ __device__ __forceinline__ TileInfo tile_info(const DecodeParams& p, const long 
 template <int KB, int VB>
 struct Cfg {
   static constexpr bool kFp16K = KB == 16;
+  static constexpr int kKBits = kFp16K ? 2 : KB;       // placeholder width when K is fp16
   static constexpr int kKRow = kFp16K ? 256 : KB * 16;  // bytes of one K token
   static constexpr int kVRow = VB * 16;
   static constexpr int kKTile = kTile * kKRow;
-  static constexpr int kKNorm = kFp16K ? 0 : 128;
+  static constexpr int kKNorm = kFp16K ? 0 : kTile * 4;
   static constexpr int kVTile = kTile * kVRow;
-  static constexpr int kBuf = kKTile + kKNorm + kVTile + 128;  // K | K norms | V | V norms
-  static constexpr int kKTab = kFp16K ? 0 : (1 << (2 * (kFp16K ? 1 : KB))) * kCopies * 8;
-  static constexpr int kVTab = (1 << (2 * VB)) * kCopies * 8;
-  static constexpr int kWts = 36 * 32;  // per warp: (w, w) x 4 heads per token, one pad row per 8 tokens
-  static constexpr int kFixed = kKTab + kVTab + kWarps * kWts + 4 * D * 4 /* q' */ + 4 * D * 4 /* combine */ +
+  static constexpr int kBuf = kKTile + kKNorm + kVTile + kTile * 4;  // K | K norms | V | V norms
+  // Pair tables.  Packed K: 256-byte rows, V entries in bytes [0,128), K entries in
+  // [128,256) of row e (16 copies x 8 bytes); fp16 K: V only, 128-byte rows.  The
+  // table base is aligned to the table size so that an entry's address is
+  // base | (e << row_shift) | copy * 8 (one OR instead of an add).
+  static constexpr int kRowShift = kFp16K ? 7 : 8;
+  static constexpr int kTabBits = kFp16K ? 2 * VB : 2 * (VB > kKBits ? VB : kKBits);
+  static constexpr int kTab = (1 << kTabBits) << kRowShift;
+  static constexpr int kWts = 18 * 32;  // per warp: (w, w) x 4 heads per token, padded rows
+  static constexpr int kSmall = kWarps * kWts + 4 * D * 4 /* q' */ + 4 * D * 4 /* combine */ +
                                 kWarps * 4 * 2 * 4 /* warp (m, l) */ + kWarps * 4 * 16 /* tile descriptors */ +
                                 (kMaxDecodeBatch + 1) * 8 + 34 * 8;
-  static constexpr int kStages = kFixed + kWarps * 4 * kBuf <= kSmemBudget   ? 4
-                                 : kFixed + kWarps * 3 * kBuf <= kSmemBudget ? 3
-                                                                             : 2;
-  static constexpr int kSmem = kFixed + kWarps * kStages * kBuf;
-  static_assert(kSmem <= kSmemBudget, "shared memory budget");
+  // the aligned table can leave a gap of up to kTab - 1024 bytes before it (shared
+  // windows start at a 1 KB multiple); buffers are placed around the table
+  static constexpr int kWorst(int stages) { return kTab + kSmall + (kWarps + 1) * stages * kBuf + 1024; }
+  static constexpr int kStages = kWorst(4) <= kSmemBudget ? 4 : kWorst(3) <= kSmemBudget ? 3 : 2;
+  static constexpr int kSmem = kSmemBudget;
+  static_assert(kWorst(kStages) <= kSmemBudget, "shared memory budget");
 };
 
-// Lane window of 16*BITS code bits starting at bit 16*BITS*r of a token
-// record, as two 32-bit words (bits 0..31 and 32..63 of the window).
-struct Win {
-  uint32_t lo, hi;
+// Bump allocator over the dynamic shared window that skips the table region.
+struct SmemLayout {
+  uint32_t cur, tab_lo, tab_hi;
+  __device__ uint32_t take(uint32_t bytes) {
+    cur = (cur + 15u) & ~15u;
+    if (cur < tab_hi && cur + bytes > tab_lo) cur = tab_hi;
+    const uint32_t at = cur;
+    cur += bytes;
+    return at;
+  }
 };
+
+// Lane window of 8*BITS code bits starting at bit 8*BITS*r of a token record.
 template <int BITS>
-__device__ __forceinline__ Win code_window(const uint8_t* rec, int r) {
+__device__ __forceinline__ uint32_t code_window(const uint8_t* rec, int r) {
   if constexpr (BITS == 4) {
-    const uint2 w = *reinterpret_cast<const uint2*>(rec + 8 * r);
-    return Win{w.x, w.y};
+    return reinterpret_cast<const uint32_t*>(rec)[r];
   } else if constexpr (BITS == 2) {
-    return Win{*reinterpret_cast<const uint32_t*>(rec + 4 * r), 0u};
+    return reinterpret_cast<const uint32_t*>(rec)[r >> 1] >> ((r & 1) * 16);
   } else {
-    const uint32_t* wd = reinterpret_cast<const uint32_t*>(rec) + ((3 * r) >> 1);
-    const uint32_t w0 = wd[0], w1 = wd[1];
-    const uint32_t sh = (r & 1) * 16;
-    return Win{__funnelshift_r(w0, w1, sh), w1 >> sh};
+    const int w = (3 * r) >> 2;  // bit 24 r
+    const uint32_t* wd = reinterpret_cast<const uint32_t*>(rec) + w;
+    return __funnelshift_r(wd[0], wd[1], (24 * r) & 31);
   }
 }
 
-// Byte offset, inside a pair table, of the entry of code pair K of a window
-// (entry = two codes; 16 copies x 8 bytes per entry; this lane's copy): the
-// field is shifted to bit 7 with one 32-bit (funnel) shift, then masked.
-template <int BITS, int K>
-__device__ __forceinline__ uint32_t pair_offset(const Win& w, uint32_t copy8) {
-  constexpr int kP = 2 * BITS * K;   // first bit of the field in the window
-  constexpr int kW = 2 * BITS;       // field width
-  uint32_t v;
-  if constexpr (kP + kW <= 32) {
-    v = kP >= 7 ? (w.lo >> (kP >= 7 ? kP - 7 : 0)) : (w.lo << (kP < 7 ? 7 - kP : 0));
-  } else if constexpr (kP >= 32) {
-    v = kP - 32 >= 7 ? (w.hi >> (kP - 32 >= 7 ? kP - 39 : 0)) : (w.hi << (kP - 32 < 7 ? 39 - kP : 0));
+// Shared address of the table entry of code pair K of a lane window:
+// basecopy = table base | (128 for K) | copy * 8.
+template <int BITS, int K, int ROWSHIFT>
+__device__ __forceinline__ uint32_t pair_addr(uint32_t win, uint32_t basecopy) {
+  if constexpr (BITS == 4 && ROWSHIFT == 8) {
+    // byte K of the window into byte 1; bytes 0, 2, 3 from basecopy
+    return __byte_perm(win, basecopy, 0x7604 | (K << 4));
   } else {
-    v = __funnelshift_r(w.lo, w.hi, kP - 7);
+    constexpr int kP = 2 * BITS * K, kW = 2 * BITS;
+    const uint32_t v = kP >= ROWSHIFT ? (win >> (kP >= ROWSHIFT ? kP - ROWSHIFT : 0))
+                                      : (win << (kP < ROWSHIFT ? ROWSHIFT - kP : 0));
+    return (v & (((1u << kW) - 1u) << ROWSHIFT)) | basecopy;
   }
-  return (v & (((1u << kW) - 1u) << 7)) | copy8;
+}
+
+__device__ __forceinline__ float2 lds64(uint32_t addr) {
+  float2 v;
+  asm("ld.shared.v2.f32 {%0, %1}, [%2];\n" : "=f"(v.x), "=f"(v.y) : "r"(addr));
+  return v;
 }
 
 template <int KB, int VB>
@@ -253,7 +271,7 @@ __device__ __forceinline__ void stage_tile(const DecodeParams& p, const TileInfo
   const int64_t row0 = (static_cast<int64_t>(ti.b) * p.hkv + ti.h) * p.cap + ti.t_begin;
   constexpr int kChunksK = C::kKRow / 16;
   const uint8_t* ksrc = C::kFp16K ? reinterpret_cast<const uint8_t*>(p.k_fp16 + row0 * D)
-                                  : reinterpret_cast<const uint8_t*>(p.k_words + row0 * (C::kFp16K ? 0 : KB * 4));
+                                  : reinterpret_cast<const uint8_t*>(p.k_words + row0 * (C::kKBits * 4));
   for (int c = lane; c < ti.n_valid * kChunksK; c += 32) cp_async16(buf + c * 16, ksrc + c * 16);
   if (!C::kFp16K && lane < ti.n_valid) cp_async4(buf + C::kKTile + lane * 4, p.k_norms + row0 + lane);
   if (!ti.hot) {
@@ -265,25 +283,34 @@ __device__ __forceinline__ void stage_tile(const DecodeParams& p, const TileInfo
   }
 }
 
+// Split kernel.  Lane = 16 g + r: token group g (tokens 8g..8g+7 of a 16-token
+// tile, one per step), coordinates 8r..8r+7 (code pairs k = 0..3).
 template <int G, int KB, int VB>
 __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeParams p) {
   using C = Cfg<KB, VB>;
   constexpr int S = C::kStages;
+  constexpr int kRS = C::kRowShift;
   extern __shared__ __align__(16) uint8_t smem[];
-  uint8_t* ktab = smem;                         // pair tables first: constant offsets
-  uint8_t* vtab = smem + C::kKTab;
-  uint8_t* stages = smem + C::kKTab + C::kVTab;
-  uint8_t* wts_all = stages + kWarps * S * C::kBuf;
-  float* qs = reinterpret_cast<float*>(wts_all + kWarps * C::kWts);
-  float* comb = qs + 4 * D;
-  float* wml = comb + 4 * D;                    // [warp][head][2]
-  int4* descs_all = reinterpret_cast<int4*>(wml + kWarps * 4 * 2);  // [warp][stage] tile descriptors
-  long long* prefix = reinterpret_cast<long long*>(descs_all + kWarps * 4);
-  long long* scan = prefix + kMaxDecodeBatch + 1;
+  const uint32_t s0 = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  SmemLayout lay;
+  lay.tab_lo = (s0 + C::kTab - 1) & ~static_cast<uint32_t>(C::kTab - 1);
+  lay.tab_hi = lay.tab_lo + C::kTab;
+  lay.cur = s0;
+  auto ptr = [&](uint32_t addr) { return smem + (addr - s0); };
+  const uint32_t tab = lay.tab_lo;
+  float* qs = reinterpret_cast<float*>(ptr(lay.take(4 * D * 4)));
+  float* comb = reinterpret_cast<float*>(ptr(lay.take(4 * D * 4)));
+  float* wml = reinterpret_cast<float*>(ptr(lay.take(kWarps * 4 * 2 * 4)));
+  int4* descs_all = reinterpret_cast<int4*>(ptr(lay.take(kWarps * 4 * 16)));
+  long long* prefix = reinterpret_cast<long long*>(ptr(lay.take((kMaxDecodeBatch + 1) * 8)));
+  long long* scan = reinterpret_cast<long long*>(ptr(lay.take(34 * 8)));
+  uint8_t* wts_all = ptr(lay.take(kWarps * C::kWts));
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g = lane >> 3, r = lane & 7;
-  const uint32_t copy8 = (lane & (kCopies - 1)) * 8u;
+  const int g = lane >> 4, r = lane & 15;
+  const uint32_t copy8 = static_cast<uint32_t>(r) * 8u;
+  const uint32_t vbase = tab | copy8;
+  const uint32_t kbase = tab | 128u | copy8;
 
   if (blockIdx.x == 0 && tid == 0 && p.status != nullptr) {
     for (int b = 0; b < p.batch; ++b) {
@@ -294,19 +321,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
       }
     }
   }
-  // pair tables: entry e = code_a | code_b << bits -> (c[code_a], c[code_b]), copies interleaved
+  // pair tables: entry e = code_a | code_b << bits -> (c[code_a], c[code_b]), 16 copies per row
   if constexpr (!C::kFp16K) {
-    constexpr int n = (1 << (2 * (C::kFp16K ? 1 : KB))) * kCopies;
+    constexpr int n = (1 << (2 * C::kKBits)) * kCopies;
     for (int i = tid; i < n; i += kThreads) {
-      const int e = i / kCopies;
-      reinterpret_cast<float2*>(ktab)[i] = make_float2(p.k_cent[e & ((1 << KB) - 1)], p.k_cent[e >> KB]);
+      const int e = i / kCopies, c = i % kCopies;
+      *reinterpret_cast<float2*>(ptr(tab + (e << kRS) + 128 + c * 8)) =
+          make_float2(p.k_cent[e & ((1 << C::kKBits) - 1)], p.k_cent[e >> C::kKBits]);
     }
   }
   {
     constexpr int n = (1 << (2 * VB)) * kCopies;
     for (int i = tid; i < n; i += kThreads) {
-      const int e = i / kCopies;
-      reinterpret_cast<float2*>(vtab)[i] = make_float2(p.v_cent[e & ((1 << VB) - 1)], p.v_cent[e >> VB]);
+      const int e = i / kCopies, c = i % kCopies;
+      *reinterpret_cast<float2*>(ptr(tab + (e << kRS) + c * 8)) =
+          make_float2(p.v_cent[e & ((1 << VB) - 1)], p.v_cent[e >> VB]);
     }
   }
   tile_prefix<kThreads>(p, prefix, scan);  // synchronizes
@@ -314,16 +343,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
   const long long t0 = total * blockIdx.x / p.grid, t1 = total * (blockIdx.x + 1) / p.grid;
   if (t0 >= t1) return;
 
-  uint8_t* wbuf = stages + warp * S * C::kBuf;
+  // per-warp staging rings of S buffers, allocated around the table in warp order
+  uint32_t ring = 0;
+  for (int w = 0; w < kWarps; ++w) {
+    const uint32_t a = lay.take(S * C::kBuf);
+    if (w == warp) ring = a;
+  }
+  if (lay.cur > s0 + static_cast<uint32_t>(C::kSmem)) {  // cannot happen within the static budget
+    if (tid == 0 && p.status != nullptr) atomicOr(p.status, TQ_DEV_ERR_LAYOUT);
+    return;
+  }
+  uint8_t* const wring = ptr(ring);
   uint8_t* wts = wts_all + warp * C::kWts;
   int4* descs = descs_all + warp * 4;
-  const int my_n = static_cast<int>((t1 - t0 - warp + kWarps - 1) / kWarps);  // tiles t0 + warp + 8 j
+  const int my_n = static_cast<int>((t1 - t0 - warp + kWarps - 1) / kWarps);  // tiles t0 + warp + 16 j
   int j_issue = 0, j = 0;
-  // stage tile j_issue and record its descriptor {b, h | hot << 16, t_begin, n_valid}
   auto issue = [&]() {
     if (j_issue < my_n) {
       const TileInfo ti = tile_info(p, prefix, t0 + warp + static_cast<long long>(kWarps) * j_issue);
-      stage_tile<KB, VB>(p, ti, wbuf + (j_issue % S) * C::kBuf, lane);
+      stage_tile<KB, VB>(p, ti, wring + (j_issue % S) * C::kBuf, lane);
       if (lane == 0) descs[j_issue % S] = make_int4(ti.b, ti.h | (ti.hot << 16), ti.t_begin, ti.n_valid);
     }
     cp_async_commit();
@@ -332,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
 #pragma unroll
   for (int s = 0; s < S - 1; ++s) issue();
 
-  float2 qr[G][8];
+  float2 qr[G][4];
   int cur_b = -1, cur_h = -1;
   long long seg = t0;
   while (seg < t1) {
@@ -345,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
         const bool neg = !C::kFp16K && sign_negative(p.seed, p.layer, si.h, tid);
 #pragma unroll
         for (int jj = 0; jj < G; ++jj) {
-          float x = half_bits_to_float(p.q[(static_cast<int64_t>(si.b) * p.hq + si.h * G + jj) * D + tid]);
+          const float x = half_bits_to_float(p.q[(static_cast<int64_t>(si.b) * p.hq + si.h * G + jj) * D + tid]);
           qs[jj * D + tid] = neg ? -x : x;
         }
       }
@@ -368,155 +406,173 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
 #pragma unroll
       for (int jj = 0; jj < G; ++jj)
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          qr[jj][k] = make_float2(fmul(qs[jj * D + 16 * r + 2 * k], qscale),
-                                  fmul(qs[jj * D + 16 * r + 2 * k + 1], qscale));
+        for (int k = 0; k < 4; ++k)
+          qr[jj][k] = make_float2(fmul(qs[jj * D + 8 * r + 2 * k], qscale),
+                                  fmul(qs[jj * D + 8 * r + 2 * k + 1], qscale));
       cur_b = si.b;
       cur_h = si.h;
     }
 
-    // per-group online-softmax state of this row
+    // online-softmax state of this row: m per (group, head), l per lane for its own heads
     float m[G], lsum[G];
-    float2 acc[G][8];
+    float2 acc[G][4];
 #pragma unroll
     for (int jj = 0; jj < G; ++jj) {
       m[jj] = -INFINITY;
       lsum[jj] = 0.0f;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) acc[jj][k] = make_float2(0.0f, 0.0f);
+      for (int k = 0; k < 4; ++k) acc[jj][k] = make_float2(0.0f, 0.0f);
     }
 
     while (j < my_n && t0 + warp + static_cast<long long>(kWarps) * j < seg_end) {
       issue();
       cp_async_wait<S - 1>();
       __syncwarp();
-
       const int4 dsc = descs[j % S];
-      TileInfo ti;
-      ti.b = dsc.x;
-      ti.h = dsc.y & 0xFFFF;
-      ti.hot = dsc.y >> 16;
-      ti.t_begin = dsc.z;
-      ti.n_valid = dsc.w;
-      const uint8_t* tb = wbuf + (j % S) * C::kBuf;
-      const bool hot = ti.hot != 0;
+      const int tb_b = dsc.x, tb_h = dsc.y & 0xFFFF, n_valid = dsc.w, t_begin = dsc.z;
+      const bool hot = (dsc.y >> 16) != 0;
+      const uint8_t* tb = wring + (j % S) * C::kBuf;
 
-      // ---- scores: P[u][h] = partial over this lane's 16 coordinates of token 8g + u
+      // ---- scores: P[u][h] = partial over this lane's 8 coordinates of token 8g + u
       float P[8][G];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int tau = 8 * g + u;
-        float2 pa[G], pb[G];
+        float2 pa[G];
 #pragma unroll
-        for (int jj = 0; jj < G; ++jj) pa[jj] = pb[jj] = make_float2(0.0f, 0.0f);
+        for (int jj = 0; jj < G; ++jj) pa[jj] = make_float2(0.0f, 0.0f);
         if constexpr (C::kFp16K) {
-          const uint4* kr = reinterpret_cast<const uint4*>(tb + tau * 256) + 2 * r;
-          const uint4 a0 = kr[0], a1 = kr[1];
-          const uint32_t wv[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+          const uint4 a0 = reinterpret_cast<const uint4*>(tb + tau * 256)[r];
+          const uint32_t wv[4] = {a0.x, a0.y, a0.z, a0.w};
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
+          for (int k = 0; k < 4; ++k) {
             const float2 kf = half2_bits_to_float2(wv[k]);
 #pragma unroll
-            for (int jj = 0; jj < G; ++jj) {
-              if (k & 1) pb[jj] = fma2(qr[jj][k], kf, pb[jj]);
-              else pa[jj] = fma2(qr[jj][k], kf, pa[jj]);
-            }
+            for (int jj = 0; jj < G; ++jj) pa[jj] = fma2(qr[jj][k], kf, pa[jj]);
           }
         } else {
-          constexpr int KBB = C::kFp16K ? 2 : KB;
-          const Win win = code_window<KBB>(tb + tau * C::kKRow, r);
-          float2 cp[8];
-          cp[0] = *reinterpret_cast<const float2*>(ktab + pair_offset<KBB, 0>(win, copy8));
-          cp[1] = *reinterpret_cast<const float2*>(ktab + pair_offset<KBB, 1>(win, copy8));
-          cp[2] = *reinterpret_cast<const float2*>(ktab + pair_offset<KBB, 2>(win, copy8));
-          cp[3] = *reinterpret_cast<const float2*>(ktab + pair_offset<KBB, 3>(win, copy8));
-          cp[4] = *reinterpret_cast<const float2*>(ktab + pair_offset<KBB, 4>(win, copy8));
-          cp[5] = *reinterpret_cast<const float2*>(ktab + pair_offset<KBB, 5>(win, copy8));
-          cp[6] = *reinterpret_cast<const float2*>(ktab + pair_offset<KBB, 6>(win, copy8));
-          cp[7] = *reinterpret_cast<const float2*>(ktab + pair_offset<KBB, 7>(win, copy8));
+          const uint32_t win = code_window<C::kKBits>(tb + tau * C::kKRow, r);
+          const float2 c0 = lds64(pair_addr<C::kKBits, 0, kRS>(win, kbase));
+          const float2 c1 = lds64(pair_addr<C::kKBits, 1, kRS>(win, kbase));
+          const float2 c2 = lds64(pair_addr<C::kKBits, 2, kRS>(win, kbase));
+          const float2 c3 = lds64(pair_addr<C::kKBits, 3, kRS>(win, kbase));
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-#pragma unroll
-            for (int jj = 0; jj < G; ++jj) {
-              if (k & 1) pb[jj] = fma2(qr[jj][k], cp[k], pb[jj]);
-              else pa[jj] = fma2(qr[jj][k], cp[k], pa[jj]);
-            }
+          for (int jj = 0; jj < G; ++jj) {
+            pa[jj] = fma2(qr[jj][0], c0, pa[jj]);
+            pa[jj] = fma2(qr[jj][1], c1, pa[jj]);
+            pa[jj] = fma2(qr[jj][2], c2, pa[jj]);
+            pa[jj] = fma2(qr[jj][3], c3, pa[jj]);
+          }
         }
 #pragma unroll
-        for (int jj = 0; jj < G; ++jj) {
-          const float2 s2 = add2(pa[jj], pb[jj]);
-          P[u][jj] = fadd(s2.x, s2.y);
-        }
+        for (int jj = 0; jj < G; ++jj) P[u][jj] = fadd(pa[jj].x, pa[jj].y);
       }
-      // ---- transposing butterfly over the 8 lanes of a group: lane r ends with token 8g + r
-      float v4[4][G], v2[2][G], s[G];
+      // ---- transposing butterfly over the 16 lanes of a group:
+      // bits 3, 2, 1 of r select the token (u = r >> 1), bit 0 the head pair
+      float v8[4][G], v4[2][G], v2[G], s2[2];
       {
-        const bool up = (r & 4) != 0;
+        const bool up = (r & 8) != 0;
 #pragma unroll
         for (int k = 0; k < 4; ++k)
 #pragma unroll
           for (int jj = 0; jj < G; ++jj) {
             const float send = up ? P[k][jj] : P[k + 4][jj];
             const float keep = up ? P[k + 4][jj] : P[k][jj];
+            v8[k][jj] = fadd(keep, __shfl_xor_sync(0xffffffffu, send, 8));
+          }
+      }
+      {
+        const bool up = (r & 4) != 0;
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+#pragma unroll
+          for (int jj = 0; jj < G; ++jj) {
+            const float send = up ? v8[k][jj] : v8[k + 2][jj];
+            const float keep = up ? v8[k + 2][jj] : v8[k][jj];
             v4[k][jj] = fadd(keep, __shfl_xor_sync(0xffffffffu, send, 4));
           }
       }
       {
         const bool up = (r & 2) != 0;
 #pragma unroll
-        for (int k = 0; k < 2; ++k)
-#pragma unroll
-          for (int jj = 0; jj < G; ++jj) {
-            const float send = up ? v4[k][jj] : v4[k + 2][jj];
-            const float keep = up ? v4[k + 2][jj] : v4[k][jj];
-            v2[k][jj] = fadd(keep, __shfl_xor_sync(0xffffffffu, send, 2));
-          }
-      }
-      {
-        const bool up = (r & 1) != 0;
-#pragma unroll
         for (int jj = 0; jj < G; ++jj) {
-          const float send = up ? v2[0][jj] : v2[1][jj];
-          const float keep = up ? v2[1][jj] : v2[0][jj];
-          s[jj] = fadd(keep, __shfl_xor_sync(0xffffffffu, send, 1));
+          const float send = up ? v4[0][jj] : v4[1][jj];
+          const float keep = up ? v4[1][jj] : v4[0][jj];
+          v2[jj] = fadd(keep, __shfl_xor_sync(0xffffffffu, send, 2));
         }
       }
-      // ---- online softmax per 8-token group; lane l holds token l
-      const bool valid = lane < ti.n_valid;
-      const float nk = C::kFp16K ? 1.0f : reinterpret_cast<const float*>(tb + C::kKTile)[lane];
-      const float nv = hot ? 1.0f : reinterpret_cast<const float*>(tb + C::kKTile + C::kKNorm + C::kVTile)[lane];
-      float alpha[G];
-      bool rescale = false;
-      float4* wrow = reinterpret_cast<float4*>(wts + (lane + g) * 32);  // padded row of token `lane`
-      float wv4[G];
+      // lane now holds the 4 head scores of token u = r >> 1 (summed over lanes r, r^1 still)
+      constexpr int GH = G >= 2 ? G / 2 : 1;  // heads kept per lane after the last stage
+      if constexpr (G >= 2) {
+        const bool up = (r & 1) != 0;
 #pragma unroll
-      for (int jj = 0; jj < G; ++jj) {
-        const float sj = valid ? fmul(s[jj], nk) : -INFINITY;
-        float gmax = sj;
-        gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, 1));
-        gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, 2));
-        gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, 4));
-        const float mn = fmaxf(m[jj], gmax);
-        alpha[jj] = mn == -INFINITY ? 1.0f : exp2f(m[jj] - mn);
-        rescale |= alpha[jj] != 1.0f;
-        const float pj = valid ? exp2f(sj - mn) : 0.0f;
-        lsum[jj] = ffma(lsum[jj], alpha[jj], pj);
-        m[jj] = mn;
-        wv4[jj] = valid ? fmul(pj, nv) : 0.0f;  // staged norms of masked rows are garbage
-      }
-      if constexpr (G == 4) {
-        wrow[0] = make_float4(wv4[0], wv4[0], wv4[1], wv4[1]);
-        wrow[1] = make_float4(wv4[2], wv4[2], wv4[3], wv4[3]);
-      } else if constexpr (G == 2) {
-        wrow[0] = make_float4(wv4[0], wv4[0], wv4[1], wv4[1]);
+        for (int q2 = 0; q2 < GH; ++q2) {
+          const float send = up ? v2[q2] : v2[q2 + GH];
+          const float keep = up ? v2[q2 + GH] : v2[q2];
+          s2[q2] = fadd(keep, __shfl_xor_sync(0xffffffffu, send, 1));
+        }
       } else {
-        reinterpret_cast<float2*>(wrow)[0] = make_float2(wv4[0], wv4[0]);
+        s2[0] = fadd(v2[0], __shfl_xor_sync(0xffffffffu, v2[0], 1));
+      }
+      // ---- online softmax per 8-token group.  Lane (g, r) owns token 8g + (r >> 1)
+      // and heads h0 = GH * (r & 1) .. h0 + GH - 1 (for G = 1 both lanes of a pair own head 0).
+      const int u_own = r >> 1;
+      const int h0 = G >= 2 ? GH * (r & 1) : 0;
+      const bool valid = 8 * g + u_own < n_valid;
+      const float nk = C::kFp16K ? 1.0f : reinterpret_cast<const float*>(tb + C::kKTile)[8 * g + u_own];
+      const float nv = hot ? 1.0f : reinterpret_cast<const float*>(tb + C::kKTile + C::kKNorm + C::kVTile)[8 * g + u_own];
+      float alpha_own[GH], w_own[GH];
+      bool rescale = false;
+#pragma unroll
+      for (int q2 = 0; q2 < GH; ++q2) {
+        const int jj = h0 + q2;
+        const float sj = valid ? fmul(s2[q2], nk) : -INFINITY;
+        float gm = sj;
+        gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 2));
+        gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 4));
+        gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 8));
+        float m_old = m[0];
+#pragma unroll
+        for (int t = 1; t < G; ++t)
+          if (t == jj) m_old = m[t];
+        const float mn = fmaxf(m_old, gm);
+        const float al = mn == -INFINITY ? 1.0f : exp2f(m_old - mn);
+        const float pj = valid ? exp2f(sj - mn) : 0.0f;
+        lsum[q2] = ffma(lsum[q2], al, pj);  // lsum[q2]: this lane's head h0 + q2
+        alpha_own[q2] = al;
+        w_own[q2] = valid ? fmul(pj, nv) : 0.0f;  // staged norms of masked rows are garbage
+        s2[q2] = mn;  // from here on: the new maximum of head h0 + q2
+      }
+      // exchange with the partner lane (other head pair) so every lane has all G maxima / alphas
+      float alpha[G];
+      if constexpr (G >= 2) {
+#pragma unroll
+        for (int q2 = 0; q2 < GH; ++q2) {
+          const float om = __shfl_xor_sync(0xffffffffu, s2[q2], 1);
+          const float oa = __shfl_xor_sync(0xffffffffu, alpha_own[q2], 1);
+          const bool hi = (r & 1) != 0;
+          m[q2] = hi ? om : s2[q2];
+          m[q2 + GH] = hi ? s2[q2] : om;
+          alpha[q2] = hi ? oa : alpha_own[q2];
+          alpha[q2 + GH] = hi ? alpha_own[q2] : oa;
+        }
+      } else {
+        m[0] = s2[0];
+        alpha[0] = alpha_own[0];
+      }
+#pragma unroll
+      for (int jj = 0; jj < G; ++jj) rescale |= alpha[jj] != 1.0f;
+      // weights (w, w) of token 8g + u_own, heads h0.. : padded row 8g + u_own + g
+      if ((r & 1) == 0 || G >= 2) {
+        float2* wrow = reinterpret_cast<float2*>(wts + (8 * g + u_own + g) * 32) + h0;
+#pragma unroll
+        for (int q2 = 0; q2 < GH; ++q2) wrow[q2] = make_float2(w_own[q2], w_own[q2]);
       }
       if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
         for (int jj = 0; jj < G; ++jj)
 #pragma unroll
-          for (int k = 0; k < 8; ++k) acc[jj][k] = mul2(acc[jj][k], make_float2(alpha[jj], alpha[jj]));
+          for (int k = 0; k < 4; ++k) acc[jj][k] = mul2(acc[jj][k], make_float2(alpha[jj], alpha[jj]));
       }
       __syncwarp();
 
@@ -537,29 +593,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
           for (int jj = 0; jj < G; ++jj) w2[jj] = wr[jj];
         }
         if (!hot) {
-          const Win win = code_window<VB>(tb + C::kKTile + C::kKNorm + tau * C::kVRow, r);
-          float2 cv[8];
-          cv[0] = *reinterpret_cast<const float2*>(vtab + pair_offset<VB, 0>(win, copy8));
-          cv[1] = *reinterpret_cast<const float2*>(vtab + pair_offset<VB, 1>(win, copy8));
-          cv[2] = *reinterpret_cast<const float2*>(vtab + pair_offset<VB, 2>(win, copy8));
-          cv[3] = *reinterpret_cast<const float2*>(vtab + pair_offset<VB, 3>(win, copy8));
-          cv[4] = *reinterpret_cast<const float2*>(vtab + pair_offset<VB, 4>(win, copy8));
-          cv[5] = *reinterpret_cast<const float2*>(vtab + pair_offset<VB, 5>(win, copy8));
-          cv[6] = *reinterpret_cast<const float2*>(vtab + pair_offset<VB, 6>(win, copy8));
-          cv[7] = *reinterpret_cast<const float2*>(vtab + pair_offset<VB, 7>(win, copy8));
+          const uint32_t win = code_window<VB>(tb + C::kKTile + C::kKNorm + tau * C::kVRow, r);
+          const float2 c0 = lds64(pair_addr<VB, 0, kRS>(win, vbase));
+          const float2 c1 = lds64(pair_addr<VB, 1, kRS>(win, vbase));
+          const float2 c2 = lds64(pair_addr<VB, 2, kRS>(win, vbase));
+          const float2 c3 = lds64(pair_addr<VB, 3, kRS>(win, vbase));
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
+          for (int jj = 0; jj < G; ++jj) {
+            acc[jj][0] = fma2(w2[jj], c0, acc[jj][0]);
+            acc[jj][1] = fma2(w2[jj], c1, acc[jj][1]);
+            acc[jj][2] = fma2(w2[jj], c2, acc[jj][2]);
+            acc[jj][3] = fma2(w2[jj], c3, acc[jj][3]);
+          }
+        } else if (tau < n_valid) {
+          const int pos = t_begin + tau;
+          const uint4 a0 = reinterpret_cast<const uint4*>(
+              p.v_ring + ((static_cast<int64_t>(tb_b) * p.hkv + tb_h) * p.hot + pos % p.hot) * D)[r];
+          const uint32_t wv[4] = {a0.x, a0.y, a0.z, a0.w};
 #pragma unroll
-            for (int jj = 0; jj < G; ++jj) acc[jj][k] = fma2(w2[jj], cv[k], acc[jj][k]);
-        } else if (tau < ti.n_valid) {
-          const int pos = ti.t_begin + tau;
-          const uint4* vr = reinterpret_cast<const uint4*>(
-                                p.v_ring + ((static_cast<int64_t>(ti.b) * p.hkv + ti.h) * p.hot + pos % p.hot) * D) +
-                            2 * r;
-          const uint4 a0 = vr[0], a1 = vr[1];
-          const uint32_t wv[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
+          for (int k = 0; k < 4; ++k) {
             const float2 vf = half2_bits_to_float2(wv[k]);
 #pragma unroll
             for (int jj = 0; jj < G; ++jj) acc[jj][k] = fma2(w2[jj], vf, acc[jj][k]);
@@ -570,30 +622,44 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
       ++j;
     }
 
-    // ---- leave the row: groups -> warp -> CTA, one partial per (CTA, row)
+    // ---- leave the row: lanes -> warp -> CTA, one partial per (CTA, row)
     for (int i = tid; i < G * D; i += kThreads) comb[i] = 0.0f;
     float mw[G];
 #pragma unroll
     for (int jj = 0; jj < G; ++jj) {
-      float mx = fmaxf(m[jj], __shfl_xor_sync(0xffffffffu, m[jj], 8));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      const float mx = fmaxf(m[jj], __shfl_xor_sync(0xffffffffu, m[jj], 16));
       const float sc = m[jj] == -INFINITY ? 0.0f : exp2f(m[jj] - mx);
-      float l = fmul(lsum[jj], sc);
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) l = fadd(l, __shfl_xor_sync(0xffffffffu, l, o));
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
+      for (int k = 0; k < 4; ++k) {
         float2 a = mul2(acc[jj][k], make_float2(sc, sc));
-        a.x = fadd(a.x, __shfl_xor_sync(0xffffffffu, a.x, 8));
-        a.y = fadd(a.y, __shfl_xor_sync(0xffffffffu, a.y, 8));
         a.x = fadd(a.x, __shfl_xor_sync(0xffffffffu, a.x, 16));
         a.y = fadd(a.y, __shfl_xor_sync(0xffffffffu, a.y, 16));
         acc[jj][k] = a;
       }
       mw[jj] = mx;
-      if (lane == 0) {
-        wml[(warp * 4 + jj) * 2] = mx;
-        wml[(warp * 4 + jj) * 2 + 1] = l;
+    }
+    // softmax mass: lane (g, r) holds heads h0.. of its own tokens, scaled to its group max
+    {
+      const int h0 = G >= 2 ? (G / 2) * (r & 1) : 0;
+      float lw[G];
+#pragma unroll
+      for (int jj = 0; jj < G; ++jj) lw[jj] = 0.0f;
+      constexpr int GH = G >= 2 ? G / 2 : 1;
+#pragma unroll
+      for (int q2 = 0; q2 < GH; ++q2) {
+#pragma unroll
+        for (int jj = 0; jj < G; ++jj)
+          if (jj == h0 + q2) lw[jj] = m[jj] == -INFINITY ? 0.0f : fmul(lsum[q2], exp2f(m[jj] - mw[jj]));
+      }
+      if (G == 1 && (r & 1)) lw[0] = 0.0f;  // both lanes of a pair hold the same token for G = 1
+#pragma unroll
+      for (int jj = 0; jj < G; ++jj) {
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) lw[jj] = fadd(lw[jj], __shfl_xor_sync(0xffffffffu, lw[jj], o));
+        if (lane == 0) {
+          wml[(warp * 4 + jj) * 2] = mw[jj];
+          wml[(warp * 4 + jj) * 2 + 1] = lw[jj];
+        }
       }
     }
     __syncthreads();
@@ -606,9 +672,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
         for (int w = 0; w < kWarps; ++w) mm = fmaxf(mm, wml[(w * 4 + jj) * 2]);
         const float sc = exp2f(mw[jj] - mm);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          atomicAdd(&comb[jj * D + 16 * r + 2 * k], fmul(acc[jj][k].x, sc));
-          atomicAdd(&comb[jj * D + 16 * r + 2 * k + 1], fmul(acc[jj][k].y, sc));
+        for (int k = 0; k < 4; ++k) {
+          atomicAdd(&comb[jj * D + 8 * r + 2 * k], fmul(acc[jj][k].x, sc));
+          atomicAdd(&comb[jj * D + 8 * r + 2 * k + 1], fmul(acc[jj][k].y, sc));
         }
       }
     }

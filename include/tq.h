@@ -58,6 +58,7 @@ typedef enum tq_status {
 /* Bits of the device status word (OR-ed together by the kernels). */
 #define TQ_DEV_ERR_APPEND_RANGE 0x1u /* start_pos < 0, bad per-sequence count, or past capacity */
 #define TQ_DEV_ERR_SEQ_LEN 0x2u      /* seq_len < 0 or seq_len > capacity (or > max_seq_len) */
+#define TQ_DEV_ERR_LAYOUT 0x4u       /* internal: a kernel's shared-memory layout did not fit (not expected) */
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char *tq_status_string(tq_status status);
