@@ -36,6 +36,7 @@
 // the softmax mass.
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 
 #include "tq_device.cuh"
 #include "tq_internal.h"
@@ -264,6 +265,59 @@ __device__ __forceinline__ float2 lds64(uint32_t addr) {
   asm("ld.shared.v2.f32 {%0, %1}, [%2];\n" : "=f"(v.x), "=f"(v.y) : "r"(addr));
   return v;
 }
+// Shared loads at a register base plus a compile-time byte offset (no address arithmetic).
+template <int OFF>
+__device__ __forceinline__ uint32_t lds32(uint32_t base) {
+  uint32_t v;
+  asm("ld.shared.u32 %0, [%1+%2];\n" : "=r"(v) : "r"(base), "n"(OFF));
+  return v;
+}
+template <int OFF>
+__device__ __forceinline__ uint4 lds128(uint32_t base) {
+  uint4 v;
+  asm("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4+%5];\n" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(base), "n"(OFF));
+  return v;
+}
+template <int OFF>
+__device__ __forceinline__ float4 lds128f(uint32_t base) {
+  float4 v;
+  asm("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4+%5];\n" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(base), "n"(OFF));
+  return v;
+}
+template <int OFF>
+__device__ __forceinline__ float2 lds64f(uint32_t base) {
+  float2 v;
+  asm("ld.shared.v2.f32 {%0, %1}, [%2+%3];\n" : "=f"(v.x), "=f"(v.y) : "r"(base), "n"(OFF));
+  return v;
+}
+
+// Per-lane part of a code-window address (bytes from the start of a tile's
+// token-record block) and the shift that aligns the lane's first code.
+template <int BITS>
+__device__ __forceinline__ uint32_t window_lane_offset(int g, int r) {
+  const uint32_t tok = 8u * g * (BITS * 16);
+  if constexpr (BITS == 4) return tok + 4u * r;
+  else if constexpr (BITS == 2) return tok + 4u * (r >> 1);
+  else return tok + 4u * ((3 * r) >> 2);
+}
+template <int BITS>
+__device__ __forceinline__ uint32_t window_lane_shift(int r) {
+  if constexpr (BITS == 4) return 0u;
+  else if constexpr (BITS == 2) return 16u * (r & 1);
+  else return (24u * r) & 31u;
+}
+// Code window of step U: 8*BITS bits of token 8g + U for this lane.
+template <int BITS, int U>
+__device__ __forceinline__ uint32_t window_at(uint32_t base, uint32_t sh) {
+  constexpr int kRec = BITS * 16;
+  if constexpr (BITS == 4) {
+    return lds32<U * kRec>(base);
+  } else if constexpr (BITS == 2) {
+    return lds32<U * kRec>(base) >> sh;
+  } else {
+    return __funnelshift_r(lds32<U * kRec>(base), lds32<U * kRec + 4>(base), sh);
+  }
+}
 
 template <int KB, int VB>
 __device__ __forceinline__ void stage_tile(const DecodeParams& p, const TileInfo& ti, uint8_t* buf, int lane) {
@@ -370,6 +424,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
 #pragma unroll
   for (int s = 0; s < S - 1; ++s) issue();
 
+  const uint32_t k_lane_off = C::kFp16K ? static_cast<uint32_t>(8 * g * 256 + 16 * r)
+                                        : window_lane_offset<C::kKBits>(g, r);
+  const uint32_t k_lane_sh = window_lane_shift<C::kKBits>(r);
+  const uint32_t v_lane_off = window_lane_offset<VB>(g, r);
+  const uint32_t v_lane_sh = window_lane_shift<VB>(r);
+  const uint32_t wts_s = static_cast<uint32_t>(__cvta_generic_to_shared(wts));
   float2 qr[G][4];
   int cur_b = -1, cur_h = -1;
   long long seg = t0;
@@ -434,38 +494,49 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
       const uint8_t* tb = wring + (j % S) * C::kBuf;
 
       // ---- scores: P[u][h] = partial over this lane's 8 coordinates of token 8g + u
+      const uint32_t tbs = ring + static_cast<uint32_t>((j % S) * C::kBuf);  // shared address of the tile
       float P[8][G];
+      {
+        const uint32_t kw = tbs + k_lane_off;
+        auto score_step = [&](auto U_) {
+          constexpr int U = decltype(U_)::value;
+          float2 pa[G];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int tau = 8 * g + u;
-        float2 pa[G];
+          for (int jj = 0; jj < G; ++jj) pa[jj] = make_float2(0.0f, 0.0f);
+          if constexpr (C::kFp16K) {
+            const uint4 a0 = lds128<U * 256>(kw);
+            const uint32_t wv[4] = {a0.x, a0.y, a0.z, a0.w};
 #pragma unroll
-        for (int jj = 0; jj < G; ++jj) pa[jj] = make_float2(0.0f, 0.0f);
-        if constexpr (C::kFp16K) {
-          const uint4 a0 = reinterpret_cast<const uint4*>(tb + tau * 256)[r];
-          const uint32_t wv[4] = {a0.x, a0.y, a0.z, a0.w};
+            for (int k = 0; k < 4; ++k) {
+              const float2 kf = half2_bits_to_float2(wv[k]);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float2 kf = half2_bits_to_float2(wv[k]);
+              for (int jj = 0; jj < G; ++jj) pa[jj] = fma2(qr[jj][k], kf, pa[jj]);
+            }
+          } else {
+            const uint32_t win = window_at<C::kKBits, U>(kw, k_lane_sh);
+            const float2 c0 = lds64(pair_addr<C::kKBits, 0, kRS>(win, kbase));
+            const float2 c1 = lds64(pair_addr<C::kKBits, 1, kRS>(win, kbase));
+            const float2 c2 = lds64(pair_addr<C::kKBits, 2, kRS>(win, kbase));
+            const float2 c3 = lds64(pair_addr<C::kKBits, 3, kRS>(win, kbase));
 #pragma unroll
-            for (int jj = 0; jj < G; ++jj) pa[jj] = fma2(qr[jj][k], kf, pa[jj]);
+            for (int jj = 0; jj < G; ++jj) {
+              pa[jj] = fma2(qr[jj][0], c0, pa[jj]);
+              pa[jj] = fma2(qr[jj][1], c1, pa[jj]);
+              pa[jj] = fma2(qr[jj][2], c2, pa[jj]);
+              pa[jj] = fma2(qr[jj][3], c3, pa[jj]);
+            }
           }
-        } else {
-          const uint32_t win = code_window<C::kKBits>(tb + tau * C::kKRow, r);
-          const float2 c0 = lds64(pair_addr<C::kKBits, 0, kRS>(win, kbase));
-          const float2 c1 = lds64(pair_addr<C::kKBits, 1, kRS>(win, kbase));
-          const float2 c2 = lds64(pair_addr<C::kKBits, 2, kRS>(win, kbase));
-          const float2 c3 = lds64(pair_addr<C::kKBits, 3, kRS>(win, kbase));
 #pragma unroll
-          for (int jj = 0; jj < G; ++jj) {
-            pa[jj] = fma2(qr[jj][0], c0, pa[jj]);
-            pa[jj] = fma2(qr[jj][1], c1, pa[jj]);
-            pa[jj] = fma2(qr[jj][2], c2, pa[jj]);
-            pa[jj] = fma2(qr[jj][3], c3, pa[jj]);
-          }
-        }
-#pragma unroll
-        for (int jj = 0; jj < G; ++jj) P[u][jj] = fadd(pa[jj].x, pa[jj].y);
+          for (int jj = 0; jj < G; ++jj) P[U][jj] = fadd(pa[jj].x, pa[jj].y);
+        };
+        score_step(std::integral_constant<int, 0>{});
+        score_step(std::integral_constant<int, 1>{});
+        score_step(std::integral_constant<int, 2>{});
+        score_step(std::integral_constant<int, 3>{});
+        score_step(std::integral_constant<int, 4>{});
+        score_step(std::integral_constant<int, 5>{});
+        score_step(std::integral_constant<int, 6>{});
+        score_step(std::integral_constant<int, 7>{});
       }
       // ---- transposing butterfly over the 16 lanes of a group:
       // bits 3, 2, 1 of r select the token (u = r >> 1), bit 0 the head pair
@@ -577,23 +648,27 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
       __syncwarp();
 
       // ---- V accumulation for tokens 8g + u
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int tau = 8 * g + u;
-        const float2* wr = reinterpret_cast<const float2*>(wts + (tau + g) * 32);
+      const uint32_t wsb = wts_s + static_cast<uint32_t>(9 * g * 32);  // padded row 8g + u + g
+      const uint32_t vw = tbs + static_cast<uint32_t>(C::kKTile + C::kKNorm) + v_lane_off;
+      auto v_step = [&](auto U_) {
+        constexpr int U = decltype(U_)::value;
+        const int tau = 8 * g + U;
         float2 w2[G];
         if constexpr (G == 4) {
-          const float4 a = reinterpret_cast<const float4*>(wr)[0], b2 = reinterpret_cast<const float4*>(wr)[1];
+          const float4 a = lds128f<U * 32>(wsb), b2 = lds128f<U * 32 + 16>(wsb);
           w2[0] = make_float2(a.x, a.y);
           w2[1] = make_float2(a.z, a.w);
           w2[2] = make_float2(b2.x, b2.y);
           w2[3] = make_float2(b2.z, b2.w);
+        } else if constexpr (G == 2) {
+          const float4 a = lds128f<U * 32>(wsb);
+          w2[0] = make_float2(a.x, a.y);
+          w2[G - 1] = make_float2(a.z, a.w);
         } else {
-#pragma unroll
-          for (int jj = 0; jj < G; ++jj) w2[jj] = wr[jj];
+          w2[0] = lds64f<U * 32>(wsb);
         }
         if (!hot) {
-          const uint32_t win = code_window<VB>(tb + C::kKTile + C::kKNorm + tau * C::kVRow, r);
+          const uint32_t win = window_at<VB, U>(vw, v_lane_sh);
           const float2 c0 = lds64(pair_addr<VB, 0, kRS>(win, vbase));
           const float2 c1 = lds64(pair_addr<VB, 1, kRS>(win, vbase));
           const float2 c2 = lds64(pair_addr<VB, 2, kRS>(win, vbase));
@@ -617,7 +692,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
             for (int jj = 0; jj < G; ++jj) acc[jj][k] = fma2(w2[jj], vf, acc[jj][k]);
           }
         }
-      }
+      };
+      v_step(std::integral_constant<int, 0>{});
+      v_step(std::integral_constant<int, 1>{});
+      v_step(std::integral_constant<int, 2>{});
+      v_step(std::integral_constant<int, 3>{});
+      v_step(std::integral_constant<int, 4>{});
+      v_step(std::integral_constant<int, 5>{});
+      v_step(std::integral_constant<int, 6>{});
+      v_step(std::integral_constant<int, 7>{});
       __syncwarp();
       ++j;
     }
