@@ -180,18 +180,14 @@ TQ_HD int compare_square(unsigned __int128 s, double m) {
   return lhs < mm2 ? -1 : (lhs > mm2 ? 1 : 0);
 }
 
-// Correctly rounded float32 of sqrt(sum of squares) of 128 fp16 values.
-//
-// Fast path: the squares (exact in float32) are summed as an unevaluated pair
-// hi + lo with TwoSum in two interleaved lanes; n = sqrt(RN(hi + lo)) is then
-// within one ulp of the answer, and the residual r = (hi + lo) - n^2 (n^2 split
-// exactly with an FMA) decides between n and its neighbours by comparison with
-// the rounding midpoints.  When r is within 2^-30 S of a midpoint the exact
-// integer sum decides (ties to even).
-TQ_HD float exact_norm(const uint32_t* w) {
+// Sum of squares of 2N fp16 values (N packed pairs) as an unevaluated pair
+// h + l: the squares are exact in float32 and are added with TwoSum in two
+// interleaved lanes, then the lanes are merged with one more TwoSum.
+template <int N>
+TQ_HD void norm_partial(const uint32_t* w, float& h_out, float& l_out) {
   float2 hi = make_float2(0.0f, 0.0f), lo = make_float2(0.0f, 0.0f);
 #pragma unroll
-  for (int j = 0; j < 64; ++j) {
+  for (int j = 0; j < N; ++j) {
     const float2 x = half2_bits_to_float2(w[j]);
     const float2 t = mul2(x, x);       // exact: 11-bit significands
     const float2 s = add2(hi, t);      // TwoSum(hi, t)
@@ -203,7 +199,27 @@ TQ_HD float exact_norm(const uint32_t* w) {
   const float h = fadd(hi.x, hi.y);
   const float hb = fsub(h, hi.x);
   const float he = fadd(fsub(hi.x, fsub(h, hb)), fsub(hi.y, hb));
-  const float l = fadd(fadd(lo.x, lo.y), he);
+  h_out = h;
+  l_out = fadd(fadd(lo.x, lo.y), he);
+}
+
+// (h, l) += (h2, l2), the high parts with TwoSum.
+TQ_HD void twosum_merge(float& h, float& l, float h2, float l2) {
+  const float s = fadd(h, h2);
+  const float bb = fsub(s, h);
+  const float e = fadd(fsub(h, fsub(s, bb)), fsub(h2, bb));
+  l = fadd(fadd(l, l2), e);
+  h = s;
+}
+
+// Correctly rounded float32 of sqrt(h + l), h + l the sum of squares of the
+// 128 fp16 values of `row` (64 packed pairs, read only in the rare exact path).
+//
+// n = sqrt(RN(h + l)) is within one ulp of the answer; the residual
+// r = (h + l) - n^2 (n^2 split exactly with an FMA) decides between n and its
+// neighbours by comparison with the rounding midpoints.  When r is within
+// 2^-30 S of a midpoint the exact integer sum decides (ties to even).
+TQ_HD float norm_from_sum(float h, float l, const uint32_t* row) {
   const float s_approx = fadd(h, l);
   if (!(s_approx > 0.0f)) return 0.0f;  // all zero (squares are >= 0)
   const float n = fsqrt(s_approx);
@@ -215,19 +231,26 @@ TQ_HD float exact_norm(const uint32_t* w) {
   const float t_up = ffma(n, u_up, fmul(fmul(u_up, u_up), 0.25f));   // (n + u/2)^2 - n^2
   const float t_dn = ffma(n, u_dn, -fmul(fmul(u_dn, u_dn), 0.25f));  // n^2 - (n - u/2)^2
   const float margin = fmul(s_approx, 9.313225746154785e-10f);       // 2^-30 S
-  const bool near_up = std::fabs(fsub(r, t_up)) <= margin;
-  const bool near_dn = std::fabs(fadd(r, t_dn)) <= margin;
+  const bool near_up = fabsf(fsub(r, t_up)) <= margin;
+  const bool near_dn = fabsf(fadd(r, t_dn)) <= margin;
   if (!near_up && !near_dn) {
     if (r > t_up) return n_up;
     if (r < -t_dn) return n_dn;
     return n;
   }
-  const unsigned __int128 se = exact_sum_squares(w);
+  const unsigned __int128 se = exact_sum_squares(row);
   const int cu = compare_square(se, static_cast<double>(n) + 0.5 * static_cast<double>(u_up));
   if (cu > 0 || (cu == 0 && (fbits(n_up) & 1u) == 0)) return n_up;
   const int cd = compare_square(se, static_cast<double>(n) - 0.5 * static_cast<double>(u_dn));
   if (cd < 0 || (cd == 0 && (fbits(n_dn) & 1u) == 0)) return n_dn;
   return n;
+}
+
+// Correctly rounded float32 norm of 128 fp16 values in one thread.
+TQ_HD float exact_norm(const uint32_t* w) {
+  float h, l;
+  norm_partial<64>(w, h, l);
+  return norm_from_sum(h, l, w);
 }
 
 // ---------------------------------------------------------------------------
@@ -278,39 +301,59 @@ TQ_HD LutEntry lut_entry(const float* thr, int n_thr, int a, int j) {
   return e;
 }
 
-// Quantize one 128-vector: fp16 pairs `w` (as loaded), sign masks `smask`
-// (bit 15 / bit 31 set where the rotation sign is -1), LUT with entries at
-// lut[j * lut_stride].  Writes BITS*4 packed words and returns the norm.
+// Walsh-Hadamard butterflies over index bits 0..4 of 32 values held as 16
+// float2 (value 2m in .x, 2m+1 in .y): bit 0 inside each pair, bits 1..4
+// between pairs with packed operations.
+TQ_HD void fwht32(float2* v) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const float a = v[j].x, b = v[j].y;
+    v[j] = make_float2(fadd(a, b), fsub(a, b));
+  }
+#pragma unroll
+  for (int hb = 1; hb < 16; hb *= 2) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      if (j & hb) continue;
+      const float2 a = v[j], b = v[j + hb];
+      v[j] = add2(a, b);
+      v[j + hb] = sub2(a, b);
+    }
+  }
+}
+
+// One butterfly stage between two holders of 32 values: the lower holder keeps
+// own + other, the upper one other - own (a single rounding either way).
+TQ_HD float2 butterfly_pair(float2 own, float2 other, bool upper) {
+  return upper ? sub2(other, own) : add2(own, other);
+}
+
+// Codes of 32 rotated coordinates z (y = z * inv) packed LSB-first into BITS
+// words.  code = base + (y >= thr) of the bucket RN(y * A) of a lookup table
+// whose buckets hold at most one threshold (entries at lut[j * stride]); y is
+// clamped to +-(1 + 1/A), which no real coordinate reaches, so that any input
+// (even NaN) lands in the table.
 template <int BITS>
-TQ_HD float quantize_vector(const uint32_t* w, const uint32_t* smask, const LutEntry* lut, int lut_stride, int lut_a,
-                            uint32_t* out_words) {
-  const float n = exact_norm(w);
-  float2 v[64];
-#pragma unroll
-  for (int j = 0; j < 64; ++j) v[j] = half2_bits_to_float2(w[j] ^ smask[j]);
-  fwht128(v);
-  const float inv = n > 0.0f ? frcp(fmul(n, kSqrtD)) : 0.0f;
+TQ_HD void pack_codes32(const float2* z, float inv, const LutEntry* lut, int stride, int lut_a, uint32_t* words) {
   const float fa = static_cast<float>(lut_a);
-  const uint32_t nb = static_cast<uint32_t>(lut_size(lut_a));
+  const float lim = (fa + 1.0f) / fa;
   const uint32_t bias = fbits(kMagic) - static_cast<uint32_t>(lut_a + 1);
-  constexpr int W = BITS * 4;
-  uint32_t acc[W];
+  uint32_t acc[BITS];
 #pragma unroll
-  for (int k = 0; k < W; ++k) acc[k] = 0u;
+  for (int k = 0; k < BITS; ++k) acc[k] = 0u;
 #pragma unroll
-  for (int i = 0; i < D; ++i) {
-    const float y = fmul((i & 1) ? v[i >> 1].y : v[i >> 1].x, inv);
-    uint32_t idx = fbits(ffma(y, fa, kMagic)) - bias;
-    idx = idx < nb ? idx : nb - 1;  // NaN guard
-    const LutEntry e = lut[idx * lut_stride];
+  for (int i = 0; i < 32; ++i) {
+    float y = fmul((i & 1) ? z[i >> 1].y : z[i >> 1].x, inv);
+    y = fminf(fmaxf(y, -lim), lim);
+    const uint32_t idx = fbits(ffma(y, fa, kMagic)) - bias;
+    const LutEntry e = lut[idx * stride];
     const uint32_t code = e.base + (y >= e.thr ? 1u : 0u);
     const int bit = i * BITS, word = bit >> 5, off = bit & 31;
     acc[word] |= code << off;
     if (off + BITS > 32) acc[word + 1] |= code >> (32 - off);
   }
 #pragma unroll
-  for (int k = 0; k < W; ++k) out_words[k] = acc[k];
-  return n;
+  for (int k = 0; k < BITS; ++k) words[k] = acc[k];
 }
 
 // Sign masks of one KV head for 64 fp16 pairs: bit 15 for element 2j, bit 31 for 2j+1.

@@ -1,12 +1,14 @@
 // Quantize-and-append kernel (one launch for K and V of every head) and the
 // hot-window evict pass.
 //
-// Work unit: a "job" is 32 consecutive tokens of one (tensor, batch, KV head).
+// Work unit: a "job" is 16 consecutive tokens of one (tensor, batch, KV head).
 // Each warp streams its jobs through a two-stage cp.async pipeline into a
-// padded shared-memory tile (272-byte rows, so that the 16-byte row reads of
-// the 32 lanes hit distinct banks), then every lane quantizes one token
-// vector entirely in registers: exact norm, sign flip, 128-point FWHT,
-// bucketed threshold lookup, LSB-first packing.
+// padded shared-memory tile (272-byte rows).  Four lanes share one token
+// vector, lane q owning coordinates 32q..32q+31, so that eight vectors are in
+// flight per warp step: exact norm (per-lane TwoSum partial sums merged across
+// the four lanes), sign flip, FWHT over index bits 0..4 in registers and bits
+// 5..6 with shuffles, bucketed threshold lookup, LSB-first packing of the
+// lane's 32 codes into exactly `bits` words.
 #include <cstring>
 
 #include "tq_device.cuh"
@@ -16,10 +18,10 @@
 namespace tq {
 namespace {
 
-constexpr int kWarps = 8;                   // warps per CTA
+constexpr int kWarps = 16;                  // warps per CTA
 constexpr int kRowBytes = 256;              // one fp16 vector
 constexpr int kRowPitch = kRowBytes + 16;   // padded smem pitch
-constexpr int kTileRows = 32;
+constexpr int kTileRows = 16;
 constexpr int kTileBytes = kTileRows * kRowPitch;
 constexpr int kLutCopies = 16;              // one LUT copy per lane of a half-warp
 
@@ -108,7 +110,7 @@ __device__ __forceinline__ void issue_tile(const QuantParams& p, long long j, ui
   const Job jb = decode_job(p, j);
   if (!jb.valid) return;
 #pragma unroll
-  for (int k = 0; k < 16; ++k) {
+  for (int k = 0; k < kTileRows / 2; ++k) {
     const int row = 2 * k + (lane >> 4), col = lane & 15;
     int pos = 0;
     const uint16_t* src = src_row(p, jb, row, &pos);
@@ -116,23 +118,59 @@ __device__ __forceinline__ void issue_tile(const QuantParams& p, long long j, ui
   }
 }
 
+// One step: 8 vectors of the tile (rows 8 * step + v), lane = v + 8 q.
 template <int BITS>
-__device__ __forceinline__ void quantize_store(const uint32_t* w, const uint32_t* smask, const LutEntry* lut,
-                                               int lut_a, uint32_t* dst_words, float* dst_norm, int lane) {
-  uint32_t out[BITS * 4];
-  const float n = quantize_vector<BITS>(w, smask, lut + (lane & (kLutCopies - 1)), kLutCopies, lut_a, out);
-  uint4* d4 = reinterpret_cast<uint4*>(dst_words);
+__device__ __forceinline__ void quantize_step(const uint8_t* tile, int row, int q, const uint32_t* smask,
+                                              const LutEntry* lut, int lut_a, uint32_t* dst_words, float* dst_norm,
+                                              bool store) {
+  const uint4* src = reinterpret_cast<const uint4*>(tile + row * kRowPitch) + 4 * q;
+  const uint4* msk = reinterpret_cast<const uint4*>(smask) + 4 * q;
+  uint32_t w[16];
+  float2 v[16];
 #pragma unroll
-  for (int k = 0; k < BITS; ++k) d4[k] = make_uint4(out[4 * k], out[4 * k + 1], out[4 * k + 2], out[4 * k + 3]);
-  *dst_norm = n;
-}
-
-__device__ __forceinline__ void quantize_any(int bits, const uint32_t* w, const uint32_t* smask, const LutEntry* lut,
-                                             int lut_a, uint32_t* dst_words, float* dst_norm, int lane) {
-  switch (bits) {
-    case 2: quantize_store<2>(w, smask, lut, lut_a, dst_words, dst_norm, lane); break;
-    case 3: quantize_store<3>(w, smask, lut, lut_a, dst_words, dst_norm, lane); break;
-    default: quantize_store<4>(w, smask, lut, lut_a, dst_words, dst_norm, lane); break;
+  for (int k = 0; k < 4; ++k) {
+    const uint4 a = src[k], m = msk[k];
+    w[4 * k] = a.x;
+    w[4 * k + 1] = a.y;
+    w[4 * k + 2] = a.z;
+    w[4 * k + 3] = a.w;
+    v[4 * k] = half2_bits_to_float2(a.x ^ m.x);
+    v[4 * k + 1] = half2_bits_to_float2(a.y ^ m.y);
+    v[4 * k + 2] = half2_bits_to_float2(a.z ^ m.z);
+    v[4 * k + 3] = half2_bits_to_float2(a.w ^ m.w);
+  }
+  // norm: per-lane partial sums, merged over the 4 lanes of the vector (q ^ 1, then q ^ 2)
+  float h, l;
+  norm_partial<16>(w, h, l);
+  twosum_merge(h, l, __shfl_xor_sync(0xffffffffu, h, 8), __shfl_xor_sync(0xffffffffu, l, 8));
+  twosum_merge(h, l, __shfl_xor_sync(0xffffffffu, h, 16), __shfl_xor_sync(0xffffffffu, l, 16));
+  const float n = norm_from_sum(h, l, reinterpret_cast<const uint32_t*>(tile + row * kRowPitch));
+  // rotation: in-lane bits 0..4, then bits 5 (q ^ 1) and 6 (q ^ 2) across lanes
+  fwht32(v);
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const float2 o = make_float2(__shfl_xor_sync(0xffffffffu, v[j].x, 8), __shfl_xor_sync(0xffffffffu, v[j].y, 8));
+    v[j] = butterfly_pair(v[j], o, (q & 1) != 0);
+  }
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const float2 o = make_float2(__shfl_xor_sync(0xffffffffu, v[j].x, 16), __shfl_xor_sync(0xffffffffu, v[j].y, 16));
+    v[j] = butterfly_pair(v[j], o, (q & 2) != 0);
+  }
+  const float inv = n > 0.0f ? frcp(fmul(n, kSqrtD)) : 0.0f;
+  uint32_t words[BITS];
+  pack_codes32<BITS>(v, inv, lut, kLutCopies, lut_a, words);
+  if (store) {
+    uint32_t* d = dst_words + q * BITS;
+    if constexpr (BITS == 4) {
+      *reinterpret_cast<uint4*>(d) = make_uint4(words[0], words[1], words[2], words[3]);
+    } else if constexpr (BITS == 2) {
+      *reinterpret_cast<uint2*>(d) = make_uint2(words[0], words[1]);
+    } else {
+#pragma unroll
+      for (int k = 0; k < BITS; ++k) d[k] = words[k];
+    }
+    if (q == 0) *dst_norm = n;
   }
 }
 
@@ -144,6 +182,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) quantize_append_kernel(const Q
   LutEntry* lut_v = lut_k + lut_k_n * kLutCopies;
   uint8_t* warp_area = reinterpret_cast<uint8_t*>(lut_v + lut_v_n * kLutCopies);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int vrow = lane & 7, q = lane >> 3;
   uint8_t* tiles = warp_area + warp * (2 * kTileBytes + 256);
   uint32_t* smask = reinterpret_cast<uint32_t*>(tiles + 2 * kTileBytes);
 
@@ -153,6 +192,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1) quantize_append_kernel(const Q
   for (int i = threadIdx.x; i < lut_v_n * kLutCopies; i += blockDim.x)
     lut_v[i] = lut_entry(p.v_thr, (1 << p.v_bits) - 1, p.v_lut_a, i / kLutCopies);
   __syncthreads();
+  const LutEntry* my_lut_k = lut_k + (lane & (kLutCopies - 1));
+  const LutEntry* my_lut_v = lut_v + (lane & (kLutCopies - 1));
 
   const long long stride = static_cast<long long>(gridDim.x) * kWarps;
   long long j = static_cast<long long>(blockIdx.x) * kWarps + warp;
@@ -175,44 +216,40 @@ __global__ void __launch_bounds__(kWarps * 32, 1) quantize_append_kernel(const Q
       smask[lane] = sign_mask_pair(p.seed, p.layer, jb.h, lane);
       smask[lane + 32] = sign_mask_pair(p.seed, p.layer, jb.h, lane + 32);
       __syncwarp();
-      int pos = 0;
-      const uint16_t* src = src_row(p, jb, lane, &pos);
-      if (src != nullptr) {
-        const uint4* row = reinterpret_cast<const uint4*>(tiles + buf * kTileBytes + lane * kRowPitch);
-        uint32_t w[64];
+      const uint8_t* tile = tiles + buf * kTileBytes;
+      const int64_t rowbase = (static_cast<int64_t>(jb.b) * p.heads + jb.h) * p.cap;
+      const bool k_tensor = jb.tensor == 0;
+      const bool copy_k = k_tensor && p.k_mode == TQ_K_FP16;
+      int cold_end = 1 << 30;
+      if (!k_tensor && p.hot > 0 && !p.evict) cold_end = jb.end - min(p.hot, jb.end);
+#pragma unroll 1
+      for (int step = 0; step < kTileRows / 8; ++step) {
+        const int row = 8 * step + vrow;
+        int pos = 0;
+        const bool have = src_row(p, jb, row, &pos) != nullptr;
+        const int64_t ridx = rowbase + pos;
+        const bool to_copy = copy_k || (!k_tensor && pos >= cold_end);
+        if (to_copy && have) {
+          // fp16 copy of the row (asym K, or V going to the hot ring): 4 x 16 bytes per lane
+          uint4* dst = copy_k ? reinterpret_cast<uint4*>(p.k_fp16 + ridx * D)
+                              : reinterpret_cast<uint4*>(
+                                    p.v_ring + ((static_cast<int64_t>(jb.b) * p.heads + jb.h) * p.hot + pos % p.hot) * D);
+          const uint4* src = reinterpret_cast<const uint4*>(tile + row * kRowPitch);
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const uint4 u = row[k];
-          w[4 * k] = u.x;
-          w[4 * k + 1] = u.y;
-          w[4 * k + 2] = u.z;
-          w[4 * k + 3] = u.w;
+          for (int k = 0; k < 4; ++k) dst[4 * q + k] = src[4 * q + k];
         }
-        const int64_t rowidx = (static_cast<int64_t>(jb.b) * p.heads + jb.h) * p.cap + pos;
-        if (jb.tensor == 0) {
-          if (p.k_mode == TQ_K_FP16) {
-            uint4* dst = reinterpret_cast<uint4*>(p.k_fp16 + rowidx * D);
-#pragma unroll
-            for (int k = 0; k < 16; ++k) dst[k] = row[k];
-          } else {
-            quantize_any(p.k_bits, w, smask, lut_k, p.k_lut_a, p.k_words + rowidx * (p.k_bits * 4),
-                         p.k_norms + rowidx, lane);
-          }
-        } else {
-          bool to_ring = false;
-          if (p.hot > 0 && !p.evict) {
-            const int cold_end = jb.end - min(p.hot, jb.end);
-            to_ring = pos >= cold_end;
-          }
-          if (to_ring) {
-            uint4* dst = reinterpret_cast<uint4*>(
-                p.v_ring + ((static_cast<int64_t>(jb.b) * p.heads + jb.h) * p.hot + pos % p.hot) * D);
-#pragma unroll
-            for (int k = 0; k < 16; ++k) dst[k] = row[k];
-          } else {
-            quantize_any(p.v_bits, w, smask, lut_v, p.v_lut_a, p.v_words + rowidx * (p.v_bits * 4),
-                         p.v_norms + rowidx, lane);
-          }
+        if (copy_k) continue;  // uniform over the warp (the whole job is fp16 K)
+        // every lane takes part in the shuffles of quantize_step; rows that are
+        // absent or go to the ring are computed but not stored
+        const int bits = k_tensor ? p.k_bits : p.v_bits;
+        const LutEntry* lut = k_tensor ? my_lut_k : my_lut_v;
+        const int lut_a = k_tensor ? p.k_lut_a : p.v_lut_a;
+        uint32_t* dw = (k_tensor ? p.k_words : p.v_words) + ridx * (bits * 4);
+        float* dn = (k_tensor ? p.k_norms : p.v_norms) + ridx;
+        switch (bits) {
+          case 2: quantize_step<2>(tile, row, q, smask, lut, lut_a, dw, dn, have && !to_copy); break;
+          case 3: quantize_step<3>(tile, row, q, smask, lut, lut_a, dw, dn, have && !to_copy); break;
+          default: quantize_step<4>(tile, row, q, smask, lut, lut_a, dw, dn, have && !to_copy); break;
         }
       }
     }
@@ -334,15 +371,42 @@ extern "C" tq_status tq_debug_quantize_rows_host(const tq_codebook* cb, uint64_t
   for (int j = 0; j < lut_size(a); ++j) lut[j] = lut_entry(cb->thresholds, n_thr, a, j);
   uint32_t smask[64];
   for (int j = 0; j < 64; ++j) smask[j] = sign_mask_pair(seed, layer, head, j);
+  // the kernel's four-lane decomposition, with the shuffles done by indexing
   for (int r = 0; r < n_rows; ++r) {
     uint32_t w[64];
     std::memcpy(w, rows + static_cast<size_t>(r) * D, sizeof(w));
-    uint32_t* out = words + static_cast<size_t>(r) * cb->bits * 4;
-    switch (cb->bits) {
-      case 2: norms[r] = quantize_vector<2>(w, smask, lut, 1, a, out); break;
-      case 3: norms[r] = quantize_vector<3>(w, smask, lut, 1, a, out); break;
-      default: norms[r] = quantize_vector<4>(w, smask, lut, 1, a, out); break;
+    float h[4], l[4];
+    float2 v[4][16];
+    for (int q = 0; q < 4; ++q) {
+      norm_partial<16>(w + 16 * q, h[q], l[q]);
+      for (int k = 0; k < 16; ++k) v[q][k] = half2_bits_to_float2(w[16 * q + k] ^ smask[16 * q + k]);
+      fwht32(v[q]);
     }
+    float h1[4], l1[4];
+    for (int q = 0; q < 4; ++q) {
+      h1[q] = h[q];
+      l1[q] = l[q];
+      twosum_merge(h1[q], l1[q], h[q ^ 1], l[q ^ 1]);
+    }
+    float hs = h1[0], ls = l1[0];
+    twosum_merge(hs, ls, h1[2], l1[2]);
+    const float n = norm_from_sum(hs, ls, w);
+    for (int stage = 1; stage <= 2; stage *= 2) {  // index bit 5 (q ^ 1), then bit 6 (q ^ 2)
+      float2 prev[4][16];
+      std::memcpy(prev, v, sizeof(prev));
+      for (int q = 0; q < 4; ++q)
+        for (int k = 0; k < 16; ++k) v[q][k] = butterfly_pair(prev[q][k], prev[q ^ stage][k], (q & stage) != 0);
+    }
+    const float inv = n > 0.0f ? frcp(fmul(n, kSqrtD)) : 0.0f;
+    uint32_t* out = words + static_cast<size_t>(r) * cb->bits * 4;
+    for (int q = 0; q < 4; ++q) {
+      switch (cb->bits) {
+        case 2: pack_codes32<2>(v[q], inv, lut, 1, a, out + 2 * q); break;
+        case 3: pack_codes32<3>(v[q], inv, lut, 1, a, out + 3 * q); break;
+        default: pack_codes32<4>(v[q], inv, lut, 1, a, out + 4 * q); break;
+      }
+    }
+    norms[r] = n;
   }
   return TQ_OK;
 }
