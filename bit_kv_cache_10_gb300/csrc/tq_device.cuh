@@ -219,6 +219,25 @@ TQ_HD void twosum_merge(float& h, float& l, float h2, float l2) {
 // r = (h + l) - n^2 (n^2 split exactly with an FMA) decides between n and its
 // neighbours by comparison with the rounding midpoints.  When r is within
 // 2^-30 S of a midpoint the exact integer sum decides (ties to even).
+// Rare path of norm_from_sum (the float residual cannot tell n from a
+// neighbour): compare the exact integer sum of squares with the squared
+// midpoints.  Kept out of line so that the per-token loops stay small.
+#ifdef __CUDACC__
+static __host__ __device__ __noinline__
+#else
+static inline
+#endif
+float norm_near_midpoint(float n, const uint32_t* row) {
+  const float n_up = bitsf(fbits(n) + 1u), n_dn = bitsf(fbits(n) - 1u);
+  const float u_up = fsub(n_up, n), u_dn = fsub(n, n_dn);
+  const unsigned __int128 se = exact_sum_squares(row);
+  const int cu = compare_square(se, static_cast<double>(n) + 0.5 * static_cast<double>(u_up));
+  if (cu > 0 || (cu == 0 && (fbits(n_up) & 1u) == 0)) return n_up;
+  const int cd = compare_square(se, static_cast<double>(n) - 0.5 * static_cast<double>(u_dn));
+  if (cd < 0 || (cd == 0 && (fbits(n_dn) & 1u) == 0)) return n_dn;
+  return n;
+}
+
 TQ_HD float norm_from_sum(float h, float l, const uint32_t* row) {
   const float s_approx = fadd(h, l);
   if (!(s_approx > 0.0f)) return 0.0f;  // all zero (squares are >= 0)
@@ -238,12 +257,7 @@ TQ_HD float norm_from_sum(float h, float l, const uint32_t* row) {
     if (r < -t_dn) return n_dn;
     return n;
   }
-  const unsigned __int128 se = exact_sum_squares(row);
-  const int cu = compare_square(se, static_cast<double>(n) + 0.5 * static_cast<double>(u_up));
-  if (cu > 0 || (cu == 0 && (fbits(n_up) & 1u) == 0)) return n_up;
-  const int cd = compare_square(se, static_cast<double>(n) - 0.5 * static_cast<double>(u_dn));
-  if (cd < 0 || (cd == 0 && (fbits(n_dn) & 1u) == 0)) return n_dn;
-  return n;
+  return norm_near_midpoint(n, row);
 }
 
 // Correctly rounded float32 norm of 128 fp16 values in one thread.

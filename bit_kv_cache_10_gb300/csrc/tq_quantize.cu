@@ -61,8 +61,10 @@ struct Job {
 
 __device__ __forceinline__ Job decode_job(const QuantParams& p, long long j) {
   Job jb;
-  jb.tensor = static_cast<int>(j % p.tensors);
-  long long r = j / p.tensors;
+  // tensor-major order: at any moment nearly all warps run the same code width
+  const long long per_tensor = p.jobs / p.tensors;
+  jb.tensor = static_cast<int>(j / per_tensor);
+  long long r = j - jb.tensor * per_tensor;
   jb.tile = static_cast<int>(r % p.tiles_per_row);
   r /= p.tiles_per_row;
   jb.h = static_cast<int>(r % p.heads);
