@@ -44,11 +44,12 @@
 namespace tq {
 namespace {
 
-constexpr int kWarps = 16;
+constexpr int kWarps = 12;
 constexpr int kThreads = kWarps * 32;
 constexpr int kTile = 16;
 constexpr int kCopies = 16;                 // pair-table copies (one per lane of a half-warp)
 constexpr int kSmemBudget = 227 * 1024;
+constexpr float kLazy = 8.0f;               // log2 headroom of the lazily raised softmax maximum
 
 struct DecodeParams {
   const uint16_t* q;
@@ -72,14 +73,6 @@ struct DecodeParams {
   float* out;     // [B, Hq, D]
 };
 
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-  const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem));
-}
-__device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
-  const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(s), "l"(gmem));
-}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
@@ -207,7 +200,7 @@ struct Cfg {
   static constexpr int kRowShift = kFp16K ? 7 : 8;
   static constexpr int kTabBits = kFp16K ? 2 * VB : 2 * (VB > kKBits ? VB : kKBits);
   static constexpr int kTab = (1 << kTabBits) << kRowShift;
-  static constexpr int kWts = 18 * 32;  // per warp: (w, w) x 4 heads per token, padded rows
+  static constexpr int kWts = kTile * 32;  // per warp: (w, w) x 4 heads per token
   static constexpr int kSmall = kWarps * kWts + 4 * D * 4 /* q' */ + 4 * D * 4 /* combine */ +
                                 kWarps * 4 * 2 * 4 /* warp (m, l) */ + kWarps * 4 * 16 /* tile descriptors */ +
                                 (kMaxDecodeBatch + 1) * 8 + 34 * 8;
@@ -231,22 +224,51 @@ struct SmemLayout {
   }
 };
 
-// Lane window of 8*BITS code bits starting at bit 8*BITS*r of a token record.
-template <int BITS>
-__device__ __forceinline__ uint32_t code_window(const uint8_t* rec, int r) {
-  if constexpr (BITS == 4) {
-    return reinterpret_cast<const uint32_t*>(rec)[r];
-  } else if constexpr (BITS == 2) {
-    return reinterpret_cast<const uint32_t*>(rec)[r >> 1] >> ((r & 1) * 16);
-  } else {
-    const int w = (3 * r) >> 2;  // bit 24 r
-    const uint32_t* wd = reinterpret_cast<const uint32_t*>(rec) + w;
-    return __funnelshift_r(wd[0], wd[1], (24 * r) & 31);
-  }
+// ---- lane maps --------------------------------------------------------------
+// K phase: lane = 8 s + rr; token slot s (0..3) and 16 coordinates per lane,
+// as 8 coordinate pairs.  Packed 4- and 2-bit K: coordinates 16 rr .. 16 rr + 15
+// (one aligned 64- or 32-bit load per token).  Packed 3-bit and fp16 K: two
+// chunks, 8 rr .. 8 rr + 7 and 64 + 8 rr .. 64 + 8 rr + 7 (equal bit shifts in
+// both chunks for 3-bit; consecutive 16-byte chunks per quarter-warp for fp16).
+template <int KB>
+__device__ __forceinline__ int k_pair_coord(int rr, int pr) {
+  if constexpr (KB == 4 || KB == 2) return 16 * rr + 2 * pr;
+  else return (pr >> 2) * 64 + 8 * rr + 2 * (pr & 3);
+}
+// Tile token of K step u (0..3) in slot s.  For 48-byte (3-bit) records the
+// four tokens of a step start 8 banks apart, so that the window loads of the
+// whole warp are conflict free; other widths take four consecutive tokens.
+template <int KB>
+__device__ __forceinline__ constexpr int k_token(int u, int s) {
+  return KB == 3 ? 8 * (u >> 1) + (u & 1) + 2 * s : 4 * u + s;
+}
+// Byte offset of the K-phase lane's first window word within a staged K tile.
+template <int KB>
+__device__ __forceinline__ uint32_t k_lane_offset(int s, int rr) {
+  constexpr int kRec = KB == 16 ? 256 : KB * 16;
+  const uint32_t tok = static_cast<uint32_t>(k_token<KB>(0, s) * kRec);
+  if constexpr (KB == 16) return tok + 16u * rr;
+  else if constexpr (KB == 4) return tok + 8u * rr;
+  else if constexpr (KB == 2) return tok + 4u * rr;
+  else return tok + 4u * ((3 * rr) >> 2);
+}
+// V phase: lane = 16 g + r, coordinates 8 r .. 8 r + 7, token 2 u + g at step u.
+template <int VB>
+__device__ __forceinline__ uint32_t v_lane_offset(int g, int r) {
+  const uint32_t tok = static_cast<uint32_t>(g * VB * 16);
+  if constexpr (VB == 4) return tok + 4u * r;
+  else if constexpr (VB == 2) return tok + 4u * (r >> 1);
+  else return tok + 4u * ((3 * r) >> 2);
+}
+template <int VB>
+__device__ __forceinline__ uint32_t v_lane_shift(int r) {
+  if constexpr (VB == 4) return 0u;
+  else if constexpr (VB == 2) return 16u * (r & 1);
+  else return (24u * r) & 31u;
 }
 
-// Shared address of the table entry of code pair K of a lane window:
-// basecopy = table base | (128 for K) | copy * 8.
+// Shared address of the table entry of code pair K (bits 2*BITS*K ..) of a
+// window: basecopy = table base | (128 for K) | copy * 8.
 template <int BITS, int K, int ROWSHIFT>
 __device__ __forceinline__ uint32_t pair_addr(uint32_t win, uint32_t basecopy) {
   if constexpr (BITS == 4 && ROWSHIFT == 8) {
@@ -273,6 +295,12 @@ __device__ __forceinline__ uint32_t lds32(uint32_t base) {
   return v;
 }
 template <int OFF>
+__device__ __forceinline__ uint2 lds64u(uint32_t base) {
+  uint2 v;
+  asm("ld.shared.v2.u32 {%0, %1}, [%2+%3];\n" : "=r"(v.x), "=r"(v.y) : "r"(base), "n"(OFF));
+  return v;
+}
+template <int OFF>
 __device__ __forceinline__ uint4 lds128(uint32_t base) {
   uint4 v;
   asm("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4+%5];\n" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(base), "n"(OFF));
@@ -291,59 +319,112 @@ __device__ __forceinline__ float2 lds64f(uint32_t base) {
   return v;
 }
 
-// Per-lane part of a code-window address (bytes from the start of a tile's
-// token-record block) and the shift that aligns the lane's first code.
-template <int BITS>
-__device__ __forceinline__ uint32_t window_lane_offset(int g, int r) {
-  const uint32_t tok = 8u * g * (BITS * 16);
-  if constexpr (BITS == 4) return tok + 4u * r;
-  else if constexpr (BITS == 2) return tok + 4u * (r >> 1);
-  else return tok + 4u * ((3 * r) >> 2);
+// Issue cursor: the tile a warp stages next, advanced by the warp stride
+// without searching the tile list again.
+struct Cursor {
+  int b, h, x;              // sequence, KV head, tile index within the (b, h) rows
+  int ce, len, tc, per_h;   // cold end, length, cold tiles, tiles of one head
+};
+__device__ __forceinline__ void cursor_seq(const DecodeParams& p, Cursor& c) {
+  const SeqTiles s = seq_tiles(p, c.b);
+  c.ce = s.ce;
+  c.len = s.len;
+  c.tc = s.tc;
+  c.per_h = s.tc + s.th;
 }
-template <int BITS>
-__device__ __forceinline__ uint32_t window_lane_shift(int r) {
-  if constexpr (BITS == 4) return 0u;
-  else if constexpr (BITS == 2) return 16u * (r & 1);
-  else return (24u * r) & 31u;
+__device__ __forceinline__ Cursor cursor_at(const DecodeParams& p, const long long* prefix, long long t) {
+  const TileInfo ti = tile_info(p, prefix, t);
+  Cursor c;
+  c.b = ti.b;
+  c.h = ti.h;
+  cursor_seq(p, c);
+  c.x = ti.hot ? c.tc + (ti.t_begin - c.ce) / kTile : ti.t_begin / kTile;
+  return c;
 }
-// Code window of step U: 8*BITS bits of token 8g + U for this lane.
-template <int BITS, int U>
-__device__ __forceinline__ uint32_t window_at(uint32_t base, uint32_t sh) {
-  constexpr int kRec = BITS * 16;
-  if constexpr (BITS == 4) {
-    return lds32<U * kRec>(base);
-  } else if constexpr (BITS == 2) {
-    return lds32<U * kRec>(base) >> sh;
-  } else {
-    return __funnelshift_r(lds32<U * kRec>(base), lds32<U * kRec + 4>(base), sh);
+__device__ __forceinline__ void cursor_advance(const DecodeParams& p, Cursor& c, int n) {
+  c.x += n;
+  while (c.x >= c.per_h) {  // per_h is 0 for empty sequences
+    c.x -= c.per_h;
+    if (++c.h == p.hkv) {
+      c.h = 0;
+      if (++c.b >= p.batch) return;  // past the tile list: never staged
+      cursor_seq(p, c);
+    }
   }
+}
+
+// 2^x with the hardware approximation (flushes results below 2^-126 to zero).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// 16-byte cp.async at a shared and a global register base plus the same
+// compile-time byte offset.
+template <int OFF>
+__device__ __forceinline__ void cp_async16_at(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0+%2], [%1+%2], 16;\n" ::"r"(dst), "l"(src), "n"(OFF));
+}
+__device__ __forceinline__ void cp_async16s(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src));
+}
+__device__ __forceinline__ void cp_async4s(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(dst), "l"(src));
+}
+// Copies `bytes` (a multiple of 16, at most 32 * 16 * N) from src to dst with the
+// 32 lanes of a warp; full 512-byte rounds are unrolled with immediate offsets.
+template <int BYTES>
+__device__ __forceinline__ void copy_full(uint32_t dst, const uint8_t* src, int lane) {
+  constexpr int kChunks = BYTES / 16, kRounds = kChunks / 32, kRest = kChunks % 32;
+  const uint32_t d = dst + 16u * lane;
+  const uint8_t* sp = src + 16 * lane;
+  static_assert(kRounds <= 8, "tile larger than 8 rounds");
+  if constexpr (kRounds > 0) cp_async16_at<0>(d, sp);
+  if constexpr (kRounds > 1) cp_async16_at<512>(d, sp);
+  if constexpr (kRounds > 2) cp_async16_at<1024>(d, sp);
+  if constexpr (kRounds > 3) cp_async16_at<1536>(d, sp);
+  if constexpr (kRounds > 4) cp_async16_at<2048>(d, sp);
+  if constexpr (kRounds > 5) cp_async16_at<2560>(d, sp);
+  if constexpr (kRounds > 6) cp_async16_at<3072>(d, sp);
+  if constexpr (kRounds > 7) cp_async16_at<3584>(d, sp);
+  if constexpr (kRest > 0)
+    if (lane < kRest) cp_async16_at<kRounds * 512>(d, sp);
 }
 
 template <int KB, int VB>
-__device__ __forceinline__ void stage_tile(const DecodeParams& p, const TileInfo& ti, uint8_t* buf, int lane) {
+__device__ __forceinline__ void stage_tile(const DecodeParams& p, int b, int h, bool hot, int t_begin, int n_valid,
+                                           uint32_t buf, int lane) {
   using C = Cfg<KB, VB>;
-  const int64_t row0 = (static_cast<int64_t>(ti.b) * p.hkv + ti.h) * p.cap + ti.t_begin;
-  constexpr int kChunksK = C::kKRow / 16;
+  const int64_t row0 = (static_cast<int64_t>(b) * p.hkv + h) * p.cap + t_begin;
   const uint8_t* ksrc = C::kFp16K ? reinterpret_cast<const uint8_t*>(p.k_fp16 + row0 * D)
                                   : reinterpret_cast<const uint8_t*>(p.k_words + row0 * (C::kKBits * 4));
-  for (int c = lane; c < ti.n_valid * kChunksK; c += 32) cp_async16(buf + c * 16, ksrc + c * 16);
-  if (!C::kFp16K && lane < ti.n_valid) cp_async4(buf + C::kKTile + lane * 4, p.k_norms + row0 + lane);
-  if (!ti.hot) {
-    constexpr int kChunksV = C::kVRow / 16;
-    uint8_t* vb = buf + C::kKTile + C::kKNorm;
-    const uint8_t* vsrc = reinterpret_cast<const uint8_t*>(p.v_words + row0 * (VB * 4));
-    for (int c = lane; c < ti.n_valid * kChunksV; c += 32) cp_async16(vb + c * 16, vsrc + c * 16);
-    if (lane < ti.n_valid) cp_async4(vb + C::kVTile + lane * 4, p.v_norms + row0 + lane);
+  const uint8_t* vsrc = reinterpret_cast<const uint8_t*>(p.v_words + row0 * (VB * 4));
+  const uint32_t vbuf = buf + C::kKTile + C::kKNorm;
+  if (n_valid == kTile) {
+    copy_full<C::kKTile>(buf, ksrc, lane);
+    if (!hot) copy_full<C::kVTile>(vbuf, vsrc, lane);
+  } else {
+    for (int c = lane; c < n_valid * (C::kKRow / 16); c += 32) cp_async16s(buf + 16u * c, ksrc + 16 * c);
+    if (!hot)
+      for (int c = lane; c < n_valid * (C::kVRow / 16); c += 32) cp_async16s(vbuf + 16u * c, vsrc + 16 * c);
   }
+  // norms: lanes 0..15 the K norms, lanes 16..31 the V norms of the tile's tokens
+  const int nl = lane & 15;
+  const bool is_k = lane < 16;
+  const bool want = nl < n_valid && (is_k ? !C::kFp16K : !hot);
+  const float* nsrc = (is_k ? p.k_norms : p.v_norms) + row0 + nl;
+  const uint32_t ndst = (is_k ? buf + C::kKTile : vbuf + C::kVTile) + 4u * nl;
+  if (want) cp_async4s(ndst, nsrc);
 }
 
-// Split kernel.  Lane = 16 g + r: token group g (tokens 8g..8g+7 of a 16-token
-// tile, one per step), coordinates 8r..8r+7 (code pairs k = 0..3).
+// Split kernel.
 template <int G, int KB, int VB>
 __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeParams p) {
   using C = Cfg<KB, VB>;
   constexpr int S = C::kStages;
   constexpr int kRS = C::kRowShift;
+  constexpr int GH = G >= 2 ? G / 2 : 1;  // heads whose scores a K-phase lane owns after the butterfly
   extern __shared__ __align__(16) uint8_t smem[];
   const uint32_t s0 = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
   SmemLayout lay;
@@ -361,7 +442,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
   uint8_t* wts_all = ptr(lay.take(kWarps * C::kWts));
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g = lane >> 4, r = lane & 15;
+  const int s = lane >> 3, rr = lane & 7;   // K phase
+  const int g = lane >> 4, r = lane & 15;   // V phase
   const uint32_t copy8 = static_cast<uint32_t>(r) * 8u;
   const uint32_t vbase = tab | copy8;
   const uint32_t kbase = tab | 128u | copy8;
@@ -410,27 +492,45 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
   uint8_t* const wring = ptr(ring);
   uint8_t* wts = wts_all + warp * C::kWts;
   int4* descs = descs_all + warp * 4;
-  const int my_n = static_cast<int>((t1 - t0 - warp + kWarps - 1) / kWarps);  // tiles t0 + warp + 16 j
+  const int my_n = static_cast<int>((t1 - t0 - warp + kWarps - 1) / kWarps);  // tiles t0 + warp + kWarps j
   int j_issue = 0, j = 0;
+  Cursor cur;
+  if (my_n > 0) cur = cursor_at(p, prefix, t0 + warp);
   auto issue = [&]() {
     if (j_issue < my_n) {
-      const TileInfo ti = tile_info(p, prefix, t0 + warp + static_cast<long long>(kWarps) * j_issue);
-      stage_tile<KB, VB>(p, ti, wring + (j_issue % S) * C::kBuf, lane);
-      if (lane == 0) descs[j_issue % S] = make_int4(ti.b, ti.h | (ti.hot << 16), ti.t_begin, ti.n_valid);
+      const bool hot = cur.x >= cur.tc;
+      const int t_begin = hot ? cur.ce + (cur.x - cur.tc) * kTile : cur.x * kTile;
+      const int n_valid = min(kTile, (hot ? cur.len : cur.ce) - t_begin);
+      stage_tile<KB, VB>(p, cur.b, cur.h, hot, t_begin, n_valid, ring + static_cast<uint32_t>((j_issue % S) * C::kBuf), lane);
+      if (lane == 0) descs[j_issue % S] = make_int4(cur.b, cur.h | (hot << 16), t_begin, n_valid);
+      cursor_advance(p, cur, kWarps);
     }
     cp_async_commit();
     ++j_issue;
   };
 #pragma unroll
-  for (int s = 0; s < S - 1; ++s) issue();
+  for (int st = 0; st < S - 1; ++st) issue();
 
-  const uint32_t k_lane_off = C::kFp16K ? static_cast<uint32_t>(8 * g * 256 + 16 * r)
-                                        : window_lane_offset<C::kKBits>(g, r);
-  const uint32_t k_lane_sh = window_lane_shift<C::kKBits>(r);
-  const uint32_t v_lane_off = window_lane_offset<VB>(g, r);
-  const uint32_t v_lane_sh = window_lane_shift<VB>(r);
+  // The butterfly is free of selects: bit 2 of rr picks which of a step pair a lane
+  // keeps, bit 1 which pair, bit 0 which heads (the lane's q' is stored in head order
+  // jj ^ h0), so every lane computes its steps in (keep, send) order from its own bases.
+  const int b2 = (rr >> 2) & 1, b1 = (rr >> 1) & 1;
+  auto step_off = [&](int u) {
+    return static_cast<uint32_t>((k_token<KB>(u, 0) - k_token<KB>(0, 0)) * C::kKRow);
+  };
+  const uint32_t k_off = k_lane_offset<KB>(s, rr);
+  const uint32_t k_off_kk = k_off + step_off(2 * b1 + b2), k_off_ks = k_off + step_off(2 * b1 + 1 - b2);
+  const uint32_t k_off_sk = k_off + step_off(2 * (1 - b1) + b2), k_off_ss = k_off + step_off(2 * (1 - b1) + 1 - b2);
+  const uint32_t k_sh = KB == 3 ? (24u * rr) & 31u : 0u;
+  const uint32_t v_off = v_lane_offset<VB>(g, r);
+  const uint32_t v_sh = v_lane_shift<VB>(r);
   const uint32_t wts_s = static_cast<uint32_t>(__cvta_generic_to_shared(wts));
-  float2 qr[G][4];
+  // after the butterfly a K-phase lane holds token u_own of slot s, heads h0 .. h0 + GH - 1
+  const int u_own = 2 * ((rr >> 1) & 1) + ((rr >> 2) & 1);
+  const int tau_own = k_token<KB>(u_own, s);
+  const int h0 = G >= 2 ? GH * (rr & 1) : 0;
+  const bool owner = G >= 2 || (rr & 1) == 0;  // for G = 1 lanes rr and rr ^ 1 hold the same score
+  float2 qr[G][8];
   int cur_b = -1, cur_h = -1;
   long long seg = t0;
   while (seg < t1) {
@@ -466,23 +566,27 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
 #pragma unroll
       for (int jj = 0; jj < G; ++jj)
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          qr[jj][k] = make_float2(fmul(qs[jj * D + 8 * r + 2 * k], qscale),
-                                  fmul(qs[jj * D + 8 * r + 2 * k + 1], qscale));
+        for (int pr = 0; pr < 8; ++pr) {
+          const int c = k_pair_coord<KB>(rr, pr), hh = jj ^ h0;
+          qr[jj][pr] = make_float2(fmul(qs[hh * D + c], qscale), fmul(qs[hh * D + c + 1], qscale));
+        }
       cur_b = si.b;
       cur_h = si.h;
     }
 
-    // online-softmax state of this row: m per (group, head), l per lane for its own heads
-    float m[G], lsum[G];
+    // online-softmax state of this row: maxima of the lane's own heads (equal on
+    // all lanes of the same parity), mass of the lane's own (token, head) pairs
+    float m_own[GH], lsum[GH];
     float2 acc[G][4];
 #pragma unroll
-    for (int jj = 0; jj < G; ++jj) {
-      m[jj] = -INFINITY;
-      lsum[jj] = 0.0f;
+    for (int i = 0; i < GH; ++i) {
+      m_own[i] = -INFINITY;
+      lsum[i] = 0.0f;
+    }
+#pragma unroll
+    for (int jj = 0; jj < G; ++jj)
 #pragma unroll
       for (int k = 0; k < 4; ++k) acc[jj][k] = make_float2(0.0f, 0.0f);
-    }
 
     while (j < my_n && t0 + warp + static_cast<long long>(kWarps) * j < seg_end) {
       issue();
@@ -492,195 +596,202 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
       const int tb_b = dsc.x, tb_h = dsc.y & 0xFFFF, n_valid = dsc.w, t_begin = dsc.z;
       const bool hot = (dsc.y >> 16) != 0;
       const uint8_t* tb = wring + (j % S) * C::kBuf;
-
-      // ---- scores: P[u][h] = partial over this lane's 8 coordinates of token 8g + u
       const uint32_t tbs = ring + static_cast<uint32_t>((j % S) * C::kBuf);  // shared address of the tile
-      float P[8][G];
+
+      // ---- K phase: partial scores over the lane's 16 coordinates, 4 tokens per step
+      float Ak[G], As[G];  // after butterfly stage A: the kept step pair and the sent one
       {
-        const uint32_t kw = tbs + k_lane_off;
-        auto score_step = [&](auto U_) {
-          constexpr int U = decltype(U_)::value;
-          float2 pa[G];
-#pragma unroll
-          for (int jj = 0; jj < G; ++jj) pa[jj] = make_float2(0.0f, 0.0f);
+        auto k_step = [&](uint32_t kw, float* P) {
+          constexpr int OFF = 0;
+          float2 c[8];
           if constexpr (C::kFp16K) {
-            const uint4 a0 = lds128<U * 256>(kw);
-            const uint32_t wv[4] = {a0.x, a0.y, a0.z, a0.w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const float2 kf = half2_bits_to_float2(wv[k]);
-#pragma unroll
-              for (int jj = 0; jj < G; ++jj) pa[jj] = fma2(qr[jj][k], kf, pa[jj]);
-            }
+            const uint4 a = lds128<OFF>(kw), b = lds128<OFF + 128>(kw);
+            c[0] = half2_bits_to_float2(a.x);
+            c[1] = half2_bits_to_float2(a.y);
+            c[2] = half2_bits_to_float2(a.z);
+            c[3] = half2_bits_to_float2(a.w);
+            c[4] = half2_bits_to_float2(b.x);
+            c[5] = half2_bits_to_float2(b.y);
+            c[6] = half2_bits_to_float2(b.z);
+            c[7] = half2_bits_to_float2(b.w);
+          } else if constexpr (KB == 4) {
+            const uint2 wv = lds64u<OFF>(kw);
+            c[0] = lds64(pair_addr<4, 0, kRS>(wv.x, kbase));
+            c[1] = lds64(pair_addr<4, 1, kRS>(wv.x, kbase));
+            c[2] = lds64(pair_addr<4, 2, kRS>(wv.x, kbase));
+            c[3] = lds64(pair_addr<4, 3, kRS>(wv.x, kbase));
+            c[4] = lds64(pair_addr<4, 0, kRS>(wv.y, kbase));
+            c[5] = lds64(pair_addr<4, 1, kRS>(wv.y, kbase));
+            c[6] = lds64(pair_addr<4, 2, kRS>(wv.y, kbase));
+            c[7] = lds64(pair_addr<4, 3, kRS>(wv.y, kbase));
+          } else if constexpr (KB == 3) {
+            const uint32_t wa = __funnelshift_r(lds32<OFF>(kw), lds32<OFF + 4>(kw), k_sh);
+            const uint32_t wb = __funnelshift_r(lds32<OFF + 24>(kw), lds32<OFF + 28>(kw), k_sh);
+            c[0] = lds64(pair_addr<3, 0, kRS>(wa, kbase));
+            c[1] = lds64(pair_addr<3, 1, kRS>(wa, kbase));
+            c[2] = lds64(pair_addr<3, 2, kRS>(wa, kbase));
+            c[3] = lds64(pair_addr<3, 3, kRS>(wa, kbase));
+            c[4] = lds64(pair_addr<3, 0, kRS>(wb, kbase));
+            c[5] = lds64(pair_addr<3, 1, kRS>(wb, kbase));
+            c[6] = lds64(pair_addr<3, 2, kRS>(wb, kbase));
+            c[7] = lds64(pair_addr<3, 3, kRS>(wb, kbase));
           } else {
-            const uint32_t win = window_at<C::kKBits, U>(kw, k_lane_sh);
-            const float2 c0 = lds64(pair_addr<C::kKBits, 0, kRS>(win, kbase));
-            const float2 c1 = lds64(pair_addr<C::kKBits, 1, kRS>(win, kbase));
-            const float2 c2 = lds64(pair_addr<C::kKBits, 2, kRS>(win, kbase));
-            const float2 c3 = lds64(pair_addr<C::kKBits, 3, kRS>(win, kbase));
-#pragma unroll
-            for (int jj = 0; jj < G; ++jj) {
-              pa[jj] = fma2(qr[jj][0], c0, pa[jj]);
-              pa[jj] = fma2(qr[jj][1], c1, pa[jj]);
-              pa[jj] = fma2(qr[jj][2], c2, pa[jj]);
-              pa[jj] = fma2(qr[jj][3], c3, pa[jj]);
-            }
+            const uint32_t wv = lds32<OFF>(kw);
+            c[0] = lds64(pair_addr<2, 0, kRS>(wv, kbase));
+            c[1] = lds64(pair_addr<2, 1, kRS>(wv, kbase));
+            c[2] = lds64(pair_addr<2, 2, kRS>(wv, kbase));
+            c[3] = lds64(pair_addr<2, 3, kRS>(wv, kbase));
+            c[4] = lds64(pair_addr<2, 4, kRS>(wv, kbase));
+            c[5] = lds64(pair_addr<2, 5, kRS>(wv, kbase));
+            c[6] = lds64(pair_addr<2, 6, kRS>(wv, kbase));
+            c[7] = lds64(pair_addr<2, 7, kRS>(wv, kbase));
           }
 #pragma unroll
-          for (int jj = 0; jj < G; ++jj) P[U][jj] = fadd(pa[jj].x, pa[jj].y);
+          for (int jj = 0; jj < G; ++jj) {
+            float2 pa = mul2(qr[jj][0], c[0]);
+#pragma unroll
+            for (int pr = 1; pr < 8; ++pr) pa = fma2(qr[jj][pr], c[pr], pa);
+            P[jj] = fadd(pa.x, pa.y);
+          }
         };
-        score_step(std::integral_constant<int, 0>{});
-        score_step(std::integral_constant<int, 1>{});
-        score_step(std::integral_constant<int, 2>{});
-        score_step(std::integral_constant<int, 3>{});
-        score_step(std::integral_constant<int, 4>{});
-        score_step(std::integral_constant<int, 5>{});
-        score_step(std::integral_constant<int, 6>{});
-        score_step(std::integral_constant<int, 7>{});
+        // stage A of the butterfly: the partner (rr ^ 4) sends what this lane keeps
+        auto stage_a = [&](const float* Pk, const float* Ps, float* A) {
+#pragma unroll
+          for (int jj = 0; jj < G; ++jj) A[jj] = fadd(Pk[jj], __shfl_xor_sync(0xffffffffu, Ps[jj], 4));
+        };
+        {
+          float Pk[G], Ps[G];
+          k_step(tbs + k_off_kk, Pk);
+          k_step(tbs + k_off_ks, Ps);
+          stage_a(Pk, Ps, Ak);
+        }
+        {
+          float Pk[G], Ps[G];
+          k_step(tbs + k_off_sk, Pk);
+          k_step(tbs + k_off_ss, Ps);
+          stage_a(Pk, Ps, As);
+        }
       }
-      // ---- transposing butterfly over the 16 lanes of a group:
-      // bits 3, 2, 1 of r select the token (u = r >> 1), bit 0 the head pair
-      float v8[4][G], v4[2][G], v2[G], s2[2];
+      // ---- stages B (rr ^ 2, step pairs) and C (rr ^ 1, head pairs) of the butterfly
+      float sc[GH];
       {
-        const bool up = (r & 8) != 0;
+        float B[G];
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
+        for (int jj = 0; jj < G; ++jj) B[jj] = fadd(Ak[jj], __shfl_xor_sync(0xffffffffu, As[jj], 2));
+        if constexpr (G >= 2) {
 #pragma unroll
-          for (int jj = 0; jj < G; ++jj) {
-            const float send = up ? P[k][jj] : P[k + 4][jj];
-            const float keep = up ? P[k + 4][jj] : P[k][jj];
-            v8[k][jj] = fadd(keep, __shfl_xor_sync(0xffffffffu, send, 8));
+          for (int i = 0; i < GH; ++i) sc[i] = fadd(B[i], __shfl_xor_sync(0xffffffffu, B[GH + i], 1));
+        } else {
+          sc[0] = fadd(B[0], __shfl_xor_sync(0xffffffffu, B[0], 1));
+        }
+      }
+      // ---- online softmax over the tile (base 2; log2 e is folded into q').  The
+      // running maximum of a head is raised only when a score exceeds it by more
+      // than kLazy, so most tiles need neither the cross-lane maximum nor a rescale
+      // (weights stay below 2^kLazy).
+      const float nk = C::kFp16K ? 1.0f : reinterpret_cast<const float*>(tb + C::kKTile)[tau_own];
+      const float nv = hot ? 1.0f : reinterpret_cast<const float*>(tb + C::kKTile + C::kKNorm + C::kVTile)[tau_own];
+      const bool full = n_valid == kTile;  // warp-uniform
+      const bool valid = tau_own < n_valid;
+      float sj[GH];
+      bool bump = false;
+#pragma unroll
+      for (int i = 0; i < GH; ++i) {
+        sj[i] = fmul(sc[i], nk);
+        if (!full) sj[i] = valid ? sj[i] : -INFINITY;  // staged data of masked rows is stale
+        bump |= sj[i] > fadd(m_own[i], kLazy);
+      }
+      if (__any_sync(0xffffffffu, bump)) {
+        float alpha[G];
+#pragma unroll
+        for (int i = 0; i < GH; ++i) {
+          float tm = sj[i];
+          tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 2));
+          tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 4));
+          tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 8));
+          tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 16));
+          const float mn = fmaxf(m_own[i], tm);  // finite: every staged tile has a valid token
+          const float al = ex2_approx(fsub(m_own[i], mn));  // 0 for the first tile of the row
+          lsum[i] = fmul(lsum[i], al);
+          m_own[i] = mn;
+          if constexpr (G >= 2) {
+            const float oa = __shfl_xor_sync(0xffffffffu, al, 1);  // head (h0 + i) ^ GH
+            const bool hi = (rr & 1) != 0;
+            alpha[i] = hi ? oa : al;
+            alpha[GH + i] = hi ? al : oa;
+          } else {
+            alpha[0] = al;
           }
-      }
-      {
-        const bool up = (r & 4) != 0;
-#pragma unroll
-        for (int k = 0; k < 2; ++k)
-#pragma unroll
-          for (int jj = 0; jj < G; ++jj) {
-            const float send = up ? v8[k][jj] : v8[k + 2][jj];
-            const float keep = up ? v8[k + 2][jj] : v8[k][jj];
-            v4[k][jj] = fadd(keep, __shfl_xor_sync(0xffffffffu, send, 4));
-          }
-      }
-      {
-        const bool up = (r & 2) != 0;
-#pragma unroll
-        for (int jj = 0; jj < G; ++jj) {
-          const float send = up ? v4[0][jj] : v4[1][jj];
-          const float keep = up ? v4[1][jj] : v4[0][jj];
-          v2[jj] = fadd(keep, __shfl_xor_sync(0xffffffffu, send, 2));
         }
-      }
-      // lane now holds the 4 head scores of token u = r >> 1 (summed over lanes r, r^1 still)
-      constexpr int GH = G >= 2 ? G / 2 : 1;  // heads kept per lane after the last stage
-      if constexpr (G >= 2) {
-        const bool up = (r & 1) != 0;
-#pragma unroll
-        for (int q2 = 0; q2 < GH; ++q2) {
-          const float send = up ? v2[q2] : v2[q2 + GH];
-          const float keep = up ? v2[q2 + GH] : v2[q2];
-          s2[q2] = fadd(keep, __shfl_xor_sync(0xffffffffu, send, 1));
-        }
-      } else {
-        s2[0] = fadd(v2[0], __shfl_xor_sync(0xffffffffu, v2[0], 1));
-      }
-      // ---- online softmax per 8-token group.  Lane (g, r) owns token 8g + (r >> 1)
-      // and heads h0 = GH * (r & 1) .. h0 + GH - 1 (for G = 1 both lanes of a pair own head 0).
-      const int u_own = r >> 1;
-      const int h0 = G >= 2 ? GH * (r & 1) : 0;
-      const bool valid = 8 * g + u_own < n_valid;
-      const float nk = C::kFp16K ? 1.0f : reinterpret_cast<const float*>(tb + C::kKTile)[8 * g + u_own];
-      const float nv = hot ? 1.0f : reinterpret_cast<const float*>(tb + C::kKTile + C::kKNorm + C::kVTile)[8 * g + u_own];
-      float alpha_own[GH], w_own[GH];
-      bool rescale = false;
-#pragma unroll
-      for (int q2 = 0; q2 < GH; ++q2) {
-        const int jj = h0 + q2;
-        const float sj = valid ? fmul(s2[q2], nk) : -INFINITY;
-        float gm = sj;
-        gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 2));
-        gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 4));
-        gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 8));
-        float m_old = m[0];
-#pragma unroll
-        for (int t = 1; t < G; ++t)
-          if (t == jj) m_old = m[t];
-        const float mn = fmaxf(m_old, gm);
-        const float al = mn == -INFINITY ? 1.0f : exp2f(m_old - mn);
-        const float pj = valid ? exp2f(sj - mn) : 0.0f;
-        lsum[q2] = ffma(lsum[q2], al, pj);  // lsum[q2]: this lane's head h0 + q2
-        alpha_own[q2] = al;
-        w_own[q2] = valid ? fmul(pj, nv) : 0.0f;  // staged norms of masked rows are garbage
-        s2[q2] = mn;  // from here on: the new maximum of head h0 + q2
-      }
-      // exchange with the partner lane (other head pair) so every lane has all G maxima / alphas
-      float alpha[G];
-      if constexpr (G >= 2) {
-#pragma unroll
-        for (int q2 = 0; q2 < GH; ++q2) {
-          const float om = __shfl_xor_sync(0xffffffffu, s2[q2], 1);
-          const float oa = __shfl_xor_sync(0xffffffffu, alpha_own[q2], 1);
-          const bool hi = (r & 1) != 0;
-          m[q2] = hi ? om : s2[q2];
-          m[q2 + GH] = hi ? s2[q2] : om;
-          alpha[q2] = hi ? oa : alpha_own[q2];
-          alpha[q2 + GH] = hi ? alpha_own[q2] : oa;
-        }
-      } else {
-        m[0] = s2[0];
-        alpha[0] = alpha_own[0];
-      }
-#pragma unroll
-      for (int jj = 0; jj < G; ++jj) rescale |= alpha[jj] != 1.0f;
-      // weights (w, w) of token 8g + u_own, heads h0.. : padded row 8g + u_own + g
-      if ((r & 1) == 0 || G >= 2) {
-        float2* wrow = reinterpret_cast<float2*>(wts + (8 * g + u_own + g) * 32) + h0;
-#pragma unroll
-        for (int q2 = 0; q2 < GH; ++q2) wrow[q2] = make_float2(w_own[q2], w_own[q2]);
-      }
-      if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
         for (int jj = 0; jj < G; ++jj)
 #pragma unroll
           for (int k = 0; k < 4; ++k) acc[jj][k] = mul2(acc[jj][k], make_float2(alpha[jj], alpha[jj]));
       }
+      float w_own[GH];
+#pragma unroll
+      for (int i = 0; i < GH; ++i) {
+        const float pj = ex2_approx(fsub(sj[i], m_own[i]));  // 0 for masked rows
+        lsum[i] = fadd(lsum[i], (G >= 2 || owner) ? pj : 0.0f);
+        w_own[i] = fmul(pj, nv);
+        if (!full) w_own[i] = valid ? w_own[i] : 0.0f;
+      }
+      // weights (w, w) of token tau_own, heads h0.. : row tau_own of 32 bytes
+      if constexpr (G == 4) {
+        *reinterpret_cast<float4*>(wts + tau_own * 32 + h0 * 8) = make_float4(w_own[0], w_own[0], w_own[1], w_own[1]);
+      } else if constexpr (G == 2) {
+        *reinterpret_cast<float2*>(wts + tau_own * 32 + h0 * 8) = make_float2(w_own[0], w_own[0]);
+      } else {
+        if (owner) *reinterpret_cast<float2*>(wts + tau_own * 32) = make_float2(w_own[0], w_own[0]);
+      }
       __syncwarp();
 
-      // ---- V accumulation for tokens 8g + u
-      const uint32_t wsb = wts_s + static_cast<uint32_t>(9 * g * 32);  // padded row 8g + u + g
-      const uint32_t vw = tbs + static_cast<uint32_t>(C::kKTile + C::kKNorm) + v_lane_off;
-      auto v_step = [&](auto U_) {
+      // ---- V phase: tokens 2u + g, 8 coordinates per lane
+      const uint32_t wsb = wts_s + static_cast<uint32_t>(g * 32);
+      const uint32_t vw = tbs + static_cast<uint32_t>(C::kKTile + C::kKNorm) + v_off;
+      auto load_w = [&](auto U_, float2* w2) {
         constexpr int U = decltype(U_)::value;
-        const int tau = 8 * g + U;
-        float2 w2[G];
         if constexpr (G == 4) {
-          const float4 a = lds128f<U * 32>(wsb), b2 = lds128f<U * 32 + 16>(wsb);
+          const float4 a = lds128f<U * 64>(wsb), b2 = lds128f<U * 64 + 16>(wsb);
           w2[0] = make_float2(a.x, a.y);
           w2[1] = make_float2(a.z, a.w);
           w2[2] = make_float2(b2.x, b2.y);
           w2[3] = make_float2(b2.z, b2.w);
         } else if constexpr (G == 2) {
-          const float4 a = lds128f<U * 32>(wsb);
+          const float4 a = lds128f<U * 64>(wsb);
           w2[0] = make_float2(a.x, a.y);
           w2[G - 1] = make_float2(a.z, a.w);
         } else {
-          w2[0] = lds64f<U * 32>(wsb);
+          w2[0] = lds64f<U * 64>(wsb);
         }
-        if (!hot) {
-          const uint32_t win = window_at<VB, U>(vw, v_lane_sh);
-          const float2 c0 = lds64(pair_addr<VB, 0, kRS>(win, vbase));
-          const float2 c1 = lds64(pair_addr<VB, 1, kRS>(win, vbase));
-          const float2 c2 = lds64(pair_addr<VB, 2, kRS>(win, vbase));
-          const float2 c3 = lds64(pair_addr<VB, 3, kRS>(win, vbase));
+      };
+      auto v_cold = [&](auto U_) {
+        constexpr int U = decltype(U_)::value;
+        constexpr int kVRec = VB * 16;
+        float2 w2[G];
+        load_w(U_, w2);
+        uint32_t win;
+        if constexpr (VB == 4) win = lds32<U * 2 * kVRec>(vw);
+        else if constexpr (VB == 2) win = lds32<U * 2 * kVRec>(vw) >> v_sh;
+        else win = __funnelshift_r(lds32<U * 2 * kVRec>(vw), lds32<U * 2 * kVRec + 4>(vw), v_sh);
+        const float2 c0 = lds64(pair_addr<VB, 0, kRS>(win, vbase));
+        const float2 c1 = lds64(pair_addr<VB, 1, kRS>(win, vbase));
+        const float2 c2 = lds64(pair_addr<VB, 2, kRS>(win, vbase));
+        const float2 c3 = lds64(pair_addr<VB, 3, kRS>(win, vbase));
 #pragma unroll
-          for (int jj = 0; jj < G; ++jj) {
-            acc[jj][0] = fma2(w2[jj], c0, acc[jj][0]);
-            acc[jj][1] = fma2(w2[jj], c1, acc[jj][1]);
-            acc[jj][2] = fma2(w2[jj], c2, acc[jj][2]);
-            acc[jj][3] = fma2(w2[jj], c3, acc[jj][3]);
-          }
-        } else if (tau < n_valid) {
+        for (int jj = 0; jj < G; ++jj) {
+          acc[jj][0] = fma2(w2[jj], c0, acc[jj][0]);
+          acc[jj][1] = fma2(w2[jj], c1, acc[jj][1]);
+          acc[jj][2] = fma2(w2[jj], c2, acc[jj][2]);
+          acc[jj][3] = fma2(w2[jj], c3, acc[jj][3]);
+        }
+      };
+      auto v_hot = [&](auto U_) {
+        constexpr int U = decltype(U_)::value;
+        const int tau = 2 * U + g;
+        float2 w2[G];
+        load_w(U_, w2);
+        if (tau < n_valid) {
           const int pos = t_begin + tau;
           const uint4 a0 = reinterpret_cast<const uint4*>(
               p.v_ring + ((static_cast<int64_t>(tb_b) * p.hkv + tb_h) * p.hot + pos % p.hot) * D)[r];
@@ -693,48 +804,61 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
           }
         }
       };
-      v_step(std::integral_constant<int, 0>{});
-      v_step(std::integral_constant<int, 1>{});
-      v_step(std::integral_constant<int, 2>{});
-      v_step(std::integral_constant<int, 3>{});
-      v_step(std::integral_constant<int, 4>{});
-      v_step(std::integral_constant<int, 5>{});
-      v_step(std::integral_constant<int, 6>{});
-      v_step(std::integral_constant<int, 7>{});
+      if (!hot) {
+        v_cold(std::integral_constant<int, 0>{});
+        v_cold(std::integral_constant<int, 1>{});
+        v_cold(std::integral_constant<int, 2>{});
+        v_cold(std::integral_constant<int, 3>{});
+        v_cold(std::integral_constant<int, 4>{});
+        v_cold(std::integral_constant<int, 5>{});
+        v_cold(std::integral_constant<int, 6>{});
+        v_cold(std::integral_constant<int, 7>{});
+      } else {
+        v_hot(std::integral_constant<int, 0>{});
+        v_hot(std::integral_constant<int, 1>{});
+        v_hot(std::integral_constant<int, 2>{});
+        v_hot(std::integral_constant<int, 3>{});
+        v_hot(std::integral_constant<int, 4>{});
+        v_hot(std::integral_constant<int, 5>{});
+        v_hot(std::integral_constant<int, 6>{});
+        v_hot(std::integral_constant<int, 7>{});
+      }
       __syncwarp();
       ++j;
     }
 
     // ---- leave the row: lanes -> warp -> CTA, one partial per (CTA, row)
     for (int i = tid; i < G * D; i += kThreads) comb[i] = 0.0f;
-    float mw[G];
+    float mw[G];  // warp maxima of all heads
+    if constexpr (G >= 2) {
+      const bool hi = (rr & 1) != 0;
 #pragma unroll
-    for (int jj = 0; jj < G; ++jj) {
-      const float mx = fmaxf(m[jj], __shfl_xor_sync(0xffffffffu, m[jj], 16));
-      const float sc = m[jj] == -INFINITY ? 0.0f : exp2f(m[jj] - mx);
+      for (int i = 0; i < GH; ++i) {
+        const float om = __shfl_xor_sync(0xffffffffu, m_own[i], 1);
+        mw[i] = hi ? om : m_own[i];
+        mw[GH + i] = hi ? m_own[i] : om;
+      }
+    } else {
+      mw[0] = m_own[0];
+    }
+#pragma unroll
+    for (int jj = 0; jj < G; ++jj)
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        float2 a = mul2(acc[jj][k], make_float2(sc, sc));
+        float2 a = acc[jj][k];
         a.x = fadd(a.x, __shfl_xor_sync(0xffffffffu, a.x, 16));
         a.y = fadd(a.y, __shfl_xor_sync(0xffffffffu, a.y, 16));
         acc[jj][k] = a;
       }
-      mw[jj] = mx;
-    }
-    // softmax mass: lane (g, r) holds heads h0.. of its own tokens, scaled to its group max
     {
-      const int h0 = G >= 2 ? (G / 2) * (r & 1) : 0;
       float lw[G];
 #pragma unroll
       for (int jj = 0; jj < G; ++jj) lw[jj] = 0.0f;
-      constexpr int GH = G >= 2 ? G / 2 : 1;
 #pragma unroll
-      for (int q2 = 0; q2 < GH; ++q2) {
+      for (int i = 0; i < GH; ++i)
 #pragma unroll
         for (int jj = 0; jj < G; ++jj)
-          if (jj == h0 + q2) lw[jj] = m[jj] == -INFINITY ? 0.0f : fmul(lsum[q2], exp2f(m[jj] - mw[jj]));
-      }
-      if (G == 1 && (r & 1)) lw[0] = 0.0f;  // both lanes of a pair hold the same token for G = 1
+          if (jj == h0 + i) lw[jj] = lsum[i];
 #pragma unroll
       for (int jj = 0; jj < G; ++jj) {
 #pragma unroll
@@ -753,11 +877,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
         float mm = -INFINITY;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) mm = fmaxf(mm, wml[(w * 4 + jj) * 2]);
-        const float sc = exp2f(mw[jj] - mm);
+        const float sc2 = exp2f(mw[jj] - mm);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          atomicAdd(&comb[jj * D + 8 * r + 2 * k], fmul(acc[jj][k].x, sc));
-          atomicAdd(&comb[jj * D + 8 * r + 2 * k + 1], fmul(acc[jj][k].y, sc));
+          atomicAdd(&comb[jj * D + 8 * r + 2 * k], fmul(acc[jj][k].x, sc2));
+          atomicAdd(&comb[jj * D + 8 * r + 2 * k + 1], fmul(acc[jj][k].y, sc2));
         }
       }
     }
