@@ -44,7 +44,7 @@
 namespace tq {
 namespace {
 
-constexpr int kWarps = 12;
+constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kTile = 16;
 constexpr int kCopies = 16;                 // pair-table copies (one per lane of a half-warp)
@@ -202,12 +202,12 @@ struct Cfg {
   static constexpr int kTab = (1 << kTabBits) << kRowShift;
   static constexpr int kWts = kTile * 32;  // per warp: (w, w) x 4 heads per token
   static constexpr int kSmall = kWarps * kWts + 4 * D * 4 /* q' */ + 4 * D * 4 /* combine */ +
-                                kWarps * 4 * 2 * 4 /* warp (m, l) */ + kWarps * 4 * 16 /* tile descriptors */ +
+                                kWarps * 4 * 2 * 4 /* warp (m, l) */ + kWarps * 8 * 16 /* tile descriptors */ +
                                 (kMaxDecodeBatch + 1) * 8 + 34 * 8;
   // the aligned table can leave a gap of up to kTab - 1024 bytes before it (shared
   // windows start at a 1 KB multiple); buffers are placed around the table
   static constexpr int kWorst(int stages) { return kTab + kSmall + (kWarps + 1) * stages * kBuf + 1024; }
-  static constexpr int kStages = kWorst(4) <= kSmemBudget ? 4 : kWorst(3) <= kSmemBudget ? 3 : 2;
+  static constexpr int kStages = kWorst(8) <= kSmemBudget ? 8 : kWorst(6) <= kSmemBudget ? 6 : kWorst(4) <= kSmemBudget ? 4 : kWorst(3) <= kSmemBudget ? 3 : 2;
   static constexpr int kSmem = kSmemBudget;
   static_assert(kWorst(kStages) <= kSmemBudget, "shared memory budget");
 };
@@ -436,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
   float* qs = reinterpret_cast<float*>(ptr(lay.take(4 * D * 4)));
   float* comb = reinterpret_cast<float*>(ptr(lay.take(4 * D * 4)));
   float* wml = reinterpret_cast<float*>(ptr(lay.take(kWarps * 4 * 2 * 4)));
-  int4* descs_all = reinterpret_cast<int4*>(ptr(lay.take(kWarps * 4 * 16)));
+  int4* descs_all = reinterpret_cast<int4*>(ptr(lay.take(kWarps * 8 * 16)));
   long long* prefix = reinterpret_cast<long long*>(ptr(lay.take((kMaxDecodeBatch + 1) * 8)));
   long long* scan = reinterpret_cast<long long*>(ptr(lay.take(34 * 8)));
   uint8_t* wts_all = ptr(lay.take(kWarps * C::kWts));
@@ -491,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
   }
   uint8_t* const wring = ptr(ring);
   uint8_t* wts = wts_all + warp * C::kWts;
-  int4* descs = descs_all + warp * 4;
+  int4* descs = descs_all + warp * 8;
   const int my_n = static_cast<int>((t1 - t0 - warp + kWarps - 1) / kWarps);  // tiles t0 + warp + kWarps j
   int j_issue = 0, j = 0;
   Cursor cur;
