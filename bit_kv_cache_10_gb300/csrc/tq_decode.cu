@@ -646,13 +646,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
             c[6] = lds64(pair_addr<2, 6, kRS>(wv, kbase));
             c[7] = lds64(pair_addr<2, 7, kRS>(wv, kbase));
           }
+          // heads interleaved: consecutive packed FMAs are independent
+          float2 pa[G];
 #pragma unroll
-          for (int jj = 0; jj < G; ++jj) {
-            float2 pa = mul2(qr[jj][0], c[0]);
+          for (int jj = 0; jj < G; ++jj) pa[jj] = mul2(qr[jj][0], c[0]);
 #pragma unroll
-            for (int pr = 1; pr < 8; ++pr) pa = fma2(qr[jj][pr], c[pr], pa);
-            P[jj] = fadd(pa.x, pa.y);
-          }
+          for (int pr = 1; pr < 8; ++pr)
+#pragma unroll
+            for (int jj = 0; jj < G; ++jj) pa[jj] = fma2(qr[jj][pr], c[pr], pa[jj]);
+#pragma unroll
+          for (int jj = 0; jj < G; ++jj) P[jj] = fadd(pa[jj].x, pa[jj].y);
         };
         // stage A of the butterfly: the partner (rr ^ 4) sends what this lane keeps
         auto stage_a = [&](const float* Pk, const float* Ps, float* A) {
