@@ -8,29 +8,30 @@
 // one contiguous, equal range per CTA, so that every SM gets the same number
 // of tiles whatever the lengths are.
 //
-// Split kernel: one CTA of 16 warps per SM (128 registers per thread).  The
+// Split kernel: one CTA of 8 warps per SM (up to 255 registers per thread).  The
 // codebook pair tables are built once per CTA in shared memory (16 copies, one
 // per lane of a half-warp, so the data-dependent lookups are bank-conflict
 // free), at a base aligned to the table size so that a lookup address is one
 // PRMT (4-bit codes) or one shift and one masked OR.  Warp w takes tiles
-// t0 + w, t0 + w + 16, ... of the CTA's range and streams them through a 3-4
-// stage cp.async ring that runs across row boundaries.  Inside a warp 16 lanes
-// share a token and each owns 8 coordinates; 2 tokens are in flight per step
-// and 8 steps cover the tile:
-//   score:   partial sum_i q'[h][i] c[code_i] over the lane's 8 coordinates
-//            for the G query heads of the group, with the two codes of a
-//            coordinate pair looked up at once in a (c_a, c_b) table; a
-//            transposing butterfly over the 16 lanes leaves each lane with
-//            the full scores of one token for half of the heads;
-//   softmax: online, per 8-token group, in base 2 (log2 e is folded into q');
-//   V:       acc[h][i] += p_h n_V c[code_i] in the rotated domain (cold rows)
-//            or += p_h v_i with the raw fp16 V (hot rows, original domain).
+// t0 + w, t0 + w + 8, ... of the CTA's range and streams them through a cp.async
+// ring of up to 8 tiles that runs across row boundaries.  Per tile:
+//   scores:  8 lanes share a token, each owning 16 coordinates (8 code pairs,
+//            each looked up at once as (c_a, c_b)); 4 tokens per step, 4 steps.
+//            Partial sums over the lane's coordinates for the G query heads,
+//            then a 3-stage transposing butterfly over the 8 lanes leaves each
+//            lane with the full scores of one token for G/2 heads;
+//   softmax: online over the tile in base 2 (log2 e is folded into q'); the
+//            running maximum is raised lazily (only when a score exceeds it by
+//            more than 2^8), so most tiles need no cross-lane maximum or rescale;
+//   V:       16 lanes share a token, each owning 8 coordinates; 2 tokens per
+//            step, 8 steps: acc[h][i] += p_h n_V c[code_i] in the rotated domain
+//            (cold rows) or += p_h v_i with the raw fp16 V (hot rows).
 // When the CTA leaves a row it combines its warps and writes one partial
 // (acc, max, sum) to workspace slot (CTA index + row index): these slots are
 // distinct for all (CTA, row) pairs because both indices only grow along the
 // tile list.  All arithmetic is float32 (packed pairs where possible).
 //
-// Merge kernel: one CTA per (sequence, query head): finds the CTAs that
+// Merge kernel: one warp per (sequence, query head): finds the CTAs that
 // covered its cold and hot rows, log-sum-exp combines their partials, rotates
 // the cold sum back once (D_h H / sqrt(d)), adds the hot sum and divides by
 // the softmax mass.
@@ -915,22 +916,38 @@ __device__ __forceinline__ int cta_of(long long t, long long total, int grid) {
 }
 __device__ __forceinline__ long long cta_start(int c, long long total, int grid) { return total * c / grid; }
 
-__global__ void __launch_bounds__(D) decode_merge_kernel(const DecodeParams p) {
-  __shared__ float y[D];
-  __shared__ long long prefix[kMaxDecodeBatch + 1];
-  __shared__ long long scan[34];
-  const int hq = blockIdx.x, b = blockIdx.y, t = threadIdx.x;
-  const int g = p.hq / p.hkv, h = hq / g, jj = hq - h * g;
-  float* out = p.out + (static_cast<int64_t>(b) * p.hq + hq) * D;
-  tile_prefix<D>(p, prefix, scan);
-  const long long total = prefix[p.batch];
+// Merge kernel: one warp per (sequence b, query head), the G warps of a CTA
+// sharing the KV head h.  Lane l holds coordinates 4 l .. 4 l + 3: it finds the
+// CTAs that covered the (b, h) rows, log-sum-exp combines their partials, rotates
+// the cold sum back (sign flips and a Hadamard transform over index bits 0..1 in
+// registers and 2..6 across lanes, 1/sqrt d), adds the hot sum and divides by the
+// softmax mass.
+__global__ void __launch_bounds__(4 * 32) decode_merge_kernel(const DecodeParams p) {
+  const int g = p.hq / p.hkv;
+  const int jj = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.x, b = blockIdx.y;
+  if (jj >= g) return;
+  float4* out = reinterpret_cast<float4*>(p.out + (static_cast<int64_t>(b) * p.hq + h * g + jj) * D);
+  // tiles of the sequences before b, and of all sequences
+  long long before = 0, total = 0;
+  for (int bb = lane; bb < p.batch; bb += 32) {
+    const SeqTiles sq = seq_tiles(p, bb);
+    const long long c = static_cast<long long>(p.hkv) * (sq.tc + sq.th);
+    total += c;
+    if (bb < b) before += c;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    before += __shfl_xor_sync(0xffffffffu, before, o);
+    total += __shfl_xor_sync(0xffffffffu, total, o);
+  }
   const SeqTiles st = seq_tiles(p, b);
   if (st.len == 0) {
-    out[t] = 0.0f;
+    out[lane] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     return;
   }
   const int per_h = st.tc + st.th;
-  const long long hbase = prefix[b] + static_cast<long long>(h) * per_h;
+  const long long hbase = before + static_cast<long long>(h) * per_h;
   // rows of this (b, h): cold [hbase, hbase + tc), hot [hbase + tc, hbase + per_h)
   float mm = -INFINITY;
   for (int kind = 0; kind < 2; ++kind) {
@@ -942,7 +959,8 @@ __global__ void __launch_bounds__(D) decode_merge_kernel(const DecodeParams p) {
       mm = fmaxf(mm, p.ws_ml[((static_cast<long long>(c) + row) * g + jj) * 2]);
     }
   }
-  float cold = 0.0f, hotv = 0.0f, l = 0.0f;
+  float y[4] = {0.0f, 0.0f, 0.0f, 0.0f}, hv[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  float l = 0.0f;
   for (int kind = 0; kind < 2; ++kind) {
     const long long rs = kind ? hbase + st.tc : hbase, re = kind ? hbase + per_h : hbase + st.tc;
     if (re <= rs) continue;
@@ -954,26 +972,40 @@ __global__ void __launch_bounds__(D) decode_merge_kernel(const DecodeParams p) {
       if (ms == -INFINITY) continue;
       const float sc = exp2f(ms - mm);
       l = ffma(p.ws_ml[(slot * g + jj) * 2 + 1], sc, l);
-      const float a = p.ws_acc[(slot * g + jj) * D + t];
-      if (kind) hotv = ffma(a, sc, hotv);
-      else cold = ffma(a, sc, cold);
+      const float4 a = reinterpret_cast<const float4*>(p.ws_acc + (slot * g + jj) * D)[lane];
+      const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (kind) hv[i] = ffma(av[i], sc, hv[i]);
+        else y[i] = ffma(av[i], sc, y[i]);
+      }
     }
   }
-  // inverse rotation of the cold sum: D_h H y / sqrt(d)
-  y[t] = cold;
-  __syncthreads();
-#pragma unroll
-  for (int s = 1; s < D; s *= 2) {
-    float v = 0.0f;
-    if ((t & s) == 0) v = fadd(y[t], y[t + s]);
-    else v = fsub(y[t - s], y[t]);
-    __syncthreads();
-    y[t] = v;
-    __syncthreads();
+  // inverse rotation of the cold sum: D_h H y / sqrt(d), index t = 4 lane + i
+  {
+    float a0 = fadd(y[0], y[1]), a1 = fsub(y[0], y[1]), a2 = fadd(y[2], y[3]), a3 = fsub(y[2], y[3]);  // bit 0
+    y[0] = fadd(a0, a2);  // bit 1
+    y[2] = fsub(a0, a2);
+    y[1] = fadd(a1, a3);
+    y[3] = fsub(a1, a3);
   }
-  float v = fmul(y[t], 1.0f / kSqrtD);
-  if (sign_negative(p.seed, p.layer, h, t)) v = -v;
-  out[t] = fadd(v, hotv) / l;
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {  // bits 2..6
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float o = __shfl_xor_sync(0xffffffffu, y[i], m);
+      y[i] = upper ? fsub(o, y[i]) : fadd(y[i], o);
+    }
+  }
+  float r[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float v = fmul(y[i], 1.0f / kSqrtD);
+    if (sign_negative(p.seed, p.layer, h, 4 * lane + i)) v = -v;
+    r[i] = fadd(v, hv[i]) / l;
+  }
+  out[lane] = make_float4(r[0], r[1], r[2], r[3]);
 }
 
 int sm_count() {
@@ -1077,7 +1109,7 @@ extern "C" tq_status tq_decode_attention(const tq_cache_desc* d, const void* q, 
     default: st = dispatch_kb<4>(p, kb, d->v_bits, s); break;
   }
   if (st != TQ_OK) return st;
-  decode_merge_kernel<<<dim3(d->num_q_heads, d->batch), D, 0, s>>>(p);
+  decode_merge_kernel<<<dim3(d->num_kv_heads, d->batch), 4 * 32, 0, s>>>(p);
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 

@@ -229,6 +229,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) quantize_append_kernel(const Q
         const int row = 8 * step + vrow;
         int pos = 0;
         const bool have = src_row(p, jb, row, &pos) != nullptr;
+        if (!__any_sync(0xffffffffu, have)) break;  // rows are filled in order: no later step has one
         const int64_t ridx = rowbase + pos;
         const bool to_copy = copy_k || (!k_tensor && pos >= cold_end);
         if (to_copy && have) {
