@@ -260,37 +260,6 @@ TQ_HD float norm_from_sum(float h, float l, const uint32_t* row) {
   return norm_near_midpoint(n, row);
 }
 
-// Correctly rounded float32 norm of 128 fp16 values in one thread.
-TQ_HD float exact_norm(const uint32_t* w) {
-  float h, l;
-  norm_partial<64>(w, h, l);
-  return norm_from_sum(h, l, w);
-}
-
-// ---------------------------------------------------------------------------
-// Walsh-Hadamard transform of 128 floats held as 64 float2 (natural order)
-// ---------------------------------------------------------------------------
-
-TQ_HD void fwht128(float2* v) {
-  // index bit 0: inside each pair
-#pragma unroll
-  for (int j = 0; j < 64; ++j) {
-    const float a = v[j].x, b = v[j].y;
-    v[j] = make_float2(fadd(a, b), fsub(a, b));
-  }
-  // index bits 1..6: between pairs, two butterflies per packed op
-#pragma unroll
-  for (int hb = 1; hb < 64; hb *= 2) {
-#pragma unroll
-    for (int j = 0; j < 64; ++j) {
-      if (j & hb) continue;
-      const float2 a = v[j], b = v[j + hb];
-      v[j] = add2(a, b);
-      v[j + hb] = sub2(a, b);
-    }
-  }
-}
-
 // ---------------------------------------------------------------------------
 // Threshold lookup: code = #{k : t_k <= y} through buckets RN(y * A)
 // ---------------------------------------------------------------------------
