@@ -442,6 +442,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
   long long* scan = reinterpret_cast<long long*>(ptr(lay.take(34 * 8)));
   uint8_t* wts_all = ptr(lay.take(kWarps * C::kWts));
 
+  // the merge grid may be launched now; it waits for this grid's completion
+  asm volatile("griddepcontrol.launch_dependents;\n");
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int s = lane >> 3, rr = lane & 7;   // K phase
   const int g = lane >> 4, r = lane & 15;   // V phase
@@ -948,37 +950,60 @@ __global__ void __launch_bounds__(4 * 32) decode_merge_kernel(const DecodeParams
   }
   const int per_h = st.tc + st.th;
   const long long hbase = before + static_cast<long long>(h) * per_h;
-  // rows of this (b, h): cold [hbase, hbase + tc), hot [hbase + tc, hbase + per_h)
-  float mm = -INFINITY;
-  for (int kind = 0; kind < 2; ++kind) {
-    const long long rs = kind ? hbase + st.tc : hbase, re = kind ? hbase + per_h : hbase + st.tc;
-    if (re <= rs) continue;
-    const int row = (b * p.hkv + h) * 2 + kind;
-    for (int c = cta_of(rs, total, p.grid); c <= cta_of(re - 1, total, p.grid); ++c) {
-      if (cta_start(c, total, p.grid) == cta_start(c + 1, total, p.grid)) continue;  // empty CTA range
-      mm = fmaxf(mm, p.ws_ml[((static_cast<long long>(c) + row) * g + jj) * 2]);
-    }
+  // rows of this (b, h): cold [hbase, hbase + tc), hot [hbase + tc, hbase + per_h);
+  // partial i < n0 comes from cold CTA c0 + i, partial n0 + i from hot CTA c1 + i
+  int c0 = 0, n0 = 0, c1 = 0, n1 = 0;
+  if (st.tc > 0) {
+    c0 = cta_of(hbase, total, p.grid);
+    n0 = cta_of(hbase + st.tc - 1, total, p.grid) - c0 + 1;
   }
-  float y[4] = {0.0f, 0.0f, 0.0f, 0.0f}, hv[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-  float l = 0.0f;
-  for (int kind = 0; kind < 2; ++kind) {
-    const long long rs = kind ? hbase + st.tc : hbase, re = kind ? hbase + per_h : hbase + st.tc;
-    if (re <= rs) continue;
-    const int row = (b * p.hkv + h) * 2 + kind;
-    for (int c = cta_of(rs, total, p.grid); c <= cta_of(re - 1, total, p.grid); ++c) {
-      if (cta_start(c, total, p.grid) == cta_start(c + 1, total, p.grid)) continue;
-      const long long slot = static_cast<long long>(c) + row;
-      const float ms = p.ws_ml[(slot * g + jj) * 2];
-      if (ms == -INFINITY) continue;
-      const float sc = exp2f(ms - mm);
-      l = ffma(p.ws_ml[(slot * g + jj) * 2 + 1], sc, l);
-      const float4 a = reinterpret_cast<const float4*>(p.ws_acc + (slot * g + jj) * D)[lane];
-      const float av[4] = {a.x, a.y, a.z, a.w};
+  if (st.th > 0) {
+    c1 = cta_of(hbase + st.tc, total, p.grid);
+    n1 = cta_of(hbase + per_h - 1, total, p.grid) - c1 + 1;
+  }
+  const int row0 = (b * p.hkv + h) * 2;
+  auto slot_of = [&](int i) {
+    return i < n0 ? static_cast<long long>(c0 + i) + row0 : static_cast<long long>(c1 + i - n0) + row0 + 1;
+  };
+  auto live = [&](int i) {  // a CTA with an empty range wrote no partial
+    const int c = i < n0 ? c0 + i : c1 + i - n0;
+    return cta_start(c, total, p.grid) != cta_start(c + 1, total, p.grid);
+  };
+  const int n = n0 + n1;
+  const unsigned live32 = __ballot_sync(0xffffffffu, lane < n && live(lane));
+  auto is_live = [&](int i) { return i < 32 ? ((live32 >> i) & 1u) != 0 : live(i); };
+  // the partials are written by the split kernel: wait for it (programmatic
+  // dependent launch lets this grid start while the split kernel finishes)
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  // (max, mass) of the partials, one per lane, then across the warp
+  float mm = -INFINITY;
+  for (int i = lane; i < n; i += 32)
+    if (is_live(i)) mm = fmaxf(mm, p.ws_ml[(slot_of(i) * g + jj) * 2]);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        if (kind) hv[i] = ffma(av[i], sc, hv[i]);
-        else y[i] = ffma(av[i], sc, y[i]);
-      }
+  for (int o = 16; o > 0; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
+  float l = 0.0f;
+  for (int i = lane; i < n; i += 32) {
+    if (!is_live(i)) continue;
+    const float ms = p.ws_ml[(slot_of(i) * g + jj) * 2];
+    if (ms != -INFINITY) l = ffma(p.ws_ml[(slot_of(i) * g + jj) * 2 + 1], exp2f(ms - mm), l);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) l = fadd(l, __shfl_xor_sync(0xffffffffu, l, o));
+  // accumulators, partial by partial (independent loads)
+  float y[4] = {0.0f, 0.0f, 0.0f, 0.0f}, hv[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll 4
+  for (int i = 0; i < n; ++i) {
+    if (!is_live(i)) continue;
+    const long long slot = slot_of(i);
+    const float ms = p.ws_ml[(slot * g + jj) * 2];
+    if (ms == -INFINITY) continue;
+    const float sc = exp2f(ms - mm);
+    const float4 a = reinterpret_cast<const float4*>(p.ws_acc + (slot * g + jj) * D)[lane];
+    const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (i >= n0) hv[k] = ffma(av[k], sc, hv[k]);
+      else y[k] = ffma(av[k], sc, y[k]);
     }
   }
   // inverse rotation of the cold sum: D_h H y / sqrt(d), index t = 4 lane + i
@@ -1109,7 +1134,19 @@ extern "C" tq_status tq_decode_attention(const tq_cache_desc* d, const void* q, 
     default: st = dispatch_kb<4>(p, kb, d->v_bits, s); break;
   }
   if (st != TQ_OK) return st;
-  decode_merge_kernel<<<dim3(d->num_kv_heads, d->batch), 4 * 32, 0, s>>>(p);
+  // programmatic dependent launch: the merge grid is scheduled as the split
+  // kernel's CTAs retire and waits (griddepcontrol.wait) for its completion
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(d->num_kv_heads, d->batch);
+  cfg.blockDim = dim3(4 * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, decode_merge_kernel, p) != cudaSuccess) return TQ_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 

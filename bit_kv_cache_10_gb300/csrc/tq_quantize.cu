@@ -59,16 +59,18 @@ struct Job {
   int count;           // rows this sequence appends
 };
 
-__device__ __forceinline__ Job decode_job(const QuantParams& p, long long j) {
+__device__ __forceinline__ Job decode_job(const QuantParams& p, long long jl) {
+  // 32-bit index arithmetic: the host keeps the job count below 2^31
+  const int j = static_cast<int>(jl);
   Job jb;
   // tensor-major order: at any moment nearly all warps run the same code width
-  const long long per_tensor = p.jobs / p.tensors;
-  jb.tensor = static_cast<int>(j / per_tensor);
-  long long r = j - jb.tensor * per_tensor;
-  jb.tile = static_cast<int>(r % p.tiles_per_row);
-  r /= p.tiles_per_row;
-  jb.h = static_cast<int>(r % p.heads);
-  jb.b = static_cast<int>(r / p.heads);
+  const int per_tensor = static_cast<int>(p.jobs) / p.tensors;
+  jb.tensor = j >= per_tensor ? 1 : 0;
+  int r = j - jb.tensor * per_tensor;
+  const int rt = r / p.tiles_per_row;
+  jb.tile = r - rt * p.tiles_per_row;
+  jb.b = rt / p.heads;
+  jb.h = rt - jb.b * p.heads;
   const int s = p.start_pos[jb.b];
   const int cnt = p.num_new != nullptr ? p.num_new[jb.b] : p.n_new;
   jb.valid = s >= 0 && cnt >= 0 && cnt <= p.n_new && static_cast<long long>(s) + cnt <= p.cap;
@@ -188,17 +190,24 @@ __global__ void __launch_bounds__(kWarps * 32, 1) quantize_append_kernel(const Q
   uint8_t* tiles = warp_area + warp * (2 * kTileBytes + 256);
   uint32_t* smask = reinterpret_cast<uint32_t*>(tiles + 2 * kTileBytes);
 
-  // threshold lookup tables, kLutCopies interleaved copies (entry j of copy c at j*copies + c)
-  for (int i = threadIdx.x; i < lut_k_n * kLutCopies; i += blockDim.x)
-    lut_k[i] = lut_entry(p.k_thr, (1 << p.k_bits) - 1, p.k_lut_a, i / kLutCopies);
-  for (int i = threadIdx.x; i < lut_v_n * kLutCopies; i += blockDim.x)
-    lut_v[i] = lut_entry(p.v_thr, (1 << p.v_bits) - 1, p.v_lut_a, i / kLutCopies);
+  // threshold lookup tables, kLutCopies interleaved copies (entry j of copy c at
+  // j*copies + c): each entry is computed once and written to its copies
+  for (int j = threadIdx.x; j < lut_k_n + lut_v_n; j += blockDim.x) {
+    const bool is_k = j < lut_k_n;
+    const LutEntry e = is_k ? lut_entry(p.k_thr, (1 << p.k_bits) - 1, p.k_lut_a, j)
+                            : lut_entry(p.v_thr, (1 << p.v_bits) - 1, p.v_lut_a, j - lut_k_n);
+    uint4* dst = reinterpret_cast<uint4*>(lut_k + j * kLutCopies);  // lut_v follows lut_k
+    const uint4 two = make_uint4(__float_as_uint(e.thr), e.base, __float_as_uint(e.thr), e.base);
+#pragma unroll
+    for (int c = 0; c < kLutCopies / 2; ++c) dst[c] = two;
+  }
   __syncthreads();
   const LutEntry* my_lut_k = lut_k + (lane & (kLutCopies - 1));
   const LutEntry* my_lut_v = lut_v + (lane & (kLutCopies - 1));
 
+  // job j goes to CTA j mod grid: small appends put one job per SM
   const long long stride = static_cast<long long>(gridDim.x) * kWarps;
-  long long j = static_cast<long long>(blockIdx.x) * kWarps + warp;
+  long long j = static_cast<long long>(warp) * gridDim.x + blockIdx.x;
   int buf = 0;
   if (j < p.jobs) issue_tile(p, j, tiles, lane);
   cp_async_commit();
@@ -283,8 +292,7 @@ tq_status launch_quantize(QuantParams& p, cudaStream_t stream) {
     return TQ_ERR_CUDA;
   const int sms = sm_count();
   if (sms <= 0) return TQ_ERR_CUDA;
-  const long long want = (p.jobs + kWarps - 1) / kWarps;
-  const int grid = static_cast<int>(want < sms ? want : sms);
+  const int grid = static_cast<int>(p.jobs < sms ? p.jobs : sms);
   quantize_append_kernel<<<grid, kWarps * 32, smem, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
@@ -306,6 +314,9 @@ extern "C" tq_status tq_quantize_append(const tq_cache_desc* d, const void* k_ne
   if (!aligned16(k_new) || !aligned16(v_new)) return TQ_ERR_INVALID_ARG;
   if (stride_b < 0 || stride_h < 0 || stride_t < 0 || (stride_b % 8) || (stride_h % 8) || (stride_t % 8))
     return TQ_ERR_INVALID_ARG;
+
+  if (static_cast<long long>(d->batch) * d->num_kv_heads * ((n_new + kTileRows - 1) / kTileRows) * 2 >= (1ll << 31))
+    return TQ_ERR_UNSUPPORTED;  // job indices are 32-bit
 
   QuantParams p;
   std::memset(&p, 0, sizeof(p));

@@ -235,6 +235,9 @@ tq_status tq_cache_buffer_bytes(const tq_cache_desc *desc, size_t *k_cache_bytes
  *
  * A start position < 0, a count outside [0, n_new] or start + count >
  * capacity sets TQ_DEV_ERR_APPEND_RANGE in d_status and skips that sequence.
+ * Before any launch: TQ_ERR_CAPACITY for n_new > capacity, TQ_ERR_UNSUPPORTED
+ * when B * Hkv * ceil(n_new / 16) * 2 reaches 2^31 (32-bit job indices),
+ * TQ_ERR_INVALID_ARG for NULL or misaligned pointers and strides.
  */
 tq_status tq_quantize_append(const tq_cache_desc *desc, const void *k_new, const void *v_new, int64_t stride_b,
                              int64_t stride_h, int64_t stride_t, int32_t n_new, const int32_t *d_start_pos,
