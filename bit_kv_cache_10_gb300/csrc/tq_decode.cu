@@ -451,15 +451,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
   const uint32_t vbase = tab | copy8;
   const uint32_t kbase = tab | 128u | copy8;
 
-  if (blockIdx.x == 0 && tid == 0 && p.status != nullptr) {
-    for (int b = 0; b < p.batch; ++b) {
-      const int len = p.seq_lens[b];
-      if (len < 0 || len > p.cap || len > p.max_seq_len) {
-        atomicOr(p.status, TQ_DEV_ERR_SEQ_LEN);
-        break;
-      }
-    }
-  }
   // pair tables: entry e = code_a | code_b << bits -> (c[code_a], c[code_b]), 16 copies per row
   if constexpr (!C::kFp16K) {
     constexpr int n = (1 << (2 * C::kKBits)) * kCopies;
@@ -475,6 +466,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
       const int e = i / kCopies, c = i % kCopies;
       *reinterpret_cast<float2*>(ptr(tab + (e << kRS) + c * 8)) =
           make_float2(p.v_cent[e & ((1 << VB) - 1)], p.v_cent[e >> VB]);
+    }
+  }
+  // launched as a programmatic dependent grid: the tables above use only the
+  // parameters; the lengths and the cache may come from the preceding grids
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  if (blockIdx.x == 0 && tid == 0 && p.status != nullptr) {
+    for (int b = 0; b < p.batch; ++b) {
+      const int len = p.seq_lens[b];
+      if (len < 0 || len > p.cap || len > p.max_seq_len) {
+        atomicOr(p.status, TQ_DEV_ERR_SEQ_LEN);
+        break;
+      }
     }
   }
   tile_prefix<kThreads>(p, prefix, scan);  // synchronizes
@@ -1046,7 +1049,17 @@ tq_status launch_split(const DecodeParams& p, cudaStream_t stream) {
   auto kern = decode_split_kernel<G, KB, VB>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) != cudaSuccess)
     return TQ_ERR_CUDA;
-  kern<<<p.grid, kThreads, C::kSmem, stream>>>(p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see griddepcontrol.wait
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return TQ_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 

@@ -179,6 +179,7 @@ __device__ __forceinline__ void quantize_step(const uint8_t* tile, int row, int 
 }
 
 __global__ void __launch_bounds__(kWarps * 32, 1) quantize_append_kernel(const QuantParams p) {
+  asm volatile("griddepcontrol.launch_dependents;\n");  // the next grid may start its prologue
   extern __shared__ __align__(16) uint8_t smem[];
   const int lut_k_n = p.k_lut_a ? lut_size(p.k_lut_a) : 0;
   const int lut_v_n = lut_size(p.v_lut_a);
@@ -202,6 +203,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1) quantize_append_kernel(const Q
     for (int c = 0; c < kLutCopies / 2; ++c) dst[c] = two;
   }
   __syncthreads();
+  // launched as a programmatic dependent grid: everything above uses only the
+  // parameters; wait here for the preceding grid (it may produce the inputs or
+  // still read the ring slots this launch overwrites)
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
   const LutEntry* my_lut_k = lut_k + (lane & (kLutCopies - 1));
   const LutEntry* my_lut_v = lut_v + (lane & (kLutCopies - 1));
 
@@ -293,7 +298,17 @@ tq_status launch_quantize(QuantParams& p, cudaStream_t stream) {
   const int sms = sm_count();
   if (sms <= 0) return TQ_ERR_CUDA;
   const int grid = static_cast<int>(p.jobs < sms ? p.jobs : sms);
-  quantize_append_kernel<<<grid, kWarps * 32, smem, stream>>>(p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kWarps * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see griddepcontrol.wait
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, quantize_append_kernel, p) != cudaSuccess) return TQ_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 
