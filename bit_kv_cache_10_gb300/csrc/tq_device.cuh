@@ -184,11 +184,11 @@ TQ_HD int compare_square(unsigned __int128 s, double m) {
 // h + l: the squares are exact in float32 and are added with TwoSum in two
 // interleaved lanes, then the lanes are merged with one more TwoSum.
 template <int N>
-TQ_HD void norm_partial(const uint32_t* w, float& h_out, float& l_out) {
+TQ_HD void norm_partial(const float2* xs, float& h_out, float& l_out) {
   float2 hi = make_float2(0.0f, 0.0f), lo = make_float2(0.0f, 0.0f);
 #pragma unroll
   for (int j = 0; j < N; ++j) {
-    const float2 x = half2_bits_to_float2(w[j]);
+    const float2 x = xs[j];  // fp16 values (or their negatives: only squares are used)
     const float2 t = mul2(x, x);       // exact: 11-bit significands
     const float2 s = add2(hi, t);      // TwoSum(hi, t)
     const float2 bb = sub2(s, hi);
@@ -306,29 +306,32 @@ TQ_HD void fwht32(float2* v) {
 }
 
 // One butterfly stage between two holders of 32 values: the lower holder keeps
-// own + other, the upper one other - own (a single rounding either way).
-TQ_HD float2 butterfly_pair(float2 own, float2 other, bool upper) {
-  return upper ? sub2(other, own) : add2(own, other);
+// own + other, the upper one other - own, as one fused multiply-add by
+// sgn = (+1, +1) or (-1, -1): RN(own * (+-1) + other) is exactly the rounded
+// sum or difference.
+TQ_HD float2 butterfly_pair(float2 own, float2 other, float2 sgn) {
+  return fma2(own, sgn, other);
 }
 
 // Codes of 32 rotated coordinates z (y = z * inv) packed LSB-first into BITS
 // words.  code = base + (y >= thr) of the bucket RN(y * A) of a lookup table
-// whose buckets hold at most one threshold (entries at lut[j * stride]); y is
-// clamped to +-(1 + 1/A), which no real coordinate reaches, so that any input
-// (even NaN) lands in the table.
+// whose buckets hold at most one threshold (entries at lut[j * stride]).  Every
+// finite coordinate has |y| <= 1 + 1/A, inside the table; the table index is
+// clamped (unsigned) to the last entry so that any other input, even NaN, still
+// reads inside the table.
 template <int BITS>
 TQ_HD void pack_codes32(const float2* z, float inv, const LutEntry* lut, int stride, int lut_a, uint32_t* words) {
   const float fa = static_cast<float>(lut_a);
-  const float lim = (fa + 1.0f) / fa;
+  const uint32_t last = static_cast<uint32_t>(lut_size(lut_a) - 1);
   const uint32_t bias = fbits(kMagic) - static_cast<uint32_t>(lut_a + 1);
   uint32_t acc[BITS];
 #pragma unroll
   for (int k = 0; k < BITS; ++k) acc[k] = 0u;
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
-    float y = fmul((i & 1) ? z[i >> 1].y : z[i >> 1].x, inv);
-    y = fminf(fmaxf(y, -lim), lim);
-    const uint32_t idx = fbits(ffma(y, fa, kMagic)) - bias;
+    const float y = fmul((i & 1) ? z[i >> 1].y : z[i >> 1].x, inv);
+    const uint32_t raw = fbits(ffma(y, fa, kMagic)) - bias;
+    const uint32_t idx = raw < last ? raw : last;
     const LutEntry e = lut[idx * stride];
     const uint32_t code = e.base + (y >= e.thr ? 1u : 0u);
     const int bit = i * BITS, word = bit >> 5, off = bit & 31;

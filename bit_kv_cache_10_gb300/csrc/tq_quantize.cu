@@ -129,15 +129,10 @@ __device__ __forceinline__ void quantize_step(const uint8_t* tile, int row, int 
                                               bool store) {
   const uint4* src = reinterpret_cast<const uint4*>(tile + row * kRowPitch) + 4 * q;
   const uint4* msk = reinterpret_cast<const uint4*>(smask) + 4 * q;
-  uint32_t w[16];
   float2 v[16];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const uint4 a = src[k], m = msk[k];
-    w[4 * k] = a.x;
-    w[4 * k + 1] = a.y;
-    w[4 * k + 2] = a.z;
-    w[4 * k + 3] = a.w;
     v[4 * k] = half2_bits_to_float2(a.x ^ m.x);
     v[4 * k + 1] = half2_bits_to_float2(a.y ^ m.y);
     v[4 * k + 2] = half2_bits_to_float2(a.z ^ m.z);
@@ -145,22 +140,23 @@ __device__ __forceinline__ void quantize_step(const uint8_t* tile, int row, int 
   }
   // norm: per-lane partial sums, merged over the 4 lanes of the vector (q ^ 1, then q ^ 2)
   float h, l;
-  norm_partial<16>(w, h, l);
+  norm_partial<16>(v, h, l);  // squares of the sign-flipped values
   twosum_merge(h, l, __shfl_xor_sync(0xffffffffu, h, 8), __shfl_xor_sync(0xffffffffu, l, 8));
   twosum_merge(h, l, __shfl_xor_sync(0xffffffffu, h, 16), __shfl_xor_sync(0xffffffffu, l, 16));
   const float n = norm_from_sum(h, l, reinterpret_cast<const uint32_t*>(tile + row * kRowPitch));
   // rotation: in-lane bits 0..4, then bits 5 (q ^ 1) and 6 (q ^ 2) across lanes
   fwht32(v);
+  // pairs are exchanged as 64-bit values, so each lands in a register pair
+  const float s1 = (q & 1) ? -1.0f : 1.0f, s2 = (q & 2) ? -1.0f : 1.0f;
+  auto xchg = [](float2 a, int m) {
+    const unsigned long long u = (static_cast<unsigned long long>(__float_as_uint(a.y)) << 32) | __float_as_uint(a.x);
+    const unsigned long long o = __shfl_xor_sync(0xffffffffu, u, m);
+    return make_float2(__uint_as_float(static_cast<uint32_t>(o)), __uint_as_float(static_cast<uint32_t>(o >> 32)));
+  };
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const float2 o = make_float2(__shfl_xor_sync(0xffffffffu, v[j].x, 8), __shfl_xor_sync(0xffffffffu, v[j].y, 8));
-    v[j] = butterfly_pair(v[j], o, (q & 1) != 0);
-  }
+  for (int j = 0; j < 16; ++j) v[j] = butterfly_pair(v[j], xchg(v[j], 8), make_float2(s1, s1));
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const float2 o = make_float2(__shfl_xor_sync(0xffffffffu, v[j].x, 16), __shfl_xor_sync(0xffffffffu, v[j].y, 16));
-    v[j] = butterfly_pair(v[j], o, (q & 2) != 0);
-  }
+  for (int j = 0; j < 16; ++j) v[j] = butterfly_pair(v[j], xchg(v[j], 16), make_float2(s2, s2));
   const float inv = n > 0.0f ? frcp(fmul(n, kSqrtD)) : 0.0f;
   uint32_t words[BITS];
   pack_codes32<BITS>(v, inv, lut, kLutCopies, lut_a, words);
@@ -407,8 +403,8 @@ extern "C" tq_status tq_debug_quantize_rows_host(const tq_codebook* cb, uint64_t
     float h[4], l[4];
     float2 v[4][16];
     for (int q = 0; q < 4; ++q) {
-      norm_partial<16>(w + 16 * q, h[q], l[q]);
       for (int k = 0; k < 16; ++k) v[q][k] = half2_bits_to_float2(w[16 * q + k] ^ smask[16 * q + k]);
+      norm_partial<16>(v[q], h[q], l[q]);
       fwht32(v[q]);
     }
     float h1[4], l1[4];
@@ -424,7 +420,10 @@ extern "C" tq_status tq_debug_quantize_rows_host(const tq_codebook* cb, uint64_t
       float2 prev[4][16];
       std::memcpy(prev, v, sizeof(prev));
       for (int q = 0; q < 4; ++q)
-        for (int k = 0; k < 16; ++k) v[q][k] = butterfly_pair(prev[q][k], prev[q ^ stage][k], (q & stage) != 0);
+        for (int k = 0; k < 16; ++k) {
+          const float sg = (q & stage) ? -1.0f : 1.0f;
+          v[q][k] = butterfly_pair(prev[q][k], prev[q ^ stage][k], make_float2(sg, sg));
+        }
     }
     const float inv = n > 0.0f ? frcp(fmul(n, kSqrtD)) : 0.0f;
     uint32_t* out = words + static_cast<size_t>(r) * cb->bits * 4;
