@@ -44,6 +44,9 @@ KB, VB = 3, 4
 LO, HI = 65536, 131072
 QB, QT = 16, 8192  # quantize workload: batch x new tokens (8 KV heads)
 FALLBACK_HBM_GBS = 6800.0
+WORKLOAD = ("long-context 3.5-bit decode: B4, 32q/8kv heads, d128, L~U[65536,131072] (+1 per step), "
+            "K 3-bit packed, V 4-bit packed + 256-token fp16 hot window; step = append 1 token per "
+            "sequence (quantize + ring evict) + decode attention of all query heads")
 
 
 def decode_bytes(lens) -> int:
@@ -222,8 +225,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": tt / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "long-context 3.5-bit decode (K3 packed, V4 cold + 256 fp16 hot), B4, 32q/8kv, "
-                               "d128, L~U[65536,131072]; each step: one (batch, KV head) row, first %d positions" % n_tok},
+        "config": {"workload": WORKLOAD, "parallelism": "host cores (oracle)"},
         "cpu_baseline": {"value": value, "unit": "GB/s", "kind": "oracle", "cores": cpu_cores(),
                          "sample": "per step one (batch, KV head) row of the decode workload, first %d context "
                                    "positions, float64 dequantize + attention for its 4 query heads" % n_tok},
@@ -429,9 +431,7 @@ def run_gpu(args):
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {
-            "workload": "long-context 3.5-bit decode: B4, 32q/8kv heads, d128, L~U[65536,131072] (+1 per step), "
-                        "K 3-bit packed, V 4-bit packed + 256-token fp16 hot window; step = append 1 token per "
-                        "sequence (quantize + ring evict) + decode attention of all query heads",
+            "workload": WORKLOAD,
             "mean_context": float(np.mean(lens0) + args.warmup + args.steps / 2),
             "l2": "inputs larger than L2: %.0f MB of packed cache read per step" % (dec_bytes / 1e6),
             "parallelism": "replicas" if world > 1 else "single GPU",
