@@ -186,18 +186,40 @@ def cpu_cores() -> int:
         return os.cpu_count() or 1
 
 
-def cpu_baseline(lens, q16, budget_s=12.0):
-    total_t, total_b, rows, row = 0.0, 0, 0, 0
-    while total_t < budget_s and rows < 2 * B * HKV:
-        b, h = row % B, (row // B) % HKV
-        dt, nb = oracle_sample_step(lens, q16, b, h, int(lens[b]))
-        total_t += dt
-        total_b += nb
-        rows += 1
-        row += 1
-    return {"value": total_b / total_t / 1e9, "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
-            "sample": "%d (batch, KV head) rows of the workload at full context (%.2f GB of algorithmic bytes), "
-                      "numpy float64 dequantize + softmax attention for the 4 query heads of each row" % (rows, total_b / 1e9)}
+def _oracle_task(args):
+    """One oracle row in a worker process: (seconds, algorithmic bytes)."""
+    lens, q16, b, h, n = args
+    return oracle_sample_step(lens, q16, b, h, n)
+
+
+def oracle_pool():
+    """Spawned worker processes, one per host core, each with single-threaded
+    BLAS, so that independent (batch, KV head) rows run on all cores."""
+    import concurrent.futures
+    import multiprocessing
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"
+    n = cpu_cores()
+    return concurrent.futures.ProcessPoolExecutor(max_workers=n, mp_context=multiprocessing.get_context("spawn")), n
+
+
+def pooled_rows(pool, tasks):
+    """Runs the row tasks on the pool; returns (wall seconds, algorithmic bytes)."""
+    t0 = time.perf_counter()
+    nbytes = sum(nb for _, nb in pool.map(_oracle_task, tasks))
+    return time.perf_counter() - t0, nbytes
+
+
+def cpu_baseline(lens, q16, pool, workers, rounds=4):
+    """The oracle on all host cores: `rounds` passes over the 32 (batch, KV head)
+    rows of the workload at full context, one row per task."""
+    tasks = [(lens, q16, b, h, int(lens[b])) for _ in range(rounds) for b in range(B) for h in range(HKV)]
+    pooled_rows(pool, tasks[:workers])  # start-up of the workers, untimed
+    wall, nbytes = pooled_rows(pool, tasks)
+    return {"value": nbytes / wall / 1e9, "unit": "GB/s", "cores": workers, "kind": "oracle",
+            "sample": "%d (batch, KV head) rows of the workload at full context (%.2f GB of algorithmic bytes) on "
+                      "%d worker processes with single-threaded BLAS: numpy float64 dequantize + softmax attention "
+                      "for the 4 query heads of each row" % (len(tasks), nbytes / 1e9, workers)}
 
 
 def run_reference(args):
@@ -206,29 +228,35 @@ def run_reference(args):
         return 0
     lens = synth.seq_lengths(SEED, B, LO, HI)
     q16 = synth.queries_fp16(SEED, B, HQ, D)
-    # size each step so that the whole run stays within a few minutes
+    pool, workers = oracle_pool()
+    # size each step (one row per worker) so that the whole run stays within a few minutes
     dt_cal, nb_cal = oracle_sample_step(lens, q16, 0, 0, 4096)
-    rate = nb_cal / dt_cal
-    per_step_bytes = max(200_000.0, min(rate * 120.0 / max(1, args.steps + args.warmup), 5e8))
+    rate = nb_cal / dt_cal  # bytes/s of one core
+    per_row_bytes = max(200_000.0, min(rate * 100.0 / max(1, args.steps + args.warmup), 5e8))
     bytes_per_token = (D * KB // 8 + 4) + (D * VB // 8 + 4)
-    n_tok = int(max(512, min(HI, per_step_bytes / bytes_per_token)))
+    n_tok = int(max(512, min(HI, per_row_bytes / bytes_per_token)))
+
+    def step_tasks(s):
+        return [(lens, q16, (s * workers + i) % B, ((s * workers + i) // B) % HKV,
+                 min(n_tok, int(lens[(s * workers + i) % B]))) for i in range(workers)]
     for s in range(args.warmup):
-        oracle_sample_step(lens, q16, s % B, (s // B) % HKV, min(n_tok, int(lens[s % B])))
+        pooled_rows(pool, step_tasks(s))
     tt, tb = 0.0, 0
     for s in range(args.steps):
-        b, h = s % B, (s // B) % HKV
-        dt, nb = oracle_sample_step(lens, q16, b, h, min(n_tok, int(lens[b])))
+        dt, nb = pooled_rows(pool, step_tasks(args.warmup + s))
         tt += dt
         tb += nb
+    pool.shutdown()
     value = tb / tt / 1e9
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": tt / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": WORKLOAD, "parallelism": "host cores (oracle)"},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "kind": "oracle", "cores": cpu_cores(),
-                         "sample": "per step one (batch, KV head) row of the decode workload, first %d context "
-                                   "positions, float64 dequantize + attention for its 4 query heads" % n_tok},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "kind": "oracle", "cores": workers,
+                         "sample": "per step one (batch, KV head) row per worker process (%d processes, "
+                                   "single-threaded BLAS), first %d context positions of each row, float64 "
+                                   "dequantize + attention for its 4 query heads" % (workers, n_tok)},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -258,6 +286,57 @@ def build_decode_cache(torch, cap):
     return tc, lens
 
 
+def build_plain_cache(torch, batch, ctx, k_fp16, seed):
+    """Decode cache of `batch` sequences of length ctx, no hot window: packed V (and
+    packed K) rows of random words with lognormal norms, or fp16 K drawn
+    N(0,1) x lognormal channel scales."""
+    from bit_kv_cache_10_gb300.cache import TurboQuantKVCache
+    tc = TurboQuantKVCache(batch, HKV, HQ, ctx, bits=(KB, VB), k_fp16=k_fp16)
+    if k_fp16:
+        sk = synth.channel_scales(seed, synth.STREAM_SCALE_K, HKV, D)
+        for b in range(batch):  # one sequence at a time to bound host memory
+            k = synth.kv_fp16(seed + b, synth.STREAM_K, 1, HKV, ctx, D, sk)
+            tc.k_cache[b].copy_(torch.from_numpy(k[0]))
+    for b in range(batch):
+        for h in range(HKV):
+            if not k_fp16:
+                kw, kn = synth.packed_row(seed, synth.STREAM_CODES_K, b, h, ctx, D * KB // 32, 12.0)
+                tc.k_cache[b, h].copy_(torch.from_numpy(kw.view(np.int32)))
+                tc.k_norms[b, h].copy_(torch.from_numpy(kn))
+            vw, vn = synth.packed_row(seed, synth.STREAM_CODES_V, b, h, ctx, D * VB // 32, 30.0)
+            tc.v_cache[b, h].copy_(torch.from_numpy(vw.view(np.int32)))
+            tc.v_norms[b, h].copy_(torch.from_numpy(vn))
+    torch.cuda.synchronize()
+    return tc
+
+
+def time_plain_decode(torch, batch, ctx, k_fp16, reps=50):
+    """Mean decode-call time (ms) and algorithmic bytes of one call on a
+    build_plain_cache cache, after 3 untimed calls."""
+    tc = build_plain_cache(torch, batch, ctx, k_fp16, SEED + 3)
+    q = torch.from_numpy(synth.queries_fp16(SEED + 3, batch, HQ, D)).cuda()
+    lens = torch.full((batch,), ctx, dtype=torch.int32, device="cuda")
+    out = torch.empty(batch, HQ, D, dtype=torch.float32, device="cuda")
+    ws = torch.empty(tc.workspace_bytes(ctx), dtype=torch.uint8, device="cuda")
+    for _ in range(3):
+        tc.decode(q, lens, ctx, out=out, workspace=ws)
+    st = torch.cuda.current_stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+    torch.cuda.synchronize()
+    ev[0].record(st)
+    for i in range(reps):
+        tc.decode(q, lens, ctx, out=out, workspace=ws)
+        ev[i + 1].record(st)
+    torch.cuda.synchronize()
+    ms = float(np.mean([ev[i].elapsed_time(ev[i + 1]) for i in range(reps)]))
+    if tc.device_status() != 0:
+        raise RuntimeError("device status set by the decode timing")
+    k_tok = D * 2 if k_fp16 else D * KB // 8 + 4
+    nbytes = batch * HKV * ctx * (k_tok + D * VB // 8 + 4) + batch * HQ * D * (2 + 4)
+    del tc
+    return ms, nbytes
+
+
 def step_inputs(n_steps):
     """Per-step new K/V tokens [S, B, Hkv, 1, D] and queries [S, B, Hq, D], fp16."""
     g = synth.rng(SEED + 1, synth.STREAM_Q)
@@ -280,6 +359,8 @@ def run_gpu(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    want_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+    pool, workers = oracle_pool() if want_cpu else (None, 0)  # spawned before any GPU work
     if world > 1:
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     torch.cuda.set_device(local)
@@ -420,6 +501,11 @@ def run_gpu(args):
     q_bytes = 2 * QB * HKV * QT * D * 2 + QB * HKV * QT * ((D * KB // 8 + 4) + (D * VB // 8 + 4))
     if qc.device_status() != 0:
         raise RuntimeError("device status set by the quantize benchmark")
+    del kq, vq, qc
+    # the other decode workloads: asym (fp16 K + 4-bit V, B8, context 16384) and the
+    # 3.5-bit Llama-3-8B-like layer (B1, context 4096; launch- and L2-bound)
+    asym_ms, asym_bytes = time_plain_decode(torch, 8, 16384, True)
+    small_ms, small_bytes = time_plain_decode(torch, 1, 4096, False, reps=200)
 
     peak, peak_kind = measured_peak()
     dec_avg_ms = float(np.mean(decode_ms))
@@ -446,13 +532,21 @@ def run_gpu(args):
                      "workload": "batch 16 x 8192 new tokens x 8 KV heads, K 3-bit / V 4-bit, lognormal channels",
                      "ms": q_avg, "hbm_gbs": q_bytes / (q_avg * 1e-3) / 1e9,
                      "frac": q_bytes / (q_avg * 1e-3) / 1e9 / peak},
+        "asym": {"value": asym_bytes / (asym_ms * 1e-3) / 1e9, "unit": "GB/s", "ms": asym_ms,
+                 "frac": asym_bytes / (asym_ms * 1e-3) / 1e9 / peak, "algorithmic_bytes_per_launch": asym_bytes,
+                 "workload": "asym decode: fp16 K + 4-bit V, B8, 32q/8kv, d128, context 16384, no hot window"},
+        "llama_layer": {"value": small_bytes / (small_ms * 1e-3) / 1e9, "unit": "GB/s", "ms": small_ms,
+                        "algorithmic_bytes_per_launch": small_bytes,
+                        "workload": "3.5-bit decode: B1, 32q/8kv, d128, context 4096, K3/V4 (launch-bound: "
+                                    "4 MB per call, inside L2)"},
         "e2e": {"value": world * e2e_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "clocks": clocks,
         "gpu_launches": args.steps * 4,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(lens0, synth.queries_fp16(SEED, B, HQ, D))
+    if want_cpu:
+        line["cpu_baseline"] = cpu_baseline(lens0, synth.queries_fp16(SEED, B, HQ, D), pool, workers)
+        pool.shutdown()
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
@@ -487,6 +581,16 @@ def run_profile(args):
         torch.cuda.synchronize()
         print(json.dumps({"profile": "decode", "steps": args.steps, "wall_ms_per_step":
                           (time.perf_counter() - t0) * 1e3 / max(1, args.steps), "status": tc.device_status()}))
+    elif args.profile == "asym":
+        tc = build_plain_cache(torch, 8, 16384, True, SEED + 3)
+        q = torch.from_numpy(synth.queries_fp16(SEED + 3, 8, HQ, D)).cuda()
+        lens = torch.full((8,), 16384, dtype=torch.int32, device="cuda")
+        out = torch.empty(8, HQ, D, dtype=torch.float32, device="cuda")
+        ws = torch.empty(tc.workspace_bytes(16384), dtype=torch.uint8, device="cuda")
+        for s in range(total):
+            tc.decode(q, lens, 16384, out=out, workspace=ws)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile": "asym", "steps": total, "status": tc.device_status()}))
     else:
         qb = args.profile_batch
         g = synth.rng(SEED + 2, synth.STREAM_K)
@@ -508,7 +612,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle timing")
-    ap.add_argument("--profile", choices=["decode", "quantize"],
+    ap.add_argument("--profile", choices=["decode", "quantize", "asym"],
                     help="run only warm-up + timed steps of one part (for ncu captures); prints a short line")
     ap.add_argument("--profile-batch", type=int, default=4, help="batch of the quantize part in --profile mode")
     args = ap.parse_args()
