@@ -467,6 +467,44 @@ def decode_attention(cache: PackedCache, q16: np.ndarray, lengths, pairs=None) -
     return out
 
 
+def sparse_v_bound(q: np.ndarray, k: np.ndarray, v: np.ndarray, tau: float) -> np.ndarray:
+    """Per-coordinate bound on how far a sparse-V decode may move one output.
+
+    Sparse-V ([mlxcel doc] environment variables: a sparse-V threshold, 0
+    disables it) skips the V rows of tokens whose softmax weight is below a
+    threshold tau while their weight still counts in the normalization.  Any
+    skipped set A of tokens with normalized weight p_j < tau changes the output
+    by sum_{j in A} p_j v_j, so every coordinate moves by at most
+    sum_{j: p_j < tau} p_j |v_ji|, which this returns (zeros for tau <= 0).
+    """
+    d = q.shape[-1]
+    if tau <= 0.0 or k.shape[0] == 0:
+        return np.zeros(d)
+    s = k @ q / math.sqrt(d)
+    p = np.exp(s - s.max())
+    p = p / p.sum()
+    skip = p < tau
+    return p[skip] @ np.abs(v[skip])
+
+
+def decode_sparse_v_bound(cache: PackedCache, q16: np.ndarray, lengths, tau: float, pairs=None) -> np.ndarray:
+    """sparse_v_bound for every (b, query head) of a decode step (same layout
+    and head grouping as decode_attention)."""
+    bsz, hq_n, d = q16.shape
+    hk = cache.v_words.shape[1]
+    g = hq_n // hk
+    out = np.full((bsz, hq_n, d), np.nan)
+    todo = pairs if pairs is not None else [(b, hq) for b in range(bsz) for hq in range(hq_n)]
+    kv = {}
+    for b, hq in todo:
+        h = hq // g
+        if (b, h) not in kv:
+            kv = {(b, h): dequantized_kv(cache, b, h, int(lengths[b]))}
+        k, v = kv[(b, h)]
+        out[b, hq] = sparse_v_bound(q16[b, hq].astype(np.float64), k, v, tau)
+    return out
+
+
 def decode_attention_rotated(cache: PackedCache, q16: np.ndarray, lengths, b: int, hq: int) -> np.ndarray:
     """Same output as ``decode_attention`` through the rotated-domain identity
     (R q).(R k_hat) = q.k_hat: scores from the rotated query and the raw

@@ -119,3 +119,65 @@ def test_turboquant_enabled_truth_table():
     assert oracle.turboquant_enabled(4.0000001) is False
     assert oracle.turboquant_enabled(4.2) is True
     assert oracle.turboquant_enabled(2, "uniform") is False
+
+
+# --- sparse-V bound ------------------------------------------------------------
+
+def _dense_weights(q, k):
+    s = k @ q / np.sqrt(q.shape[-1])
+    p = np.exp(s - s.max())
+    return p / p.sum()
+
+
+def test_sparse_v_bound_is_zero_when_off():
+    g = np.random.default_rng(3)
+    q, k, v = g.standard_normal(8), g.standard_normal((20, 8)), g.standard_normal((20, 8))
+    assert np.all(oracle.sparse_v_bound(q, k, v, 0.0) == 0.0)
+    assert np.all(oracle.sparse_v_bound(q, k[:0], v[:0], 0.5) == 0.0)
+
+
+def test_sparse_v_bound_with_every_token_skippable_is_the_weighted_abs_sum():
+    g = np.random.default_rng(4)
+    q, k, v = g.standard_normal(8), g.standard_normal((15, 8)), g.standard_normal((15, 8))
+    p = _dense_weights(q, k)
+    expect = sum(p[j] * np.abs(v[j]) for j in range(15))
+    np.testing.assert_allclose(oracle.sparse_v_bound(q, k, v, 1.0 + 1e-9), expect, rtol=1e-12)
+
+
+def test_sparse_v_bound_covers_every_skipped_subset_by_brute_force():
+    # every subset of the tokens below the threshold, its V rows removed with the
+    # softmax mass kept, moves each coordinate by no more than the bound
+    import itertools
+    g = np.random.default_rng(5)
+    d, n = 4, 7
+    q, k, v = 2.0 * g.standard_normal(d), g.standard_normal((n, d)), g.standard_normal((n, d))
+    p = _dense_weights(q, k)
+    tau = float(np.sort(p)[4])  # four tokens lie below it
+    below = [j for j in range(n) if p[j] < tau]
+    assert len(below) == 4
+    bound = oracle.sparse_v_bound(q, k, v, tau)
+    dense = p @ v
+    worst = np.zeros(d)
+    for r in range(len(below) + 1):
+        for sub in itertools.combinations(below, r):
+            kept = [j for j in range(n) if j not in sub]
+            out = p[kept] @ v[kept]
+            worst = np.maximum(worst, np.abs(out - dense))
+    assert np.all(worst <= bound + 1e-15)
+    # with values of one sign the bound is reached by skipping all of them
+    vp = np.abs(v)
+    bound_p = oracle.sparse_v_bound(q, k, vp, tau)
+    np.testing.assert_allclose(p[below] @ vp[below], bound_p, rtol=1e-13)
+
+
+def test_decode_sparse_v_bound_matches_per_row_bound():
+    rng = np.random.default_rng(6)
+    d, L = 128, 40
+    k16 = rng.standard_normal((1, 2, L, d)).astype(np.float16)
+    v16 = rng.standard_normal((1, 2, L, d)).astype(np.float16)
+    q16 = (3.0 * rng.standard_normal((1, 4, d))).astype(np.float16)
+    c = oracle.build_cache(k16, v16, [L], L, 3, 4)
+    out = oracle.decode_sparse_v_bound(c, q16, [L], 0.01)
+    for hq in range(4):
+        k, v = oracle.dequantized_kv(c, 0, hq // 2, L)
+        np.testing.assert_array_equal(out[0, hq], oracle.sparse_v_bound(q16[0, hq].astype(np.float64), k, v, 0.01))
