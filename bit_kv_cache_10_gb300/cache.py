@@ -22,12 +22,14 @@ class TurboQuantKVCache:
 
     ``bits`` may be fractional (K gets floor, V gets ceil) or a (k_bits,
     v_bits) pair; ``k_fp16=True`` keeps K in fp16 (the asym modes);
-    ``hot_window`` > 0 keeps the newest V tokens in an fp16 ring.
+    ``hot_window`` > 0 keeps the newest V tokens in an fp16 ring;
+    ``sparse_v_threshold`` > 0 lets decode skip the V rows of (token, head)
+    pairs whose softmax weight is below it (0 decodes densely).
     """
 
     def __init__(self, batch: int, num_kv_heads: int, num_q_heads: int, capacity: int, bits=3.5,
                  head_dim: int = 128, k_fp16: bool = False, hot_window: int = 0, seed: int = 0, layer: int = 0,
-                 device="cuda"):
+                 device="cuda", sparse_v_threshold: float = 0.0):
         if isinstance(bits, tuple):
             k_bits, v_bits = bits
         else:
@@ -61,6 +63,7 @@ class TurboQuantKVCache:
         d.v_norms = self.v_norms.data_ptr()
         d.v_hot = self.v_hot.data_ptr() if self.v_hot is not None else None
         d.d_status = self.status.data_ptr()
+        d.sparse_v_threshold = float(sparse_v_threshold)
         self._workspace = None
 
     # -- update ---------------------------------------------------------------

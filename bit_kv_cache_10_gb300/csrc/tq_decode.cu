@@ -70,6 +70,7 @@ struct DecodeParams {
   float v_cent[16];
   float* ws_acc;  // [slots][G][D]
   float* ws_ml;   // [slots][G][2] (max, sum)
+  float sparse_tau;  // sparse-V threshold (0: dense)
   int grid;       // CTAs of the split kernel
   float* out;     // [B, Hq, D]
 };
@@ -536,6 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
   const int tau_own = k_token<KB>(u_own, s);
   const int h0 = G >= 2 ? GH * (rr & 1) : 0;
   const bool owner = G >= 2 || (rr & 1) == 0;  // for G = 1 lanes rr and rr ^ 1 hold the same score
+  const bool sparse = p.sparse_tau > 0.0f;
   float2 qr[G][8];
   int cur_b = -1, cur_h = -1;
   long long seg = t0;
@@ -744,6 +746,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
         lsum[i] = fadd(lsum[i], (G >= 2 || owner) ? pj : 0.0f);
         w_own[i] = fmul(pj, nv);
         if (!full) w_own[i] = valid ? w_own[i] : 0.0f;
+        // sparse V: a weight below tau relative to the (lazily raised) running
+        // maximum, hence below tau after normalization, contributes no V
+        if (sparse && pj < p.sparse_tau) w_own[i] = 0.0f;
+      }
+      // V steps (2 tokens each) that carry a nonzero weight, warp-uniform
+      uint32_t stepmask = 0xFFu;
+      if (sparse) {
+        bool keep = false;
+#pragma unroll
+        for (int i = 0; i < GH; ++i) keep |= w_own[i] != 0.0f;
+        stepmask = __reduce_or_sync(0xffffffffu, keep ? 1u << (tau_own >> 1) : 0u);
       }
       // weights (w, w) of token tau_own, heads h0.. : row tau_own of 32 bytes
       if constexpr (G == 4) {
@@ -813,7 +826,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
           }
         }
       };
-      if (!hot) {
+      if (!hot && stepmask == 0xFFu) {
         v_cold(std::integral_constant<int, 0>{});
         v_cold(std::integral_constant<int, 1>{});
         v_cold(std::integral_constant<int, 2>{});
@@ -822,6 +835,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
         v_cold(std::integral_constant<int, 5>{});
         v_cold(std::integral_constant<int, 6>{});
         v_cold(std::integral_constant<int, 7>{});
+      } else if (!hot) {  // sparse V: only the steps with a nonzero weight
+        if (stepmask & 0x01u) v_cold(std::integral_constant<int, 0>{});
+        if (stepmask & 0x02u) v_cold(std::integral_constant<int, 1>{});
+        if (stepmask & 0x04u) v_cold(std::integral_constant<int, 2>{});
+        if (stepmask & 0x08u) v_cold(std::integral_constant<int, 3>{});
+        if (stepmask & 0x10u) v_cold(std::integral_constant<int, 4>{});
+        if (stepmask & 0x20u) v_cold(std::integral_constant<int, 5>{});
+        if (stepmask & 0x40u) v_cold(std::integral_constant<int, 6>{});
+        if (stepmask & 0x80u) v_cold(std::integral_constant<int, 7>{});
       } else {
         v_hot(std::integral_constant<int, 0>{});
         v_hot(std::integral_constant<int, 1>{});
@@ -1137,6 +1159,7 @@ extern "C" tq_status tq_decode_attention(const tq_cache_desc* d, const void* q, 
   p.ws_acc = static_cast<float*>(workspace);
   p.ws_ml = p.ws_acc + slots * g * D;
   p.grid = sms < kMaxDecodeCtas ? sms : kMaxDecodeCtas;
+  p.sparse_tau = d->sparse_v_threshold;
   p.out = out;
 
   const int kb = d->k_mode == TQ_K_FP16 ? 16 : d->k_bits;

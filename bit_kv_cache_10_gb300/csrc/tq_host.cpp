@@ -245,6 +245,7 @@ tq_status validate_desc(const tq_cache_desc* d) {
   if (!aligned16(d->k_cache) || !aligned16(d->v_cache) || !aligned16(d->v_norms)) return TQ_ERR_INVALID_ARG;
   if (d->k_mode == TQ_K_PACKED && (d->k_norms == nullptr || !aligned16(d->k_norms))) return TQ_ERR_INVALID_ARG;
   if (d->hot_window > 0 && (d->v_hot == nullptr || !aligned16(d->v_hot))) return TQ_ERR_INVALID_ARG;
+  if (!(d->sparse_v_threshold >= 0.0f && d->sparse_v_threshold <= 1.0f)) return TQ_ERR_INVALID_ARG;  // NaN too
   return TQ_OK;
 }
 

@@ -51,7 +51,7 @@ class TQCacheDesc(ctypes.Structure):
         ("hot_window", c_int32), ("layer", c_int32), ("seed", c_uint64),
         ("k_cb", TQCodebook), ("v_cb", TQCodebook),
         ("k_cache", c_void_p), ("k_norms", c_void_p), ("v_cache", c_void_p), ("v_norms", c_void_p),
-        ("v_hot", c_void_p), ("d_status", c_void_p),
+        ("v_hot", c_void_p), ("d_status", c_void_p), ("sparse_v_threshold", ctypes.c_float),
     ]
 
 

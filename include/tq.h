@@ -176,6 +176,15 @@ typedef struct tq_cache_desc {
   float *v_norms;
   void *v_hot;
   uint32_t *d_status;
+  /* Sparse-V threshold tau of decode ([mlxcel doc] environment variables: a
+   * sparse-V threshold, 0 disables it).  0 (the default of
+   * tq_cache_desc_init) decodes densely.  With 0 < tau <= 1 decode skips the V
+   * accumulation of every (token, query head) whose softmax weight relative to
+   * the running maximum of its row is below tau; the weight still counts in
+   * the normalization.  Each skipped token then has a normalized weight below
+   * tau, so each output coordinate moves by at most sum_{p_j < tau} p_j |v_j|
+   * from the dense result.  NaN, negative or > 1 values are TQ_ERR_INVALID_ARG. */
+  float sparse_v_threshold;
 } tq_cache_desc;
 
 /*

@@ -124,6 +124,12 @@ def test_entry_points_reject_bad_arguments_before_launch():
     assert L.tq_dequantize(d, 0, 0, 0, 60, 5, fake, None) == N.TQ_ERR_CAPACITY
     d.k_norms = fake + 4
     assert L.tq_quantize_append(d, fake, fake, 0, 0, 0, 1, fake, None, None) == N.TQ_ERR_INVALID_ARG
+    d.k_norms = fake
+    # the sparse-V threshold must lie in [0, 1] (NaN included in the refusal)
+    for tau in (float("nan"), -1e-6, 1.5, float("inf")):
+        d.sparse_v_threshold = tau
+        assert L.tq_decode_attention(d, fake, fake, 64, fake, fake, 1 << 30, None) == N.TQ_ERR_INVALID_ARG
+    assert N.tq_cache_desc_init(1, 8, 32, 128, 64, N.TQ_K_PACKED, 3, 4).sparse_v_threshold == 0.0
 
 
 def test_workspace_and_buffer_sizes():

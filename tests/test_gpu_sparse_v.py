@@ -1,0 +1,71 @@
+"""Sparse-V decode on the GPU against the oracle's dense attention and its
+sparse-V deviation bound: with threshold tau every skipped (token, head) has a
+normalized softmax weight below tau, so each output coordinate may move from
+the dense result by at most sum_{p_j < tau} p_j |v_j| (plus the usual float32
+tolerance).  A threshold below every nonzero weight skips nothing that adds to
+the result and must reproduce the dense decode bit for bit."""
+import numpy as np
+import pytest
+
+import oracle
+from bit_kv_cache_10_gb300 import synth
+from bit_kv_cache_10_gb300 import native as N
+
+from helpers import ATTN_MAX_ABS
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+D = 128
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu_library():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+    from bit_kv_cache_10_gb300 import build
+    build.build()
+    N.lib()
+
+
+def _dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+@pytest.mark.parametrize("hot", [0, 64])
+def test_sparse_v_stays_within_the_oracle_bound(hot):
+    from bit_kv_cache_10_gb300.cache import TurboQuantKVCache
+    B, HQ, HK, cap = 2, 8, 2, 3000
+    lens = np.array([3000, 1777], np.int32)
+    sk = synth.channel_scales(11, synth.STREAM_SCALE_K, HK, D)
+    sv = synth.channel_scales(11, synth.STREAM_SCALE_V, HK, D)
+    k = synth.kv_fp16(11, synth.STREAM_K, B, HK, cap, D, sk)
+    v = synth.kv_fp16(11, synth.STREAM_V, B, HK, cap, D, sv)
+    q = (2.0 * synth.queries_fp16(11, B, HQ, D).astype(np.float32)).astype(np.float16)  # peaked softmax
+    oc = oracle.build_cache(k, v, lens, cap, 3, 4, hot_window=hot)
+    tc = TurboQuantKVCache(B, HK, HQ, cap, bits=(3, 4), hot_window=hot)
+    tc.k_cache.copy_(_dev(oc.k_words.view(np.int32)))
+    tc.k_norms.copy_(_dev(oc.k_norms))
+    tc.v_cache.copy_(_dev(oc.v_words.view(np.int32)))
+    tc.v_norms.copy_(_dev(oc.v_norms))
+    if hot:
+        tc.v_hot.copy_(_dev(oc.v_hot))
+    ql, sl = _dev(q), _dev(lens)
+    dense = tc.decode(ql, sl, cap).cpu().numpy()
+    ref = oracle.decode_attention(oc, q, lens)
+    assert np.abs(dense - ref).max() <= ATTN_MAX_ABS
+
+    tc.desc.sparse_v_threshold = 1e-30  # below every weight that is not already zero
+    same = tc.decode(ql, sl, cap).cpu().numpy()
+    np.testing.assert_array_equal(same, dense)
+
+    for tau in (1e-4, 0.02):
+        tc.desc.sparse_v_threshold = tau
+        got = tc.decode(ql, sl, cap).cpu().numpy()
+        bound = oracle.decode_sparse_v_bound(oc, q, lens, tau)
+        excess = np.abs(got - ref) - bound
+        assert np.all(np.isfinite(got))
+        assert excess.max() <= ATTN_MAX_ABS, "tau %g: deviation beyond the sparse-V bound by %.3g" % (tau, excess.max())
+        if tau == 0.02:
+            assert not np.array_equal(got, dense), "tau 0.02 skipped nothing"
+    assert tc.device_status() == 0
