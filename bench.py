@@ -72,12 +72,14 @@ def measured_peak():
 
 def profile_traffic():
     """dram bytes per decode launch from the committed ncu summary, if it was
-    taken on the current decode kernel source; else None."""
+    taken on the current decode kernel sources (split kernel header + decode
+    translation unit); else None."""
     path = os.path.join(ROOT, "profiles", "decode_long_context.md")
-    src = os.path.join(ROOT, "bit_kv_cache_10_gb300", "csrc", "tq_decode.cu")
+    csrc = os.path.join(ROOT, "bit_kv_cache_10_gb300", "csrc")
     try:
         text = open(path).read()
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        src = b"".join(open(os.path.join(csrc, f), "rb").read() for f in ("tq_decode_split.cuh", "tq_decode.cu"))
+        sha = hashlib.sha256(src).hexdigest()[:16]
         m = re.search(r"traffic_bytes_per_step:\s*([0-9]+)", text)
         s = re.search(r"decode_source_sha256_16:\s*([0-9a-f]+)", text)
         if m and s and s.group(1) == sha:

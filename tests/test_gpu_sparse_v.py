@@ -69,3 +69,24 @@ def test_sparse_v_stays_within_the_oracle_bound(hot):
         if tau == 0.02:
             assert not np.array_equal(got, dense), "tau 0.02 skipped nothing"
     assert tc.device_status() == 0
+
+
+def test_decode_is_bit_reproducible():
+    # the split CTAs combine their warps in a fixed order and the merge reads the
+    # partials in a fixed order: repeated calls give identical outputs
+    from bit_kv_cache_10_gb300.cache import TurboQuantKVCache
+    B, HQ, HK, cap = 2, 8, 2, 5000
+    tc = TurboQuantKVCache(B, HK, HQ, cap, bits=(3, 4), hot_window=32)
+    for b in range(B):
+        for h in range(HK):
+            kw, kn = synth.packed_row(13, synth.STREAM_CODES_K, b, h, cap, 12, 12.0)
+            vw, vn = synth.packed_row(13, synth.STREAM_CODES_V, b, h, cap, 16, 30.0)
+            tc.k_cache[b, h].copy_(_dev(kw.view(np.int32)))
+            tc.k_norms[b, h].copy_(_dev(kn))
+            tc.v_cache[b, h].copy_(_dev(vw.view(np.int32)))
+            tc.v_norms[b, h].copy_(_dev(vn))
+    tc.v_hot.copy_(_dev(synth.kv_fp16(13, synth.STREAM_V, B, HK, 32, D)))
+    q, sl = _dev(synth.queries_fp16(13, B, HQ, D)), _dev(np.array([5000, 4321], np.int32))
+    first = tc.decode(q, sl, cap).cpu().numpy()
+    for _ in range(3):
+        np.testing.assert_array_equal(tc.decode(q, sl, cap).cpu().numpy(), first)
