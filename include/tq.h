@@ -176,8 +176,8 @@ typedef struct tq_cache_desc {
   float *v_norms;
   void *v_hot;
   uint32_t *d_status;
-  /* Sparse-V threshold tau of decode ([mlxcel doc] environment variables: a
-   * sparse-V threshold, 0 disables it).  0 (the default of
+  /* Sparse-V threshold tau of decode ([mlxcel doc] "Environment variables":
+   * a threshold setting whose zero value turns sparse V off).  0 (the default of
    * tq_cache_desc_init) decodes densely.  With 0 < tau <= 1 decode skips the V
    * accumulation of every (token, query head) whose softmax weight relative to
    * the running maximum of its row is below tau; the weight still counts in

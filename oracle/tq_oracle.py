@@ -470,9 +470,9 @@ def decode_attention(cache: PackedCache, q16: np.ndarray, lengths, pairs=None) -
 def sparse_v_bound(q: np.ndarray, k: np.ndarray, v: np.ndarray, tau: float) -> np.ndarray:
     """Per-coordinate bound on how far a sparse-V decode may move one output.
 
-    Sparse-V ([mlxcel doc] environment variables: a sparse-V threshold, 0
-    disables it) skips the V rows of tokens whose softmax weight is below a
-    threshold tau while their weight still counts in the normalization.  Any
+    Sparse-V ([mlxcel doc] "Environment variables": a threshold setting whose
+    zero value turns it off) skips the V rows of tokens whose softmax weight is
+    below a threshold tau while their weight still counts in the normalization.  Any
     skipped set A of tokens with normalized weight p_j < tau changes the output
     by sum_{j in A} p_j v_j, so every coordinate moves by at most
     sum_{j: p_j < tau} p_j |v_ji|, which this returns (zeros for tau <= 0).
