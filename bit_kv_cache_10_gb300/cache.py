@@ -24,12 +24,17 @@ class TurboQuantKVCache:
     v_bits) pair; ``k_fp16=True`` keeps K in fp16 (the asym modes);
     ``hot_window`` > 0 keeps the newest V tokens in an fp16 ring;
     ``sparse_v_threshold`` > 0 lets decode skip the V rows of (token, head)
-    pairs whose softmax weight is below it (0 decodes densely).
+    pairs whose softmax weight is below it (0 decodes densely);
+    ``block_size`` > 0 selects the paged layout: K/V and norms live in pools of
+    ``num_blocks`` blocks (default: enough for every sequence at full
+    capacity) and ``block_table`` [B, capacity / block_size] (int32, on the
+    device, initially sequence b -> blocks b * n .. b * n + n - 1) maps each
+    sequence's positions to blocks; it may be rewritten between calls.
     """
 
     def __init__(self, batch: int, num_kv_heads: int, num_q_heads: int, capacity: int, bits=3.5,
                  head_dim: int = 128, k_fp16: bool = False, hot_window: int = 0, seed: int = 0, layer: int = 0,
-                 device="cuda", sparse_v_threshold: float = 0.0):
+                 device="cuda", sparse_v_threshold: float = 0.0, block_size: int = 0, num_blocks=None):
         if isinstance(bits, tuple):
             k_bits, v_bits = bits
         else:
@@ -45,7 +50,19 @@ class TurboQuantKVCache:
         self.head_dim, self.capacity, self.hot_window = head_dim, capacity, hot_window
         self.k_bits = 16 if k_fp16 else k_bits
         self.v_bits = v_bits
-        shape = (batch, num_kv_heads, capacity)
+        if block_size > 0:
+            if capacity % block_size:
+                raise ValueError("capacity must be a multiple of block_size")
+            max_blocks = capacity // block_size
+            num_blocks = batch * max_blocks if num_blocks is None else int(num_blocks)
+            self.block_table = (torch.arange(batch * max_blocks, dtype=torch.int32, device=self.device)
+                                .view(batch, max_blocks) % num_blocks).contiguous()
+            N.tq_cache_desc_set_paged(self.desc, block_size, max_blocks, num_blocks, self.block_table.data_ptr())
+            shape = (num_blocks, num_kv_heads, block_size)  # pools
+        else:
+            self.block_table = None
+            shape = (batch, num_kv_heads, capacity)
+        self.block_size, self.num_blocks = block_size, (num_blocks if block_size > 0 else 0)
         if k_fp16:
             self.k_cache = torch.zeros(*shape, head_dim, dtype=torch.float16, device=self.device)
             self.k_norms = None

@@ -118,7 +118,7 @@ __global__ void __launch_bounds__(4 * 32) decode_merge_kernel(const DecodeParams
   for (int i = 0; i < 4; ++i) {
     float v = fmul(y[i], 1.0f / kSqrtD);
     if (sign_negative(p.seed, p.layer, h, 4 * lane + i)) v = -v;
-    r[i] = fadd(v, hv[i]) / l;
+    r[i] = l > 0.0f ? fadd(v, hv[i]) / l : 0.0f;  // no token read (every block outside the pool): zero
   }
   out[lane] = make_float4(r[0], r[1], r[2], r[3]);
 }
@@ -175,6 +175,7 @@ extern "C" tq_status tq_decode_attention(const tq_cache_desc* d, const void* q, 
   p.v_words = static_cast<const uint32_t*>(d->v_cache);
   p.v_norms = d->v_norms;
   p.v_ring = static_cast<const uint16_t*>(d->v_hot);
+  p.map = make_row_map(d);
   p.status = d->d_status;
   p.seed = d->seed;
   p.layer = d->layer;

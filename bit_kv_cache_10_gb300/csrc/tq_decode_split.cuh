@@ -56,6 +56,7 @@ struct DecodeParams {
   const uint32_t* v_words;
   const float* v_norms;
   const uint16_t* v_ring;
+  RowMap map;     // cache row of (b, h, t): contiguous or through the block table
   uint32_t* status;
   uint64_t seed;
   int layer;
@@ -398,30 +399,51 @@ __device__ __forceinline__ void copy_full(uint32_t dst, const uint8_t* src, int 
     if (lane < kRest) cp_async16_at<kRounds * 512>(d, sp);
 }
 
+// Stages tile [t_begin, t_begin + n_valid) of (b, h); returns the number of
+// tokens the consumer may read (0 when the block table maps the tile outside
+// the pool, after flagging TQ_DEV_ERR_BLOCK).  Cold tiles start at a multiple of
+// the tile size and never straddle a block; a hot tile (K only) may straddle one
+// boundary and is then copied token by token.
 template <int KB, int VB>
-__device__ __forceinline__ void stage_tile(const DecodeParams& p, int b, int h, bool hot, int t_begin, int n_valid,
-                                           uint32_t buf, int lane) {
+__device__ __forceinline__ int stage_tile(const DecodeParams& p, int b, int h, bool hot, int t_begin, int n_valid,
+                                          uint32_t buf, int lane) {
   using C = Cfg<KB, VB>;
-  const int64_t row0 = (static_cast<int64_t>(b) * p.hkv + h) * p.cap + t_begin;
-  const uint8_t* ksrc = C::kFp16K ? reinterpret_cast<const uint8_t*>(p.k_fp16 + row0 * D)
-                                  : reinterpret_cast<const uint8_t*>(p.k_words + row0 * (C::kKBits * 4));
-  const uint8_t* vsrc = reinterpret_cast<const uint8_t*>(p.v_words + row0 * (VB * 4));
+  const long long row0 = p.map.row(b, h, t_begin);
+  const long long rowl = p.map.row(b, h, t_begin + n_valid - 1);
+  if (row0 < 0 || rowl < 0) {  // outside the pool: nothing is staged, the tile is read as empty
+    if (lane == 0 && p.status != nullptr) atomicOr(p.status, TQ_DEV_ERR_BLOCK);
+    return 0;
+  }
+  const bool straddle = rowl - row0 != n_valid - 1;
+  const uint8_t* kbase = C::kFp16K ? reinterpret_cast<const uint8_t*>(p.k_fp16)
+                                   : reinterpret_cast<const uint8_t*>(p.k_words);
+  const uint8_t* ksrc = kbase + row0 * C::kKRow;
+  const uint8_t* vsrc = reinterpret_cast<const uint8_t*>(p.v_words) + row0 * (VB * 16);
   const uint32_t vbuf = buf + C::kKTile + C::kKNorm;
-  if (n_valid == kTile) {
+  if (n_valid == kTile && !straddle) {
     copy_full<C::kKTile>(buf, ksrc, lane);
     if (!hot) copy_full<C::kVTile>(vbuf, vsrc, lane);
-  } else {
+  } else if (!straddle) {
     for (int c = lane; c < n_valid * (C::kKRow / 16); c += 32) cp_async16s(buf + 16u * c, ksrc + 16 * c);
     if (!hot)
       for (int c = lane; c < n_valid * (C::kVRow / 16); c += 32) cp_async16s(vbuf + 16u * c, vsrc + 16 * c);
+  } else {  // hot tile across a block boundary: K token by token
+    constexpr int kPer = C::kKRow / 16;
+    for (int c = lane; c < n_valid * kPer; c += 32) {
+      const int tok = c / kPer;
+      const long long r = p.map.row(b, h, t_begin + tok);  // in the pool: both ends were checked
+      cp_async16s(buf + 16u * c, kbase + r * C::kKRow + (c - tok * kPer) * 16);
+    }
   }
   // norms: lanes 0..15 the K norms, lanes 16..31 the V norms of the tile's tokens
   const int nl = lane & 15;
   const bool is_k = lane < 16;
   const bool want = nl < n_valid && (is_k ? !C::kFp16K : !hot);
-  const float* nsrc = (is_k ? p.k_norms : p.v_norms) + row0 + nl;
+  const long long rn = straddle ? p.map.row(b, h, t_begin + nl) : row0 + nl;
+  const float* nsrc = (is_k ? p.k_norms : p.v_norms) + rn;
   const uint32_t ndst = (is_k ? buf + C::kKTile : vbuf + C::kVTile) + 4u * nl;
   if (want) cp_async4s(ndst, nsrc);
+  return n_valid;
 }
 
 // Split kernel.
@@ -512,8 +534,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
       const bool hot = cur.x >= cur.tc;
       const int t_begin = hot ? cur.ce + (cur.x - cur.tc) * kTile : cur.x * kTile;
       const int n_valid = min(kTile, (hot ? cur.len : cur.ce) - t_begin);
-      stage_tile<KB, VB>(p, cur.b, cur.h, hot, t_begin, n_valid, ring + static_cast<uint32_t>((j_issue % S) * C::kBuf), lane);
-      if (lane == 0) descs[j_issue % S] = make_int4(cur.b, cur.h | (hot << 16), t_begin, n_valid);
+      const int staged = stage_tile<KB, VB>(p, cur.b, cur.h, hot, t_begin, n_valid,
+                                            ring + static_cast<uint32_t>((j_issue % S) * C::kBuf), lane);
+      if (lane == 0) descs[j_issue % S] = make_int4(cur.b, cur.h | (hot << 16), t_begin, staged);
       cursor_advance(p, cur, kWarps);
     }
     cp_async_commit();
@@ -746,7 +769,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
       float w_own[GH];
 #pragma unroll
       for (int i = 0; i < GH; ++i) {
-        const float pj = ex2_approx(fsub(sj[i], m_own[i]));  // 0 for masked rows
+        float pj = ex2_approx(fsub(sj[i], m_own[i]));
+        if (!full) pj = valid ? pj : 0.0f;  // masked rows (also before any valid token: -inf - -inf)
         lsum[i] = fadd(lsum[i], (G >= 2 || owner) ? pj : 0.0f);
         w_own[i] = fmul(pj, nv);
         if (!full) w_own[i] = valid ? w_own[i] : 0.0f;

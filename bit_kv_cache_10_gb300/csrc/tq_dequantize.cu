@@ -20,6 +20,8 @@ struct DequantParams {
   int which;  // 0 = K, 1 = V
   int b, seq_len, token_start, n_tokens;
   int hkv, cap, hot;
+  RowMap map;     // cache row of (b, h, t): contiguous or through the block table
+  uint32_t* status;
   int bits;       // packed bits, 16 for fp16 K
   const uint32_t* words;
   const float* norms;
@@ -36,10 +38,14 @@ __global__ void __launch_bounds__(kQWarps * 32) dequantize_kernel(const DequantP
   const int h = blockIdx.y;
   if (t >= p.n_tokens) return;
   const int pos = p.token_start + t;
-  const int64_t row = (static_cast<int64_t>(p.b) * p.hkv + h) * p.cap + pos;
   float4* dst = reinterpret_cast<float4*>(p.out + (static_cast<int64_t>(h) * p.n_tokens + t) * D) + lane;
-
   const bool ring = p.which == 1 && p.hot > 0 && pos >= p.seq_len - min(p.hot, p.seq_len);
+  const long long row = ring ? 0 : p.map.row(p.b, h, pos);
+  if (row < 0) {  // block-table entry outside the pool
+    if (lane == 0 && p.status != nullptr) atomicOr(p.status, TQ_DEV_ERR_BLOCK);
+    *dst = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    return;
+  }
   if (p.bits == 16 || ring) {
     const uint16_t* src = ring ? p.fp16 + ((static_cast<int64_t>(p.b) * p.hkv + h) * p.hot + pos % p.hot) * D
                                : p.fp16 + row * D;
@@ -110,6 +116,8 @@ extern "C" tq_status tq_dequantize(const tq_cache_desc* d, int32_t which, int32_
   p.hkv = d->num_kv_heads;
   p.cap = d->capacity;
   p.hot = which == 1 ? d->hot_window : 0;
+  p.map = make_row_map(d);
+  p.status = d->d_status;
   p.seed = d->seed;
   p.layer = d->layer;
   if (which == 0) {

@@ -13,9 +13,40 @@
 #include <cstdint>
 #include <cstring>
 
+#include "tq.h"
 #include "tq_signs.h"
 
 namespace tq {
+
+// Cache row of token t of (sequence b, KV head h): the contiguous layout
+// [B, Hkv, cap] or, with a block table, row (block * Hkv + h) * bs + t % bs of
+// block table[b][t / bs] (bs = 2^shift).  -1 for a table entry outside the pool.
+struct RowMap {
+  int hkv, cap;
+  const int32_t* table;  // nullptr: contiguous
+  int max_blocks, shift, num_blocks;
+#ifdef __CUDACC__
+  __device__ __forceinline__ long long row(int b, int h, int t) const {
+    if (table == nullptr) return (static_cast<long long>(b) * hkv + h) * cap + t;
+    const int blk = table[b * max_blocks + (t >> shift)];
+    if (blk < 0 || blk >= num_blocks) return -1;
+    return ((static_cast<long long>(blk) * hkv + h) << shift) | (t & ((1 << shift) - 1));
+  }
+#endif
+};
+
+inline RowMap make_row_map(const tq_cache_desc* d) {
+  RowMap m{d->num_kv_heads, d->capacity, nullptr, 0, 0, 0};
+  if (d->block_size > 0) {
+    m.table = d->block_table;
+    m.max_blocks = d->max_blocks_per_seq;
+    int sh = 0;
+    while ((1 << sh) < d->block_size) ++sh;
+    m.shift = sh;
+    m.num_blocks = d->num_blocks;
+  }
+  return m;
+}
 
 constexpr int D = 128;               // head_dim of the kernels
 constexpr float kLog2e = 1.4426950408889634f;

@@ -183,11 +183,27 @@ tq_status tq_cache_desc_init(tq_cache_desc* desc, int32_t batch, int32_t num_kv_
   return tq::validate_shape(desc);  // the buffer pointers are still NULL here
 }
 
+tq_status tq_cache_desc_set_paged(tq_cache_desc* d, int32_t block_size, int32_t max_blocks_per_seq,
+                                  int32_t num_blocks, const int32_t* d_block_table) {
+  if (d == nullptr || d_block_table == nullptr || (reinterpret_cast<uintptr_t>(d_block_table) & 3u) != 0)
+    return TQ_ERR_INVALID_ARG;
+  if (block_size < 16 || block_size > 4096 || (block_size & (block_size - 1)) != 0) return TQ_ERR_INVALID_ARG;
+  if (max_blocks_per_seq < 1 || num_blocks < 1) return TQ_ERR_INVALID_ARG;
+  if (static_cast<long long>(max_blocks_per_seq) * block_size != d->capacity) return TQ_ERR_INVALID_ARG;
+  d->block_size = block_size;
+  d->max_blocks_per_seq = max_blocks_per_seq;
+  d->num_blocks = num_blocks;
+  d->block_table = d_block_table;
+  return tq::validate_shape(d);
+}
+
 tq_status tq_cache_buffer_bytes(const tq_cache_desc* d, size_t* k_cache_bytes, size_t* k_norms_bytes,
                                 size_t* v_cache_bytes, size_t* v_norms_bytes, size_t* v_hot_bytes) {
   if (d == nullptr || d->batch < 1 || d->num_kv_heads < 1 || d->capacity < 1 || d->head_dim < 1)
     return TQ_ERR_INVALID_ARG;
-  const size_t rows = static_cast<size_t>(d->batch) * d->num_kv_heads * d->capacity;
+  const size_t rows = d->block_size > 0
+                          ? static_cast<size_t>(d->num_blocks) * d->num_kv_heads * d->block_size
+                          : static_cast<size_t>(d->batch) * d->num_kv_heads * d->capacity;
   const bool kfp16 = d->k_mode == TQ_K_FP16;
   if (k_cache_bytes)
     *k_cache_bytes = kfp16 ? rows * d->head_dim * 2 : rows * tq::words_per_token(d->head_dim, d->k_bits) * 4;
@@ -235,6 +251,14 @@ tq_status validate_shape(const tq_cache_desc* d) {
   if (quant_lut_scale(d->v_cb.thresholds, (1 << d->v_bits) - 1) == 0) return TQ_ERR_UNSUPPORTED;
   if (d->k_mode == TQ_K_PACKED && quant_lut_scale(d->k_cb.thresholds, (1 << d->k_bits) - 1) == 0)
     return TQ_ERR_UNSUPPORTED;
+  if (d->block_size != 0) {  // paged layout
+    if (d->block_size < 16 || d->block_size > 4096 || (d->block_size & (d->block_size - 1)) != 0)
+      return TQ_ERR_INVALID_ARG;
+    if (d->max_blocks_per_seq < 1 || d->num_blocks < 1 || d->block_table == nullptr) return TQ_ERR_INVALID_ARG;
+    if (static_cast<long long>(d->max_blocks_per_seq) * d->block_size != d->capacity) return TQ_ERR_INVALID_ARG;
+    if (static_cast<long long>(d->num_blocks) * d->num_kv_heads * d->block_size >= (1ll << 40))
+      return TQ_ERR_UNSUPPORTED;
+  }
   return TQ_OK;
 }
 

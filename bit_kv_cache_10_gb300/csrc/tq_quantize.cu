@@ -40,6 +40,7 @@ struct QuantParams {
   uint32_t* v_words;
   float* v_norms;
   uint16_t* v_ring;
+  RowMap map;  // cache row of (b, h, t): contiguous or through the block table
   uint32_t* status;
   uint64_t seed;
   int layer;
@@ -229,7 +230,6 @@ __global__ void __launch_bounds__(kWarps * 32, 1) quantize_append_kernel(const Q
       smask[lane + 32] = sign_mask_pair(p.seed, p.layer, jb.h, lane + 32);
       __syncwarp();
       const uint8_t* tile = tiles + buf * kTileBytes;
-      const int64_t rowbase = (static_cast<int64_t>(jb.b) * p.heads + jb.h) * p.cap;
       const bool k_tensor = jb.tensor == 0;
       const bool copy_k = k_tensor && p.k_mode == TQ_K_FP16;
       int cold_end = 1 << 30;
@@ -240,9 +240,11 @@ __global__ void __launch_bounds__(kWarps * 32, 1) quantize_append_kernel(const Q
         int pos = 0;
         const bool have = src_row(p, jb, row, &pos) != nullptr;
         if (!__any_sync(0xffffffffu, have)) break;  // rows are filled in order: no later step has one
-        const int64_t ridx = rowbase + pos;
+        const long long ridx = have ? p.map.row(jb.b, jb.h, pos) : 0;  // cache row (block table or contiguous)
         const bool to_copy = copy_k || (!k_tensor && pos >= cold_end);
-        if (to_copy && have) {
+        const bool to_ring = !copy_k && to_copy;  // hot V goes to the per-sequence ring, not the pool
+        if (have && ridx < 0 && !to_ring && p.status != nullptr) atomicOr(p.status, TQ_DEV_ERR_BLOCK);
+        if (to_copy && have && (to_ring || ridx >= 0)) {
           // fp16 copy of the row (asym K, or V going to the hot ring): 4 x 16 bytes per lane
           uint4* dst = copy_k ? reinterpret_cast<uint4*>(p.k_fp16 + ridx * D)
                               : reinterpret_cast<uint4*>(
@@ -260,9 +262,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1) quantize_append_kernel(const Q
         uint32_t* dw = (k_tensor ? p.k_words : p.v_words) + ridx * (bits * 4);
         float* dn = (k_tensor ? p.k_norms : p.v_norms) + ridx;
         switch (bits) {
-          case 2: quantize_step<2>(tile, row, q, smask, lut, lut_a, dw, dn, have && !to_copy); break;
-          case 3: quantize_step<3>(tile, row, q, smask, lut, lut_a, dw, dn, have && !to_copy); break;
-          default: quantize_step<4>(tile, row, q, smask, lut, lut_a, dw, dn, have && !to_copy); break;
+          case 2: quantize_step<2>(tile, row, q, smask, lut, lut_a, dw, dn, have && !to_copy && ridx >= 0); break;
+          case 3: quantize_step<3>(tile, row, q, smask, lut, lut_a, dw, dn, have && !to_copy && ridx >= 0); break;
+          default: quantize_step<4>(tile, row, q, smask, lut, lut_a, dw, dn, have && !to_copy && ridx >= 0); break;
         }
       }
     }
@@ -352,6 +354,7 @@ extern "C" tq_status tq_quantize_append(const tq_cache_desc* d, const void* k_ne
   p.v_words = static_cast<uint32_t*>(d->v_cache);
   p.v_norms = d->v_norms;
   p.v_ring = static_cast<uint16_t*>(d->v_hot);
+  p.map = make_row_map(d);
   p.status = d->d_status;
   p.seed = d->seed;
   p.layer = d->layer;

@@ -31,7 +31,9 @@ EXPORTED = (
     "tq_status_string", "tq_build_codebook", "tq_split_bits", "tq_turboquant_enabled", "tq_rotation_signs",
     "tq_cache_desc_init", "tq_cache_buffer_bytes", "tq_quantize_append", "tq_decode_workspace_bytes",
     "tq_decode_attention", "tq_dequantize", "tq_debug_quantize_rows_host", "tq_decode_attention_no_alloc",
+    "tq_cache_desc_set_paged",
 )
+TQ_DEV_ERR_APPEND_RANGE, TQ_DEV_ERR_SEQ_LEN, TQ_DEV_ERR_LAYOUT, TQ_DEV_ERR_BLOCK = 0x1, 0x2, 0x4, 0x8
 TQ_NO_ALLOC_WORKSPACE_BYTES = 16 << 20
 
 
@@ -52,6 +54,8 @@ class TQCacheDesc(ctypes.Structure):
         ("k_cb", TQCodebook), ("v_cb", TQCodebook),
         ("k_cache", c_void_p), ("k_norms", c_void_p), ("v_cache", c_void_p), ("v_norms", c_void_p),
         ("v_hot", c_void_p), ("d_status", c_void_p), ("sparse_v_threshold", ctypes.c_float),
+        ("block_size", c_int32), ("max_blocks_per_seq", c_int32), ("num_blocks", c_int32), ("reserved", c_int32),
+        ("block_table", c_void_p),
     ]
 
 
@@ -83,6 +87,8 @@ def lib() -> ctypes.CDLL:
         L.tq_rotation_signs.argtypes = [c_uint64, c_int32, c_int32, c_int32, POINTER(c_int8)]
         L.tq_cache_desc_init.restype = c_int32
         L.tq_cache_desc_init.argtypes = [POINTER(TQCacheDesc)] + [c_int32] * 9 + [c_uint64, c_int32]
+        L.tq_cache_desc_set_paged.restype = c_int32
+        L.tq_cache_desc_set_paged.argtypes = [POINTER(TQCacheDesc), c_int32, c_int32, c_int32, c_void_p]
         L.tq_cache_buffer_bytes.restype = c_int32
         L.tq_cache_buffer_bytes.argtypes = [POINTER(TQCacheDesc)] + [POINTER(c_size_t)] * 5
         L.tq_quantize_append.restype = c_int32
@@ -144,6 +150,12 @@ def tq_cache_desc_init(batch, num_kv_heads, num_q_heads, head_dim, capacity, k_m
     _check(lib().tq_cache_desc_init(ctypes.byref(d), batch, num_kv_heads, num_q_heads, head_dim, capacity, k_mode,
                                     k_bits, v_bits, hot_window, seed, layer), "tq_cache_desc_init")
     return d
+
+
+def tq_cache_desc_set_paged(desc: TQCacheDesc, block_size: int, max_blocks_per_seq: int, num_blocks: int,
+                            block_table_ptr: int) -> None:
+    _check(lib().tq_cache_desc_set_paged(ctypes.byref(desc), block_size, max_blocks_per_seq, num_blocks,
+                                         block_table_ptr), "tq_cache_desc_set_paged")
 
 
 def tq_cache_buffer_bytes(desc: TQCacheDesc) -> dict:

@@ -59,6 +59,7 @@ typedef enum tq_status {
 #define TQ_DEV_ERR_APPEND_RANGE 0x1u /* start_pos < 0, bad per-sequence count, or past capacity */
 #define TQ_DEV_ERR_SEQ_LEN 0x2u      /* seq_len < 0 or seq_len > capacity (or > max_seq_len) */
 #define TQ_DEV_ERR_LAYOUT 0x4u       /* internal: a kernel's shared-memory layout did not fit (not expected) */
+#define TQ_DEV_ERR_BLOCK 0x8u        /* paged layout: a block-table entry outside [0, num_blocks) */
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char *tq_status_string(tq_status status);
@@ -185,6 +186,16 @@ typedef struct tq_cache_desc {
    * tau, so each output coordinate moves by at most sum_{p_j < tau} p_j |v_j|
    * from the dense result.  NaN, negative or > 1 values are TQ_ERR_INVALID_ARG. */
   float sparse_v_threshold;
+  /* Paged layout (tq_cache_desc_set_paged; all zero / NULL = contiguous).
+   * Token t of (sequence b, KV head h) lives in block
+   * block_table[b * max_blocks_per_seq + t / block_size] of the pools, at row
+   * (block * Hkv + h) * block_size + t % block_size of k_cache, k_norms,
+   * v_cache and v_norms.  The fp16 hot ring stays per sequence. */
+  int32_t block_size;          /* tokens per block: a power of two in [16, 4096] */
+  int32_t max_blocks_per_seq;  /* capacity = max_blocks_per_seq * block_size */
+  int32_t num_blocks;          /* blocks in each pool */
+  int32_t reserved;
+  const int32_t *block_table;  /* device int32 [B, max_blocks_per_seq] */
 } tq_cache_desc;
 
 /*
@@ -197,8 +208,26 @@ tq_status tq_cache_desc_init(tq_cache_desc *desc, int32_t batch, int32_t num_kv_
                              int32_t v_bits, int32_t hot_window, uint64_t seed, int32_t layer);
 
 /*
+ * Switch a descriptor from tq_cache_desc_init to the paged layout: the
+ * packed K/V (or fp16 K) and norm buffers become pools of num_blocks blocks of
+ * block_size tokens per KV head, and each sequence maps its positions to
+ * blocks through d_block_table (device int32 [B, max_blocks_per_seq], owned
+ * by the caller, read at every launch, so blocks can be remapped between
+ * calls).  block_size must be a power of two in [16, 4096] and
+ * max_blocks_per_seq * block_size must equal the descriptor's capacity
+ * (TQ_ERR_INVALID_ARG otherwise).  This is the block-table layout of the
+ * serving paths of [mlxcel doc] "Paged cache and server batching" (blocks adopted
+ * and donated between sequences; paged decode equal to the contiguous one).
+ * A block-table entry outside [0, num_blocks) met by a kernel sets
+ * TQ_DEV_ERR_BLOCK and that token is skipped (decode: treated as absent).
+ */
+tq_status tq_cache_desc_set_paged(tq_cache_desc *desc, int32_t block_size, int32_t max_blocks_per_seq,
+                                  int32_t num_blocks, const int32_t *d_block_table);
+
+/*
  * Bytes of each buffer the descriptor needs (0 for a buffer the mode does
- * not use).  Any output pointer may be NULL.  Host only.
+ * not use; in the paged layout the pools of num_blocks blocks).  Any output
+ * pointer may be NULL.  Host only.
  */
 tq_status tq_cache_buffer_bytes(const tq_cache_desc *desc, size_t *k_cache_bytes, size_t *k_norms_bytes,
                                 size_t *v_cache_bytes, size_t *v_norms_bytes, size_t *v_hot_bytes);

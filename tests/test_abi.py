@@ -175,3 +175,24 @@ def test_host_quantizer_special_vectors():
     assert norms[2] == np.float32(1.0)      # tie goes to the even neighbour
     assert norms[0] == 0 and np.all(oracle.unpack(words[:1], 3, 128) == 4)
     compare_packed(words, oracle.pack(codes, 3), y, 3, oracle.codebook(128, 3).thresholds32, "special")
+
+
+def test_paged_layout_validation_and_pool_sizes():
+    d = N.tq_cache_desc_init(2, 8, 32, 128, 4096, N.TQ_K_PACKED, 3, 4, hot_window=64)
+    fake = 1 << 20
+    for bs, mb, nb, tab in [(24, 4096 // 24, 10, fake), (8, 512, 10, fake), (8192, 1, 10, fake),
+                            (64, 63, 10, fake), (64, 64, 0, fake), (64, 64, 10, None), (64, 64, 10, fake + 2)]:
+        with pytest.raises(N.TQError) as e:
+            N.tq_cache_desc_set_paged(d, bs, mb, nb, tab)
+        assert e.value.status == N.TQ_ERR_INVALID_ARG
+    N.tq_cache_desc_set_paged(d, 64, 64, 200, fake)
+    assert (d.block_size, d.max_blocks_per_seq, d.num_blocks, d.block_table) == (64, 64, 200, fake)
+    sizes = N.tq_cache_buffer_bytes(d)
+    rows = 200 * 8 * 64  # pools of 200 blocks of 64 tokens per KV head
+    assert sizes == {"k_cache": rows * 48, "k_norms": rows * 4, "v_cache": rows * 64, "v_norms": rows * 4,
+                     "v_hot": 2 * 8 * 64 * 256}
+    # a corrupted paged descriptor is refused before any launch
+    L = N.lib()
+    d.k_cache = d.v_cache = d.k_norms = d.v_norms = d.v_hot = fake
+    d.block_table = None
+    assert L.tq_decode_attention(d, fake, fake, 64, fake, fake, 1 << 30, None) == N.TQ_ERR_INVALID_ARG
