@@ -1,6 +1,7 @@
 // Decode attention over the packed cache: the host entry points, the merge
-// kernel and the dense split-K instantiations (the split kernel itself is in
-// tq_decode_split.cuh, its sparse-V instantiations in tq_decode_sparse.cu).
+// kernel and the dense contiguous split-K instantiations (the split kernel
+// itself is in tq_decode_split.cuh; its sparse-V and paged instantiations are in
+// tq_decode_sparse.cu, tq_decode_paged.cu and tq_decode_paged_sparse.cu).
 #include <mutex>
 
 #include "tq_decode_split.cuh"
@@ -191,8 +192,9 @@ extern "C" tq_status tq_decode_attention(const tq_cache_desc* d, const void* q, 
 
   const int kb = d->k_mode == TQ_K_FP16 ? 16 : d->k_bits;
   tq_status st;
-  st = p.sparse_tau > 0.0f ? dispatch_split_sparse(p, g, kb, d->v_bits, s)
-                           : dispatch_split_variant<false>(p, g, kb, d->v_bits, s);
+  const bool sparse = p.sparse_tau > 0.0f, paged = d->block_size > 0;
+  if (paged) st = sparse ? dispatch_split_paged_sparse(p, g, kb, d->v_bits, s) : dispatch_split_paged(p, g, kb, d->v_bits, s);
+  else st = sparse ? dispatch_split_sparse(p, g, kb, d->v_bits, s) : dispatch_split_variant<false, false>(p, g, kb, d->v_bits, s);
   if (st != TQ_OK) return st;
   // programmatic dependent launch: the merge grid is scheduled as the split
   // kernel's CTAs retire and waits (griddepcontrol.wait) for its completion

@@ -1,11 +1,11 @@
-// Sparse-V instantiations of the split-K decode kernel (a translation unit of
-// their own so that the two variants compile in parallel).
+// Sparse-V instantiations of the split-K decode kernel (contiguous layout), a
+// translation unit of their own so that the variants compile in parallel.
 #include "tq_decode_split.cuh"
 
 namespace tq {
 
 tq_status dispatch_split_sparse(const DecodeParams& p, int g, int kb, int vb, cudaStream_t s) {
-  return dispatch_split_variant<true>(p, g, kb, vb, s);
+  return dispatch_split_variant<true, false>(p, g, kb, vb, s);
 }
 
 }  // namespace tq

@@ -399,14 +399,14 @@ __device__ __forceinline__ void copy_full(uint32_t dst, const uint8_t* src, int 
     if (lane < kRest) cp_async16_at<kRounds * 512>(d, sp);
 }
 
-// Stages tile [t_begin, t_begin + n_valid) of (b, h); returns the number of
-// tokens the consumer may read (0 when the block table maps the tile outside
-// the pool, after flagging TQ_DEV_ERR_BLOCK).  Cold tiles start at a multiple of
-// the tile size and never straddle a block; a hot tile (K only) may straddle one
-// boundary and is then copied token by token.
+// Paged staging of tile [t_begin, t_begin + n_valid) of (b, h); returns the
+// number of tokens the consumer may read (0 when the block table maps the tile
+// outside the pool, after flagging TQ_DEV_ERR_BLOCK).  Cold tiles start at a
+// multiple of the tile size and never straddle a block; a hot tile (K only)
+// may straddle one boundary and is then copied token by token.
 template <int KB, int VB>
-__device__ __forceinline__ int stage_tile(const DecodeParams& p, int b, int h, bool hot, int t_begin, int n_valid,
-                                          uint32_t buf, int lane) {
+__device__ __forceinline__ int stage_tile_paged(const DecodeParams& p, int b, int h, bool hot, int t_begin, int n_valid,
+                                             uint32_t buf, int lane) {
   using C = Cfg<KB, VB>;
   const long long row0 = p.map.row(b, h, t_begin);
   const long long rowl = p.map.row(b, h, t_begin + n_valid - 1);
@@ -420,10 +420,7 @@ __device__ __forceinline__ int stage_tile(const DecodeParams& p, int b, int h, b
   const uint8_t* ksrc = kbase + row0 * C::kKRow;
   const uint8_t* vsrc = reinterpret_cast<const uint8_t*>(p.v_words) + row0 * (VB * 16);
   const uint32_t vbuf = buf + C::kKTile + C::kKNorm;
-  if (n_valid == kTile && !straddle) {
-    copy_full<C::kKTile>(buf, ksrc, lane);
-    if (!hot) copy_full<C::kVTile>(vbuf, vsrc, lane);
-  } else if (!straddle) {
+  if (!straddle) {
     for (int c = lane; c < n_valid * (C::kKRow / 16); c += 32) cp_async16s(buf + 16u * c, ksrc + 16 * c);
     if (!hot)
       for (int c = lane; c < n_valid * (C::kVRow / 16); c += 32) cp_async16s(vbuf + 16u * c, vsrc + 16 * c);
@@ -435,19 +432,48 @@ __device__ __forceinline__ int stage_tile(const DecodeParams& p, int b, int h, b
       cp_async16s(buf + 16u * c, kbase + r * C::kKRow + (c - tok * kPer) * 16);
     }
   }
-  // norms: lanes 0..15 the K norms, lanes 16..31 the V norms of the tile's tokens
   const int nl = lane & 15;
   const bool is_k = lane < 16;
   const bool want = nl < n_valid && (is_k ? !C::kFp16K : !hot);
-  const long long rn = straddle ? p.map.row(b, h, t_begin + nl) : row0 + nl;
+  const long long rn = straddle ? p.map.row(b, h, t_begin + min(nl, n_valid - 1)) : row0 + nl;
   const float* nsrc = (is_k ? p.k_norms : p.v_norms) + rn;
   const uint32_t ndst = (is_k ? buf + C::kKTile : vbuf + C::kVTile) + 4u * nl;
   if (want) cp_async4s(ndst, nsrc);
   return n_valid;
 }
 
+// Stages tile [t_begin, t_begin + n_valid) of (b, h) into buf; returns the
+// number of tokens the consumer may read.
+template <int KB, int VB, bool PAGED>
+__device__ __forceinline__ int stage_tile(const DecodeParams& p, int b, int h, bool hot, int t_begin, int n_valid,
+                                          uint32_t buf, int lane) {
+  using C = Cfg<KB, VB>;
+  if constexpr (PAGED) return stage_tile_paged<KB, VB>(p, b, h, hot, t_begin, n_valid, buf, lane);
+  const int64_t row0 = (static_cast<int64_t>(b) * p.hkv + h) * p.cap + t_begin;
+  const uint8_t* ksrc = C::kFp16K ? reinterpret_cast<const uint8_t*>(p.k_fp16 + row0 * D)
+                                  : reinterpret_cast<const uint8_t*>(p.k_words + row0 * (C::kKBits * 4));
+  const uint8_t* vsrc = reinterpret_cast<const uint8_t*>(p.v_words + row0 * (VB * 4));
+  const uint32_t vbuf = buf + C::kKTile + C::kKNorm;
+  if (n_valid == kTile) {
+    copy_full<C::kKTile>(buf, ksrc, lane);
+    if (!hot) copy_full<C::kVTile>(vbuf, vsrc, lane);
+  } else {
+    for (int c = lane; c < n_valid * (C::kKRow / 16); c += 32) cp_async16s(buf + 16u * c, ksrc + 16 * c);
+    if (!hot)
+      for (int c = lane; c < n_valid * (C::kVRow / 16); c += 32) cp_async16s(vbuf + 16u * c, vsrc + 16 * c);
+  }
+  // norms: lanes 0..15 the K norms, lanes 16..31 the V norms of the tile's tokens
+  const int nl = lane & 15;
+  const bool is_k = lane < 16;
+  const bool want = nl < n_valid && (is_k ? !C::kFp16K : !hot);
+  const float* nsrc = (is_k ? p.k_norms : p.v_norms) + row0 + nl;
+  const uint32_t ndst = (is_k ? buf + C::kKTile : vbuf + C::kVTile) + 4u * nl;
+  if (want) cp_async4s(ndst, nsrc);
+  return n_valid;
+}
+
 // Split kernel.
-template <int G, int KB, int VB, bool SPARSE>
+template <int G, int KB, int VB, bool SPARSE, bool PAGED>
 __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeParams p) {
   using C = Cfg<KB, VB>;
   constexpr int S = C::kStages;
@@ -534,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
       const bool hot = cur.x >= cur.tc;
       const int t_begin = hot ? cur.ce + (cur.x - cur.tc) * kTile : cur.x * kTile;
       const int n_valid = min(kTile, (hot ? cur.len : cur.ce) - t_begin);
-      const int staged = stage_tile<KB, VB>(p, cur.b, cur.h, hot, t_begin, n_valid,
+      const int staged = stage_tile<KB, VB, PAGED>(p, cur.b, cur.h, hot, t_begin, n_valid,
                                             ring + static_cast<uint32_t>((j_issue % S) * C::kBuf), lane);
       if (lane == 0) descs[j_issue % S] = make_int4(cur.b, cur.h | (hot << 16), t_begin, staged);
       cursor_advance(p, cur, kWarps);
@@ -980,10 +1006,10 @@ __device__ __forceinline__ int cta_of(long long t, long long total, int grid) {
 }
 __device__ __forceinline__ long long cta_start(int c, long long total, int grid) { return total * c / grid; }
 
-template <int G, int KB, int VB, bool SPARSE>
+template <int G, int KB, int VB, bool SPARSE, bool PAGED>
 tq_status launch_split(const DecodeParams& p, cudaStream_t stream) {
   using C = Cfg<KB, VB>;
-  auto kern = decode_split_kernel<G, KB, VB, SPARSE>;
+  auto kern = decode_split_kernel<G, KB, VB, SPARSE, PAGED>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) != cudaSuccess)
     return TQ_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
@@ -1000,38 +1026,42 @@ tq_status launch_split(const DecodeParams& p, cudaStream_t stream) {
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 
-template <int G, int KB, bool SPARSE>
+template <int G, int KB, bool SPARSE, bool PAGED>
 tq_status dispatch_vb(const DecodeParams& p, int vb, cudaStream_t s) {
   switch (vb) {
-    case 2: return launch_split<G, KB, 2, SPARSE>(p, s);
-    case 3: return launch_split<G, KB, 3, SPARSE>(p, s);
-    default: return launch_split<G, KB, 4, SPARSE>(p, s);
+    case 2: return launch_split<G, KB, 2, SPARSE, PAGED>(p, s);
+    case 3: return launch_split<G, KB, 3, SPARSE, PAGED>(p, s);
+    default: return launch_split<G, KB, 4, SPARSE, PAGED>(p, s);
   }
 }
 
-template <int G, bool SPARSE>
+template <int G, bool SPARSE, bool PAGED>
 tq_status dispatch_kb(const DecodeParams& p, int kb, int vb, cudaStream_t s) {
   switch (kb) {
-    case 2: return dispatch_vb<G, 2, SPARSE>(p, vb, s);
-    case 3: return dispatch_vb<G, 3, SPARSE>(p, vb, s);
-    case 4: return dispatch_vb<G, 4, SPARSE>(p, vb, s);
-    default: return dispatch_vb<G, 16, SPARSE>(p, vb, s);
+    case 2: return dispatch_vb<G, 2, SPARSE, PAGED>(p, vb, s);
+    case 3: return dispatch_vb<G, 3, SPARSE, PAGED>(p, vb, s);
+    case 4: return dispatch_vb<G, 4, SPARSE, PAGED>(p, vb, s);
+    default: return dispatch_vb<G, 16, SPARSE, PAGED>(p, vb, s);
   }
 }
 
-// Split kernels of one variant (dense or sparse V) for any group size and widths.
-template <bool SPARSE>
+// Split kernels of one variant (dense or sparse V, contiguous or paged) for any
+// group size and widths.
+template <bool SPARSE, bool PAGED>
 tq_status dispatch_split_variant(const DecodeParams& p, int g, int kb, int vb, cudaStream_t s) {
   switch (g) {
-    case 1: return dispatch_kb<1, SPARSE>(p, kb, vb, s);
-    case 2: return dispatch_kb<2, SPARSE>(p, kb, vb, s);
-    default: return dispatch_kb<4, SPARSE>(p, kb, vb, s);
+    case 1: return dispatch_kb<1, SPARSE, PAGED>(p, kb, vb, s);
+    case 2: return dispatch_kb<2, SPARSE, PAGED>(p, kb, vb, s);
+    default: return dispatch_kb<4, SPARSE, PAGED>(p, kb, vb, s);
   }
 }
 
 }  // namespace
 
-// Split-K launch of the sparse-V variant (in its own translation unit).
+// Split-K launches of the other variants, each in a translation unit of its own
+// (the dense contiguous one is in tq_decode.cu).
 tq_status dispatch_split_sparse(const DecodeParams& p, int g, int kb, int vb, cudaStream_t s);
+tq_status dispatch_split_paged(const DecodeParams& p, int g, int kb, int vb, cudaStream_t s);
+tq_status dispatch_split_paged_sparse(const DecodeParams& p, int g, int kb, int vb, cudaStream_t s);
 
 }  // namespace tq

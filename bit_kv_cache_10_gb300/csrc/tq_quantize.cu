@@ -175,6 +175,7 @@ __device__ __forceinline__ void quantize_step(const uint8_t* tile, int row, int 
   }
 }
 
+template <bool PAGED>
 __global__ void __launch_bounds__(kWarps * 32, 1) quantize_append_kernel(const QuantParams p) {
   asm volatile("griddepcontrol.launch_dependents;\n");  // the next grid may start its prologue
   extern __shared__ __align__(16) uint8_t smem[];
@@ -240,7 +241,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1) quantize_append_kernel(const Q
         int pos = 0;
         const bool have = src_row(p, jb, row, &pos) != nullptr;
         if (!__any_sync(0xffffffffu, have)) break;  // rows are filled in order: no later step has one
-        const long long ridx = have ? p.map.row(jb.b, jb.h, pos) : 0;  // cache row (block table or contiguous)
+        long long ridx = (static_cast<long long>(jb.b) * p.heads + jb.h) * p.cap + pos;  // cache row
+        if constexpr (PAGED) ridx = have ? p.map.row(jb.b, jb.h, pos) : 0;  // through the block table
         const bool to_copy = copy_k || (!k_tensor && pos >= cold_end);
         const bool to_ring = !copy_k && to_copy;  // hot V goes to the per-sequence ring, not the pool
         if (have && ridx < 0 && !to_ring && p.status != nullptr) atomicOr(p.status, TQ_DEV_ERR_BLOCK);
@@ -290,8 +292,9 @@ int sm_count() {
 tq_status launch_quantize(QuantParams& p, cudaStream_t stream) {
   if (p.jobs <= 0) return TQ_OK;
   const size_t smem = quant_smem_bytes(p.k_lut_a, p.v_lut_a);
-  if (cudaFuncSetAttribute(quantize_append_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem)) != cudaSuccess)
+  const bool paged = p.map.table != nullptr;
+  auto kern = paged ? quantize_append_kernel<true> : quantize_append_kernel<false>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
     return TQ_ERR_CUDA;
   const int sms = sm_count();
   if (sms <= 0) return TQ_ERR_CUDA;
@@ -306,7 +309,7 @@ tq_status launch_quantize(QuantParams& p, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, quantize_append_kernel, p) != cudaSuccess) return TQ_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return TQ_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 
