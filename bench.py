@@ -339,6 +339,42 @@ def time_plain_decode(torch, batch, ctx, k_fp16, reps=50):
     return ms, nbytes
 
 
+def paged_decode_ms(torch, tc, lens0, q, seqs, max_len, bs=64, reps=20):
+    """Mean decode-call time of a paged copy of `tc` (blocks of `bs` tokens in a
+    randomly permuted pool), after 3 untimed calls."""
+    from bit_kv_cache_10_gb300.cache import TurboQuantKVCache
+    cap = (tc.capacity + bs - 1) // bs * bs
+    mb = cap // bs
+    nb = B * mb
+    pg = TurboQuantKVCache(B, HKV, HQ, cap, bits=(KB, VB), hot_window=W, block_size=bs, num_blocks=nb)
+    table = torch.from_numpy(np.random.default_rng(SEED).permutation(nb).astype(np.int32).reshape(B, mb)).cuda()
+    pg.block_table.copy_(table)
+    for name in ("k_cache", "k_norms", "v_cache", "v_norms"):
+        src, dst = getattr(tc, name), getattr(pg, name)
+        for b in range(B):
+            full = torch.zeros((HKV, cap) + tuple(src.shape[3:]), dtype=src.dtype, device=src.device)
+            full[:, :tc.capacity] = src[b]
+            dst[table[b].long()] = full.view((HKV, mb, bs) + tuple(src.shape[3:])).transpose(0, 1)
+    pg.v_hot.copy_(tc.v_hot)
+    out = torch.empty(B, HQ, D, dtype=torch.float32, device="cuda")
+    ws = torch.empty(pg.workspace_bytes(max_len), dtype=torch.uint8, device="cuda")
+    for _ in range(3):
+        pg.decode(q, seqs, max_len, out=out, workspace=ws)
+    st = torch.cuda.current_stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+    torch.cuda.synchronize()
+    ev[0].record(st)
+    for i in range(reps):
+        pg.decode(q, seqs, max_len, out=out, workspace=ws)
+        ev[i + 1].record(st)
+    torch.cuda.synchronize()
+    if pg.device_status() != 0:
+        raise RuntimeError("device status set by the paged decode")
+    ms = float(np.mean([ev[i].elapsed_time(ev[i + 1]) for i in range(reps)]))
+    del pg
+    return ms
+
+
 def step_inputs(n_steps):
     """Per-step new K/V tokens [S, B, Hkv, 1, D] and queries [S, B, Hq, D], fp16."""
     g = synth.rng(SEED + 1, synth.STREAM_Q)
@@ -455,6 +491,9 @@ def run_gpu(args):
     if tc.device_status() != 0:
         raise RuntimeError("device status set by the sparse-V decode")
 
+    # paged layout: the same cache copied into 64-token blocks scattered over a pool
+    paged_ms = paged_decode_ms(torch, tc, lens0, q_dev[sv_s], seqs[sv_s], max_len)
+
     # end to end through the public API with host buffers
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
     h_k, h_v, h_q = pin(kn), pin(vn), pin(qn)
@@ -555,6 +594,10 @@ def run_gpu(args):
                      "value": decode_bytes(lens0 + sv_s + 1) / (sparse_ms * 1e-3) / 1e9, "unit": "GB/s",
                      "note": "same long-context decode call with V skipped for weights below 1e-3 of the running "
                              "maximum (random synthetic codes: diffuse attention, few skips)"},
+        "paged": {"block_size": 64, "ms": paged_ms,
+                  "value": decode_bytes(lens0 + sv_s + 1) / (paged_ms * 1e-3) / 1e9, "unit": "GB/s",
+                  "note": "same long-context decode call on a block-table copy of the cache (64-token blocks, "
+                          "permuted pool)"},
         "asym": {"value": asym_bytes / (asym_ms * 1e-3) / 1e9, "unit": "GB/s", "ms": asym_ms,
                  "frac": asym_bytes / (asym_ms * 1e-3) / 1e9 / peak, "algorithmic_bytes_per_launch": asym_bytes,
                  "workload": "asym decode: fp16 K + 4-bit V, B8, 32q/8kv, d128, context 16384, no hot window"},
