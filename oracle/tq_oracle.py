@@ -23,6 +23,9 @@ Sources (pages, by title and section):
   - "Available modes": fp16 K + 4-bit V (asym), 4-bit K and V (sym), hot fp16
     V window + packed cold tail (delegated).
   - "WHT head-dimension constraint": power-of-two head_dim only.
+  - "Available modes" and the "Measured speed and the memory trade-off" table:
+    the int8 mode, per-token INT8 absmax quantization of K and V (~2x), whose
+    dequantization is a scale-and-add with no rotation and no codebook.
 
 Where the pages leave a step open this file takes the plainest reading; every
 such reading is listed in the design notes and repeated at the function.
@@ -349,6 +352,54 @@ def dequantize_rows(codes: np.ndarray, norms32: np.ndarray, rot: np.ndarray, cb:
 
 
 # --------------------------------------------------------------------------
+# Per-token INT8 absmax mode
+# --------------------------------------------------------------------------
+
+INT8_LEVEL = 127  # largest code magnitude: the absmax maps to +-127
+
+
+def int8_quantize_rows(x16: np.ndarray):
+    """Per-token INT8 absmax quantization of fp16 rows [N, d].
+
+    [mlxcel doc, "Available modes"]: the int8 mode quantizes each token with
+    its absolute maximum.  Reading (the pages give no formula): one float32
+    scale per (token, KV head) vector, s = fp32(max_i |x_i|) / 127 (float32
+    division, correctly rounded), and code_i = the integer nearest to the
+    float32 quotient fp32(x_i) / s (float32 division), ties to even, clamped
+    to [-127, 127].  A zero vector gets s = 0 and all codes 0.  The quotient
+    and the rounding are taken in float32, the precision the kernel decides in.
+    Returns (codes int8 [N, d], scales float32 [N]).
+    """
+    x = np.ascontiguousarray(x16).reshape(-1, x16.shape[-1]).astype(np.float32)
+    amax = np.abs(x).max(axis=1) if x.shape[1] else np.zeros(x.shape[0], np.float32)
+    s = (amax / np.float32(INT8_LEVEL)).astype(np.float32)
+    safe = np.where(s > 0, s, np.float32(1.0)).astype(np.float32)
+    quot = (x / safe[:, None]).astype(np.float32)
+    codes = np.clip(np.rint(quot), -INT8_LEVEL, INT8_LEVEL)
+    codes = np.where((s > 0)[:, None], codes, 0).astype(np.int8)
+    return codes.reshape(x16.shape), s.reshape(x16.shape[:-1])
+
+
+def int8_dequantize_rows(codes: np.ndarray, scales32: np.ndarray) -> np.ndarray:
+    """x_hat = s * code, float64 [N, d] (exact: a float32 scale times a code of
+    at most 8 bits fits in float64).  [mlxcel doc, "Measured speed and the
+    memory trade-off"]: int8 dequantization is a scale-and-add."""
+    return scales32.astype(np.float64)[..., None] * codes.astype(np.float64)
+
+
+def int8_words(codes: np.ndarray) -> np.ndarray:
+    """Stored form of int8 codes [N, d]: uint32 words [N, d/4], code i in byte
+    i mod 4 (bits 8 (i mod 4) ..) of word i // 4 as two's complement, i.e. the
+    LSB-first bitstream of ``pack`` with 8-bit fields."""
+    return pack(codes.view(np.uint8), 8)
+
+
+def int8_codes(words: np.ndarray, d: int) -> np.ndarray:
+    """Inverse of ``int8_words``."""
+    return unpack(words, 8, d).view(np.int8)
+
+
+# --------------------------------------------------------------------------
 # A packed cache as the oracle sees it, and decode attention over it
 # --------------------------------------------------------------------------
 
@@ -359,6 +410,8 @@ class PackedCache:
 
     k_fp16 is None for packed K; then k_words [B, Hkv, cap, d*kb/32] uint32
     and k_norms [B, Hkv, cap] float32.  v_words / v_norms likewise for V.
+    With codec "int8" (k_bits = v_bits = 8) the words hold int8 codes
+    (``int8_words``) and the norms the per-token absmax scales.
     With hot_window W > 0, v_hot [B, Hkv, W, d] fp16 holds position p of the
     last min(W, L) positions in slot p mod W and the packed V covers the rest.
     """
@@ -374,6 +427,7 @@ class PackedCache:
     v_norms: np.ndarray
     hot_window: int = 0
     v_hot: np.ndarray | None = None
+    codec: str = "turbo"  # "int8": K and V words hold int8 codes, the norms hold absmax scales
 
 
 def cold_end(length: int, hot_window: int) -> int:
@@ -382,11 +436,15 @@ def cold_end(length: int, hot_window: int) -> int:
 
 
 def build_cache(k16: np.ndarray, v16: np.ndarray, lengths, capacity: int, k_bits: int, v_bits: int,
-                seed: int = 0, layer: int = 0, k_fp16: bool = False, hot_window: int = 0) -> PackedCache:
+                seed: int = 0, layer: int = 0, k_fp16: bool = False, hot_window: int = 0,
+                codec: str = "turbo") -> PackedCache:
     """Quantize full fp16 K/V [B, Hkv, T, d] into the state a cache holds after
-    its sequences reached ``lengths`` (positions >= L of a row stay zero)."""
+    its sequences reached ``lengths`` (positions >= L of a row stay zero).
+    codec "int8" stores K and V with ``int8_quantize_rows`` (bits ignored)."""
     b_, hk, t_, d = k16.shape
     lengths = np.asarray(lengths)
+    if codec == "int8":
+        return _build_int8_cache(k16, v16, lengths, capacity, seed, layer, hot_window)
     wk = d * k_bits // 32
     wv = d * v_bits // 32
     cb_k = None if k_fp16 else codebook(d, k_bits)
@@ -417,9 +475,39 @@ def build_cache(k16: np.ndarray, v16: np.ndarray, lengths, capacity: int, k_bits
                        hot_window, v_hot)
 
 
+def _build_int8_cache(k16, v16, lengths, capacity, seed, layer, hot_window) -> PackedCache:
+    b_, hk, _, d = k16.shape
+    k_words = np.zeros((b_, hk, capacity, d // 4), np.uint32)
+    k_norms = np.zeros((b_, hk, capacity), np.float32)
+    v_words = np.zeros((b_, hk, capacity, d // 4), np.uint32)
+    v_norms = np.zeros((b_, hk, capacity), np.float32)
+    v_hot = np.zeros((b_, hk, hot_window, d), np.float16) if hot_window > 0 else None
+    for b in range(b_):
+        length = int(lengths[b])
+        ce = cold_end(length, hot_window)
+        for h in range(hk):
+            codes, s = int8_quantize_rows(k16[b, h, :length])
+            k_words[b, h, :length] = int8_words(codes)
+            k_norms[b, h, :length] = s
+            codes, s = int8_quantize_rows(v16[b, h, :ce])
+            v_words[b, h, :ce] = int8_words(codes)
+            v_norms[b, h, :ce] = s
+            for p in range(ce, length):
+                v_hot[b, h, p % hot_window] = v16[b, h, p]
+    return PackedCache(seed, layer, d, 8, 8, k_words, k_norms, None, v_words, v_norms, hot_window, v_hot, "int8")
+
+
 def dequantized_kv(cache: PackedCache, b: int, h: int, length: int):
     """Float64 K and V of positions [0, length) of one (batch, KV head) row."""
     d = cache.head_dim
+    if cache.codec == "int8":
+        k = int8_dequantize_rows(int8_codes(cache.k_words[b, h, :length], d), cache.k_norms[b, h, :length])
+        ce = cold_end(length, cache.hot_window)
+        v = np.empty((length, d), np.float64)
+        v[:ce] = int8_dequantize_rows(int8_codes(cache.v_words[b, h, :ce], d), cache.v_norms[b, h, :ce])
+        for p in range(ce, length):
+            v[p] = cache.v_hot[b, h, p % cache.hot_window].astype(np.float64)
+        return k, v
     rot = rotation(cache.seed, cache.layer, h, d)
     if cache.k_fp16 is not None:
         k = cache.k_fp16[b, h, :length].astype(np.float64)
