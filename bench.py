@@ -339,6 +339,73 @@ def time_plain_decode(torch, batch, ctx, k_fp16, reps=50):
     return ms, nbytes
 
 
+# int8-mode scales giving K and V the magnitudes of the packed workload (|k| ~ 12,
+# |v| ~ 30): a uniform random code has rms 73.3, a 128-vector of them norm ~ 829
+INT8_K_SCALE, INT8_V_SCALE = 12.0 / 829.4, 30.0 / 829.4
+
+
+def build_int8_cache(torch, lens, cap):
+    """int8-mode cache (no hot window) with random codes and lognormal scales
+    in rows [0, L_b) of every (b, h)."""
+    from bit_kv_cache_10_gb300.cache import TurboQuantKVCache
+    tc = TurboQuantKVCache(len(lens), HKV, HQ, cap, bits="int8")
+    for b, L in enumerate(lens):
+        L = int(L)
+        for h in range(HKV):
+            kw, ks = synth.packed_row(SEED + 7, synth.STREAM_CODES_K, b, h, L, D // 4, INT8_K_SCALE)
+            vw, vs = synth.packed_row(SEED + 7, synth.STREAM_CODES_V, b, h, L, D // 4, INT8_V_SCALE)
+            tc.k_cache[b, h, :L].copy_(torch.from_numpy(kw.view(np.int32)))
+            tc.k_norms[b, h, :L].copy_(torch.from_numpy(ks))
+            tc.v_cache[b, h, :L].copy_(torch.from_numpy(vw.view(np.int32)))
+            tc.v_norms[b, h, :L].copy_(torch.from_numpy(vs))
+    torch.cuda.synchronize()
+    return tc
+
+
+def time_int8(torch, lens, reps=20):
+    """int8 mode on the long-context lengths: mean decode-call time (ms) and its
+    algorithmic bytes (128 code bytes + a 4-byte scale for K and for V of every
+    position, fp16 queries, float32 outputs); then the quantize-append time of
+    the quantize workload (B16 x 8192 tokens x 8 heads)."""
+    from bit_kv_cache_10_gb300.cache import TurboQuantKVCache
+    cap = int(np.max(lens))
+    tc = build_int8_cache(torch, lens, cap)
+    q = torch.from_numpy(synth.queries_fp16(SEED + 7, len(lens), HQ, D)).cuda()
+    sl = torch.from_numpy(np.asarray(lens, np.int32)).cuda()
+    out = torch.empty(len(lens), HQ, D, dtype=torch.float32, device="cuda")
+    ws = torch.empty(tc.workspace_bytes(cap), dtype=torch.uint8, device="cuda")
+    st = torch.cuda.current_stream()
+
+    def timed(fn, n):
+        for _ in range(3):
+            fn()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+        torch.cuda.synchronize()
+        ev[0].record(st)
+        for i in range(n):
+            fn()
+            ev[i + 1].record(st)
+        torch.cuda.synchronize()
+        return float(np.mean([ev[i].elapsed_time(ev[i + 1]) for i in range(n)]))
+
+    dec_ms = timed(lambda: tc.decode(q, sl, cap, out=out, workspace=ws), reps)
+    if tc.device_status() != 0:
+        raise RuntimeError("device status set by the int8 decode timing")
+    dec_bytes = int(np.sum(lens)) * HKV * 2 * (D + 4) + len(lens) * HQ * D * (2 + 4)
+    del tc, ws
+    g = synth.rng(SEED + 2, synth.STREAM_K)
+    kq = torch.from_numpy(g.standard_normal((QB, HKV, QT, D), dtype=np.float32).astype(np.float16)).cuda()
+    vq = torch.from_numpy(g.standard_normal((QB, HKV, QT, D), dtype=np.float32).astype(np.float16)).cuda()
+    qc = TurboQuantKVCache(QB, HKV, HKV * 4, QT, bits="int8")
+    zero = torch.zeros(QB, dtype=torch.int32, device="cuda")
+    q_ms = timed(lambda: qc.append(kq, vq, zero), 10)
+    if qc.device_status() != 0:
+        raise RuntimeError("device status set by the int8 quantize timing")
+    q_bytes = 2 * QB * HKV * QT * (D * 2 + D + 4)
+    del kq, vq, qc
+    return dec_ms, dec_bytes, q_ms, q_bytes
+
+
 def paged_decode_ms(torch, tc, lens0, q, seqs, max_len, bs=64, reps=20):
     """Mean decode-call time of a paged copy of `tc` (blocks of `bs` tokens in a
     randomly permuted pool), after 3 untimed calls."""
@@ -564,6 +631,7 @@ def run_gpu(args):
     # 3.5-bit Llama-3-8B-like layer (B1, context 4096; launch- and L2-bound)
     asym_ms, asym_bytes = time_plain_decode(torch, 8, 16384, True)
     small_ms, small_bytes = time_plain_decode(torch, 1, 4096, False, reps=200)
+    i8_ms, i8_bytes, i8q_ms, i8q_bytes = time_int8(torch, lens0)
 
     peak, peak_kind = measured_peak()
     dec_avg_ms = float(np.mean(decode_ms))
@@ -601,6 +669,12 @@ def run_gpu(args):
         "asym": {"value": asym_bytes / (asym_ms * 1e-3) / 1e9, "unit": "GB/s", "ms": asym_ms,
                  "frac": asym_bytes / (asym_ms * 1e-3) / 1e9 / peak, "algorithmic_bytes_per_launch": asym_bytes,
                  "workload": "asym decode: fp16 K + 4-bit V, B8, 32q/8kv, d128, context 16384, no hot window"},
+        "int8": {"value": i8_bytes / (i8_ms * 1e-3) / 1e9, "unit": "GB/s", "ms": i8_ms,
+                 "frac": i8_bytes / (i8_ms * 1e-3) / 1e9 / peak, "algorithmic_bytes_per_launch": i8_bytes,
+                 "workload": "int8-mode decode (per-token INT8 absmax K and V, no hot window): B4, 32q/8kv, "
+                             "d128, the long-context lengths",
+                 "quantize_mtokens_s": QB * QT / (i8q_ms * 1e-3) / 1e6, "quantize_ms": i8q_ms,
+                 "quantize_hbm_gbs": i8q_bytes / (i8q_ms * 1e-3) / 1e9},
         "llama_layer": {"value": small_bytes / (small_ms * 1e-3) / 1e9, "unit": "GB/s", "ms": small_ms,
                         "algorithmic_bytes_per_launch": small_bytes,
                         "workload": "3.5-bit decode: B1, 32q/8kv, d128, context 4096, K3/V4 (launch-bound: "
@@ -647,6 +721,18 @@ def run_profile(args):
         torch.cuda.synchronize()
         print(json.dumps({"profile": "decode", "steps": args.steps, "wall_ms_per_step":
                           (time.perf_counter() - t0) * 1e3 / max(1, args.steps), "status": tc.device_status()}))
+    elif args.profile == "int8":
+        lens = synth.seq_lengths(SEED, B, LO, HI)
+        cap = int(np.max(lens))
+        tc = build_int8_cache(torch, lens, cap)
+        q = torch.from_numpy(synth.queries_fp16(SEED + 7, B, HQ, D)).cuda()
+        sl = torch.from_numpy(np.asarray(lens, np.int32)).cuda()
+        out = torch.empty(B, HQ, D, dtype=torch.float32, device="cuda")
+        ws = torch.empty(tc.workspace_bytes(cap), dtype=torch.uint8, device="cuda")
+        for s in range(total):
+            tc.decode(q, sl, cap, out=out, workspace=ws)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile": "int8", "steps": total, "status": tc.device_status()}))
     elif args.profile == "asym":
         tc = build_plain_cache(torch, 8, 16384, True, SEED + 3)
         q = torch.from_numpy(synth.queries_fp16(SEED + 3, 8, HQ, D)).cuda()
@@ -678,7 +764,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle timing")
-    ap.add_argument("--profile", choices=["decode", "quantize", "asym"],
+    ap.add_argument("--profile", choices=["decode", "quantize", "asym", "int8"],
                     help="run only warm-up + timed steps of one part (for ncu captures); prints a short line")
     ap.add_argument("--profile-batch", type=int, default=4, help="batch of the quantize part in --profile mode")
     args = ap.parse_args()

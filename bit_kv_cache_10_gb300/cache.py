@@ -20,8 +20,10 @@ def _stream_handle(device) -> int:
 class TurboQuantKVCache:
     """Packed K/V cache of one attention layer.
 
-    ``bits`` may be fractional (K gets floor, V gets ceil) or a (k_bits,
-    v_bits) pair; ``k_fp16=True`` keeps K in fp16 (the asym modes);
+    ``bits`` may be fractional (K gets floor, V gets ceil), a (k_bits,
+    v_bits) pair, or "int8" for the per-token INT8 absmax mode (int8 K and V
+    codes, the norms buffers holding the absmax scales; no rotation);
+    ``k_fp16=True`` keeps K in fp16 (the asym modes);
     ``hot_window`` > 0 keeps the newest V tokens in an fp16 ring;
     ``sparse_v_threshold`` > 0 lets decode skip the V rows of (token, head)
     pairs whose softmax weight is below it (0 decodes densely);
@@ -35,15 +37,22 @@ class TurboQuantKVCache:
     def __init__(self, batch: int, num_kv_heads: int, num_q_heads: int, capacity: int, bits=3.5,
                  head_dim: int = 128, k_fp16: bool = False, hot_window: int = 0, seed: int = 0, layer: int = 0,
                  device="cuda", sparse_v_threshold: float = 0.0, block_size: int = 0, num_blocks=None):
-        if isinstance(bits, tuple):
+        int8 = isinstance(bits, str)
+        if int8:
+            if bits != "int8" or k_fp16:
+                raise ValueError('bits must be a number, a (k_bits, v_bits) pair or "int8" (with packed K)')
+            k_bits, v_bits = 8, 8
+        elif isinstance(bits, tuple):
             k_bits, v_bits = bits
         else:
             k_bits, v_bits = N.tq_split_bits(float(bits))
+        self.int8 = int8
+        mode = N.TQ_KV_INT8 if int8 else N.TQ_K_FP16 if k_fp16 else N.TQ_K_PACKED
         self.device = torch.device(device)
         if self.device.type == "cuda" and self.device.index is None:
             self.device = torch.device("cuda", torch.cuda.current_device())
         self.desc = N.tq_cache_desc_init(batch, num_kv_heads, num_q_heads, head_dim, capacity,
-                                         N.TQ_K_FP16 if k_fp16 else N.TQ_K_PACKED, 0 if k_fp16 else k_bits, v_bits,
+                                         mode, 0 if k_fp16 else k_bits, v_bits,
                                          hot_window, seed, layer)
         d = self.desc
         self.batch, self.num_kv_heads, self.num_q_heads = batch, num_kv_heads, num_q_heads

@@ -13,8 +13,8 @@ namespace {
 // sharing the KV head h.  Lane l holds coordinates 4 l .. 4 l + 3: it finds the
 // CTAs that covered the (b, h) rows, log-sum-exp combines their partials, rotates
 // the cold sum back (sign flips and a Hadamard transform over index bits 0..1 in
-// registers and 2..6 across lanes, 1/sqrt d), adds the hot sum and divides by the
-// softmax mass.
+// registers and 2..6 across lanes, 1/sqrt d; not in the int8 mode), adds the hot
+// sum and divides by the softmax mass.
 __global__ void __launch_bounds__(4 * 32) decode_merge_kernel(const DecodeParams p) {
   const int g = p.hq / p.hkv;
   const int jj = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -97,7 +97,14 @@ __global__ void __launch_bounds__(4 * 32) decode_merge_kernel(const DecodeParams
       else y[k] = ffma(av[k], sc, y[k]);
     }
   }
-  // inverse rotation of the cold sum: D_h H y / sqrt(d), index t = 4 lane + i
+  // inverse rotation of the cold sum: D_h H y / sqrt(d), index t = 4 lane + i (the
+  // int8 mode sums V unrotated)
+  if (!p.rotated) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) y[i] = l > 0.0f ? fadd(y[i], hv[i]) / l : 0.0f;
+    out[lane] = make_float4(y[0], y[1], y[2], y[3]);
+    return;
+  }
   {
     float a0 = fadd(y[0], y[1]), a1 = fsub(y[0], y[1]), a2 = fadd(y[2], y[3]), a3 = fsub(y[2], y[3]);  // bit 0
     y[0] = fadd(a0, a2);  // bit 1
@@ -188,6 +195,7 @@ extern "C" tq_status tq_decode_attention(const tq_cache_desc* d, const void* q, 
   p.ws_ml = p.ws_acc + slots * g * D;
   p.grid = sms < kMaxDecodeCtas ? sms : kMaxDecodeCtas;
   p.sparse_tau = d->sparse_v_threshold;
+  p.rotated = d->k_mode != TQ_KV_INT8;
   p.out = out;
 
   const int kb = d->k_mode == TQ_K_FP16 ? 16 : d->k_bits;

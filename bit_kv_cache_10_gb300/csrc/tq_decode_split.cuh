@@ -65,6 +65,7 @@ struct DecodeParams {
   float* ws_acc;  // [slots][G][D]
   float* ws_ml;   // [slots][G][2] (max, sum)
   float sparse_tau;  // sparse-V threshold (0: dense)
+  int rotated;    // 1: V is summed in the rotated domain (packed modes); 0: int8 mode
   int grid;       // CTAs of the split kernel
   float* out;     // [B, Hq, D]
 };
@@ -193,6 +194,8 @@ __device__ __forceinline__ TileInfo tile_info(const DecodeParams& p, const long 
 template <int KB, int VB>
 struct Cfg {
   static constexpr bool kFp16K = KB == 16;
+  static constexpr bool kInt8 = KB == 8;               // int8 mode: K and V int8 codes with absmax scales
+  static_assert(!kInt8 || VB == 8, "the int8 mode has int8 K and V");
   static constexpr int kKBits = kFp16K ? 2 : KB;       // placeholder width when K is fp16
   static constexpr int kKRow = kFp16K ? 256 : KB * 16;  // bytes of one K token
   static constexpr int kVRow = VB * 16;
@@ -204,8 +207,9 @@ struct Cfg {
   // [128,256) of row e (16 copies x 8 bytes); fp16 K: V only, 128-byte rows.  The
   // table base is aligned to the table size so that an entry's address is
   // base | (e << row_shift) | copy * 8 (one OR instead of an add).
+  // The int8 mode needs no table: a 1 KB placeholder keeps the layout code uniform.
   static constexpr int kRowShift = kFp16K ? 7 : 8;
-  static constexpr int kTabBits = kFp16K ? 2 * VB : 2 * (VB > kKBits ? VB : kKBits);
+  static constexpr int kTabBits = kInt8 ? 2 : kFp16K ? 2 * VB : 2 * (VB > kKBits ? VB : kKBits);
   static constexpr int kTab = (1 << kTabBits) << kRowShift;
   static constexpr int kWts = kTile * 32;  // per warp: (w, w) x 4 heads per token
   static constexpr int kSmall = kWarps * kWts + 4 * D * 4 /* q' */ + 4 * D * 4 /* combine */ +
@@ -239,7 +243,7 @@ struct SmemLayout {
 // both chunks for 3-bit; consecutive 16-byte chunks per quarter-warp for fp16).
 template <int KB>
 __device__ __forceinline__ int k_pair_coord(int rr, int pr) {
-  if constexpr (KB == 4 || KB == 2) return 16 * rr + 2 * pr;
+  if constexpr (KB == 4 || KB == 2 || KB == 8) return 16 * rr + 2 * pr;
   else return (pr >> 2) * 64 + 8 * rr + 2 * (pr & 3);
 }
 // Tile token of K step u (0..3) in slot s.  For 48-byte (3-bit) records the
@@ -254,7 +258,7 @@ template <int KB>
 __device__ __forceinline__ uint32_t k_lane_offset(int s, int rr) {
   constexpr int kRec = KB == 16 ? 256 : KB * 16;
   const uint32_t tok = static_cast<uint32_t>(k_token<KB>(0, s) * kRec);
-  if constexpr (KB == 16) return tok + 16u * rr;
+  if constexpr (KB == 16 || KB == 8) return tok + 16u * rr;
   else if constexpr (KB == 4) return tok + 8u * rr;
   else if constexpr (KB == 2) return tok + 4u * rr;
   else return tok + 4u * ((3 * rr) >> 2);
@@ -263,13 +267,14 @@ __device__ __forceinline__ uint32_t k_lane_offset(int s, int rr) {
 template <int VB>
 __device__ __forceinline__ uint32_t v_lane_offset(int g, int r) {
   const uint32_t tok = static_cast<uint32_t>(g * VB * 16);
-  if constexpr (VB == 4) return tok + 4u * r;
+  if constexpr (VB == 8) return tok + 8u * r;
+  else if constexpr (VB == 4) return tok + 4u * r;
   else if constexpr (VB == 2) return tok + 4u * (r >> 1);
   else return tok + 4u * ((3 * r) >> 2);
 }
 template <int VB>
 __device__ __forceinline__ uint32_t v_lane_shift(int r) {
-  if constexpr (VB == 4) return 0u;
+  if constexpr (VB == 4 || VB == 8) return 0u;
   else if constexpr (VB == 2) return 16u * (r & 1);
   else return (24u * r) & 31u;
 }
@@ -293,6 +298,17 @@ __device__ __forceinline__ float2 lds64(uint32_t addr) {
   float2 v;
   asm("ld.shared.v2.f32 {%0, %1}, [%2];\n" : "=f"(v.x), "=f"(v.y) : "r"(addr));
   return v;
+}
+
+// Two int8 codes (bytes K and K + 1 of a word) as exact floats: the biased
+// byte u = code + 128 goes into the low mantissa byte of 2^23, and one packed
+// subtraction of 2^23 + 128 leaves the code.  `xw` is the word with every byte
+// already biased (w ^ 0x80808080).
+template <int K>
+__device__ __forceinline__ float2 int8_pair(uint32_t xw) {
+  const float a = __uint_as_float(__byte_perm(xw, 0x4B000000u, 0x7440 | K));
+  const float b = __uint_as_float(__byte_perm(xw, 0x4B000000u, 0x7440 | (K + 1)));
+  return add2(make_float2(a, b), make_float2(-8388736.0f, -8388736.0f));
 }
 // Shared loads at a register base plus a compile-time byte offset (no address arithmetic).
 template <int OFF>
@@ -348,6 +364,13 @@ __device__ __forceinline__ Cursor cursor_at(const DecodeParams& p, const long lo
   c.x = ti.hot ? c.tc + (ti.t_begin - c.ce) / kTile : ti.t_begin / kTile;
   return c;
 }
+// First token and token count of the tile a cursor points at.
+__device__ __forceinline__ int cursor_t_begin(const Cursor& c) {
+  return c.x >= c.tc ? c.ce + (c.x - c.tc) * kTile : c.x * kTile;
+}
+__device__ __forceinline__ int cursor_n_valid(const Cursor& c) {
+  return min(kTile, (c.x >= c.tc ? c.len : c.ce) - cursor_t_begin(c));
+}
 __device__ __forceinline__ void cursor_advance(const DecodeParams& p, Cursor& c, int n) {
   c.x += n;
   while (c.x >= c.per_h) {  // per_h is 0 for empty sequences
@@ -399,43 +422,63 @@ __device__ __forceinline__ void copy_full(uint32_t dst, const uint8_t* src, int 
     if (lane < kRest) cp_async16_at<kRounds * 512>(d, sp);
 }
 
-// Paged staging of tile [t_begin, t_begin + n_valid) of (b, h); returns the
-// number of tokens the consumer may read (0 when the block table maps the tile
-// outside the pool, after flagging TQ_DEV_ERR_BLOCK).  Cold tiles start at a
-// multiple of the tile size and never straddle a block; a hot tile (K only)
-// may straddle one boundary and is then copied token by token.
+// Block-table entries of the first and the last token of a tile.  The kernel
+// loads them one issue ahead, so that their latency hides behind the
+// consumption of a tile instead of stalling the copies that depend on them.
+struct TileBlocks {
+  int first, last;
+};
+__device__ __forceinline__ TileBlocks load_tile_blocks(const DecodeParams& p, int b, int t_begin, int n_valid) {
+  const int32_t* row = p.map.table + static_cast<long long>(b) * p.map.max_blocks;
+  TileBlocks tb;
+  tb.first = __ldg(row + (t_begin >> p.map.shift));
+  tb.last = __ldg(row + ((t_begin + n_valid - 1) >> p.map.shift));
+  return tb;
+}
+
+// Paged staging of tile [t_begin, t_begin + n_valid) of (b, h) whose block-table
+// entries are tb; returns the number of tokens the consumer may read (0 when
+// the table maps the tile outside the pool, after flagging TQ_DEV_ERR_BLOCK).
+// Cold tiles start at a multiple of the tile size and never straddle a block
+// (blocks hold at least one tile); a hot tile (K only) may straddle one boundary
+// and is then copied token by token.
 template <int KB, int VB>
-__device__ __forceinline__ int stage_tile_paged(const DecodeParams& p, int b, int h, bool hot, int t_begin, int n_valid,
-                                             uint32_t buf, int lane) {
+__device__ __forceinline__ int stage_tile_paged(const DecodeParams& p, int h, bool hot, int t_begin, int n_valid,
+                                             TileBlocks tb, uint32_t buf, int lane) {
   using C = Cfg<KB, VB>;
-  const long long row0 = p.map.row(b, h, t_begin);
-  const long long rowl = p.map.row(b, h, t_begin + n_valid - 1);
-  if (row0 < 0 || rowl < 0) {  // outside the pool: nothing is staged, the tile is read as empty
+  const int sh = p.map.shift;
+  const long long row0 = p.map.in_block(tb.first, h, t_begin);
+  if (row0 < 0 || p.map.in_block(tb.last, h, 0) < 0) {  // outside the pool: the tile is read as empty
     if (lane == 0 && p.status != nullptr) atomicOr(p.status, TQ_DEV_ERR_BLOCK);
     return 0;
   }
-  const bool straddle = rowl - row0 != n_valid - 1;
+  const int blk0 = t_begin >> sh;
+  const bool straddle = ((t_begin + n_valid - 1) >> sh) != blk0;
   const uint8_t* kbase = C::kFp16K ? reinterpret_cast<const uint8_t*>(p.k_fp16)
                                    : reinterpret_cast<const uint8_t*>(p.k_words);
   const uint8_t* ksrc = kbase + row0 * C::kKRow;
   const uint8_t* vsrc = reinterpret_cast<const uint8_t*>(p.v_words) + row0 * (VB * 16);
   const uint32_t vbuf = buf + C::kKTile + C::kKNorm;
-  if (!straddle) {
+  if (!straddle && n_valid == kTile) {
+    copy_full<C::kKTile>(buf, ksrc, lane);
+    if (!hot) copy_full<C::kVTile>(vbuf, vsrc, lane);
+  } else if (!straddle) {
     for (int c = lane; c < n_valid * (C::kKRow / 16); c += 32) cp_async16s(buf + 16u * c, ksrc + 16 * c);
     if (!hot)
       for (int c = lane; c < n_valid * (C::kVRow / 16); c += 32) cp_async16s(vbuf + 16u * c, vsrc + 16 * c);
   } else {  // hot tile across a block boundary: K token by token
     constexpr int kPer = C::kKRow / 16;
     for (int c = lane; c < n_valid * kPer; c += 32) {
-      const int tok = c / kPer;
-      const long long r = p.map.row(b, h, t_begin + tok);  // in the pool: both ends were checked
-      cp_async16s(buf + 16u * c, kbase + r * C::kKRow + (c - tok * kPer) * 16);
+      const int t = t_begin + c / kPer;
+      const long long r = p.map.in_block((t >> sh) == blk0 ? tb.first : tb.last, h, t);
+      cp_async16s(buf + 16u * c, kbase + r * C::kKRow + (c % kPer) * 16);
     }
   }
   const int nl = lane & 15;
   const bool is_k = lane < 16;
   const bool want = nl < n_valid && (is_k ? !C::kFp16K : !hot);
-  const long long rn = straddle ? p.map.row(b, h, t_begin + min(nl, n_valid - 1)) : row0 + nl;
+  const int tn = t_begin + min(nl, n_valid - 1);
+  const long long rn = straddle ? p.map.in_block((tn >> sh) == blk0 ? tb.first : tb.last, h, tn) : row0 + nl;
   const float* nsrc = (is_k ? p.k_norms : p.v_norms) + rn;
   const uint32_t ndst = (is_k ? buf + C::kKTile : vbuf + C::kVTile) + 4u * nl;
   if (want) cp_async4s(ndst, nsrc);
@@ -446,9 +489,9 @@ __device__ __forceinline__ int stage_tile_paged(const DecodeParams& p, int b, in
 // number of tokens the consumer may read.
 template <int KB, int VB, bool PAGED>
 __device__ __forceinline__ int stage_tile(const DecodeParams& p, int b, int h, bool hot, int t_begin, int n_valid,
-                                          uint32_t buf, int lane) {
+                                          TileBlocks tb, uint32_t buf, int lane) {
   using C = Cfg<KB, VB>;
-  if constexpr (PAGED) return stage_tile_paged<KB, VB>(p, b, h, hot, t_begin, n_valid, buf, lane);
+  if constexpr (PAGED) return stage_tile_paged<KB, VB>(p, h, hot, t_begin, n_valid, tb, buf, lane);
   const int64_t row0 = (static_cast<int64_t>(b) * p.hkv + h) * p.cap + t_begin;
   const uint8_t* ksrc = C::kFp16K ? reinterpret_cast<const uint8_t*>(p.k_fp16 + row0 * D)
                                   : reinterpret_cast<const uint8_t*>(p.k_words + row0 * (C::kKBits * 4));
@@ -505,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
   const uint32_t kbase = tab | 128u | copy8;
 
   // pair tables: entry e = code_a | code_b << bits -> (c[code_a], c[code_b]), 16 copies per row
-  if constexpr (!C::kFp16K) {
+  if constexpr (!C::kFp16K && !C::kInt8) {
     constexpr int n = (1 << (2 * C::kKBits)) * kCopies;
     for (int i = tid; i < n; i += kThreads) {
       const int e = i / kCopies, c = i % kCopies;
@@ -513,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
           make_float2(p.k_cent[e & ((1 << C::kKBits) - 1)], p.k_cent[e >> C::kKBits]);
     }
   }
-  {
+  if constexpr (!C::kInt8) {
     constexpr int n = (1 << (2 * VB)) * kCopies;
     for (int i = tid; i < n; i += kThreads) {
       const int e = i / kCopies, c = i % kCopies;
@@ -554,16 +597,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
   const int my_n = static_cast<int>((t1 - t0 - warp + kWarps - 1) / kWarps);  // tiles t0 + warp + kWarps j
   int j_issue = 0, j = 0;
   Cursor cur;
-  if (my_n > 0) cur = cursor_at(p, prefix, t0 + warp);
+  TileBlocks tb{0, 0};  // paged: block-table entries of the tile the cursor points at
+  if (my_n > 0) {
+    cur = cursor_at(p, prefix, t0 + warp);
+    if constexpr (PAGED) tb = load_tile_blocks(p, cur.b, cursor_t_begin(cur), cursor_n_valid(cur));
+  }
   auto issue = [&]() {
     if (j_issue < my_n) {
       const bool hot = cur.x >= cur.tc;
-      const int t_begin = hot ? cur.ce + (cur.x - cur.tc) * kTile : cur.x * kTile;
-      const int n_valid = min(kTile, (hot ? cur.len : cur.ce) - t_begin);
-      const int staged = stage_tile<KB, VB, PAGED>(p, cur.b, cur.h, hot, t_begin, n_valid,
-                                            ring + static_cast<uint32_t>((j_issue % S) * C::kBuf), lane);
+      const int t_begin = cursor_t_begin(cur);
+      const int n_valid = cursor_n_valid(cur);
+      const int staged = stage_tile<KB, VB, PAGED>(p, cur.b, cur.h, hot, t_begin, n_valid, tb,
+                                                   ring + static_cast<uint32_t>((j_issue % S) * C::kBuf), lane);
       if (lane == 0) descs[j_issue % S] = make_int4(cur.b, cur.h | (hot << 16), t_begin, staged);
       cursor_advance(p, cur, kWarps);
+      if constexpr (PAGED)
+        if (j_issue + 1 < my_n) tb = load_tile_blocks(p, cur.b, cursor_t_begin(cur), cursor_n_valid(cur));
     }
     cp_async_commit();
     ++j_issue;
@@ -598,10 +647,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
     const TileInfo si = tile_info(p, prefix, seg);
     const long long seg_end = si.row_end < t1 ? si.row_end : t1;
     if (si.b != cur_b || si.h != cur_h) {
-      // rotated query of the G heads: (log2 e / d) H D q for packed K, (log2 e / sqrt d) q for fp16 K
+      // rotated query of the G heads: (log2 e / d) H D q for packed K, (log2 e / sqrt d) q for fp16
+      // K and in the int8 mode (no rotation)
+      constexpr bool kRotQ = !C::kFp16K && !C::kInt8;
       __syncthreads();
       if (tid < D) {
-        const bool neg = !C::kFp16K && sign_negative(p.seed, p.layer, si.h, tid);
+        const bool neg = kRotQ && sign_negative(p.seed, p.layer, si.h, tid);
 #pragma unroll
         for (int jj = 0; jj < G; ++jj) {
           const float x = half_bits_to_float(p.q[(static_cast<int64_t>(si.b) * p.hq + si.h * G + jj) * D + tid]);
@@ -609,7 +660,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
         }
       }
       __syncthreads();
-      if constexpr (!C::kFp16K) {
+      if constexpr (kRotQ) {
 #pragma unroll
         for (int st = 1; st < D; st *= 2) {
           if (tid < D && (tid & st) == 0) {
@@ -623,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
           __syncthreads();
         }
       }
-      const float qscale = C::kFp16K ? kLog2e / kSqrtD : kLog2e / static_cast<float>(D);
+      const float qscale = kRotQ ? kLog2e / static_cast<float>(D) : kLog2e / kSqrtD;
 #pragma unroll
       for (int jj = 0; jj < G; ++jj)
 #pragma unroll
@@ -675,6 +726,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
             c[5] = half2_bits_to_float2(b.y);
             c[6] = half2_bits_to_float2(b.z);
             c[7] = half2_bits_to_float2(b.w);
+          } else if constexpr (C::kInt8) {
+            const uint4 a = lds128<OFF>(kw);
+            const uint32_t x0 = a.x ^ 0x80808080u, x1 = a.y ^ 0x80808080u;
+            const uint32_t x2 = a.z ^ 0x80808080u, x3 = a.w ^ 0x80808080u;
+            c[0] = int8_pair<0>(x0);
+            c[1] = int8_pair<2>(x0);
+            c[2] = int8_pair<0>(x1);
+            c[3] = int8_pair<2>(x1);
+            c[4] = int8_pair<0>(x2);
+            c[5] = int8_pair<2>(x2);
+            c[6] = int8_pair<0>(x3);
+            c[7] = int8_pair<2>(x3);
           } else if constexpr (KB == 4) {
             const uint2 wv = lds64u<OFF>(kw);
             c[0] = lds64(pair_addr<4, 0, kRS>(wv.x, kbase));
@@ -846,6 +909,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
         constexpr int kVRec = VB * 16;
         float2 w2[G];
         load_w(U_, w2);
+        if constexpr (VB == 8) {  // int8 mode: codes of coordinates 8 r .. 8 r + 7, no table
+          const uint2 wv = lds64u<U * 2 * kVRec>(vw);
+          const uint32_t x0 = wv.x ^ 0x80808080u, x1 = wv.y ^ 0x80808080u;
+          const float2 c0 = int8_pair<0>(x0), c1 = int8_pair<2>(x0);
+          const float2 c2 = int8_pair<0>(x1), c3 = int8_pair<2>(x1);
+#pragma unroll
+          for (int jj = 0; jj < G; ++jj) {
+            acc[jj][0] = fma2(w2[jj], c0, acc[jj][0]);
+            acc[jj][1] = fma2(w2[jj], c1, acc[jj][1]);
+            acc[jj][2] = fma2(w2[jj], c2, acc[jj][2]);
+            acc[jj][3] = fma2(w2[jj], c3, acc[jj][3]);
+          }
+          return;
+        }
         uint32_t win;
         if constexpr (VB == 4) win = lds32<U * 2 * kVRec>(vw);
         else if constexpr (VB == 2) win = lds32<U * 2 * kVRec>(vw) >> v_sh;
@@ -1038,6 +1115,7 @@ tq_status dispatch_vb(const DecodeParams& p, int vb, cudaStream_t s) {
 template <int G, bool SPARSE, bool PAGED>
 tq_status dispatch_kb(const DecodeParams& p, int kb, int vb, cudaStream_t s) {
   switch (kb) {
+    case 8: return launch_split<G, 8, 8, SPARSE, PAGED>(p, s);  // int8 mode
     case 2: return dispatch_vb<G, 2, SPARSE, PAGED>(p, vb, s);
     case 3: return dispatch_vb<G, 3, SPARSE, PAGED>(p, vb, s);
     case 4: return dispatch_vb<G, 4, SPARSE, PAGED>(p, vb, s);

@@ -1,5 +1,5 @@
 // Dequantize kernel: packed token vectors back to float32,
-// x_hat = n * D_h * H * c[codes] / sqrt(d).
+// x_hat = n * D_h * H * c[codes] / sqrt(d) (int8 mode: x_hat = s * code).
 //
 // One warp per token vector: lane l owns coordinates 4l..4l+3, looks up their
 // centroids, runs the two low butterfly stages in registers and the five
@@ -52,6 +52,15 @@ __global__ void __launch_bounds__(kQWarps * 32) dequantize_kernel(const DequantP
     const uint2 w = reinterpret_cast<const uint2*>(src)[lane];
     const float2 a = half2_bits_to_float2(w.x), c = half2_bits_to_float2(w.y);
     *dst = make_float4(a.x, a.y, c.x, c.y);
+    return;
+  }
+  if (p.bits == 8) {  // int8 mode: s * code, word l holds the codes of coordinates 4l..4l+3
+    const uint32_t w = p.words[row * 32 + lane];
+    const float s = p.norms[row];
+    float res[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) res[k] = fmul(s, static_cast<float>(static_cast<int8_t>((w >> (8 * k)) & 0xFFu)));
+    *dst = make_float4(res[0], res[1], res[2], res[3]);
     return;
   }
   // codes of coordinates 4l..4l+3: bits [4*l*bits, 4*l*bits + 4*bits) of the record
@@ -125,13 +134,13 @@ extern "C" tq_status tq_dequantize(const tq_cache_desc* d, int32_t which, int32_
     p.words = static_cast<const uint32_t*>(d->k_cache);
     p.norms = d->k_norms;
     p.fp16 = static_cast<const uint16_t*>(d->k_cache);
-    if (p.bits != 16) std::memcpy(p.cent, d->k_cb.centroids, sizeof(p.cent));
+    if (p.bits != 16 && p.bits != 8) std::memcpy(p.cent, d->k_cb.centroids, sizeof(p.cent));
   } else {
     p.bits = d->v_bits;
     p.words = static_cast<const uint32_t*>(d->v_cache);
     p.norms = d->v_norms;
     p.fp16 = static_cast<const uint16_t*>(d->v_hot);
-    std::memcpy(p.cent, d->v_cb.centroids, sizeof(p.cent));
+    if (p.bits != 8) std::memcpy(p.cent, d->v_cb.centroids, sizeof(p.cent));
   }
   p.out = out;
   const dim3 grid((n_tokens + kQWarps - 1) / kQWarps, d->num_kv_heads);

@@ -26,11 +26,14 @@ struct RowMap {
   const int32_t* table;  // nullptr: contiguous
   int max_blocks, shift, num_blocks;
 #ifdef __CUDACC__
-  __device__ __forceinline__ long long row(int b, int h, int t) const {
-    if (table == nullptr) return (static_cast<long long>(b) * hkv + h) * cap + t;
-    const int blk = table[b * max_blocks + (t >> shift)];
+  // Pool row of position t of head h inside pool block blk; -1 outside the pool.
+  __device__ __forceinline__ long long in_block(int blk, int h, int t) const {
     if (blk < 0 || blk >= num_blocks) return -1;
     return ((static_cast<long long>(blk) * hkv + h) << shift) | (t & ((1 << shift) - 1));
+  }
+  __device__ __forceinline__ long long row(int b, int h, int t) const {
+    if (table == nullptr) return (static_cast<long long>(b) * hkv + h) * cap + t;
+    return in_block(table[b * max_blocks + (t >> shift)], h, t);
   }
 #endif
 };

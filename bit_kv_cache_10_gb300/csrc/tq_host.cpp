@@ -172,6 +172,10 @@ tq_status tq_cache_desc_init(tq_cache_desc* desc, int32_t batch, int32_t num_kv_
   desc->hot_window = hot_window;
   desc->layer = layer;
   desc->seed = seed;
+  if (k_mode == TQ_KV_INT8) {  // no codebooks
+    if (head_dim != tq::kHeadDim || k_bits != 8 || v_bits != 8) return TQ_ERR_UNSUPPORTED;
+    return tq::validate_shape(desc);
+  }
   if (head_dim != tq::kHeadDim || v_bits < tq::kMinBits || v_bits > tq::kMaxBits) return TQ_ERR_UNSUPPORTED;
   if (k_mode == TQ_K_PACKED) {
     if (k_bits < tq::kMinBits || k_bits > tq::kMaxBits) return TQ_ERR_UNSUPPORTED;
@@ -240,17 +244,21 @@ tq_status validate_shape(const tq_cache_desc* d) {
   if (d->num_q_heads % d->num_kv_heads != 0) return TQ_ERR_INVALID_ARG;
   const int g = d->num_q_heads / d->num_kv_heads;
   if (g != 1 && g != 2 && g != 4) return TQ_ERR_UNSUPPORTED;
-  if (d->k_mode != TQ_K_PACKED && d->k_mode != TQ_K_FP16) return TQ_ERR_INVALID_ARG;
-  if (d->k_mode == TQ_K_PACKED) {
-    if (d->k_bits < kMinBits || d->k_bits > kMaxBits) return TQ_ERR_UNSUPPORTED;
-    if (!codebook_matches(d->k_cb, d->head_dim, d->k_bits)) return TQ_ERR_INVALID_ARG;
+  if (d->k_mode != TQ_K_PACKED && d->k_mode != TQ_K_FP16 && d->k_mode != TQ_KV_INT8) return TQ_ERR_INVALID_ARG;
+  if (d->k_mode == TQ_KV_INT8) {
+    if (d->k_bits != 8 || d->v_bits != 8) return TQ_ERR_UNSUPPORTED;
+  } else {
+    if (d->k_mode == TQ_K_PACKED) {
+      if (d->k_bits < kMinBits || d->k_bits > kMaxBits) return TQ_ERR_UNSUPPORTED;
+      if (!codebook_matches(d->k_cb, d->head_dim, d->k_bits)) return TQ_ERR_INVALID_ARG;
+    }
+    if (d->v_bits < kMinBits || d->v_bits > kMaxBits) return TQ_ERR_UNSUPPORTED;
+    if (!codebook_matches(d->v_cb, d->head_dim, d->v_bits)) return TQ_ERR_INVALID_ARG;
+    if (quant_lut_scale(d->v_cb.thresholds, (1 << d->v_bits) - 1) == 0) return TQ_ERR_UNSUPPORTED;
+    if (d->k_mode == TQ_K_PACKED && quant_lut_scale(d->k_cb.thresholds, (1 << d->k_bits) - 1) == 0)
+      return TQ_ERR_UNSUPPORTED;
   }
-  if (d->v_bits < kMinBits || d->v_bits > kMaxBits) return TQ_ERR_UNSUPPORTED;
-  if (!codebook_matches(d->v_cb, d->head_dim, d->v_bits)) return TQ_ERR_INVALID_ARG;
   if (d->hot_window < 0 || d->hot_window > d->capacity) return TQ_ERR_INVALID_ARG;
-  if (quant_lut_scale(d->v_cb.thresholds, (1 << d->v_bits) - 1) == 0) return TQ_ERR_UNSUPPORTED;
-  if (d->k_mode == TQ_K_PACKED && quant_lut_scale(d->k_cb.thresholds, (1 << d->k_bits) - 1) == 0)
-    return TQ_ERR_UNSUPPORTED;
   if (d->block_size != 0) {  // paged layout
     if (d->block_size < 16 || d->block_size > 4096 || (d->block_size & (d->block_size - 1)) != 0)
       return TQ_ERR_INVALID_ARG;
@@ -267,7 +275,7 @@ tq_status validate_desc(const tq_cache_desc* d) {
   if (s != TQ_OK) return s;
   if (d->k_cache == nullptr || d->v_cache == nullptr || d->v_norms == nullptr) return TQ_ERR_INVALID_ARG;
   if (!aligned16(d->k_cache) || !aligned16(d->v_cache) || !aligned16(d->v_norms)) return TQ_ERR_INVALID_ARG;
-  if (d->k_mode == TQ_K_PACKED && (d->k_norms == nullptr || !aligned16(d->k_norms))) return TQ_ERR_INVALID_ARG;
+  if (d->k_mode != TQ_K_FP16 && (d->k_norms == nullptr || !aligned16(d->k_norms))) return TQ_ERR_INVALID_ARG;
   if (d->hot_window > 0 && (d->v_hot == nullptr || !aligned16(d->v_hot))) return TQ_ERR_INVALID_ARG;
   if (!(d->sparse_v_threshold >= 0.0f && d->sparse_v_threshold <= 1.0f)) return TQ_ERR_INVALID_ARG;  // NaN too
   return TQ_OK;

@@ -175,12 +175,65 @@ __device__ __forceinline__ void quantize_step(const uint8_t* tile, int row, int 
   }
 }
 
+// Code of x in the int8 mode for a scale s > 0: the float32 quotient x / s
+// (IEEE division) rounded to the nearest integer, ties to even, clamped to
+// [-127, 127].
+__device__ __forceinline__ uint32_t int8_code(float x, float s) {
+  const int c = __float2int_rn(__fdiv_rn(x, s));
+  return static_cast<uint32_t>(min(127, max(-127, c)));
+}
+
+// One step of the int8 mode ([mlxcel doc] "Available modes": per-token INT8
+// absmax): 8 vectors of the tile with the lane decomposition of quantize_step
+// (lane q holds coordinates 32q .. 32q + 31).  s = fp32(max |x_i|) / 127,
+// code_i = int8_code(x_i, s); a zero vector gets s = 0 and zero codes.  The
+// lane packs its 32 codes into 8 words, code i in byte i mod 4.
+__device__ __forceinline__ void quantize_step_int8(const uint8_t* tile, int row, int q, uint32_t* dst_words,
+                                                   float* dst_scale, bool store) {
+  const uint4* src = reinterpret_cast<const uint4*>(tile + row * kRowPitch) + 4 * q;
+  uint32_t w[16];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint4 a = src[k];
+    w[4 * k] = a.x;
+    w[4 * k + 1] = a.y;
+    w[4 * k + 2] = a.z;
+    w[4 * k + 3] = a.w;
+  }
+  // the magnitudes of finite fp16 values order like their bits without the sign
+  uint32_t m = 0u;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) m = __vmaxu2(m, w[k] & 0x7FFF7FFFu);
+  m = max(m & 0xFFFFu, m >> 16);
+  m = max(m, __shfl_xor_sync(0xffffffffu, m, 8));
+  m = max(m, __shfl_xor_sync(0xffffffffu, m, 16));
+  const float s = __fdiv_rn(half_bits_to_float(m), 127.0f);
+  uint32_t words[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const float2 a = half2_bits_to_float2(w[2 * k]), b = half2_bits_to_float2(w[2 * k + 1]);
+    uint32_t word = 0u;
+    if (s > 0.0f) {
+      const uint32_t lo = __byte_perm(int8_code(a.x, s), int8_code(a.y, s), 0x0040);
+      const uint32_t hi = __byte_perm(int8_code(b.x, s), int8_code(b.y, s), 0x0040);
+      word = __byte_perm(lo, hi, 0x5410);
+    }
+    words[k] = word;
+  }
+  if (store) {
+    uint4* d = reinterpret_cast<uint4*>(dst_words + 8 * q);
+    d[0] = make_uint4(words[0], words[1], words[2], words[3]);
+    d[1] = make_uint4(words[4], words[5], words[6], words[7]);
+    if (q == 0) *dst_scale = s;
+  }
+}
+
 template <bool PAGED>
 __global__ void __launch_bounds__(kWarps * 32, 1) quantize_append_kernel(const QuantParams p) {
   asm volatile("griddepcontrol.launch_dependents;\n");  // the next grid may start its prologue
   extern __shared__ __align__(16) uint8_t smem[];
   const int lut_k_n = p.k_lut_a ? lut_size(p.k_lut_a) : 0;
-  const int lut_v_n = lut_size(p.v_lut_a);
+  const int lut_v_n = p.v_lut_a ? lut_size(p.v_lut_a) : 0;  // 0: int8 mode
   LutEntry* lut_k = reinterpret_cast<LutEntry*>(smem);
   LutEntry* lut_v = lut_k + lut_k_n * kLutCopies;
   uint8_t* warp_area = reinterpret_cast<uint8_t*>(lut_v + lut_v_n * kLutCopies);
@@ -226,9 +279,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1) quantize_append_kernel(const Q
       if (jb.tile == 0 && jb.tensor == (p.evict ? 1 : 0) && jb.h == 0 && lane == 0 && p.status != nullptr)
         atomicOr(p.status, TQ_DEV_ERR_APPEND_RANGE);
     } else {
-      // rotation-sign masks of this head
-      smask[lane] = sign_mask_pair(p.seed, p.layer, jb.h, lane);
-      smask[lane + 32] = sign_mask_pair(p.seed, p.layer, jb.h, lane + 32);
+      if (p.k_mode != TQ_KV_INT8) {  // rotation-sign masks of this head
+        smask[lane] = sign_mask_pair(p.seed, p.layer, jb.h, lane);
+        smask[lane + 32] = sign_mask_pair(p.seed, p.layer, jb.h, lane + 32);
+      }
       __syncwarp();
       const uint8_t* tile = tiles + buf * kTileBytes;
       const bool k_tensor = jb.tensor == 0;
@@ -264,6 +318,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) quantize_append_kernel(const Q
         uint32_t* dw = (k_tensor ? p.k_words : p.v_words) + ridx * (bits * 4);
         float* dn = (k_tensor ? p.k_norms : p.v_norms) + ridx;
         switch (bits) {
+          case 8: quantize_step_int8(tile, row, q, dw, dn, have && !to_copy && ridx >= 0); break;
           case 2: quantize_step<2>(tile, row, q, smask, lut, lut_a, dw, dn, have && !to_copy && ridx >= 0); break;
           case 3: quantize_step<3>(tile, row, q, smask, lut, lut_a, dw, dn, have && !to_copy && ridx >= 0); break;
           default: quantize_step<4>(tile, row, q, smask, lut, lut_a, dw, dn, have && !to_copy && ridx >= 0); break;
@@ -277,8 +332,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1) quantize_append_kernel(const Q
 }
 
 size_t quant_smem_bytes(int k_lut_a, int v_lut_a) {
-  const size_t luts = (static_cast<size_t>(k_lut_a ? lut_size(k_lut_a) : 0) + lut_size(v_lut_a)) * kLutCopies *
-                      sizeof(LutEntry);
+  const size_t luts = (static_cast<size_t>(k_lut_a ? lut_size(k_lut_a) : 0) + (v_lut_a ? lut_size(v_lut_a) : 0)) *
+                      kLutCopies * sizeof(LutEntry);
   return luts + static_cast<size_t>(kWarps) * (2 * kTileBytes + 256);
 }
 
@@ -349,7 +404,7 @@ extern "C" tq_status tq_quantize_append(const tq_cache_desc* d, const void* k_ne
   p.cap = d->capacity;
   p.hot = d->hot_window;
   p.k_mode = d->k_mode;
-  p.k_bits = d->k_mode == TQ_K_PACKED ? d->k_bits : 0;
+  p.k_bits = d->k_mode == TQ_K_FP16 ? 0 : d->k_bits;  // 8 in the int8 mode
   p.v_bits = d->v_bits;
   p.k_words = static_cast<uint32_t*>(d->k_cache);
   p.k_norms = d->k_norms;
@@ -365,8 +420,10 @@ extern "C" tq_status tq_quantize_append(const tq_cache_desc* d, const void* k_ne
     std::memcpy(p.k_thr, d->k_cb.thresholds, sizeof(p.k_thr));
     p.k_lut_a = quant_lut_scale(d->k_cb.thresholds, (1 << d->k_bits) - 1);
   }
-  std::memcpy(p.v_thr, d->v_cb.thresholds, sizeof(p.v_thr));
-  p.v_lut_a = quant_lut_scale(d->v_cb.thresholds, (1 << d->v_bits) - 1);
+  if (d->k_mode != TQ_KV_INT8) {
+    std::memcpy(p.v_thr, d->v_cb.thresholds, sizeof(p.v_thr));
+    p.v_lut_a = quant_lut_scale(d->v_cb.thresholds, (1 << d->v_bits) - 1);
+  }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
   if (d->hot_window > 0) {  // V tokens leaving the ring are quantized before their slots are reused

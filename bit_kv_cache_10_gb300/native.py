@@ -23,6 +23,7 @@ TQ_ERR_CUDA = -5
 TQ_ERR_DEVICE = -6
 TQ_K_PACKED = 0
 TQ_K_FP16 = 1
+TQ_KV_INT8 = 2
 TQ_DEV_ERR_APPEND_RANGE = 0x1
 TQ_DEV_ERR_SEQ_LEN = 0x2
 

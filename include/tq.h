@@ -132,7 +132,9 @@ tq_status tq_rotation_signs(uint64_t seed, int32_t layer, int32_t head, int32_t 
 /* ------------------------------------------------------------------------ */
 
 enum { TQ_K_PACKED = 0, /* K quantized like V (symmetric turbo modes) */
-       TQ_K_FP16 = 1    /* K kept fp16, V packed (the "asym" modes of [mlxcel doc] "Available modes") */ };
+       TQ_K_FP16 = 1,   /* K kept fp16, V packed (the "asym" modes of [mlxcel doc] "Available modes") */
+       TQ_KV_INT8 = 2   /* K and V both per-token INT8 absmax, no rotation and no codebook (the int8
+                           mode of [mlxcel doc] "Available modes"); k_bits = v_bits = 8 */ };
 
 /*
  * Describes one layer's KV cache.  All pointers are caller-owned device
@@ -155,6 +157,13 @@ enum { TQ_K_PACKED = 0, /* K quantized like V (symmetric turbo modes) */
  * "Manual Cache Operations": packed uint32 buffers, several codes per word).
  * The per-token norm is the correctly rounded float32 of the exact norm.
  *
+ * TQ_KV_INT8: k_cache and v_cache hold [B, Hkv, cap, head_dim/4] uint32 words
+ * of int8 codes (code i in byte i mod 4 of word i/4, two's complement: the
+ * bitstream above with b = 8), and k_norms / v_norms the per-token float32
+ * scales s = fp32(max_i |x_i|) / 127; code_i = round-half-even(fp32(x_i) / s)
+ * in [-127, 127] (a zero vector has s = 0 and zero codes), dequantized as
+ * s * code_i.  The hot V window works as in the packed modes.
+ *
  * GQA: query head hq reads KV head hq / (num_q_heads / num_kv_heads).
  */
 typedef struct tq_cache_desc {
@@ -163,14 +172,14 @@ typedef struct tq_cache_desc {
   int32_t num_q_heads;   /* Hq, a multiple of Hkv */
   int32_t head_dim;      /* d; the kernels implement d = 128 */
   int32_t capacity;      /* cap >= 1 tokens per (sequence, KV head) */
-  int32_t k_mode;        /* TQ_K_PACKED or TQ_K_FP16 */
-  int32_t k_bits;        /* 2..4 when K is packed (ignored for TQ_K_FP16) */
-  int32_t v_bits;        /* 2..4 */
+  int32_t k_mode;        /* TQ_K_PACKED, TQ_K_FP16 or TQ_KV_INT8 */
+  int32_t k_bits;        /* 2..4 when K is packed, 8 for TQ_KV_INT8 (ignored for TQ_K_FP16) */
+  int32_t v_bits;        /* 2..4, 8 for TQ_KV_INT8 */
   int32_t hot_window;    /* 0 = none; else 1..cap fp16 V ring length */
   int32_t layer;         /* rotation-sign stream, [0, 2^31) */
   uint64_t seed;         /* rotation-sign seed */
-  tq_codebook k_cb;      /* built for (head_dim, k_bits) when K is packed */
-  tq_codebook v_cb;      /* built for (head_dim, v_bits) */
+  tq_codebook k_cb;      /* built for (head_dim, k_bits) when K is packed (unused for TQ_KV_INT8) */
+  tq_codebook v_cb;      /* built for (head_dim, v_bits) (unused for TQ_KV_INT8) */
   void *k_cache;
   float *k_norms;
   void *v_cache;
@@ -200,8 +209,9 @@ typedef struct tq_cache_desc {
 
 /*
  * Fill the shape and mode fields of `desc`, build both codebooks (host, as
- * tq_build_codebook) and set every pointer to NULL.  The caller then sets
- * the buffer pointers.  Validates like the launch entry points.
+ * tq_build_codebook; none for TQ_KV_INT8, which needs k_bits = v_bits = 8)
+ * and set every pointer to NULL.  The caller then sets the buffer pointers.
+ * Validates like the launch entry points.
  */
 tq_status tq_cache_desc_init(tq_cache_desc *desc, int32_t batch, int32_t num_kv_heads, int32_t num_q_heads,
                              int32_t head_dim, int32_t capacity, int32_t k_mode, int32_t k_bits,
@@ -266,6 +276,8 @@ tq_status tq_cache_buffer_bytes(const tq_cache_desc *desc, size_t *k_cache_bytes
  *   stream        CUDA stream
  *
  * TQ_K_FP16: K rows are copied into the fp16 K cache.
+ * TQ_KV_INT8: K and V rows get their absmax scale and int8 codes (see the
+ * descriptor); no rotation.
  * hot_window W > 0: after the call positions [end - W, end) of V (end =
  * start + n_new) are in the fp16 ring and [0, end - W) are packed; V tokens
  * that leave the ring are quantized before their slot is reused (one extra
@@ -300,8 +312,8 @@ size_t tq_decode_workspace_bytes(const tq_cache_desc *desc, int32_t max_seq_len)
  *   out[b, hq] = sum_j softmax_j(q.k_j / sqrt(d)) v_j,   j < seq_len_b
  *
  * with k_j, v_j the dequantized tokens n_j R^T c[codes_j] (or the raw fp16 K
- * in TQ_K_FP16 mode, and the raw fp16 V of the hot ring for the newest
- * min(W, L) positions).  The query is rotated once, scores are
+ * in TQ_K_FP16 mode, s_j code_j in TQ_KV_INT8 mode, and the raw fp16 V of the
+ * hot ring for the newest min(W, L) positions).  The query is rotated once, scores are
  * n_j * sum_i (R q)_i c[code_ji], the softmax runs online over split-K
  * chunks of the context, V is accumulated in the rotated domain and rotated
  * back once per output by a reduction kernel.
@@ -355,7 +367,8 @@ tq_status tq_decode_attention_no_alloc(const tq_cache_desc *desc, const void *q,
 /*
  * Dequantize positions [token_start, token_start + n_tokens) of sequence b
  * for all KV heads: x_hat = n R^T c[codes] as float32 ([MLX-VLM deep-dive]
- * FAQ "Where is the dequantization logic implemented?").  which = 0 reads
+ * FAQ "Where is the dequantization logic implemented?"); TQ_KV_INT8: the
+ * float32 product s * code.  which = 0 reads
  * K, 1 reads V.  For V with a hot window, positions >= seq_len - min(W,
  * seq_len) return the fp16 ring value; seq_len is the host-known length of
  * sequence b (only used for that split).  TQ_K_FP16 K returns the stored

@@ -196,3 +196,19 @@ def test_paged_layout_validation_and_pool_sizes():
     d.k_cache = d.v_cache = d.k_norms = d.v_norms = d.v_hot = fake
     d.block_table = None
     assert L.tq_decode_attention(d, fake, fake, 64, fake, fake, 1 << 30, None) == N.TQ_ERR_INVALID_ARG
+
+
+def test_int8_mode_descriptor_and_sizes():
+    d = N.tq_cache_desc_init(4, 8, 32, 128, 4096, N.TQ_KV_INT8, 8, 8)
+    rows = 4 * 8 * 4096
+    sizes = N.tq_cache_buffer_bytes(d)
+    # 128 one-byte codes and a float32 scale per token-head (the ~2x of the int8 mode)
+    assert sizes == {"k_cache": rows * 128, "k_norms": rows * 4, "v_cache": rows * 128, "v_norms": rows * 4,
+                     "v_hot": 0}
+    assert (sizes["k_cache"] + sizes["k_norms"]) // rows == 128 + 4
+    for kb, vb in ((4, 8), (8, 4), (8, 3), (16, 8)):
+        with pytest.raises(N.TQError) as e:
+            N.tq_cache_desc_init(4, 8, 32, 128, 4096, N.TQ_KV_INT8, kb, vb)
+        assert e.value.status == N.TQ_ERR_UNSUPPORTED
+    with pytest.raises(N.TQError):  # a mode value the library does not know
+        N.tq_cache_desc_init(4, 8, 32, 128, 4096, 3, 8, 8)
