@@ -555,6 +555,35 @@ def decode_attention(cache: PackedCache, q16: np.ndarray, lengths, pairs=None) -
     return out
 
 
+def multi_query_attention(cache: PackedCache, q16: np.ndarray, lengths, triples=None) -> np.ndarray:
+    """Causal attention of the T newest tokens of every sequence, fp16 queries
+    [B, T, Hq, d] -> float64 [B, T, Hq, d].
+
+    The multi-token counterpart of ``decode_attention`` (prefill chunks and
+    speculative verification; [mlxcel doc, "Measured speed and the memory
+    trade-off"] reports prefill for every mode).  Reading: with L_b positions
+    stored (the T new ones included), query i sits at position L_b - T + i and
+    attends to positions 0 .. L_b - T + i; a query before position 0 gets zeros.
+    ``triples`` optionally restricts the work to a list of (b, i, hq); the other
+    outputs are left NaN.
+    """
+    bsz, t_n, hq_n, d = q16.shape
+    hk = cache.v_words.shape[1]
+    g = hq_n // hk
+    out = np.full((bsz, t_n, hq_n, d), np.nan)
+    todo = triples if triples is not None else [(b, i, hq) for b in range(bsz) for i in range(t_n)
+                                                for hq in range(hq_n)]
+    kv = {}
+    for b, i, hq in todo:
+        h = hq // g
+        if (b, h) not in kv:
+            kv = {(b, h): dequantized_kv(cache, b, h, int(lengths[b]))}
+        k, v = kv[(b, h)]
+        n = max(0, int(lengths[b]) - t_n + i + 1)
+        out[b, i, hq] = attention_one(q16[b, i, hq].astype(np.float64), k[:n], v[:n])
+    return out
+
+
 def sparse_v_bound(q: np.ndarray, k: np.ndarray, v: np.ndarray, tau: float) -> np.ndarray:
     """Per-coordinate bound on how far a sparse-V decode may move one output.
 

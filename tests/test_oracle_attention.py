@@ -181,3 +181,50 @@ def test_decode_sparse_v_bound_matches_per_row_bound():
     for hq in range(4):
         k, v = oracle.dequantized_kv(c, 0, hq // 2, L)
         np.testing.assert_array_equal(out[0, hq], oracle.sparse_v_bound(q16[0, hq].astype(np.float64), k, v, 0.01))
+
+
+def _masked_softmax_attention(q, k, v, pos):
+    """Textbook causal attention of a block of queries: scores for every (query,
+    key) pair, -inf above the diagonal given by the query positions, row softmax."""
+    s = q @ k.T / math.sqrt(q.shape[-1])
+    s = np.where(np.arange(k.shape[0])[None, :] <= pos[:, None], s, -np.inf)
+    w = np.exp(s - s.max(axis=1, keepdims=True))
+    w = np.where(np.isfinite(s), w, 0.0)
+    return (w @ v) / w.sum(axis=1, keepdims=True)
+
+
+@pytest.mark.parametrize("codec", ["turbo", "int8"])
+def test_multi_query_attention_is_causal_block_attention(codec):
+    rng = np.random.default_rng(21)
+    B, HK, HQ, T, D, NQ = 2, 2, 4, 40, 128, 5
+    k = rng.standard_normal((B, HK, T, D)).astype(np.float16)
+    v = rng.standard_normal((B, HK, T, D)).astype(np.float16)
+    lens = np.array([40, 23])
+    cache = oracle.build_cache(k, v, lens, T, 3, 4, hot_window=7, codec=codec)
+    q = (rng.standard_normal((B, NQ, HQ, D)) * 0.5).astype(np.float16)
+    got = oracle.multi_query_attention(cache, q, lens)
+    for b in range(B):
+        for hq in range(HQ):
+            kk, vv = oracle.dequantized_kv(cache, b, hq // 2, int(lens[b]))
+            pos = lens[b] - NQ + np.arange(NQ)
+            want = _masked_softmax_attention(q[b, :, hq].astype(np.float64), kk, vv, pos)
+            np.testing.assert_allclose(got[b, :, hq], want, rtol=1e-12, atol=1e-12)
+
+
+def test_multi_query_with_one_token_is_decode_and_early_queries_are_zero():
+    rng = np.random.default_rng(22)
+    B, HK, HQ, T, D = 3, 1, 2, 20, 128
+    k = rng.standard_normal((B, HK, T, D)).astype(np.float16)
+    v = rng.standard_normal((B, HK, T, D)).astype(np.float16)
+    lens = np.array([20, 3, 0])
+    cache = oracle.build_cache(k, v, lens, T, 4, 4)
+    q = rng.standard_normal((B, 1, HQ, D)).astype(np.float16)
+    one = oracle.multi_query_attention(cache, q, lens)[:, 0]
+    dec = oracle.decode_attention(cache, q[:, 0], lens)
+    np.testing.assert_array_equal(one[:2], dec[:2])
+    assert np.all(one[2] == 0)
+    q5 = rng.standard_normal((B, 5, HQ, D)).astype(np.float16)
+    out = oracle.multi_query_attention(cache, q5, lens)
+    assert np.all(out[1, :2] == 0) and np.all(out[2] == 0)  # positions -2, -1 and an empty sequence
+    # the last query of a block sees exactly what a decode at the full length sees
+    np.testing.assert_array_equal(out[:2, 4], oracle.decode_attention(cache, q5[:, 4], lens)[:2])
