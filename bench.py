@@ -44,6 +44,8 @@ KB, VB = 3, 4
 LO, HI = 65536, 131072
 QB, QT = 16, 8192  # quantize workload: batch x new tokens (8 KV heads)
 FALLBACK_HBM_GBS = 6800.0
+# float32 multiply-add peak: 152 SMs x 128 FMA lanes x 2.07 GHz (maximum SM clock)
+FP32_FMA_PEAK = 152 * 128 * 2.07e9
 WORKLOAD = ("long-context 3.5-bit decode: B4, 32q/8kv heads, d128, L~U[65536,131072] (+1 per step), "
             "K 3-bit packed, V 4-bit packed + 256-token fp16 hot window; step = append 1 token per "
             "sequence (quantize + ring evict) + decode attention of all query heads")
@@ -406,15 +408,16 @@ def time_int8(torch, lens, reps=20):
     return dec_ms, dec_bytes, q_ms, q_bytes
 
 
-def paged_decode_ms(torch, tc, lens0, q, seqs, max_len, bs=64, reps=20):
-    """Mean decode-call time of a paged copy of `tc` (blocks of `bs` tokens in a
-    randomly permuted pool), after 3 untimed calls."""
+def paged_copy(torch, tc, bs=64, permute=True):
+    """Block-table copy of the decode cache `tc`: blocks of `bs` tokens in a
+    randomly permuted pool (or in order)."""
     from bit_kv_cache_10_gb300.cache import TurboQuantKVCache
     cap = (tc.capacity + bs - 1) // bs * bs
     mb = cap // bs
     nb = B * mb
     pg = TurboQuantKVCache(B, HKV, HQ, cap, bits=(KB, VB), hot_window=W, block_size=bs, num_blocks=nb)
-    table = torch.from_numpy(np.random.default_rng(SEED).permutation(nb).astype(np.int32).reshape(B, mb)).cuda()
+    order = np.random.default_rng(SEED).permutation(nb) if permute else np.arange(nb)
+    table = torch.from_numpy(order.astype(np.int32).reshape(B, mb)).cuda()
     pg.block_table.copy_(table)
     for name in ("k_cache", "k_norms", "v_cache", "v_norms"):
         src, dst = getattr(tc, name), getattr(pg, name)
@@ -423,6 +426,12 @@ def paged_decode_ms(torch, tc, lens0, q, seqs, max_len, bs=64, reps=20):
             full[:, :tc.capacity] = src[b]
             dst[table[b].long()] = full.view((HKV, mb, bs) + tuple(src.shape[3:])).transpose(0, 1)
     pg.v_hot.copy_(tc.v_hot)
+    return pg
+
+
+def paged_decode_ms(torch, tc, lens0, q, seqs, max_len, bs=64, reps=20, permute=True):
+    """Mean decode-call time of a paged copy of `tc`, after 3 untimed calls."""
+    pg = paged_copy(torch, tc, bs, permute)
     out = torch.empty(B, HQ, D, dtype=torch.float32, device="cuda")
     ws = torch.empty(pg.workspace_bytes(max_len), dtype=torch.uint8, device="cuda")
     for _ in range(3):
@@ -557,9 +566,32 @@ def run_gpu(args):
     tc.desc.sparse_v_threshold = 0.0
     if tc.device_status() != 0:
         raise RuntimeError("device status set by the sparse-V decode")
+    # speculative verification on the same cache: the 8 newest tokens of every
+    # sequence attend causally (each query one more sequence of the split work list)
+    mq_n = 8
+    mq_q = torch.from_numpy(synth.queries_fp16(SEED + 9, B * mq_n, HQ, D).reshape(B, mq_n, HQ, D)).cuda()
+    mq_out = torch.empty(B, mq_n, HQ, D, dtype=torch.float32, device="cuda")
+    mq_ws = torch.empty(native.tq_multi_query_workspace_bytes(tc.desc, mq_n, max_len), dtype=torch.uint8,
+                        device="cuda")
+    for _ in range(3):
+        tc.multi_query(mq_q, seqs[sv_s], max_len, out=mq_out, workspace=mq_ws)
+    mev = [torch.cuda.Event(enable_timing=True) for _ in range(11)]
+    torch.cuda.synchronize()
+    mev[0].record(stream)
+    for i in range(10):
+        tc.multi_query(mq_q, seqs[sv_s], max_len, out=mq_out, workspace=mq_ws)
+        mev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    mq_ms = float(np.mean([mev[i].elapsed_time(mev[i + 1]) for i in range(10)]))
+    if tc.device_status() != 0:
+        raise RuntimeError("device status set by the multi-query attention")
+    mq_lens = lens0 + sv_s + 1
+    mq_pairs = int(sum(max(0, int(L) - mq_n + i + 1) for L in mq_lens for i in range(mq_n)))  # (query, key) pairs
+    mq_fma = mq_pairs * HQ * 2 * D  # score and V multiply-adds per (query, key, head)
 
     # paged layout: the same cache copied into 64-token blocks scattered over a pool
     paged_ms = paged_decode_ms(torch, tc, lens0, q_dev[sv_s], seqs[sv_s], max_len)
+    paged_inorder_ms = paged_decode_ms(torch, tc, lens0, q_dev[sv_s], seqs[sv_s], max_len, permute=False)
 
     # end to end through the public API with host buffers
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
@@ -662,10 +694,15 @@ def run_gpu(args):
                      "value": decode_bytes(lens0 + sv_s + 1) / (sparse_ms * 1e-3) / 1e9, "unit": "GB/s",
                      "note": "same long-context decode call with V skipped for weights below 1e-3 of the running "
                              "maximum (random synthetic codes: diffuse attention, few skips)"},
-        "paged": {"block_size": 64, "ms": paged_ms,
+        "paged": {"block_size": 64, "ms": paged_ms, "ms_blocks_in_order": paged_inorder_ms,
                   "value": decode_bytes(lens0 + sv_s + 1) / (paged_ms * 1e-3) / 1e9, "unit": "GB/s",
                   "note": "same long-context decode call on a block-table copy of the cache (64-token blocks, "
                           "permuted pool)"},
+        "multi_query": {"n_query": mq_n, "ms": mq_ms, "value": mq_fma / (mq_ms * 1e-3) / 1e12, "unit": "T FMA/s",
+                        "frac": mq_fma / (mq_ms * 1e-3) / FP32_FMA_PEAK, "bound": "alu",
+                        "peak": FP32_FMA_PEAK / 1e12, "cache_gbs": decode_bytes(mq_lens) / (mq_ms * 1e-3) / 1e9,
+                        "workload": "speculative verification: the 8 newest tokens of each long-context sequence, "
+                                    "causal, B4, 32q/8kv, K3/V4 + 256 fp16 hot V"},
         "asym": {"value": asym_bytes / (asym_ms * 1e-3) / 1e9, "unit": "GB/s", "ms": asym_ms,
                  "frac": asym_bytes / (asym_ms * 1e-3) / 1e9 / peak, "algorithmic_bytes_per_launch": asym_bytes,
                  "workload": "asym decode: fp16 K + 4-bit V, B8, 32q/8kv, d128, context 16384, no hot window"},
@@ -721,6 +758,18 @@ def run_profile(args):
         torch.cuda.synchronize()
         print(json.dumps({"profile": "decode", "steps": args.steps, "wall_ms_per_step":
                           (time.perf_counter() - t0) * 1e3 / max(1, args.steps), "status": tc.device_status()}))
+    elif args.profile == "paged":
+        tc, lens0 = build_decode_cache(torch, HI + 64)
+        pg = paged_copy(torch, tc)
+        del tc
+        q = torch.from_numpy(synth.queries_fp16(SEED, B, HQ, D)).cuda()
+        sl = torch.from_numpy(np.asarray(lens0, np.int32)).cuda()
+        out = torch.empty(B, HQ, D, dtype=torch.float32, device="cuda")
+        ws = torch.empty(pg.workspace_bytes(HI), dtype=torch.uint8, device="cuda")
+        for s in range(total):
+            pg.decode(q, sl, HI, out=out, workspace=ws)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile": "paged", "steps": total, "status": pg.device_status()}))
     elif args.profile == "int8":
         lens = synth.seq_lengths(SEED, B, LO, HI)
         cap = int(np.max(lens))
@@ -764,7 +813,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle timing")
-    ap.add_argument("--profile", choices=["decode", "quantize", "asym", "int8"],
+    ap.add_argument("--profile", choices=["decode", "quantize", "asym", "int8", "paged"],
                     help="run only warm-up + timed steps of one part (for ncu captures); prints a short line")
     ap.add_argument("--profile-batch", type=int, default=4, help="batch of the quantize part in --profile mode")
     args = ap.parse_args()

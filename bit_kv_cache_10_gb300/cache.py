@@ -136,6 +136,30 @@ class TurboQuantKVCache:
                               _stream_handle(self.device))
         return out
 
+    def multi_query(self, q: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
+                    out: torch.Tensor | None = None, workspace: torch.Tensor | None = None) -> torch.Tensor:
+        """Causal attention of the n_query newest tokens of every sequence: fp16 q
+        [B, n_query, Hq, d] (query i of sequence b at position seq_lens[b] -
+        n_query + i, its K/V already appended); returns float32 [B, n_query, Hq, d]."""
+        if (q.dtype != torch.float16 or not q.is_contiguous() or q.dim() != 4 or q.shape[0] != self.batch
+                or q.shape[2:] != (self.num_q_heads, self.head_dim)):
+            raise ValueError("q must be a contiguous fp16 tensor [B, n_query, Hq, d]")
+        if seq_lens.dtype != torch.int32 or seq_lens.device != self.device or not seq_lens.is_contiguous():
+            raise ValueError("seq_lens must be a contiguous int32 tensor on the cache device")
+        nq = q.shape[1]
+        if out is None:
+            out = torch.empty(self.batch, nq, self.num_q_heads, self.head_dim, dtype=torch.float32,
+                              device=self.device)
+        need = N.tq_multi_query_workspace_bytes(self.desc, nq, max_seq_len)
+        if workspace is None:
+            if self._workspace is None or self._workspace.numel() < need:
+                self._workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=self.device)
+            workspace = self._workspace
+        N.tq_multi_query_attention(self.desc, q.data_ptr(), nq, seq_lens.data_ptr(), max_seq_len, out.data_ptr(),
+                                   workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                   _stream_handle(self.device))
+        return out
+
     # -- inspection -------------------------------------------------------------
     def dequantize(self, which: int, b: int, seq_len: int, token_start: int, n_tokens: int) -> torch.Tensor:
         """float32 [Hkv, n_tokens, d] of positions [token_start, token_start + n_tokens) of sequence b."""

@@ -24,7 +24,7 @@ __global__ void __launch_bounds__(4 * 32) decode_merge_kernel(const DecodeParams
   // tiles of the sequences before b, and of all sequences
   long long before = 0, total = 0;
   for (int bb = lane; bb < p.batch; bb += 32) {
-    const SeqTiles sq = seq_tiles(p, bb);
+    const SeqTiles sq = seq_tiles<true>(p, bb);  // the general form also holds for one query token
     const long long c = static_cast<long long>(p.hkv) * (sq.tc + sq.th);
     total += c;
     if (bb < b) before += c;
@@ -34,7 +34,7 @@ __global__ void __launch_bounds__(4 * 32) decode_merge_kernel(const DecodeParams
     before += __shfl_xor_sync(0xffffffffu, before, o);
     total += __shfl_xor_sync(0xffffffffu, total, o);
   }
-  const SeqTiles st = seq_tiles(p, b);
+  const SeqTiles st = seq_tiles<true>(p, b);
   if (st.len == 0) {
     out[lane] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     return;
@@ -141,28 +141,23 @@ int sm_count() {
 }  // namespace
 }  // namespace tq
 
-extern "C" size_t tq_decode_workspace_bytes(const tq_cache_desc* d, int32_t max_seq_len) {
-  using namespace tq;
-  if (validate_shape(d) != TQ_OK || max_seq_len < 0) return 0;
-  if (max_seq_len == 0) return 0;
-  return decode_workspace_bytes(d);
-}
+namespace tq {
+namespace {
 
-extern "C" tq_status tq_decode_attention(const tq_cache_desc* d, const void* q, const int32_t* d_seq_lens,
-                                         int32_t max_seq_len, float* out, void* workspace, size_t workspace_bytes,
-                                         tq_stream_t stream) {
-  using namespace tq;
-  const tq_status vs = validate_desc(d);
-  if (vs != TQ_OK) return vs;
-  if (q == nullptr || d_seq_lens == nullptr || out == nullptr || max_seq_len < 0) return TQ_ERR_INVALID_ARG;
+// Split-K attention of nq query tokens per sequence (the newest nq positions,
+// causal; nq = 1 is decode) over the cache: the work list holds B nq
+// sequences, sequence b nq + i being query token i of cache sequence b.
+tq_status run_attention(const tq_cache_desc* d, const void* q, int nq, const int32_t* d_seq_lens, int32_t max_seq_len,
+                        float* out, void* workspace, size_t workspace_bytes, cudaStream_t s) {
+  if (q == nullptr || d_seq_lens == nullptr || out == nullptr || max_seq_len < 0 || nq < 1) return TQ_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(out)) return TQ_ERR_INVALID_ARG;
-  if (d->batch > kMaxDecodeBatch) return TQ_ERR_UNSUPPORTED;
+  if (static_cast<long long>(d->batch) * nq > kMaxDecodeBatch) return TQ_ERR_UNSUPPORTED;
+  if (nq > 1 && d->sparse_v_threshold > 0.0f) return TQ_ERR_UNSUPPORTED;  // several query tokens: dense V
   if (static_cast<long long>(d->num_kv_heads) * (d->capacity / 32 + d->hot_window / 32 + 2) >= (1ll << 31))
     return TQ_ERR_UNSUPPORTED;  // tiles of one sequence must fit in 32 bits
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const size_t out_bytes = static_cast<size_t>(d->batch) * d->num_q_heads * D * sizeof(float);
+  const size_t out_bytes = static_cast<size_t>(d->batch) * nq * d->num_q_heads * D * sizeof(float);
   if (max_seq_len == 0) return cudaMemsetAsync(out, 0, out_bytes, s) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
-  const size_t need = tq_decode_workspace_bytes(d, max_seq_len);
+  const size_t need = decode_workspace_bytes(d, nq);
   if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < need) return TQ_ERR_WORKSPACE;
   const int sms = sm_count();
   if (sms <= 0) return TQ_ERR_CUDA;
@@ -172,7 +167,8 @@ extern "C" tq_status tq_decode_attention(const tq_cache_desc* d, const void* q, 
   p.q = static_cast<const uint16_t*>(q);
   p.seq_lens = d_seq_lens;
   p.max_seq_len = max_seq_len;
-  p.batch = d->batch;
+  p.batch = d->batch * nq;
+  p.nq = nq;
   p.hkv = d->num_kv_heads;
   p.hq = d->num_q_heads;
   p.cap = d->capacity;
@@ -188,9 +184,9 @@ extern "C" tq_status tq_decode_attention(const tq_cache_desc* d, const void* q, 
   p.seed = d->seed;
   p.layer = d->layer;
   if (d->k_mode == TQ_K_PACKED) std::memcpy(p.k_cent, d->k_cb.centroids, sizeof(p.k_cent));
-  std::memcpy(p.v_cent, d->v_cb.centroids, sizeof(p.v_cent));
+  if (d->k_mode != TQ_KV_INT8) std::memcpy(p.v_cent, d->v_cb.centroids, sizeof(p.v_cent));
   const int g = d->num_q_heads / d->num_kv_heads;
-  const size_t slots = decode_workspace_slots(d);
+  const size_t slots = decode_workspace_slots(d, nq);
   p.ws_acc = static_cast<float*>(workspace);
   p.ws_ml = p.ws_acc + slots * g * D;
   p.grid = sms < kMaxDecodeCtas ? sms : kMaxDecodeCtas;
@@ -201,13 +197,18 @@ extern "C" tq_status tq_decode_attention(const tq_cache_desc* d, const void* q, 
   const int kb = d->k_mode == TQ_K_FP16 ? 16 : d->k_bits;
   tq_status st;
   const bool sparse = p.sparse_tau > 0.0f, paged = d->block_size > 0;
-  if (paged) st = sparse ? dispatch_split_paged_sparse(p, g, kb, d->v_bits, s) : dispatch_split_paged(p, g, kb, d->v_bits, s);
-  else st = sparse ? dispatch_split_sparse(p, g, kb, d->v_bits, s) : dispatch_split_variant<false, false>(p, g, kb, d->v_bits, s);
+  if (nq > 1) {
+    st = paged ? dispatch_split_multi_paged(p, g, kb, d->v_bits, s) : dispatch_split_multi(p, g, kb, d->v_bits, s);
+  } else if (paged) {
+    st = sparse ? dispatch_split_paged_sparse(p, g, kb, d->v_bits, s) : dispatch_split_paged(p, g, kb, d->v_bits, s);
+  } else {
+    st = sparse ? dispatch_split_sparse(p, g, kb, d->v_bits, s) : dispatch_split_variant<false, false>(p, g, kb, d->v_bits, s);
+  }
   if (st != TQ_OK) return st;
   // programmatic dependent launch: the merge grid is scheduled as the split
   // kernel's CTAs retire and waits (griddepcontrol.wait) for its completion
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(d->num_kv_heads, d->batch);
+  cfg.gridDim = dim3(d->num_kv_heads, p.batch);
   cfg.blockDim = dim3(4 * 32);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
@@ -218,6 +219,43 @@ extern "C" tq_status tq_decode_attention(const tq_cache_desc* d, const void* q, 
   cfg.numAttrs = 1;
   if (cudaLaunchKernelEx(&cfg, decode_merge_kernel, p) != cudaSuccess) return TQ_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace tq
+
+extern "C" size_t tq_decode_workspace_bytes(const tq_cache_desc* d, int32_t max_seq_len) {
+  using namespace tq;
+  if (validate_shape(d) != TQ_OK || max_seq_len < 0) return 0;
+  if (max_seq_len == 0) return 0;
+  return decode_workspace_bytes(d);
+}
+
+extern "C" tq_status tq_decode_attention(const tq_cache_desc* d, const void* q, const int32_t* d_seq_lens,
+                                         int32_t max_seq_len, float* out, void* workspace, size_t workspace_bytes,
+                                         tq_stream_t stream) {
+  using namespace tq;
+  const tq_status vs = validate_desc(d);
+  if (vs != TQ_OK) return vs;
+  return run_attention(d, q, 1, d_seq_lens, max_seq_len, out, workspace, workspace_bytes,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" size_t tq_multi_query_workspace_bytes(const tq_cache_desc* d, int32_t n_query, int32_t max_seq_len) {
+  using namespace tq;
+  if (validate_shape(d) != TQ_OK || max_seq_len < 0 || n_query < 1) return 0;
+  if (max_seq_len == 0) return 0;
+  return decode_workspace_bytes(d, n_query);
+}
+
+extern "C" tq_status tq_multi_query_attention(const tq_cache_desc* d, const void* q, int32_t n_query,
+                                              const int32_t* d_seq_lens, int32_t max_seq_len, float* out,
+                                              void* workspace, size_t workspace_bytes, tq_stream_t stream) {
+  using namespace tq;
+  const tq_status vs = validate_desc(d);
+  if (vs != TQ_OK) return vs;
+  return run_attention(d, q, n_query, d_seq_lens, max_seq_len, out, workspace, workspace_bytes,
+                       reinterpret_cast<cudaStream_t>(stream));
 }
 
 // ---------------------------------------------------------------------------

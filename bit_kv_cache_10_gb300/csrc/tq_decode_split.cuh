@@ -6,7 +6,10 @@
 // min(W, L) positions, whose V is read from the fp16 ring).  Rows are cut into
 // 16-token tiles and listed in (b, h, cold/hot) order; the list is split into
 // one contiguous, equal range per CTA, so that every SM gets the same number
-// of tiles whatever the lengths are.
+// of tiles whatever the lengths are.  For attention of nq query tokens per
+// sequence (MQ variants) every query token is a sequence of the list of its
+// own, whose length is its causal prefix; its tiles are read from the cache
+// rows of the sequence it belongs to.
 //
 // Split kernel: one CTA of 8 warps per SM (up to 255 registers per thread).  The
 // codebook pair tables are built once per CTA in shared memory (16 copies, one
@@ -49,7 +52,8 @@ struct DecodeParams {
   const uint16_t* q;
   const int* seq_lens;
   int max_seq_len;
-  int batch, hkv, hq, cap, hot;
+  int batch, hkv, hq, cap, hot;  // batch: sequences x nq query tokens (the work list's "sequences")
+  int nq;         // query tokens per cache sequence (1: decode)
   const uint32_t* k_words;
   const float* k_norms;
   const uint16_t* k_fp16;
@@ -85,19 +89,32 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
 
-// Length of sequence b, or 0 when it is outside [0, min(cap, max_seq_len)].
+// Length of cache sequence b, or 0 when it is outside [0, min(cap, max_seq_len)].
 __device__ __forceinline__ int seq_len(const DecodeParams& p, int b) {
   const int len = p.seq_lens[b];
   return (len >= 0 && len <= p.cap && len <= p.max_seq_len) ? len : 0;
 }
 
+// Cache sequence of work-list sequence v (v itself for decode; MQ: kernels
+// compiled for several query tokens per sequence).
+template <bool MQ>
+__device__ __forceinline__ int cache_seq(const DecodeParams& p, int v) { return MQ ? v / p.nq : v; }
+
 struct SeqTiles {
   int len, ce, tc, th;  // length, cold end, cold tiles, hot tiles
 };
-__device__ __forceinline__ SeqTiles seq_tiles(const DecodeParams& p, int b) {
+// Work-list sequence v is query token i = v mod nq of cache sequence b = v / nq:
+// with the cache holding L positions it sits at position L - nq + i and attends
+// to the prefix [0, L - nq + i + 1) (causal).  The cold end is the cache
+// sequence's, so that hot positions are the ones in the fp16 ring.
+template <bool MQ>
+__device__ __forceinline__ SeqTiles seq_tiles(const DecodeParams& p, int v) {
   SeqTiles s;
-  s.len = seq_len(p, b);
-  s.ce = p.hot > 0 ? s.len - min(p.hot, s.len) : s.len;
+  const int b = cache_seq<MQ>(p, v);
+  const int L = seq_len(p, b);
+  s.len = MQ ? max(0, L - (p.nq - 1 - (v - b * p.nq))) : L;
+  const int ce = p.hot > 0 ? L - min(p.hot, L) : L;
+  s.ce = min(ce, s.len);
   s.tc = (s.ce + kTile - 1) / kTile;
   s.th = (s.len - s.ce + kTile - 1) / kTile;
   return s;
@@ -106,7 +123,7 @@ __device__ __forceinline__ SeqTiles seq_tiles(const DecodeParams& p, int b) {
 // Exclusive prefix (over sequences) of the tile counts, prefix[0..B], in
 // shared memory; all threads of the block must call it.  Uses `scratch`
 // (at least 33 long longs).
-template <int NT>
+template <int NT, bool MQ>
 __device__ void tile_prefix(const DecodeParams& p, long long* prefix, long long* scratch) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int kPer = (kMaxDecodeBatch + NT - 1) / NT;
@@ -117,7 +134,7 @@ __device__ void tile_prefix(const DecodeParams& p, long long* prefix, long long*
     const int b = tid * kPer + i;
     long long c = 0;
     if (b < p.batch) {
-      const SeqTiles s = seq_tiles(p, b);
+      const SeqTiles s = seq_tiles<MQ>(p, b);
       c = static_cast<long long>(p.hkv) * (s.tc + s.th);
     }
     v[i] = c;
@@ -159,6 +176,7 @@ struct TileInfo {
   long long row_start, row_end;  // tile-list range of the row
 };
 
+template <bool MQ>
 __device__ __forceinline__ TileInfo tile_info(const DecodeParams& p, const long long* prefix, long long t) {
   int lo = 0, hi = p.batch;  // largest b with prefix[b] <= t
   while (hi - lo > 1) {
@@ -168,7 +186,7 @@ __device__ __forceinline__ TileInfo tile_info(const DecodeParams& p, const long 
   }
   TileInfo ti;
   ti.b = lo;
-  const SeqTiles s = seq_tiles(p, lo);
+  const SeqTiles s = seq_tiles<MQ>(p, lo);
   const int per_h = s.tc + s.th;
   const int rem = static_cast<int>(t - prefix[lo]);  // < Hkv * per_h < 2^31 (checked on the host)
   ti.h = rem / per_h;
@@ -345,22 +363,24 @@ __device__ __forceinline__ float2 lds64f(uint32_t base) {
 // Issue cursor: the tile a warp stages next, advanced by the warp stride
 // without searching the tile list again.
 struct Cursor {
-  int b, h, x;              // sequence, KV head, tile index within the (b, h) rows
+  int b, h, x;              // work-list sequence, KV head, tile index within the (b, h) rows
   int ce, len, tc, per_h;   // cold end, length, cold tiles, tiles of one head
 };
+template <bool MQ>
 __device__ __forceinline__ void cursor_seq(const DecodeParams& p, Cursor& c) {
-  const SeqTiles s = seq_tiles(p, c.b);
+  const SeqTiles s = seq_tiles<MQ>(p, c.b);
   c.ce = s.ce;
   c.len = s.len;
   c.tc = s.tc;
   c.per_h = s.tc + s.th;
 }
+template <bool MQ>
 __device__ __forceinline__ Cursor cursor_at(const DecodeParams& p, const long long* prefix, long long t) {
-  const TileInfo ti = tile_info(p, prefix, t);
+  const TileInfo ti = tile_info<MQ>(p, prefix, t);
   Cursor c;
   c.b = ti.b;
   c.h = ti.h;
-  cursor_seq(p, c);
+  cursor_seq<MQ>(p, c);
   c.x = ti.hot ? c.tc + (ti.t_begin - c.ce) / kTile : ti.t_begin / kTile;
   return c;
 }
@@ -371,6 +391,7 @@ __device__ __forceinline__ int cursor_t_begin(const Cursor& c) {
 __device__ __forceinline__ int cursor_n_valid(const Cursor& c) {
   return min(kTile, (c.x >= c.tc ? c.len : c.ce) - cursor_t_begin(c));
 }
+template <bool MQ>
 __device__ __forceinline__ void cursor_advance(const DecodeParams& p, Cursor& c, int n) {
   c.x += n;
   while (c.x >= c.per_h) {  // per_h is 0 for empty sequences
@@ -378,7 +399,7 @@ __device__ __forceinline__ void cursor_advance(const DecodeParams& p, Cursor& c,
     if (++c.h == p.hkv) {
       c.h = 0;
       if (++c.b >= p.batch) return;  // past the tile list: never staged
-      cursor_seq(p, c);
+      cursor_seq<MQ>(p, c);
     }
   }
 }
@@ -516,7 +537,7 @@ __device__ __forceinline__ int stage_tile(const DecodeParams& p, int b, int h, b
 }
 
 // Split kernel.
-template <int G, int KB, int VB, bool SPARSE, bool PAGED>
+template <int G, int KB, int VB, bool SPARSE, bool PAGED, bool MQ>
 __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeParams p) {
   using C = Cfg<KB, VB>;
   constexpr int S = C::kStages;
@@ -568,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
   // parameters; the lengths and the cache may come from the preceding grids
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
   if (blockIdx.x == 0 && tid == 0 && p.status != nullptr) {
-    for (int b = 0; b < p.batch; ++b) {
+    for (int b = 0; b < p.batch / p.nq; ++b) {
       const int len = p.seq_lens[b];
       if (len < 0 || len > p.cap || len > p.max_seq_len) {
         atomicOr(p.status, TQ_DEV_ERR_SEQ_LEN);
@@ -576,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
       }
     }
   }
-  tile_prefix<kThreads>(p, prefix, scan);  // synchronizes
+  tile_prefix<kThreads, MQ>(p, prefix, scan);  // synchronizes
   const long long total = prefix[p.batch];
   const long long t0 = total * blockIdx.x / p.grid, t1 = total * (blockIdx.x + 1) / p.grid;
   if (t0 >= t1) return;
@@ -599,20 +620,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
   Cursor cur;
   TileBlocks tb{0, 0};  // paged: block-table entries of the tile the cursor points at
   if (my_n > 0) {
-    cur = cursor_at(p, prefix, t0 + warp);
-    if constexpr (PAGED) tb = load_tile_blocks(p, cur.b, cursor_t_begin(cur), cursor_n_valid(cur));
+    cur = cursor_at<MQ>(p, prefix, t0 + warp);
+    if constexpr (PAGED) tb = load_tile_blocks(p, cache_seq<MQ>(p, cur.b), cursor_t_begin(cur), cursor_n_valid(cur));
   }
   auto issue = [&]() {
     if (j_issue < my_n) {
       const bool hot = cur.x >= cur.tc;
       const int t_begin = cursor_t_begin(cur);
       const int n_valid = cursor_n_valid(cur);
-      const int staged = stage_tile<KB, VB, PAGED>(p, cur.b, cur.h, hot, t_begin, n_valid, tb,
+      const int cb = cache_seq<MQ>(p, cur.b);
+      const int staged = stage_tile<KB, VB, PAGED>(p, cb, cur.h, hot, t_begin, n_valid, tb,
                                                    ring + static_cast<uint32_t>((j_issue % S) * C::kBuf), lane);
-      if (lane == 0) descs[j_issue % S] = make_int4(cur.b, cur.h | (hot << 16), t_begin, staged);
-      cursor_advance(p, cur, kWarps);
+      if (lane == 0) descs[j_issue % S] = make_int4(cb, cur.h | (hot << 16), t_begin, staged);
+      cursor_advance<MQ>(p, cur, kWarps);
       if constexpr (PAGED)
-        if (j_issue + 1 < my_n) tb = load_tile_blocks(p, cur.b, cursor_t_begin(cur), cursor_n_valid(cur));
+        if (j_issue + 1 < my_n) tb = load_tile_blocks(p, cache_seq<MQ>(p, cur.b), cursor_t_begin(cur), cursor_n_valid(cur));
     }
     cp_async_commit();
     ++j_issue;
@@ -644,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
   int cur_b = -1, cur_h = -1;
   long long seg = t0;
   while (seg < t1) {
-    const TileInfo si = tile_info(p, prefix, seg);
+    const TileInfo si = tile_info<MQ>(p, prefix, seg);
     const long long seg_end = si.row_end < t1 ? si.row_end : t1;
     if (si.b != cur_b || si.h != cur_h) {
       // rotated query of the G heads: (log2 e / d) H D q for packed K, (log2 e / sqrt d) q for fp16
@@ -705,7 +727,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
       cp_async_wait<S - 1>();
       __syncwarp();
       const int4 dsc = descs[j % S];
-      const int tb_b = dsc.x, tb_h = dsc.y & 0xFFFF, n_valid = dsc.w, t_begin = dsc.z;
+      const int tb_b = dsc.x, tb_h = dsc.y & 0xFFFF, n_valid = dsc.w, t_begin = dsc.z;  // tb_b: cache sequence
       const bool hot = (dsc.y >> 16) != 0;
       const uint8_t* tb = wring + (j % S) * C::kBuf;
       const uint32_t tbs = ring + static_cast<uint32_t>((j % S) * C::kBuf);  // shared address of the tile
@@ -1083,10 +1105,10 @@ __device__ __forceinline__ int cta_of(long long t, long long total, int grid) {
 }
 __device__ __forceinline__ long long cta_start(int c, long long total, int grid) { return total * c / grid; }
 
-template <int G, int KB, int VB, bool SPARSE, bool PAGED>
+template <int G, int KB, int VB, bool SPARSE, bool PAGED, bool MQ>
 tq_status launch_split(const DecodeParams& p, cudaStream_t stream) {
   using C = Cfg<KB, VB>;
-  auto kern = decode_split_kernel<G, KB, VB, SPARSE, PAGED>;
+  auto kern = decode_split_kernel<G, KB, VB, SPARSE, PAGED, MQ>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) != cudaSuccess)
     return TQ_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
@@ -1103,34 +1125,34 @@ tq_status launch_split(const DecodeParams& p, cudaStream_t stream) {
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 
-template <int G, int KB, bool SPARSE, bool PAGED>
+template <int G, int KB, bool SPARSE, bool PAGED, bool MQ>
 tq_status dispatch_vb(const DecodeParams& p, int vb, cudaStream_t s) {
   switch (vb) {
-    case 2: return launch_split<G, KB, 2, SPARSE, PAGED>(p, s);
-    case 3: return launch_split<G, KB, 3, SPARSE, PAGED>(p, s);
-    default: return launch_split<G, KB, 4, SPARSE, PAGED>(p, s);
+    case 2: return launch_split<G, KB, 2, SPARSE, PAGED, MQ>(p, s);
+    case 3: return launch_split<G, KB, 3, SPARSE, PAGED, MQ>(p, s);
+    default: return launch_split<G, KB, 4, SPARSE, PAGED, MQ>(p, s);
   }
 }
 
-template <int G, bool SPARSE, bool PAGED>
+template <int G, bool SPARSE, bool PAGED, bool MQ>
 tq_status dispatch_kb(const DecodeParams& p, int kb, int vb, cudaStream_t s) {
   switch (kb) {
-    case 8: return launch_split<G, 8, 8, SPARSE, PAGED>(p, s);  // int8 mode
-    case 2: return dispatch_vb<G, 2, SPARSE, PAGED>(p, vb, s);
-    case 3: return dispatch_vb<G, 3, SPARSE, PAGED>(p, vb, s);
-    case 4: return dispatch_vb<G, 4, SPARSE, PAGED>(p, vb, s);
-    default: return dispatch_vb<G, 16, SPARSE, PAGED>(p, vb, s);
+    case 8: return launch_split<G, 8, 8, SPARSE, PAGED, MQ>(p, s);  // int8 mode
+    case 2: return dispatch_vb<G, 2, SPARSE, PAGED, MQ>(p, vb, s);
+    case 3: return dispatch_vb<G, 3, SPARSE, PAGED, MQ>(p, vb, s);
+    case 4: return dispatch_vb<G, 4, SPARSE, PAGED, MQ>(p, vb, s);
+    default: return dispatch_vb<G, 16, SPARSE, PAGED, MQ>(p, vb, s);
   }
 }
 
-// Split kernels of one variant (dense or sparse V, contiguous or paged) for any
-// group size and widths.
-template <bool SPARSE, bool PAGED>
+// Split kernels of one variant (dense or sparse V, contiguous or paged, one or
+// several query tokens per sequence) for any group size and widths.
+template <bool SPARSE, bool PAGED, bool MQ = false>
 tq_status dispatch_split_variant(const DecodeParams& p, int g, int kb, int vb, cudaStream_t s) {
   switch (g) {
-    case 1: return dispatch_kb<1, SPARSE, PAGED>(p, kb, vb, s);
-    case 2: return dispatch_kb<2, SPARSE, PAGED>(p, kb, vb, s);
-    default: return dispatch_kb<4, SPARSE, PAGED>(p, kb, vb, s);
+    case 1: return dispatch_kb<1, SPARSE, PAGED, MQ>(p, kb, vb, s);
+    case 2: return dispatch_kb<2, SPARSE, PAGED, MQ>(p, kb, vb, s);
+    default: return dispatch_kb<4, SPARSE, PAGED, MQ>(p, kb, vb, s);
   }
 }
 
@@ -1141,5 +1163,7 @@ tq_status dispatch_split_variant(const DecodeParams& p, int g, int kb, int vb, c
 tq_status dispatch_split_sparse(const DecodeParams& p, int g, int kb, int vb, cudaStream_t s);
 tq_status dispatch_split_paged(const DecodeParams& p, int g, int kb, int vb, cudaStream_t s);
 tq_status dispatch_split_paged_sparse(const DecodeParams& p, int g, int kb, int vb, cudaStream_t s);
+tq_status dispatch_split_multi(const DecodeParams& p, int g, int kb, int vb, cudaStream_t s);
+tq_status dispatch_split_multi_paged(const DecodeParams& p, int g, int kb, int vb, cudaStream_t s);
 
 }  // namespace tq

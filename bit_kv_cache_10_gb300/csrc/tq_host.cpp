@@ -281,13 +281,13 @@ tq_status validate_desc(const tq_cache_desc* d) {
   return TQ_OK;
 }
 
-size_t decode_workspace_slots(const tq_cache_desc* d) {
-  return static_cast<size_t>(kMaxDecodeCtas) + 2 * static_cast<size_t>(d->batch) * d->num_kv_heads;
+size_t decode_workspace_slots(const tq_cache_desc* d, int nq) {
+  return static_cast<size_t>(kMaxDecodeCtas) + 2 * static_cast<size_t>(d->batch) * nq * d->num_kv_heads;
 }
 
-size_t decode_workspace_bytes(const tq_cache_desc* d) {
+size_t decode_workspace_bytes(const tq_cache_desc* d, int nq) {
   const size_t g = static_cast<size_t>(d->num_q_heads / d->num_kv_heads);
-  return decode_workspace_slots(d) * g * (kHeadDim + 2) * sizeof(float);
+  return decode_workspace_slots(d, nq) * g * (kHeadDim + 2) * sizeof(float);
 }
 
 int quant_lut_scale(const float* t, int n) {

@@ -25,9 +25,10 @@ tq_status validate_desc(const tq_cache_desc* d);
 
 // Decode workspace: one partial (G heads x (d accumulators + max + sum)) per
 // (split-K CTA, row) pair, at slot CTA + row; rows are the cold and hot rows of
-// every (sequence, KV head), so kMaxDecodeCtas + 2 B Hkv slots always suffice.
-size_t decode_workspace_slots(const tq_cache_desc* d);
-size_t decode_workspace_bytes(const tq_cache_desc* d);
+// every (sequence, query token, KV head), so kMaxDecodeCtas + 2 B nq Hkv slots
+// always suffice (nq query tokens per sequence; 1 for decode).
+size_t decode_workspace_slots(const tq_cache_desc* d, int nq = 1);
+size_t decode_workspace_bytes(const tq_cache_desc* d, int nq = 1);
 
 // Bucket scale of the threshold lookup table used by the quantize kernel: the
 // smallest power of two A for which every bucket RN(y*A) holds at most one

@@ -32,7 +32,7 @@ EXPORTED = (
     "tq_status_string", "tq_build_codebook", "tq_split_bits", "tq_turboquant_enabled", "tq_rotation_signs",
     "tq_cache_desc_init", "tq_cache_buffer_bytes", "tq_quantize_append", "tq_decode_workspace_bytes",
     "tq_decode_attention", "tq_dequantize", "tq_debug_quantize_rows_host", "tq_decode_attention_no_alloc",
-    "tq_cache_desc_set_paged",
+    "tq_cache_desc_set_paged", "tq_multi_query_workspace_bytes", "tq_multi_query_attention",
 )
 TQ_DEV_ERR_APPEND_RANGE, TQ_DEV_ERR_SEQ_LEN, TQ_DEV_ERR_LAYOUT, TQ_DEV_ERR_BLOCK = 0x1, 0x2, 0x4, 0x8
 TQ_NO_ALLOC_WORKSPACE_BYTES = 16 << 20
@@ -100,6 +100,11 @@ def lib() -> ctypes.CDLL:
         L.tq_decode_attention.restype = c_int32
         L.tq_decode_attention.argtypes = [POINTER(TQCacheDesc), c_void_p, c_void_p, c_int32, c_void_p, c_void_p,
                                           c_size_t, c_void_p]
+        L.tq_multi_query_workspace_bytes.restype = c_size_t
+        L.tq_multi_query_workspace_bytes.argtypes = [POINTER(TQCacheDesc), c_int32, c_int32]
+        L.tq_multi_query_attention.restype = c_int32
+        L.tq_multi_query_attention.argtypes = [POINTER(TQCacheDesc), c_void_p, c_int32, c_void_p, c_int32, c_void_p,
+                                               c_void_p, c_size_t, c_void_p]
         L.tq_decode_attention_no_alloc.restype = c_int32
         L.tq_decode_attention_no_alloc.argtypes = [POINTER(TQCacheDesc), c_void_p, c_void_p, c_int32, c_void_p,
                                                    c_void_p]
@@ -178,6 +183,15 @@ def tq_decode_workspace_bytes(desc, max_seq_len: int) -> int:
 def tq_decode_attention(desc, q_ptr, d_seq_lens_ptr, max_seq_len, out_ptr, ws_ptr, ws_bytes, stream):
     _check(lib().tq_decode_attention(ctypes.byref(desc), q_ptr, d_seq_lens_ptr, max_seq_len, out_ptr, ws_ptr,
                                      ws_bytes, stream), "tq_decode_attention")
+
+
+def tq_multi_query_workspace_bytes(desc, n_query: int, max_seq_len: int) -> int:
+    return int(lib().tq_multi_query_workspace_bytes(ctypes.byref(desc), n_query, max_seq_len))
+
+
+def tq_multi_query_attention(desc, q_ptr, n_query, d_seq_lens_ptr, max_seq_len, out_ptr, ws_ptr, ws_bytes, stream):
+    _check(lib().tq_multi_query_attention(ctypes.byref(desc), q_ptr, n_query, d_seq_lens_ptr, max_seq_len, out_ptr,
+                                          ws_ptr, ws_bytes, stream), "tq_multi_query_attention")
 
 
 def tq_decode_attention_no_alloc(desc, q_ptr, d_seq_lens_ptr, max_seq_len, out_ptr, stream):

@@ -334,6 +334,38 @@ tq_status tq_decode_attention(const tq_cache_desc *desc, const void *q, const in
                               tq_stream_t stream);
 
 /*
+ * Attention of the n_query newest tokens of every sequence over the cache, each
+ * query causal over the positions up to its own: the multi-token (prefill chunk
+ * or speculative verification) counterpart of tq_decode_attention, whose
+ * prefill ratios [mlxcel doc] "Measured speed and the memory trade-off" reports
+ * for every mode.  The new tokens' K/V must already be appended.  With
+ * L_b = d_seq_lens[b], query i (0 <= i < n_query) of sequence b sits at
+ * position L_b - n_query + i and
+ *
+ *   out[b, i, hq] = sum_{j <= L_b - n_query + i} softmax_j(q[b, i, hq].k_j / sqrt(d)) v_j
+ *
+ * (zeros when L_b - n_query + i < 0), with k_j, v_j as in tq_decode_attention;
+ * n_query = 1 computes what tq_decode_attention computes.  Each query token
+ * is one more sequence of the split-K work list, so a call costs about
+ * n_query decode calls of the same lengths.
+ *
+ *   q            fp16 device [B, n_query, Hq, head_dim] (contiguous)
+ *   n_query      >= 1; B * n_query <= 512
+ *   d_seq_lens   device int32 [B]: positions stored per sequence, the new
+ *                tokens included; each in [0, min(capacity, max_seq_len)]
+ *   out          float32 device [B, n_query, Hq, head_dim]
+ *   workspace    >= tq_multi_query_workspace_bytes(desc, n_query, max_seq_len)
+ *
+ * Errors as tq_decode_attention; TQ_ERR_UNSUPPORTED when B * n_query > 512
+ * or, with n_query > 1, when the descriptor's sparse-V threshold is nonzero
+ * (several query tokens accumulate V densely).
+ */
+size_t tq_multi_query_workspace_bytes(const tq_cache_desc *desc, int32_t n_query, int32_t max_seq_len);
+tq_status tq_multi_query_attention(const tq_cache_desc *desc, const void *q, int32_t n_query,
+                                   const int32_t *d_seq_lens, int32_t max_seq_len, float *out, void *workspace,
+                                   size_t workspace_bytes, tq_stream_t stream);
+
+/*
  * Decode attention for callers that cannot allocate device memory.  The pages
  * have no counterpart of this entry point; it exists for hosts that hand a
  * library only input and output pointers (plugin interfaces with no scratch

@@ -212,3 +212,30 @@ def test_int8_mode_descriptor_and_sizes():
         assert e.value.status == N.TQ_ERR_UNSUPPORTED
     with pytest.raises(N.TQError):  # a mode value the library does not know
         N.tq_cache_desc_init(4, 8, 32, 128, 4096, 3, 8, 8)
+
+
+def test_multi_query_arguments_and_workspace():
+    d = N.tq_cache_desc_init(4, 8, 32, 128, 4096, N.TQ_K_PACKED, 3, 4, hot_window=256)
+    # one partial slot per (split CTA, row): rows = 2 (cold, hot) x B x n_query x Hkv
+    per_slot = 4 * (128 + 2) * 4
+    assert N.tq_multi_query_workspace_bytes(d, 1, 100) == N.tq_decode_workspace_bytes(d, 100)
+    assert N.tq_multi_query_workspace_bytes(d, 8, 100) == (512 + 2 * 4 * 8 * 8) * per_slot
+    assert N.tq_multi_query_workspace_bytes(d, 0, 100) == 0
+    L = N.lib()
+    fake = 1 << 20
+    d.k_cache = d.v_cache = d.k_norms = d.v_norms = d.v_hot = fake
+    big = 1 << 30
+    assert L.tq_multi_query_attention(d, fake, 0, fake, 64, fake, fake, big, None) == N.TQ_ERR_INVALID_ARG
+    assert L.tq_multi_query_attention(d, fake, 129, fake, 64, fake, fake, big, None) == N.TQ_ERR_UNSUPPORTED
+    assert L.tq_multi_query_attention(d, fake + 8, 2, fake, 64, fake, fake, big, None) == N.TQ_ERR_INVALID_ARG
+    need = N.tq_multi_query_workspace_bytes(d, 4, 64)
+    assert L.tq_multi_query_attention(d, fake, 4, fake, 64, fake, fake, need - 16, None) == N.TQ_ERR_WORKSPACE
+
+
+def test_multi_query_refuses_sparse_v():
+    d = N.tq_cache_desc_init(2, 8, 32, 128, 4096, N.TQ_K_PACKED, 3, 4)
+    fake = 1 << 20
+    d.k_cache = d.v_cache = d.k_norms = d.v_norms = fake
+    d.sparse_v_threshold = 1e-3
+    L = N.lib()
+    assert L.tq_multi_query_attention(d, fake, 4, fake, 64, fake, fake, 1 << 30, None) == N.TQ_ERR_UNSUPPORTED
