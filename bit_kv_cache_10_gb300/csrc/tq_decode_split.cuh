@@ -461,45 +461,47 @@ __device__ __forceinline__ TileBlocks load_tile_blocks(const DecodeParams& p, in
 // entries are tb; returns the number of tokens the consumer may read (0 when
 // the table maps the tile outside the pool, after flagging TQ_DEV_ERR_BLOCK).
 // Cold tiles start at a multiple of the tile size and never straddle a block
-// (blocks hold at least one tile); a hot tile (K only) may straddle one boundary
-// and is then copied token by token.
+// (blocks hold at least one tile); a hot tile (K only) that straddles a block
+// boundary is copied token by token.  The common case (a full tile inside one
+// valid block) takes one branch; the others share the second.
 template <int KB, int VB>
 __device__ __forceinline__ int stage_tile_paged(const DecodeParams& p, int h, bool hot, int t_begin, int n_valid,
                                              TileBlocks tb, uint32_t buf, int lane) {
   using C = Cfg<KB, VB>;
   const int sh = p.map.shift;
-  const long long row0 = p.map.in_block(tb.first, h, t_begin);
-  if (row0 < 0 || p.map.in_block(tb.last, h, 0) < 0) {  // outside the pool: the tile is read as empty
-    if (lane == 0 && p.status != nullptr) atomicOr(p.status, TQ_DEV_ERR_BLOCK);
-    return 0;
-  }
-  const int blk0 = t_begin >> sh;
-  const bool straddle = ((t_begin + n_valid - 1) >> sh) != blk0;
+  const unsigned nb = static_cast<unsigned>(p.map.num_blocks);
+  const bool in_pool = static_cast<unsigned>(tb.first) < nb && static_cast<unsigned>(tb.last) < nb;
+  const bool one_block = tb.first == tb.last && ((t_begin + n_valid - 1) >> sh) == (t_begin >> sh);
+  const long long row0 = ((static_cast<long long>(tb.first) * p.map.hkv + h) << sh) + (t_begin & ((1 << sh) - 1));
   const uint8_t* kbase = C::kFp16K ? reinterpret_cast<const uint8_t*>(p.k_fp16)
                                    : reinterpret_cast<const uint8_t*>(p.k_words);
-  const uint8_t* ksrc = kbase + row0 * C::kKRow;
-  const uint8_t* vsrc = reinterpret_cast<const uint8_t*>(p.v_words) + row0 * (VB * 16);
   const uint32_t vbuf = buf + C::kKTile + C::kKNorm;
-  if (!straddle && n_valid == kTile) {
-    copy_full<C::kKTile>(buf, ksrc, lane);
-    if (!hot) copy_full<C::kVTile>(vbuf, vsrc, lane);
-  } else if (!straddle) {
-    for (int c = lane; c < n_valid * (C::kKRow / 16); c += 32) cp_async16s(buf + 16u * c, ksrc + 16 * c);
-    if (!hot)
-      for (int c = lane; c < n_valid * (C::kVRow / 16); c += 32) cp_async16s(vbuf + 16u * c, vsrc + 16 * c);
-  } else {  // hot tile across a block boundary: K token by token
+  long long rn = row0 + (lane & 15);  // norm row of the lane's token
+  if (in_pool && one_block && n_valid == kTile) {
+    copy_full<C::kKTile>(buf, kbase + row0 * C::kKRow, lane);
+    if (!hot) copy_full<C::kVTile>(vbuf, reinterpret_cast<const uint8_t*>(p.v_words) + row0 * (VB * 16), lane);
+  } else {
+    if (!in_pool) {  // outside the pool: nothing is staged, the tile is read as empty
+      if (lane == 0 && p.status != nullptr) atomicOr(p.status, TQ_DEV_ERR_BLOCK);
+      return 0;
+    }
+    const int blk0 = t_begin >> sh;
     constexpr int kPer = C::kKRow / 16;
-    for (int c = lane; c < n_valid * kPer; c += 32) {
+    for (int c = lane; c < n_valid * kPer; c += 32) {  // K token by token (a partial or a straddling tile)
       const int t = t_begin + c / kPer;
       const long long r = p.map.in_block((t >> sh) == blk0 ? tb.first : tb.last, h, t);
       cp_async16s(buf + 16u * c, kbase + r * C::kKRow + (c % kPer) * 16);
     }
+    if (!hot) {  // cold tiles never straddle
+      const uint8_t* vsrc = reinterpret_cast<const uint8_t*>(p.v_words) + row0 * (VB * 16);
+      for (int c = lane; c < n_valid * (C::kVRow / 16); c += 32) cp_async16s(vbuf + 16u * c, vsrc + 16 * c);
+    }
+    const int tn = t_begin + min(lane & 15, n_valid - 1);
+    rn = p.map.in_block((tn >> sh) == blk0 ? tb.first : tb.last, h, tn);
   }
   const int nl = lane & 15;
   const bool is_k = lane < 16;
   const bool want = nl < n_valid && (is_k ? !C::kFp16K : !hot);
-  const int tn = t_begin + min(nl, n_valid - 1);
-  const long long rn = straddle ? p.map.in_block((tn >> sh) == blk0 ? tb.first : tb.last, h, tn) : row0 + nl;
   const float* nsrc = (is_k ? p.k_norms : p.v_norms) + rn;
   const uint32_t ndst = (is_k ? buf + C::kKTile : vbuf + C::kVTile) + 4u * nl;
   if (want) cp_async4s(ndst, nsrc);
