@@ -63,6 +63,23 @@ def decode_bytes(lens) -> int:
     return total + len(lens) * HQ * D * (2 + 4)
 
 
+def max_over_ranks(ms: float, world: int, dist=None, device="cpu") -> float:
+    """Duration of the whole job's timed region: the maximum over the ranks
+    (every rank runs the same replica workload, so the slowest one ends it)."""
+    if world <= 1:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, ms: float, world: int) -> float:
+    """Whole-job throughput in units x 1e9 per second: `world` replicas each
+    processed `units_per_rank` within `ms` milliseconds."""
+    return world * units_per_rank / (ms * 1e-3) / 1e9
+
+
 def measured_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -531,11 +548,8 @@ def run_gpu(args):
     if status != 0:
         raise RuntimeError("device status %#x during the benchmark" % status)
     step_bytes = [decode_bytes(lens0 + args.warmup + i + 1) for i in range(args.steps)]
-    if world > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = world * sum(step_bytes) / (total_ms * 1e-3) / 1e9
+    total_ms = max_over_ranks(total_ms, world, dist, "cuda")
+    value = job_throughput(sum(step_bytes), total_ms, world)
     s0 = args.warmup + args.steps
 
     clocks = ClockSampler.summarize(clock_rows, "timed region")
@@ -617,13 +631,15 @@ def run_gpu(args):
     for i in range(e2e_warm):
         e2e_step(s0 + i)
     torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for i in range(e2e_steps):
         e2e_step(s0 + e2e_warm + i)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dist, "cuda")
     e2e_bytes = sum(decode_bytes(lens0 + s0 + e2e_warm + i + 1) for i in range(e2e_steps))
     h2d = kn[0].nbytes + vn[0].nbytes + qn[0].nbytes + B * 4
     d2h = B * HQ * D * 4
@@ -716,7 +732,7 @@ def run_gpu(args):
                         "algorithmic_bytes_per_launch": small_bytes,
                         "workload": "3.5-bit decode: B1, 32q/8kv, d128, context 4096, K3/V4 (launch-bound: "
                                     "4 MB per call, inside L2)"},
-        "e2e": {"value": world * e2e_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": job_throughput(e2e_bytes, e2e_ms, world), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "clocks": clocks,
         "gpu_launches": args.steps * 4,
