@@ -213,6 +213,25 @@ def _oracle_task(args):
     return oracle_sample_step(lens, q16, b, h, n)
 
 
+def _oracle_quant_task(args):
+    """Oracle quantize of n token vectors of K and of V of one (batch, KV head)
+    of the quantize workload (N(0,1) x lognormal channel scales) in a worker
+    process: (seconds, token-heads)."""
+    import oracle
+    b, h, n = args
+    rows = []
+    for stream, scale_stream in ((synth.STREAM_K, synth.STREAM_SCALE_K), (synth.STREAM_V, synth.STREAM_SCALE_V)):
+        s = synth.channel_scales(SEED + 2, scale_stream, HKV, D)[h]
+        rows.append((synth.row_rng(SEED + 2, stream, b, h).standard_normal((n, D)) * s).astype(np.float16))
+    rot = oracle.rotation(0, 0, h, D)
+    cbs = (oracle.codebook(D, KB), oracle.codebook(D, VB))  # built (or cached) outside the timed part
+    t0 = time.perf_counter()
+    for x, bits, cb in zip(rows, (KB, VB), cbs):
+        codes, _, _ = oracle.quantize_rows(x, rot, cb)
+        oracle.pack(codes, bits)
+    return time.perf_counter() - t0, n
+
+
 def oracle_pool():
     """Spawned worker processes, one per host core, each with single-threaded
     BLAS, so that independent (batch, KV head) rows run on all cores."""
@@ -237,10 +256,19 @@ def cpu_baseline(lens, q16, pool, workers, rounds=4):
     tasks = [(lens, q16, b, h, int(lens[b])) for _ in range(rounds) for b in range(B) for h in range(HKV)]
     pooled_rows(pool, tasks[:workers])  # start-up of the workers, untimed
     wall, nbytes = pooled_rows(pool, tasks)
+    # quantize: 2048-token slices of (batch, KV head) rows of the quantize workload, K 3-bit and V 4-bit
+    qtasks = [(i % QB, (i // QB) % HKV, 2048) for i in range(4 * workers)]
+    list(pool.map(_oracle_quant_task, qtasks[:workers]))  # untimed: codebooks built in every worker
+    t0 = time.perf_counter()
+    token_heads = sum(n for _, n in pool.map(_oracle_quant_task, qtasks))
+    qwall = time.perf_counter() - t0
     return {"value": nbytes / wall / 1e9, "unit": "GB/s", "cores": workers, "kind": "oracle",
             "sample": "%d (batch, KV head) rows of the workload at full context (%.2f GB of algorithmic bytes) on "
                       "%d worker processes with single-threaded BLAS: numpy float64 dequantize + softmax attention "
-                      "for the 4 query heads of each row" % (len(tasks), nbytes / 1e9, workers)}
+                      "for the 4 query heads of each row" % (len(tasks), nbytes / 1e9, workers),
+            "quantize": {"value": token_heads / HKV / qwall / 1e6, "unit": "Mtokens/s",
+                         "sample": "%d slices of 2048 tokens of one (batch, KV head) of the quantize workload, K 3-bit "
+                                   "and V 4-bit (a token = one position with all 8 KV heads)" % len(qtasks)}}
 
 
 def run_reference(args):

@@ -18,7 +18,7 @@
 namespace tq {
 namespace {
 
-constexpr int kWarps = 16;                  // warps per CTA
+constexpr int kWarps = 20;                  // warps per CTA (96 registers each: the register file)
 constexpr int kRowBytes = 256;              // one fp16 vector
 constexpr int kRowPitch = kRowBytes + 16;   // padded smem pitch
 constexpr int kTileRows = 16;
