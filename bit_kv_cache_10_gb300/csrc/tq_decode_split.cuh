@@ -229,7 +229,7 @@ struct Cfg {
   static constexpr int kRowShift = kFp16K ? 7 : 8;
   static constexpr int kTabBits = kInt8 ? 2 : kFp16K ? 2 * VB : 2 * (VB > kKBits ? VB : kKBits);
   static constexpr int kTab = (1 << kTabBits) << kRowShift;
-  static constexpr int kWts = kTile * 32;  // per warp: (w, w) x 4 heads per token
+  static constexpr int kWts = kTile * 32;  // per warp: up to 4 head weights per token (16 bytes used)
   static constexpr int kSmall = kWarps * kWts + 4 * D * 4 /* q' */ + 4 * D * 4 /* combine */ +
                                 kWarps * 4 * 2 * 4 /* warp (m, l) */ + kWarps * 8 * 16 /* tile descriptors */ +
                                 (kMaxDecodeBatch + 1) * 8 + 34 * 8;
@@ -899,33 +899,34 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
         for (int i = 0; i < GH; ++i) keep |= w_own[i] != 0.0f;
         stepmask = __reduce_or_sync(0xffffffffu, keep ? 1u << (tau_own >> 1) : 0u);
       }
-      // weights (w, w) of token tau_own, heads h0.. : row tau_own of 32 bytes
+      // weights of token tau_own, heads h0.. : row tau_own of 4 G bytes
       if constexpr (G == 4) {
-        *reinterpret_cast<float4*>(wts + tau_own * 32 + h0 * 8) = make_float4(w_own[0], w_own[0], w_own[1], w_own[1]);
+        *reinterpret_cast<float2*>(wts + tau_own * 16 + h0 * 4) = make_float2(w_own[0], w_own[1]);
       } else if constexpr (G == 2) {
-        *reinterpret_cast<float2*>(wts + tau_own * 32 + h0 * 8) = make_float2(w_own[0], w_own[0]);
+        *reinterpret_cast<float*>(wts + tau_own * 8 + h0 * 4) = w_own[0];
       } else {
-        if (owner) *reinterpret_cast<float2*>(wts + tau_own * 32) = make_float2(w_own[0], w_own[0]);
+        if (owner) *reinterpret_cast<float*>(wts + tau_own * 4) = w_own[0];
       }
       __syncwarp();
 
       // ---- V phase: tokens 2u + g, 8 coordinates per lane
-      const uint32_t wsb = wts_s + static_cast<uint32_t>(g * 32);
+      const uint32_t wsb = wts_s + static_cast<uint32_t>(g * 4 * G);
       const uint32_t vw = tbs + static_cast<uint32_t>(C::kKTile + C::kKNorm) + v_off;
       auto load_w = [&](auto U_, float2* w2) {
         constexpr int U = decltype(U_)::value;
-        if constexpr (G == 4) {
-          const float4 a = lds128f<U * 64>(wsb), b2 = lds128f<U * 64 + 16>(wsb);
-          w2[0] = make_float2(a.x, a.y);
-          w2[1] = make_float2(a.z, a.w);
-          w2[2] = make_float2(b2.x, b2.y);
-          w2[3] = make_float2(b2.z, b2.w);
+        if constexpr (G == 4) {  // one 16-byte broadcast per step, the (w, w) pairs built in registers
+          const float4 a = lds128f<U * 32>(wsb);
+          w2[0] = make_float2(a.x, a.x);
+          w2[1] = make_float2(a.y, a.y);
+          w2[2] = make_float2(a.z, a.z);
+          w2[3] = make_float2(a.w, a.w);
         } else if constexpr (G == 2) {
-          const float4 a = lds128f<U * 64>(wsb);
-          w2[0] = make_float2(a.x, a.y);
-          w2[G - 1] = make_float2(a.z, a.w);
+          const float2 a = lds64f<U * 16>(wsb);
+          w2[0] = make_float2(a.x, a.x);
+          w2[G - 1] = make_float2(a.y, a.y);
         } else {
-          w2[0] = lds64f<U * 64>(wsb);
+          const float a = __uint_as_float(lds32<U * 8>(wsb));
+          w2[0] = make_float2(a, a);
         }
       };
       auto v_cold = [&](auto U_) {
