@@ -2,8 +2,12 @@
 // hot-window evict pass.
 //
 // Work unit: a "job" is 16 consecutive tokens of one (tensor, batch, KV head).
-// Each warp streams its jobs through a two-stage cp.async pipeline into a
-// padded shared-memory tile (272-byte rows).  Four lanes share one token
+// Each of the CTA's 32 warps loads its next job into its own padded
+// shared-memory tile (272-byte rows) with cp.async as soon as it has finished
+// the current one; the other resident warps hide the latency (more warps beat
+// a second buffer: the kernel is bound by instruction fetch and issue, and
+// 32 warps at 64 registers ran 20 % faster than 20 double-buffered warps at
+// 96).  Four lanes share one token
 // vector, lane q owning coordinates 32q..32q+31, so that eight vectors are in
 // flight per warp step: exact norm (per-lane TwoSum partial sums merged across
 // the four lanes), sign flip, FWHT over index bits 0..4 in registers and bits
@@ -18,7 +22,7 @@
 namespace tq {
 namespace {
 
-constexpr int kWarps = 20;                  // warps per CTA (96 registers each: the register file)
+constexpr int kWarps = 32;                  // warps per CTA (64 registers each: the register file)
 constexpr int kRowBytes = 256;              // one fp16 vector
 constexpr int kRowPitch = kRowBytes + 16;   // padded smem pitch
 constexpr int kTileRows = 16;
@@ -48,6 +52,8 @@ struct QuantParams {
   float v_thr[15];
   int k_lut_a, v_lut_a;
   int evict;           // 0: append pass, 1: evict ring tokens that turn cold
+  int fuse_evict;      // append pass of at most W tokens: each V job evicts its ring slots first
+                       // (selects the FUSE variant of the kernel)
   int tiles_per_row;   // jobs per (tensor, batch, head)
   int tensors;         // 2 (K and V) for the append pass, 1 (V) for evict
   long long jobs;
@@ -109,7 +115,6 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem));
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
-__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;\n" ::); }
 
 __device__ __forceinline__ void issue_tile(const QuantParams& p, long long j, uint8_t* tile, int lane) {
   const Job jb = decode_job(p, j);
@@ -123,12 +128,13 @@ __device__ __forceinline__ void issue_tile(const QuantParams& p, long long j, ui
   }
 }
 
-// One step: 8 vectors of the tile (rows 8 * step + v), lane = v + 8 q.
+// One step: 8 vectors (a staged tile row or a ring row in global memory; rowp
+// is the lane's vector), lane = v + 8 q.
 template <int BITS>
-__device__ __forceinline__ void quantize_step(const uint8_t* tile, int row, int q, const uint32_t* smask,
+__device__ __forceinline__ void quantize_step(const uint8_t* rowp, int q, const uint32_t* smask,
                                               const LutEntry* lut, int lut_a, uint32_t* dst_words, float* dst_norm,
                                               bool store) {
-  const uint4* src = reinterpret_cast<const uint4*>(tile + row * kRowPitch) + 4 * q;
+  const uint4* src = reinterpret_cast<const uint4*>(rowp) + 4 * q;
   const uint4* msk = reinterpret_cast<const uint4*>(smask) + 4 * q;
   float2 v[16];
 #pragma unroll
@@ -144,7 +150,7 @@ __device__ __forceinline__ void quantize_step(const uint8_t* tile, int row, int 
   norm_partial<16>(v, h, l);  // squares of the sign-flipped values
   twosum_merge(h, l, __shfl_xor_sync(0xffffffffu, h, 8), __shfl_xor_sync(0xffffffffu, l, 8));
   twosum_merge(h, l, __shfl_xor_sync(0xffffffffu, h, 16), __shfl_xor_sync(0xffffffffu, l, 16));
-  const float n = norm_from_sum(h, l, reinterpret_cast<const uint32_t*>(tile + row * kRowPitch));
+  const float n = norm_from_sum(h, l, reinterpret_cast<const uint32_t*>(rowp));
   // rotation: in-lane bits 0..4, then bits 5 (q ^ 1) and 6 (q ^ 2) across lanes
   fwht32(v);
   // pairs are exchanged as 64-bit values, so each lands in a register pair
@@ -184,13 +190,13 @@ __device__ __forceinline__ uint32_t int8_code(float x, float s) {
 }
 
 // One step of the int8 mode ([mlxcel doc] "Available modes": per-token INT8
-// absmax): 8 vectors of the tile with the lane decomposition of quantize_step
+// absmax): 8 vectors with the lane decomposition of quantize_step
 // (lane q holds coordinates 32q .. 32q + 31).  s = fp32(max |x_i|) / 127,
 // code_i = int8_code(x_i, s); a zero vector gets s = 0 and zero codes.  The
 // lane packs its 32 codes into 8 words, code i in byte i mod 4.
-__device__ __forceinline__ void quantize_step_int8(const uint8_t* tile, int row, int q, uint32_t* dst_words,
-                                                   float* dst_scale, bool store) {
-  const uint4* src = reinterpret_cast<const uint4*>(tile + row * kRowPitch) + 4 * q;
+__device__ __forceinline__ void quantize_step_int8(const uint8_t* rowp, int q, uint32_t* dst_words, float* dst_scale,
+                                                   bool store) {
+  const uint4* src = reinterpret_cast<const uint4*>(rowp) + 4 * q;
   uint32_t w[16];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
@@ -228,7 +234,7 @@ __device__ __forceinline__ void quantize_step_int8(const uint8_t* tile, int row,
   }
 }
 
-template <bool PAGED>
+template <bool PAGED, bool FUSE>
 __global__ void __launch_bounds__(kWarps * 32, 1) quantize_append_kernel(const QuantParams p) {
   asm volatile("griddepcontrol.launch_dependents;\n");  // the next grid may start its prologue
   extern __shared__ __align__(16) uint8_t smem[];
@@ -239,8 +245,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1) quantize_append_kernel(const Q
   uint8_t* warp_area = reinterpret_cast<uint8_t*>(lut_v + lut_v_n * kLutCopies);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int vrow = lane & 7, q = lane >> 3;
-  uint8_t* tiles = warp_area + warp * (2 * kTileBytes + 256);
-  uint32_t* smask = reinterpret_cast<uint32_t*>(tiles + 2 * kTileBytes);
+  uint8_t* tiles = warp_area + warp * (kTileBytes + 256);
+  uint32_t* smask = reinterpret_cast<uint32_t*>(tiles + kTileBytes);
 
   // threshold lookup tables, kLutCopies interleaved copies (entry j of copy c at
   // j*copies + c): each entry is computed once and written to its copies
@@ -264,14 +270,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1) quantize_append_kernel(const Q
   // job j goes to CTA j mod grid: small appends put one job per SM
   const long long stride = static_cast<long long>(gridDim.x) * kWarps;
   long long j = static_cast<long long>(warp) * gridDim.x + blockIdx.x;
-  int buf = 0;
   if (j < p.jobs) issue_tile(p, j, tiles, lane);
   cp_async_commit();
   for (; j < p.jobs; j += stride) {
-    const long long jn = j + stride;
-    if (jn < p.jobs) issue_tile(p, jn, tiles + (buf ^ 1) * kTileBytes, lane);
-    cp_async_commit();
-    cp_async_wait1();
+    asm volatile("cp.async.wait_all;\n" ::);
     __syncwarp();
 
     const Job jb = decode_job(p, j);
@@ -284,11 +286,20 @@ __global__ void __launch_bounds__(kWarps * 32, 1) quantize_append_kernel(const Q
         smask[lane + 32] = sign_mask_pair(p.seed, p.layer, jb.h, lane + 32);
       }
       __syncwarp();
-      const uint8_t* tile = tiles + buf * kTileBytes;
+      const uint8_t* tile = tiles;
       const bool k_tensor = jb.tensor == 0;
       const bool copy_k = k_tensor && p.k_mode == TQ_K_FP16;
       int cold_end = 1 << 30;
       if (!k_tensor && p.hot > 0 && !p.evict) cold_end = jb.end - min(p.hot, jb.end);
+      auto quantize_row = [&](const uint8_t* rowp, int bits, const LutEntry* lut, int lut_a, uint32_t* dw, float* dn,
+                              bool store) {
+        switch (bits) {
+          case 8: quantize_step_int8(rowp, q, dw, dn, store); break;
+          case 2: quantize_step<2>(rowp, q, smask, lut, lut_a, dw, dn, store); break;
+          case 3: quantize_step<3>(rowp, q, smask, lut, lut_a, dw, dn, store); break;
+          default: quantize_step<4>(rowp, q, smask, lut, lut_a, dw, dn, store); break;
+        }
+      };
 #pragma unroll 1
       for (int step = 0; step < kTileRows / 8; ++step) {
         const int row = 8 * step + vrow;
@@ -300,33 +311,47 @@ __global__ void __launch_bounds__(kWarps * 32, 1) quantize_append_kernel(const Q
         const bool to_copy = copy_k || (!k_tensor && pos >= cold_end);
         const bool to_ring = !copy_k && to_copy;  // hot V goes to the per-sequence ring, not the pool
         if (have && ridx < 0 && !to_ring && p.status != nullptr) atomicOr(p.status, TQ_DEV_ERR_BLOCK);
+        const int64_t slot = (static_cast<int64_t>(jb.b) * p.heads + jb.h) * p.hot + (p.hot > 0 ? pos % p.hot : 0);
+        if (FUSE && !k_tensor) {
+          // appends of at most W tokens: the ring slot this row takes holds
+          // position pos - W, which turns cold now; it is quantized from the
+          // ring before the slot is overwritten below (one job owns the slot)
+          const int old = pos - p.hot;
+          long long oidx = (static_cast<long long>(jb.b) * p.heads + jb.h) * p.cap + old;
+          if constexpr (PAGED) oidx = have && old >= 0 ? p.map.row(jb.b, jb.h, old) : 0;
+          const bool ev = have && old >= 0;
+          if (ev && oidx < 0 && p.status != nullptr) atomicOr(p.status, TQ_DEV_ERR_BLOCK);
+          if (__any_sync(0xffffffffu, ev && oidx >= 0)) {
+            const uint8_t* src = ev ? reinterpret_cast<const uint8_t*>(p.v_ring + slot * D) : tile + row * kRowPitch;
+            quantize_row(src, p.v_bits, my_lut_v, p.v_lut_a, p.v_words + oidx * (p.v_bits * 4), p.v_norms + oidx,
+                         ev && oidx >= 0);
+          }
+          __syncwarp();
+        }
         if (to_copy && have && (to_ring || ridx >= 0)) {
           // fp16 copy of the row (asym K, or V going to the hot ring): 4 x 16 bytes per lane
           uint4* dst = copy_k ? reinterpret_cast<uint4*>(p.k_fp16 + ridx * D)
-                              : reinterpret_cast<uint4*>(
-                                    p.v_ring + ((static_cast<int64_t>(jb.b) * p.heads + jb.h) * p.hot + pos % p.hot) * D);
+                              : reinterpret_cast<uint4*>(p.v_ring + slot * D);
           const uint4* src = reinterpret_cast<const uint4*>(tile + row * kRowPitch);
 #pragma unroll
           for (int k = 0; k < 4; ++k) dst[4 * q + k] = src[4 * q + k];
         }
         if (copy_k) continue;  // uniform over the warp (the whole job is fp16 K)
         // every lane takes part in the shuffles of quantize_step; rows that are
-        // absent or go to the ring are computed but not stored
+        // absent or go to the ring are computed but not stored (a step with no
+        // stored row is skipped)
+        const bool store = have && !to_copy && ridx >= 0;
+        if (!__any_sync(0xffffffffu, store)) continue;
         const int bits = k_tensor ? p.k_bits : p.v_bits;
-        const LutEntry* lut = k_tensor ? my_lut_k : my_lut_v;
-        const int lut_a = k_tensor ? p.k_lut_a : p.v_lut_a;
-        uint32_t* dw = (k_tensor ? p.k_words : p.v_words) + ridx * (bits * 4);
-        float* dn = (k_tensor ? p.k_norms : p.v_norms) + ridx;
-        switch (bits) {
-          case 8: quantize_step_int8(tile, row, q, dw, dn, have && !to_copy && ridx >= 0); break;
-          case 2: quantize_step<2>(tile, row, q, smask, lut, lut_a, dw, dn, have && !to_copy && ridx >= 0); break;
-          case 3: quantize_step<3>(tile, row, q, smask, lut, lut_a, dw, dn, have && !to_copy && ridx >= 0); break;
-          default: quantize_step<4>(tile, row, q, smask, lut, lut_a, dw, dn, have && !to_copy && ridx >= 0); break;
-        }
+        quantize_row(tile + row * kRowPitch, bits, k_tensor ? my_lut_k : my_lut_v, k_tensor ? p.k_lut_a : p.v_lut_a,
+                     (k_tensor ? p.k_words : p.v_words) + ridx * (bits * 4), (k_tensor ? p.k_norms : p.v_norms) + ridx,
+                     store);
       }
     }
     __syncwarp();
-    buf ^= 1;
+    const long long jn = j + stride;
+    if (jn < p.jobs) issue_tile(p, jn, tiles, lane);
+    cp_async_commit();
   }
   asm volatile("cp.async.wait_all;\n" ::);
 }
@@ -334,7 +359,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) quantize_append_kernel(const Q
 size_t quant_smem_bytes(int k_lut_a, int v_lut_a) {
   const size_t luts = (static_cast<size_t>(k_lut_a ? lut_size(k_lut_a) : 0) + (v_lut_a ? lut_size(v_lut_a) : 0)) *
                       kLutCopies * sizeof(LutEntry);
-  return luts + static_cast<size_t>(kWarps) * (2 * kTileBytes + 256);
+  return luts + static_cast<size_t>(kWarps) * (kTileBytes + 256);
 }
 
 int sm_count() {
@@ -348,7 +373,8 @@ tq_status launch_quantize(QuantParams& p, cudaStream_t stream) {
   if (p.jobs <= 0) return TQ_OK;
   const size_t smem = quant_smem_bytes(p.k_lut_a, p.v_lut_a);
   const bool paged = p.map.table != nullptr;
-  auto kern = paged ? quantize_append_kernel<true> : quantize_append_kernel<false>;
+  auto kern = paged ? (p.fuse_evict ? quantize_append_kernel<true, true> : quantize_append_kernel<true, false>)
+                    : (p.fuse_evict ? quantize_append_kernel<false, true> : quantize_append_kernel<false, false>);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
     return TQ_ERR_CUDA;
   const int sms = sm_count();
@@ -426,7 +452,11 @@ extern "C" tq_status tq_quantize_append(const tq_cache_desc* d, const void* k_ne
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
-  if (d->hot_window > 0) {  // V tokens leaving the ring are quantized before their slots are reused
+  // V tokens leaving the ring are quantized before their slots are reused: by the
+  // append launch itself when at most W tokens are appended (every slot is then
+  // taken by one new row, whose job evicts it first), else by a launch before it
+  p.fuse_evict = d->hot_window > 0 && n_new <= d->hot_window;
+  if (d->hot_window > 0 && !p.fuse_evict) {
     QuantParams e = p;
     e.evict = 1;
     e.tensors = 1;

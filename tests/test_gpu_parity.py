@@ -384,3 +384,43 @@ def test_dequantize_matches_oracle():
                 ref = (kr if which == 0 else vr)[7:257]
                 scale = np.maximum(np.linalg.norm(ref, axis=1, keepdims=True), 1e-30)
                 assert np.all(np.abs(got[h] - ref) <= 1e-5 * scale), (kfp16, which, h)
+
+
+@pytest.mark.parametrize("bits", [3.5, "int8"])
+def test_append_chunks_within_the_hot_window(bits):
+    """Appends of at most W tokens evict the ring slots they take inside the same
+    launch; rows whose slot held a position (pos - W >= 0) turn cold, the others
+    do not.  Chunks of 8 and 40 (= W) tokens on sequences shorter and longer
+    than W."""
+    HK, HQ, CAP, W = 2, 8, 400, 40
+    pre = np.array([10, 39, 100, 0], np.int32)
+    B = len(pre)
+    k = synth.kv_fp16(41, 1, B, HK, CAP, D, synth.channel_scales(41, 4, HK, D))
+    v = synth.kv_fp16(41, 2, B, HK, CAP, D, synth.channel_scales(41, 5, HK, D))
+    tc = _cache(batch=B, num_kv_heads=HK, num_q_heads=HQ, capacity=CAP, bits=bits, hot_window=W)
+    kd, vd = _dev(k), _dev(v)
+    tc.append(kd, vd, _dev(np.zeros(B, np.int32)), _dev(pre))
+    lens = pre.copy()
+    for n in (8, 40, 1, 8):
+        idx = torch.from_numpy(lens.astype(np.int64)).cuda()
+        kn = torch.stack([kd[b, :, idx[b]:idx[b] + n] for b in range(B)]).contiguous()
+        vn = torch.stack([vd[b, :, idx[b]:idx[b] + n] for b in range(B)]).contiguous()
+        tc.append(kn, vn, _dev(lens))
+        lens = lens + n
+    assert tc.device_status() == 0
+    if bits == "int8":
+        oc = oracle.build_cache(k, v, lens, CAP, 8, 8, hot_window=W, codec="int8")
+        gw = tc.v_cache.cpu().numpy().view(np.uint32)
+        gs = tc.v_norms.cpu().numpy()
+        for b in range(B):
+            ce = int(lens[b]) - min(W, int(lens[b]))
+            np.testing.assert_array_equal(gw[b, :, :ce], oc.v_words[b, :, :ce])
+            np.testing.assert_array_equal(gs[b, :, :ce], oc.v_norms[b, :, :ce])
+    else:
+        oc = oracle.build_cache(k, v, lens, CAP, 3, 4, hot_window=W)
+        check_quantized(tc, v, 1, 4, lens - np.minimum(W, lens), what="chunked cold V")
+    np.testing.assert_array_equal(tc.v_hot.cpu().numpy(), oc.v_hot)
+    q = synth.queries_fp16(41, B, HQ, D)
+    upload(tc, oc)
+    got, ref = decode_both(tc, oc, q, lens, CAP)
+    assert_attention_close(got, ref, "chunked appends")
