@@ -1,5 +1,6 @@
-// Split-K decode kernel over the packed cache, included by the dense and the
-// sparse-V translation units (each instantiates one variant).
+// Split-K decode kernel over the packed cache, included by the decode
+// translation units (dense or sparse V, contiguous or paged layout, one or
+// several query tokens per sequence; each instantiates one variant).
 //
 // Work list.  Every (sequence b, KV head h) has a cold row (the packed
 // positions [0, L - min(W, L))) and, with a hot window, a hot row (the newest
