@@ -16,6 +16,9 @@ namespace {
 // registers and 2..6 across lanes, 1/sqrt d; not in the int8 mode), adds the hot
 // sum and divides by the softmax mass.
 __global__ void __launch_bounds__(4 * 32) decode_merge_kernel(const DecodeParams p) {
+  // a following programmatic dependent grid (the next append) may start its
+  // parameter-only prologue now; it waits for this grid before touching memory
+  asm volatile("griddepcontrol.launch_dependents;\n");
   const int g = p.hq / p.hkv;
   const int jj = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.x, b = blockIdx.y;

@@ -356,13 +356,225 @@ __global__ void __launch_bounds__(kWarps * 32, 1) quantize_append_kernel(const Q
   asm volatile("cp.async.wait_all;\n" ::);
 }
 
+// ---------------------------------------------------------------------------
+// Small appends (at most kSmallMax tokens per sequence: the decode step's one
+// token).  The latency of one quantized vector is then the critical path, so
+// one warp takes one token vector, lane l holding coordinates 4l..4l+3.  The
+// arithmetic is that of quantize_step stage for stage (exact norm, sign flip,
+// FWHT over index bits 0..6 in that order, the same scaling and threshold
+// lookup), so the stored words and norms are the same.
+// ---------------------------------------------------------------------------
+int sm_count_q();
+constexpr int kSmallMax = 16;   // tokens per sequence appended by the small-append kernel
+constexpr int kSmallWarps = 4;  // warps (token vectors in flight) per CTA
+
+// Lane l's 4 BITS-bit codes sit at stream offset 4 l BITS; word w of the token
+// is the OR of the lanes' contributions to it, and lane w stores it.
+template <int BITS>
+__device__ __forceinline__ void store_codes_warp(uint32_t val, int lane, uint32_t* dst, bool store) {
+  constexpr int kW = 4 * BITS;  // words of a d = 128 vector
+  const int off = 4 * BITS * lane;
+  const int lo = off >> 5;
+  const uint64_t c = static_cast<uint64_t>(val) << (off & 31);
+  const uint32_t c_lo = static_cast<uint32_t>(c), c_hi = static_cast<uint32_t>(c >> 32);
+  uint32_t mine = 0u;
+#pragma unroll
+  for (int w = 0; w < kW; ++w) {
+    const uint32_t word = __reduce_or_sync(0xffffffffu, (lo == w ? c_lo : 0u) | (lo + 1 == w ? c_hi : 0u));
+    if (lane == w) mine = word;
+  }
+  if (store && lane < kW) dst[lane] = mine;
+}
+
+// One token vector per warp: x = the lane's 4 fp16 values, sm = their sign
+// masks, row = the vector in memory (read only by the rare exact-norm path).
+template <int BITS>
+__device__ __forceinline__ void quantize_vector_warp(const uint16_t* row, uint2 x, uint2 sm, const LutEntry* lut,
+                                                     int lut_a, uint32_t* dst_words, float* dst_norm, bool store,
+                                                     int lane) {
+  float2 v[2] = {half2_bits_to_float2(x.x ^ sm.x), half2_bits_to_float2(x.y ^ sm.y)};
+  float h, l;
+  norm_partial<2>(v, h, l);
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1)
+    twosum_merge(h, l, __shfl_xor_sync(0xffffffffu, h, m), __shfl_xor_sync(0xffffffffu, l, m));
+  const float n = norm_from_sum(h, l, reinterpret_cast<const uint32_t*>(row));
+  // FWHT: index bits 0 and 1 inside the lane, bits 2..6 across lanes (lane bit k - 2)
+  float z[4];
+  {
+    const float a0 = fadd(v[0].x, v[0].y), a1 = fsub(v[0].x, v[0].y);
+    const float a2 = fadd(v[1].x, v[1].y), a3 = fsub(v[1].x, v[1].y);
+    z[0] = fadd(a0, a2);
+    z[1] = fadd(a1, a3);
+    z[2] = fsub(a0, a2);
+    z[3] = fsub(a1, a3);
+  }
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float o = __shfl_xor_sync(0xffffffffu, z[k], m);
+      z[k] = upper ? fsub(o, z[k]) : fadd(z[k], o);
+    }
+  }
+  const float inv = n > 0.0f ? frcp(fmul(n, kSqrtD)) : 0.0f;
+  const float fa = static_cast<float>(lut_a);
+  const uint32_t last = static_cast<uint32_t>(lut_size(lut_a) - 1);
+  const uint32_t bias = fbits(kMagic) - static_cast<uint32_t>(lut_a + 1);
+  uint32_t val = 0u;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float y = fmul(z[k], inv);
+    const uint32_t raw = fbits(ffma(y, fa, kMagic)) - bias;
+    const LutEntry e = lut[(raw < last ? raw : last) * kLutCopies];
+    val |= (e.base + (y >= e.thr ? 1u : 0u)) << (BITS * k);
+  }
+  store_codes_warp<BITS>(val, lane, dst_words, store);
+  if (store && lane == 0) *dst_norm = n;
+}
+
+// The int8 mode for one token vector per warp (arithmetic of quantize_step_int8).
+__device__ __forceinline__ void quantize_vector_warp_int8(uint2 x, uint32_t* dst_words, float* dst_scale, bool store,
+                                                          int lane) {
+  uint32_t m = __vmaxu2(x.x & 0x7FFF7FFFu, x.y & 0x7FFF7FFFu);
+  m = __reduce_max_sync(0xffffffffu, max(m & 0xFFFFu, m >> 16));
+  const float s = __fdiv_rn(half_bits_to_float(m), 127.0f);
+  const float2 a = half2_bits_to_float2(x.x), b = half2_bits_to_float2(x.y);
+  uint32_t word = 0u;
+  if (s > 0.0f) {
+    const uint32_t lo = __byte_perm(int8_code(a.x, s), int8_code(a.y, s), 0x0040);
+    const uint32_t hi = __byte_perm(int8_code(b.x, s), int8_code(b.y, s), 0x0040);
+    word = __byte_perm(lo, hi, 0x5410);
+  }
+  if (store) {
+    dst_words[lane] = word;
+    if (lane == 0) *dst_scale = s;
+  }
+}
+
+template <bool PAGED>
+__global__ void __launch_bounds__(kSmallWarps * 32) quantize_small_kernel(const QuantParams p) {
+  asm volatile("griddepcontrol.launch_dependents;\n");
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int lut_k_n = p.k_lut_a ? lut_size(p.k_lut_a) : 0;
+  const int lut_v_n = p.v_lut_a ? lut_size(p.v_lut_a) : 0;
+  LutEntry* lut_k = reinterpret_cast<LutEntry*>(smem);
+  LutEntry* lut_v = lut_k + lut_k_n * kLutCopies;
+  for (int j = threadIdx.x; j < lut_k_n + lut_v_n; j += blockDim.x) {
+    const bool is_k = j < lut_k_n;
+    const LutEntry e = is_k ? lut_entry(p.k_thr, (1 << p.k_bits) - 1, p.k_lut_a, j)
+                            : lut_entry(p.v_thr, (1 << p.v_bits) - 1, p.v_lut_a, j - lut_k_n);
+    uint4* dst = reinterpret_cast<uint4*>(lut_k + j * kLutCopies);
+    const uint4 two = make_uint4(__float_as_uint(e.thr), e.base, __float_as_uint(e.thr), e.base);
+#pragma unroll
+    for (int c = 0; c < kLutCopies / 2; ++c) dst[c] = two;
+  }
+  __syncthreads();
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");  // the inputs and the ring may come from the previous grid
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const LutEntry* my_lut_k = lut_k + (lane & (kLutCopies - 1));
+  const LutEntry* my_lut_v = lut_v + (lane & (kLutCopies - 1));
+  const long long per_tensor = static_cast<long long>(p.batch) * p.heads * p.n_new;
+  for (long long vi = static_cast<long long>(blockIdx.x) * kSmallWarps + warp; vi < 2 * per_tensor;
+       vi += static_cast<long long>(gridDim.x) * kSmallWarps) {
+    const int tensor = vi >= per_tensor ? 1 : 0;  // 0 = K, 1 = V
+    const long long r = vi - tensor * per_tensor;
+    const int t = static_cast<int>(r % p.n_new);
+    const int bh = static_cast<int>(r / p.n_new);
+    const int b = bh / p.heads, h = bh - b * p.heads;
+    const int s = p.start_pos[b];
+    const int cnt = p.num_new != nullptr ? p.num_new[b] : p.n_new;
+    if (!(s >= 0 && cnt >= 0 && cnt <= p.n_new && static_cast<long long>(s) + cnt <= p.cap)) {
+      if (t == 0 && h == 0 && tensor == 0 && lane == 0 && p.status != nullptr)
+        atomicOr(p.status, TQ_DEV_ERR_APPEND_RANGE);
+      continue;
+    }
+    if (t >= cnt) continue;
+    const int pos = s + t;
+    const uint16_t* src = (tensor ? p.v_src : p.k_src) + b * p.stride_b + h * p.stride_h + t * p.stride_t;
+    const uint2 x = reinterpret_cast<const uint2*>(src)[lane];
+    if (tensor == 0 && p.k_mode == TQ_K_FP16) {  // asym K: stored verbatim
+      const long long ridx = PAGED ? p.map.row(b, h, pos) : (static_cast<long long>(b) * p.heads + h) * p.cap + pos;
+      if (ridx < 0) {
+        if (lane == 0 && p.status != nullptr) atomicOr(p.status, TQ_DEV_ERR_BLOCK);
+      } else {
+        reinterpret_cast<uint2*>(p.k_fp16 + ridx * D)[lane] = x;
+      }
+      continue;
+    }
+    const uint2 sm = p.k_mode == TQ_KV_INT8 ? make_uint2(0u, 0u)
+                                            : make_uint2(sign_mask_pair(p.seed, p.layer, h, 2 * lane),
+                                                         sign_mask_pair(p.seed, p.layer, h, 2 * lane + 1));
+    // what to quantize: the new row, or for V with a hot window the ring row
+    // position pos - W leaves (the new row takes its slot: at most W tokens
+    // are appended, so one vector owns each slot)
+    const uint16_t* qrow = src;
+    uint2 qx = x;
+    int qpos = pos;
+    uint16_t* ring = nullptr;
+    if (tensor == 1 && p.hot > 0) {
+      ring = p.v_ring + ((static_cast<int64_t>(b) * p.heads + h) * p.hot + pos % p.hot) * D;
+      qpos = pos - p.hot;
+      qrow = ring;
+      qx = qpos >= 0 ? reinterpret_cast<const uint2*>(ring)[lane] : make_uint2(0u, 0u);
+    }
+    if (qpos >= 0) {
+      const long long ridx = PAGED ? p.map.row(b, h, qpos) : (static_cast<long long>(b) * p.heads + h) * p.cap + qpos;
+      if (ridx < 0 && lane == 0 && p.status != nullptr) atomicOr(p.status, TQ_DEV_ERR_BLOCK);
+      const int bits = tensor ? p.v_bits : p.k_bits;
+      const LutEntry* lut = tensor ? my_lut_v : my_lut_k;
+      const int lut_a = tensor ? p.v_lut_a : p.k_lut_a;
+      uint32_t* dw = (tensor ? p.v_words : p.k_words) + (ridx < 0 ? 0 : ridx) * (bits * 4);
+      float* dn = (tensor ? p.v_norms : p.k_norms) + (ridx < 0 ? 0 : ridx);
+      const bool store = ridx >= 0;
+      switch (bits) {
+        case 8: quantize_vector_warp_int8(qx, dw, dn, store, lane); break;
+        case 2: quantize_vector_warp<2>(qrow, qx, sm, lut, lut_a, dw, dn, store, lane); break;
+        case 3: quantize_vector_warp<3>(qrow, qx, sm, lut, lut_a, dw, dn, store, lane); break;
+        default: quantize_vector_warp<4>(qrow, qx, sm, lut, lut_a, dw, dn, store, lane); break;
+      }
+    }
+    if (ring != nullptr) {  // the slot's old row has been read (and quantized)
+      __syncwarp();
+      reinterpret_cast<uint2*>(ring)[lane] = x;
+    }
+  }
+}
+
+tq_status launch_small(const QuantParams& p, cudaStream_t stream) {
+  const size_t smem = (static_cast<size_t>(p.k_lut_a ? lut_size(p.k_lut_a) : 0) + (p.v_lut_a ? lut_size(p.v_lut_a) : 0)) *
+                      kLutCopies * sizeof(LutEntry);
+  const bool paged = p.map.table != nullptr;
+  auto kern = paged ? quantize_small_kernel<true> : quantize_small_kernel<false>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
+    return TQ_ERR_CUDA;
+  const int sms = sm_count_q();
+  if (sms <= 0) return TQ_ERR_CUDA;
+  const long long vectors = 2ll * p.batch * p.heads * p.n_new;
+  const long long want = (vectors + kSmallWarps - 1) / kSmallWarps;
+  const int grid = static_cast<int>(want < 4ll * sms ? want : 4ll * sms);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kSmallWarps * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see griddepcontrol.wait
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return TQ_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
 size_t quant_smem_bytes(int k_lut_a, int v_lut_a) {
   const size_t luts = (static_cast<size_t>(k_lut_a ? lut_size(k_lut_a) : 0) + (v_lut_a ? lut_size(v_lut_a) : 0)) *
                       kLutCopies * sizeof(LutEntry);
   return luts + static_cast<size_t>(kWarps) * (kTileBytes + 256);
 }
 
-int sm_count() {
+int sm_count_q() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
@@ -377,7 +589,7 @@ tq_status launch_quantize(QuantParams& p, cudaStream_t stream) {
                     : (p.fuse_evict ? quantize_append_kernel<false, true> : quantize_append_kernel<false, false>);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
     return TQ_ERR_CUDA;
-  const int sms = sm_count();
+  const int sms = sm_count_q();
   if (sms <= 0) return TQ_ERR_CUDA;
   const int grid = static_cast<int>(p.jobs < sms ? p.jobs : sms);
   cudaLaunchConfig_t cfg = {};
@@ -452,6 +664,7 @@ extern "C" tq_status tq_quantize_append(const tq_cache_desc* d, const void* k_ne
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
+  if (n_new <= kSmallMax && (d->hot_window == 0 || n_new <= d->hot_window)) return launch_small(p, s);
   // V tokens leaving the ring are quantized before their slots are reused: by the
   // append launch itself when at most W tokens are appended (every slot is then
   // taken by one new row, whose job evicts it first), else by a launch before it

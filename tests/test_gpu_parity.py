@@ -424,3 +424,23 @@ def test_append_chunks_within_the_hot_window(bits):
     upload(tc, oc)
     got, ref = decode_both(tc, oc, q, lens, CAP)
     assert_attention_close(got, ref, "chunked appends")
+
+
+@pytest.mark.parametrize("bits", [(2, 3), 3.5, (4, 4), "int8"])
+def test_small_and_bulk_appends_store_the_same_words(bits):
+    """Appends of at most 16 tokens use the one-warp-per-vector kernel, longer
+    ones the four-lanes-per-vector kernel; both must store identical words and
+    norms (same arithmetic, stage for stage)."""
+    B, HK, T = 3, 4, 48
+    k = synth.kv_fp16(51, 1, B, HK, T, D, synth.channel_scales(51, 4, HK, D))
+    v = synth.kv_fp16(51, 2, B, HK, T, D, synth.channel_scales(51, 5, HK, D))
+    k[0, 1, 5] = 0.0  # a zero vector
+    bulk = _cache(batch=B, num_kv_heads=HK, num_q_heads=HK, capacity=T, bits=bits)
+    small = _cache(batch=B, num_kv_heads=HK, num_q_heads=HK, capacity=T, bits=bits)
+    bulk.append(_dev(k), _dev(v), _dev(np.zeros(B, np.int32)))
+    for c in range(0, T, 16):
+        small.append(_dev(k[:, :, c:c + 16]), _dev(v[:, :, c:c + 16]), _dev(np.full(B, c, np.int32)))
+    assert bulk.device_status() == 0 and small.device_status() == 0
+    for name in ("k_cache", "k_norms", "v_cache", "v_norms"):
+        np.testing.assert_array_equal(getattr(small, name).cpu().numpy(), getattr(bulk, name).cpu().numpy(),
+                                      err_msg=name)
