@@ -238,7 +238,9 @@ struct Cfg {
   // windows start at a 1 KB multiple); buffers are placed around the table
   static constexpr int kWorst(int stages) { return kTab + kSmall + (kWarps + 1) * stages * kBuf + 1024; }
   static constexpr int kStages = kWorst(8) <= kSmemBudget ? 8 : kWorst(6) <= kSmemBudget ? 6 : kWorst(4) <= kSmemBudget ? 4 : kWorst(3) <= kSmemBudget ? 3 : 2;
-  static constexpr int kSmem = kSmemBudget;
+  // requested dynamic shared memory: the layout's bound (1 KB multiple), so that
+  // a small kernel (the decode step's append) can share the SM with a CTA
+  static constexpr int kSmem = (kWorst(kStages) + 1023) / 1024 * 1024;
   static_assert(kWorst(kStages) <= kSmemBudget, "shared memory budget");
 };
 

@@ -366,7 +366,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1) quantize_append_kernel(const Q
 // ---------------------------------------------------------------------------
 int sm_count_q();
 constexpr int kSmallMax = 16;   // tokens per sequence appended by the small-append kernel
-constexpr int kSmallWarps = 4;  // warps (token vectors in flight) per CTA
+constexpr int kSmallWarps = 2;  // warps (token vectors in flight) per CTA
+// One copy of each lookup table: the kernel is latency-bound and small enough
+// (a few KB of shared memory, 64 threads) to share an SM with a decode CTA.
 
 // Lane l's 4 BITS-bit codes sit at stream offset 4 l BITS; word w of the token
 // is the OR of the lanes' contributions to it, and lane w stores it.
@@ -391,7 +393,7 @@ __device__ __forceinline__ void store_codes_warp(uint32_t val, int lane, uint32_
 template <int BITS>
 __device__ __forceinline__ void quantize_vector_warp(const uint16_t* row, uint2 x, uint2 sm, const LutEntry* lut,
                                                      int lut_a, uint32_t* dst_words, float* dst_norm, bool store,
-                                                     int lane) {
+                                                     int lane) {  // lut: one copy
   float2 v[2] = {half2_bits_to_float2(x.x ^ sm.x), half2_bits_to_float2(x.y ^ sm.y)};
   float h, l;
   norm_partial<2>(v, h, l);
@@ -427,7 +429,7 @@ __device__ __forceinline__ void quantize_vector_warp(const uint16_t* row, uint2 
   for (int k = 0; k < 4; ++k) {
     const float y = fmul(z[k], inv);
     const uint32_t raw = fbits(ffma(y, fa, kMagic)) - bias;
-    const LutEntry e = lut[(raw < last ? raw : last) * kLutCopies];
+    const LutEntry e = lut[raw < last ? raw : last];
     val |= (e.base + (y >= e.thr ? 1u : 0u)) << (BITS * k);
   }
   store_codes_warp<BITS>(val, lane, dst_words, store);
@@ -460,21 +462,15 @@ __global__ void __launch_bounds__(kSmallWarps * 32) quantize_small_kernel(const 
   const int lut_k_n = p.k_lut_a ? lut_size(p.k_lut_a) : 0;
   const int lut_v_n = p.v_lut_a ? lut_size(p.v_lut_a) : 0;
   LutEntry* lut_k = reinterpret_cast<LutEntry*>(smem);
-  LutEntry* lut_v = lut_k + lut_k_n * kLutCopies;
-  for (int j = threadIdx.x; j < lut_k_n + lut_v_n; j += blockDim.x) {
-    const bool is_k = j < lut_k_n;
-    const LutEntry e = is_k ? lut_entry(p.k_thr, (1 << p.k_bits) - 1, p.k_lut_a, j)
-                            : lut_entry(p.v_thr, (1 << p.v_bits) - 1, p.v_lut_a, j - lut_k_n);
-    uint4* dst = reinterpret_cast<uint4*>(lut_k + j * kLutCopies);
-    const uint4 two = make_uint4(__float_as_uint(e.thr), e.base, __float_as_uint(e.thr), e.base);
-#pragma unroll
-    for (int c = 0; c < kLutCopies / 2; ++c) dst[c] = two;
-  }
+  LutEntry* lut_v = lut_k + lut_k_n;
+  for (int j = threadIdx.x; j < lut_k_n + lut_v_n; j += blockDim.x)
+    lut_k[j] = j < lut_k_n ? lut_entry(p.k_thr, (1 << p.k_bits) - 1, p.k_lut_a, j)
+                           : lut_entry(p.v_thr, (1 << p.v_bits) - 1, p.v_lut_a, j - lut_k_n);
   __syncthreads();
   asm volatile("griddepcontrol.wait;\n" ::: "memory");  // the inputs and the ring may come from the previous grid
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const LutEntry* my_lut_k = lut_k + (lane & (kLutCopies - 1));
-  const LutEntry* my_lut_v = lut_v + (lane & (kLutCopies - 1));
+  const LutEntry* my_lut_k = lut_k;
+  const LutEntry* my_lut_v = lut_v;
   const long long per_tensor = static_cast<long long>(p.batch) * p.heads * p.n_new;
   for (long long vi = static_cast<long long>(blockIdx.x) * kSmallWarps + warp; vi < 2 * per_tensor;
        vi += static_cast<long long>(gridDim.x) * kSmallWarps) {
@@ -544,7 +540,7 @@ __global__ void __launch_bounds__(kSmallWarps * 32) quantize_small_kernel(const 
 
 tq_status launch_small(const QuantParams& p, cudaStream_t stream) {
   const size_t smem = (static_cast<size_t>(p.k_lut_a ? lut_size(p.k_lut_a) : 0) + (p.v_lut_a ? lut_size(p.v_lut_a) : 0)) *
-                      kLutCopies * sizeof(LutEntry);
+                      sizeof(LutEntry);
   const bool paged = p.map.table != nullptr;
   auto kern = paged ? quantize_small_kernel<true> : quantize_small_kernel<false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
