@@ -361,14 +361,15 @@ __global__ void __launch_bounds__(kWarps * 32, 1) quantize_append_kernel(const Q
 // token).  The latency of one quantized vector is then the critical path, so
 // one warp takes one token vector, lane l holding coordinates 4l..4l+3.  The
 // arithmetic is that of quantize_step stage for stage (exact norm, sign flip,
-// FWHT over index bits 0..6 in that order, the same scaling and threshold
-// lookup), so the stored words and norms are the same.
+// FWHT over index bits 0..6 in that order, the same scaling; the code is the
+// same count of thresholds, found by binary search instead of the bucketed
+// table, which this kernel need not build), so the stored words and norms are
+// the same.
 // ---------------------------------------------------------------------------
 int sm_count_q();
 constexpr int kSmallMax = 16;   // tokens per sequence appended by the small-append kernel
-constexpr int kSmallWarps = 2;  // warps (token vectors in flight) per CTA
-// One copy of each lookup table: the kernel is latency-bound and small enough
-// (a few KB of shared memory, 64 threads) to share an SM with a decode CTA.
+constexpr int kSmallWarps = 2;  // warps (token vectors in flight) per CTA: small enough to share
+                                // an SM with a decode CTA
 
 // Lane l's 4 BITS-bit codes sit at stream offset 4 l BITS; word w of the token
 // is the OR of the lanes' contributions to it, and lane w stores it.
@@ -388,12 +389,23 @@ __device__ __forceinline__ void store_codes_warp(uint32_t val, int lane, uint32_
   if (store && lane < kW) dst[lane] = mine;
 }
 
-// One token vector per warp: x = the lane's 4 fp16 values, sm = their sign
-// masks, row = the vector in memory (read only by the rare exact-norm path).
+// Code of y: the number of float32 thresholds t_k <= y, by binary search over
+// the 2^BITS - 1 sorted thresholds (the same count the bucketed table gives).
 template <int BITS>
-__device__ __forceinline__ void quantize_vector_warp(const uint16_t* row, uint2 x, uint2 sm, const LutEntry* lut,
-                                                     int lut_a, uint32_t* dst_words, float* dst_norm, bool store,
-                                                     int lane) {  // lut: one copy
+__device__ __forceinline__ uint32_t threshold_code(float y, const float* thr) {
+  uint32_t lo = 0u;
+#pragma unroll
+  for (int step = 1 << (BITS - 1); step > 0; step >>= 1)
+    if (y >= thr[lo + step - 1]) lo += step;
+  return lo;
+}
+
+// One token vector per warp: x = the lane's 4 fp16 values, sm = their sign
+// masks, row = the vector in memory (read only by the rare exact-norm path),
+// thr = the codebook's thresholds.
+template <int BITS>
+__device__ __forceinline__ void quantize_vector_warp(const uint16_t* row, uint2 x, uint2 sm, const float* thr,
+                                                     uint32_t* dst_words, float* dst_norm, bool store, int lane) {
   float2 v[2] = {half2_bits_to_float2(x.x ^ sm.x), half2_bits_to_float2(x.y ^ sm.y)};
   float h, l;
   norm_partial<2>(v, h, l);
@@ -421,17 +433,9 @@ __device__ __forceinline__ void quantize_vector_warp(const uint16_t* row, uint2 
     }
   }
   const float inv = n > 0.0f ? frcp(fmul(n, kSqrtD)) : 0.0f;
-  const float fa = static_cast<float>(lut_a);
-  const uint32_t last = static_cast<uint32_t>(lut_size(lut_a) - 1);
-  const uint32_t bias = fbits(kMagic) - static_cast<uint32_t>(lut_a + 1);
   uint32_t val = 0u;
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const float y = fmul(z[k], inv);
-    const uint32_t raw = fbits(ffma(y, fa, kMagic)) - bias;
-    const LutEntry e = lut[raw < last ? raw : last];
-    val |= (e.base + (y >= e.thr ? 1u : 0u)) << (BITS * k);
-  }
+  for (int k = 0; k < 4; ++k) val |= threshold_code<BITS>(fmul(z[k], inv), thr) << (BITS * k);
   store_codes_warp<BITS>(val, lane, dst_words, store);
   if (store && lane == 0) *dst_norm = n;
 }
@@ -458,19 +462,12 @@ __device__ __forceinline__ void quantize_vector_warp_int8(uint2 x, uint32_t* dst
 template <bool PAGED>
 __global__ void __launch_bounds__(kSmallWarps * 32) quantize_small_kernel(const QuantParams p) {
   asm volatile("griddepcontrol.launch_dependents;\n");
-  extern __shared__ __align__(16) uint8_t smem[];
-  const int lut_k_n = p.k_lut_a ? lut_size(p.k_lut_a) : 0;
-  const int lut_v_n = p.v_lut_a ? lut_size(p.v_lut_a) : 0;
-  LutEntry* lut_k = reinterpret_cast<LutEntry*>(smem);
-  LutEntry* lut_v = lut_k + lut_k_n;
-  for (int j = threadIdx.x; j < lut_k_n + lut_v_n; j += blockDim.x)
-    lut_k[j] = j < lut_k_n ? lut_entry(p.k_thr, (1 << p.k_bits) - 1, p.k_lut_a, j)
-                           : lut_entry(p.v_thr, (1 << p.v_bits) - 1, p.v_lut_a, j - lut_k_n);
+  __shared__ float thr_s[2][16];  // K and V thresholds
+  if (threadIdx.x < 32) thr_s[threadIdx.x >> 4][threadIdx.x & 15] = (threadIdx.x & 15) < 15
+      ? (threadIdx.x < 16 ? p.k_thr[threadIdx.x & 15] : p.v_thr[threadIdx.x & 15]) : INFINITY;
   __syncthreads();
   asm volatile("griddepcontrol.wait;\n" ::: "memory");  // the inputs and the ring may come from the previous grid
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const LutEntry* my_lut_k = lut_k;
-  const LutEntry* my_lut_v = lut_v;
   const long long per_tensor = static_cast<long long>(p.batch) * p.heads * p.n_new;
   for (long long vi = static_cast<long long>(blockIdx.x) * kSmallWarps + warp; vi < 2 * per_tensor;
        vi += static_cast<long long>(gridDim.x) * kSmallWarps) {
@@ -479,6 +476,9 @@ __global__ void __launch_bounds__(kSmallWarps * 32) quantize_small_kernel(const 
     const int t = static_cast<int>(r % p.n_new);
     const int bh = static_cast<int>(r / p.n_new);
     const int b = bh / p.heads, h = bh - b * p.heads;
+    // the input row does not depend on the start position: its load overlaps that one
+    const uint16_t* src = (tensor ? p.v_src : p.k_src) + b * p.stride_b + h * p.stride_h + t * p.stride_t;
+    const uint2 x = reinterpret_cast<const uint2*>(src)[lane];
     const int s = p.start_pos[b];
     const int cnt = p.num_new != nullptr ? p.num_new[b] : p.n_new;
     if (!(s >= 0 && cnt >= 0 && cnt <= p.n_new && static_cast<long long>(s) + cnt <= p.cap)) {
@@ -488,8 +488,6 @@ __global__ void __launch_bounds__(kSmallWarps * 32) quantize_small_kernel(const 
     }
     if (t >= cnt) continue;
     const int pos = s + t;
-    const uint16_t* src = (tensor ? p.v_src : p.k_src) + b * p.stride_b + h * p.stride_h + t * p.stride_t;
-    const uint2 x = reinterpret_cast<const uint2*>(src)[lane];
     if (tensor == 0 && p.k_mode == TQ_K_FP16) {  // asym K: stored verbatim
       const long long ridx = PAGED ? p.map.row(b, h, pos) : (static_cast<long long>(b) * p.heads + h) * p.cap + pos;
       if (ridx < 0) {
@@ -519,16 +517,15 @@ __global__ void __launch_bounds__(kSmallWarps * 32) quantize_small_kernel(const 
       const long long ridx = PAGED ? p.map.row(b, h, qpos) : (static_cast<long long>(b) * p.heads + h) * p.cap + qpos;
       if (ridx < 0 && lane == 0 && p.status != nullptr) atomicOr(p.status, TQ_DEV_ERR_BLOCK);
       const int bits = tensor ? p.v_bits : p.k_bits;
-      const LutEntry* lut = tensor ? my_lut_v : my_lut_k;
-      const int lut_a = tensor ? p.v_lut_a : p.k_lut_a;
+      const float* thr = thr_s[tensor];
       uint32_t* dw = (tensor ? p.v_words : p.k_words) + (ridx < 0 ? 0 : ridx) * (bits * 4);
       float* dn = (tensor ? p.v_norms : p.k_norms) + (ridx < 0 ? 0 : ridx);
       const bool store = ridx >= 0;
       switch (bits) {
         case 8: quantize_vector_warp_int8(qx, dw, dn, store, lane); break;
-        case 2: quantize_vector_warp<2>(qrow, qx, sm, lut, lut_a, dw, dn, store, lane); break;
-        case 3: quantize_vector_warp<3>(qrow, qx, sm, lut, lut_a, dw, dn, store, lane); break;
-        default: quantize_vector_warp<4>(qrow, qx, sm, lut, lut_a, dw, dn, store, lane); break;
+        case 2: quantize_vector_warp<2>(qrow, qx, sm, thr, dw, dn, store, lane); break;
+        case 3: quantize_vector_warp<3>(qrow, qx, sm, thr, dw, dn, store, lane); break;
+        default: quantize_vector_warp<4>(qrow, qx, sm, thr, dw, dn, store, lane); break;
       }
     }
     if (ring != nullptr) {  // the slot's old row has been read (and quantized)
@@ -539,12 +536,8 @@ __global__ void __launch_bounds__(kSmallWarps * 32) quantize_small_kernel(const 
 }
 
 tq_status launch_small(const QuantParams& p, cudaStream_t stream) {
-  const size_t smem = (static_cast<size_t>(p.k_lut_a ? lut_size(p.k_lut_a) : 0) + (p.v_lut_a ? lut_size(p.v_lut_a) : 0)) *
-                      sizeof(LutEntry);
   const bool paged = p.map.table != nullptr;
   auto kern = paged ? quantize_small_kernel<true> : quantize_small_kernel<false>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
-    return TQ_ERR_CUDA;
   const int sms = sm_count_q();
   if (sms <= 0) return TQ_ERR_CUDA;
   const long long vectors = 2ll * p.batch * p.heads * p.n_new;
@@ -553,7 +546,7 @@ tq_status launch_small(const QuantParams& p, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kSmallWarps * 32);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see griddepcontrol.wait
