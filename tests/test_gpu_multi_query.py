@@ -139,3 +139,22 @@ def test_multi_query_paged_equals_contiguous_and_limits():
     with pytest.raises(N.TQError) as e:
         flat.multi_query(big, sl, cap)
     assert e.value.status == N.TQ_ERR_UNSUPPORTED
+
+
+def test_multi_query_at_the_work_list_limit():
+    """B x n_query = 512 work-list sequences (the limit), short ragged contexts."""
+    B, HQ, HK, CAP, NQ = 64, 8, 2, 96, 8
+    lens = np.random.default_rng(62).integers(0, CAP + 1, size=B).astype(np.int32)
+    k = synth.kv_fp16(62, 1, B, HK, CAP, D)
+    v = synth.kv_fp16(62, 2, B, HK, CAP, D)
+    tc = _cache(batch=B, num_kv_heads=HK, num_q_heads=HQ, capacity=CAP, bits="int8")
+    tc.append(_dev(k), _dev(v), _dev(np.zeros(B, np.int32)), _dev(lens))
+    oc = oracle.build_cache(k, v, lens, CAP, 8, 8, codec="int8")
+    q = _queries(62, B, NQ, HQ)
+    got = tc.multi_query(_dev(q), _dev(lens), CAP).cpu().numpy()
+    ref = oracle.multi_query_attention(oc, q, lens)
+    for b in range(B):
+        first = max(0, NQ - int(lens[b]))
+        assert np.all(got[b, :first] == 0)
+        if first < NQ:
+            assert_attention_close(got[b, first:], ref[b, first:], "limit b=%d" % b)

@@ -444,3 +444,29 @@ def test_small_and_bulk_appends_store_the_same_words(bits):
     for name in ("k_cache", "k_norms", "v_cache", "v_norms"):
         np.testing.assert_array_equal(getattr(small, name).cpu().numpy(), getattr(bulk, name).cpu().numpy(),
                                       err_msg=name)
+
+
+def test_largest_batch_of_ragged_sequences():
+    """The largest batch one decode call takes (512 sequences: the per-sequence tile
+    prefix is held in shared memory), lengths 0..200 including empty sequences,
+    G = 4, K4/V4 with a 16-token hot window."""
+    B, HK, HQ, CAP, W = 512, 1, 4, 200, 16
+    rng = np.random.default_rng(61)
+    lens = rng.integers(0, CAP + 1, size=B).astype(np.int32)
+    lens[:3] = [0, 1, CAP]
+    k = synth.kv_fp16(61, 1, B, HK, CAP, D)
+    v = synth.kv_fp16(61, 2, B, HK, CAP, D)
+    q = synth.queries_fp16(61, B, HQ, D)
+    oc = oracle.build_cache(k, v, lens, CAP, 4, 4, hot_window=W)
+    tc = _cache(batch=B, num_kv_heads=HK, num_q_heads=HQ, capacity=CAP, bits=(4, 4), hot_window=W)
+    upload(tc, oc)
+    got, ref = decode_both(tc, oc, q, lens, CAP)
+    empty = lens == 0
+    assert np.all(got[empty] == 0)
+    assert_attention_close(got[~empty], ref[~empty], "512 ragged sequences")
+    assert tc.device_status() == 0
+    # one sequence more is refused before any launch
+    big = _cache(batch=B + 1, num_kv_heads=HK, num_q_heads=HQ, capacity=16, bits=(4, 4))
+    with pytest.raises(N.TQError) as e:
+        big.decode(_dev(np.zeros((B + 1, HQ, D), np.float16)), _dev(np.zeros(B + 1, np.int32)), 16)
+    assert e.value.status == N.TQ_ERR_UNSUPPORTED
