@@ -949,22 +949,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
             acc[jj][2] = fma2(w2[jj], c2, acc[jj][2]);
             acc[jj][3] = fma2(w2[jj], c3, acc[jj][3]);
           }
-          return;
-        }
-        uint32_t win;
-        if constexpr (VB == 4) win = lds32<U * 2 * kVRec>(vw);
-        else if constexpr (VB == 2) win = lds32<U * 2 * kVRec>(vw) >> v_sh;
-        else win = __funnelshift_r(lds32<U * 2 * kVRec>(vw), lds32<U * 2 * kVRec + 4>(vw), v_sh);
-        const float2 c0 = lds64(pair_addr<VB, 0, kRS>(win, vbase));
-        const float2 c1 = lds64(pair_addr<VB, 1, kRS>(win, vbase));
-        const float2 c2 = lds64(pair_addr<VB, 2, kRS>(win, vbase));
-        const float2 c3 = lds64(pair_addr<VB, 3, kRS>(win, vbase));
+        } else {  // packed codes: one pair-table lookup per two coordinates
+          uint32_t win;
+          if constexpr (VB == 4) win = lds32<U * 2 * kVRec>(vw);
+          else if constexpr (VB == 2) win = lds32<U * 2 * kVRec>(vw) >> v_sh;
+          else win = __funnelshift_r(lds32<U * 2 * kVRec>(vw), lds32<U * 2 * kVRec + 4>(vw), v_sh);
+          const float2 c0 = lds64(pair_addr<VB, 0, kRS>(win, vbase));
+          const float2 c1 = lds64(pair_addr<VB, 1, kRS>(win, vbase));
+          const float2 c2 = lds64(pair_addr<VB, 2, kRS>(win, vbase));
+          const float2 c3 = lds64(pair_addr<VB, 3, kRS>(win, vbase));
 #pragma unroll
-        for (int jj = 0; jj < G; ++jj) {
-          acc[jj][0] = fma2(w2[jj], c0, acc[jj][0]);
-          acc[jj][1] = fma2(w2[jj], c1, acc[jj][1]);
-          acc[jj][2] = fma2(w2[jj], c2, acc[jj][2]);
-          acc[jj][3] = fma2(w2[jj], c3, acc[jj][3]);
+          for (int jj = 0; jj < G; ++jj) {
+            acc[jj][0] = fma2(w2[jj], c0, acc[jj][0]);
+            acc[jj][1] = fma2(w2[jj], c1, acc[jj][1]);
+            acc[jj][2] = fma2(w2[jj], c2, acc[jj][2]);
+            acc[jj][3] = fma2(w2[jj], c3, acc[jj][3]);
+          }
         }
       };
       auto v_hot = [&](auto U_) {
