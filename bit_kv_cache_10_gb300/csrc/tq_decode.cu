@@ -69,35 +69,55 @@ __global__ void __launch_bounds__(4 * 32) decode_merge_kernel(const DecodeParams
   // the partials are written by the split kernel: wait for it (programmatic
   // dependent launch lets this grid start while the split kernel finishes)
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
-  // (max, mass) of the partials, one per lane, then across the warp
-  float mm = -INFINITY;
-  for (int i = lane; i < n; i += 32)
-    if (is_live(i)) mm = fmaxf(mm, p.ws_ml[(slot_of(i) * g + jj) * 2]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
-  float l = 0.0f;
-  for (int i = lane; i < n; i += 32) {
-    if (!is_live(i)) continue;
-    const float ms = p.ws_ml[(slot_of(i) * g + jj) * 2];
-    if (ms != -INFINITY) l = ffma(p.ws_ml[(slot_of(i) * g + jj) * 2 + 1], exp2f(ms - mm), l);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) l = fadd(l, __shfl_xor_sync(0xffffffffu, l, o));
-  // accumulators, partial by partial (independent loads)
+  float mm = -INFINITY, l = 0.0f;
   float y[4] = {0.0f, 0.0f, 0.0f, 0.0f}, hv[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll 4
-  for (int i = 0; i < n; ++i) {
-    if (!is_live(i)) continue;
-    const long long slot = slot_of(i);
-    const float ms = p.ws_ml[(slot * g + jj) * 2];
-    if (ms == -INFINITY) continue;
-    const float sc = exp2f(ms - mm);
-    const float4 a = reinterpret_cast<const float4*>(p.ws_acc + (slot * g + jj) * D)[lane];
+  auto add_partial = [&](int i, float sc, const float4 a) {
     const float av[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       if (i >= n0) hv[k] = ffma(av[k], sc, hv[k]);
       else y[k] = ffma(av[k], sc, y[k]);
+    }
+  };
+  if (n <= 32) {
+    // one partial per lane: its (max, mass) read once, its scale shared by shuffles;
+    // the accumulator loads do not wait on the scales (a partial that was not
+    // written has scale 0 and its loaded values are not used)
+    float2 ml = make_float2(-INFINITY, 0.0f);
+    if (lane < n && ((live32 >> lane) & 1u))
+      ml = reinterpret_cast<const float2*>(p.ws_ml)[slot_of(lane) * g + jj];
+    mm = ml.x;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
+    const float sc_l = ml.x == -INFINITY ? 0.0f : exp2f(ml.x - mm);
+    l = fmul(ml.y, sc_l);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) l = fadd(l, __shfl_xor_sync(0xffffffffu, l, o));
+#pragma unroll 4
+    for (int i = 0; i < n; ++i) {
+      const float4 a = reinterpret_cast<const float4*>(p.ws_acc + (slot_of(i) * g + jj) * D)[lane];
+      const float sc = __shfl_sync(0xffffffffu, sc_l, i);
+      if (sc != 0.0f) add_partial(i, sc, a);
+    }
+  } else {
+    // (max, mass) of the partials, several per lane, then across the warp
+    for (int i = lane; i < n; i += 32)
+      if (is_live(i)) mm = fmaxf(mm, p.ws_ml[(slot_of(i) * g + jj) * 2]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
+    for (int i = lane; i < n; i += 32) {
+      if (!is_live(i)) continue;
+      const float ms = p.ws_ml[(slot_of(i) * g + jj) * 2];
+      if (ms != -INFINITY) l = ffma(p.ws_ml[(slot_of(i) * g + jj) * 2 + 1], exp2f(ms - mm), l);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) l = fadd(l, __shfl_xor_sync(0xffffffffu, l, o));
+    for (int i = 0; i < n; ++i) {  // accumulators, partial by partial
+      if (!is_live(i)) continue;
+      const long long slot = slot_of(i);
+      const float ms = p.ws_ml[(slot * g + jj) * 2];
+      if (ms == -INFINITY) continue;
+      add_partial(i, exp2f(ms - mm), reinterpret_cast<const float4*>(p.ws_acc + (slot * g + jj) * D)[lane]);
     }
   }
   // inverse rotation of the cold sum: D_h H y / sqrt(d), index t = 4 lane + i (the
