@@ -218,7 +218,12 @@ struct Cfg {
   static constexpr int kKBits = kFp16K ? 2 : KB;       // placeholder width when K is fp16
   static constexpr int kKRow = kFp16K ? 256 : KB * 16;  // bytes of one K token
   static constexpr int kVRow = VB * 16;
-  static constexpr int kKTile = kTile * kKRow;
+  // fp16 and int8 K: scores on the tensor cores (their values are exact in fp16);
+  // the staged K rows are padded so that the MMA operand loads of 4 tokens by 4
+  // lanes each fall in distinct banks (288 = 256 + 32, 144 = 128 + 16 bytes)
+  static constexpr bool kMmaK = kFp16K || kInt8;
+  static constexpr int kKPitch = kFp16K ? kKRow + 32 : kInt8 ? kKRow + 16 : kKRow;
+  static constexpr int kKTile = kTile * kKPitch;
   static constexpr int kKNorm = kFp16K ? 0 : kTile * 4;
   static constexpr int kVTile = kTile * kVRow;
   static constexpr int kBuf = kKTile + kKNorm + kVTile + kTile * 4;  // K | K norms | V | V norms
@@ -319,6 +324,26 @@ __device__ __forceinline__ float2 lds64(uint32_t addr) {
   float2 v;
   asm("ld.shared.v2.f32 {%0, %1}, [%2];\n" : "=f"(v.x), "=f"(v.y) : "r"(addr));
   return v;
+}
+
+// D += A B on the tensor cores, m16n8k16, f16 operands, f32 accumulators.  Only
+// A rows 0..7 are used (the query heads): their fragment registers a1 and a3
+// (rows 8..15) are zero.
+__device__ __forceinline__ void mma_16816(float& d0, float& d1, float& d2, float& d3, uint32_t a0, uint32_t a2,
+                                          uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};\n"
+      : "+f"(d0), "+f"(d1), "+f"(d2), "+f"(d3)
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+// Two int8 codes (bytes K and K + 1 of a biased word xw = w ^ 0x80808080) as an
+// exact f16 pair: the byte u = code + 128 becomes the mantissa of 1024 + u, and
+// one packed subtraction of 1152 leaves the code.
+template <int K>
+__device__ __forceinline__ uint32_t int8_half2(uint32_t xw) {
+  const uint32_t h = __byte_perm(xw, 0x64646464u, 0x4040 | (K + 1) << 8 | K);
+  const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&h), __floats2half2_rn(1152.0f, 1152.0f));
+  return *reinterpret_cast<const uint32_t*>(&r);
 }
 
 // Two int8 codes (bytes K and K + 1 of a word) as exact floats: the biased
@@ -446,6 +471,41 @@ __device__ __forceinline__ void copy_full(uint32_t dst, const uint8_t* src, int 
     if (lane < kRest) cp_async16_at<kRounds * 512>(d, sp);
 }
 
+// 16-byte cp.async with distinct compile-time offsets at the shared and the
+// global side.
+template <int DOFF, int SOFF>
+__device__ __forceinline__ void cp_async16_at2(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0+%2], [%1+%3], 16;\n" ::"r"(dst), "l"(src), "n"(DOFF), "n"(SOFF));
+}
+// Copies a full K tile of 16 rows of ROW bytes from contiguous global rows into
+// shared rows of PITCH bytes: round r moves 512 bytes, rows 32 r / (ROW / 16) ..
+template <int ROW, int PITCH>
+__device__ __forceinline__ void copy_full_pitched(uint32_t dst, const uint8_t* src, int lane) {
+  if constexpr (ROW == PITCH) {
+    copy_full<kTile * ROW>(dst, src, lane);
+  } else {
+    constexpr int kRC = ROW / 16, kRounds = kTile * ROW / 512, kRowsPerRound = 32 / kRC;
+    static_assert(32 % kRC == 0 && kRounds <= 8, "pitched copy layout");
+    const uint32_t d = dst + static_cast<uint32_t>((lane / kRC) * PITCH + (lane % kRC) * 16);
+    const uint8_t* sp = src + 16 * lane;
+    constexpr int kD = kRowsPerRound * PITCH;
+    if constexpr (kRounds > 0) cp_async16_at2<0 * kD, 0>(d, sp);
+    if constexpr (kRounds > 1) cp_async16_at2<1 * kD, 512>(d, sp);
+    if constexpr (kRounds > 2) cp_async16_at2<2 * kD, 1024>(d, sp);
+    if constexpr (kRounds > 3) cp_async16_at2<3 * kD, 1536>(d, sp);
+    if constexpr (kRounds > 4) cp_async16_at2<4 * kD, 2048>(d, sp);
+    if constexpr (kRounds > 5) cp_async16_at2<5 * kD, 2560>(d, sp);
+    if constexpr (kRounds > 6) cp_async16_at2<6 * kD, 3072>(d, sp);
+    if constexpr (kRounds > 7) cp_async16_at2<7 * kD, 3584>(d, sp);
+  }
+}
+// Shared offset of 16-byte chunk c of a K tile (chunks numbered row-major over
+// the contiguous global rows).
+template <int ROW, int PITCH>
+__device__ __forceinline__ uint32_t k_chunk_dst(int c) {
+  return static_cast<uint32_t>((c / (ROW / 16)) * PITCH + (c % (ROW / 16)) * 16);
+}
+
 // Block-table entries of the first and the last token of a tile.  The kernel
 // loads them one issue ahead, so that their latency hides behind the
 // consumption of a tile instead of stalling the copies that depend on them.
@@ -481,7 +541,7 @@ __device__ __forceinline__ int stage_tile_paged(const DecodeParams& p, int h, bo
   const uint32_t vbuf = buf + C::kKTile + C::kKNorm;
   long long rn = row0 + (lane & 15);  // norm row of the lane's token
   if (in_pool && one_block && n_valid == kTile) {
-    copy_full<C::kKTile>(buf, kbase + row0 * C::kKRow, lane);
+    copy_full_pitched<C::kKRow, C::kKPitch>(buf, kbase + row0 * C::kKRow, lane);
     if (!hot) copy_full<C::kVTile>(vbuf, reinterpret_cast<const uint8_t*>(p.v_words) + row0 * (VB * 16), lane);
   } else {
     if (!in_pool) {  // outside the pool: nothing is staged, the tile is read as empty
@@ -493,7 +553,7 @@ __device__ __forceinline__ int stage_tile_paged(const DecodeParams& p, int h, bo
     for (int c = lane; c < n_valid * kPer; c += 32) {  // K token by token (a partial or a straddling tile)
       const int t = t_begin + c / kPer;
       const long long r = p.map.in_block((t >> sh) == blk0 ? tb.first : tb.last, h, t);
-      cp_async16s(buf + 16u * c, kbase + r * C::kKRow + (c % kPer) * 16);
+      cp_async16s(buf + k_chunk_dst<C::kKRow, C::kKPitch>(c), kbase + r * C::kKRow + (c % kPer) * 16);
     }
     if (!hot) {  // cold tiles never straddle
       const uint8_t* vsrc = reinterpret_cast<const uint8_t*>(p.v_words) + row0 * (VB * 16);
@@ -524,10 +584,11 @@ __device__ __forceinline__ int stage_tile(const DecodeParams& p, int b, int h, b
   const uint8_t* vsrc = reinterpret_cast<const uint8_t*>(p.v_words + row0 * (VB * 4));
   const uint32_t vbuf = buf + C::kKTile + C::kKNorm;
   if (n_valid == kTile) {
-    copy_full<C::kKTile>(buf, ksrc, lane);
+    copy_full_pitched<C::kKRow, C::kKPitch>(buf, ksrc, lane);
     if (!hot) copy_full<C::kVTile>(vbuf, vsrc, lane);
   } else {
-    for (int c = lane; c < n_valid * (C::kKRow / 16); c += 32) cp_async16s(buf + 16u * c, ksrc + 16 * c);
+    for (int c = lane; c < n_valid * (C::kKRow / 16); c += 32)
+      cp_async16s(buf + k_chunk_dst<C::kKRow, C::kKPitch>(c), ksrc + 16 * c);
     if (!hot)
       for (int c = lane; c < n_valid * (C::kVRow / 16); c += 32) cp_async16s(vbuf + 16u * c, vsrc + 16 * c);
   }
@@ -668,14 +729,30 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
   const bool owner = G >= 2 || (rr & 1) == 0;  // for G = 1 lanes rr and rr ^ 1 hold the same score
   constexpr bool sparse = SPARSE;
   float2 qr[G][8];
+  uint32_t qa[8][2];  // MMA variants: the A fragments (fp16 query) of the 8 coordinate chunks
+  const int gq = lane >> 2, tq = lane & 3;  // MMA: group (query head, token) and thread in the group
   int cur_b = -1, cur_h = -1;
   long long seg = t0;
   while (seg < t1) {
     const TileInfo si = tile_info<MQ>(p, prefix, seg);
     const long long seg_end = si.row_end < t1 ? si.row_end : t1;
-    if (si.b != cur_b || si.h != cur_h) {
-      // rotated query of the G heads: (log2 e / d) H D q for packed K, (log2 e / sqrt d) q for fp16
-      // K and in the int8 mode (no rotation)
+    if (C::kMmaK && (si.b != cur_b || si.h != cur_h)) {
+      // fp16 or int8 K: the raw fp16 query of head gq (exact) as MMA A fragments; chunk c
+      // holds coordinates 16 c + 4 tq .. + 3, the order the B fragments read K in
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint2 v = make_uint2(0u, 0u);
+        if (gq < G)
+          v = *reinterpret_cast<const uint2*>(p.q + (static_cast<int64_t>(si.b) * p.hq + si.h * G + gq) * D +
+                                              16 * c + 4 * tq);
+        qa[c][0] = v.x;
+        qa[c][1] = v.y;
+      }
+      cur_b = si.b;
+      cur_h = si.h;
+    }
+    if (!C::kMmaK && (si.b != cur_b || si.h != cur_h)) {
+      // rotated query of the G heads: (log2 e / d) H D q for packed K
       constexpr bool kRotQ = !C::kFp16K && !C::kInt8;
       __syncthreads();
       if (tid < D) {
@@ -737,178 +814,259 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
       const uint8_t* tb = wring + (j % S) * C::kBuf;
       const uint32_t tbs = ring + static_cast<uint32_t>((j % S) * C::kBuf);  // shared address of the tile
 
-      // ---- K phase: partial scores over the lane's 16 coordinates, 4 tokens per step
-      float Ak[G], As[G];  // after butterfly stage A: the kept step pair and the sent one
-      {
-        auto k_step = [&](uint32_t kw, float* P) {
-          constexpr int OFF = 0;
-          float2 c[8];
-          if constexpr (C::kFp16K) {
-            const uint4 a = lds128<OFF>(kw), b = lds128<OFF + 128>(kw);
-            c[0] = half2_bits_to_float2(a.x);
-            c[1] = half2_bits_to_float2(a.y);
-            c[2] = half2_bits_to_float2(a.z);
-            c[3] = half2_bits_to_float2(a.w);
-            c[4] = half2_bits_to_float2(b.x);
-            c[5] = half2_bits_to_float2(b.y);
-            c[6] = half2_bits_to_float2(b.z);
-            c[7] = half2_bits_to_float2(b.w);
-          } else if constexpr (C::kInt8) {
-            const uint4 a = lds128<OFF>(kw);
-            const uint32_t x0 = a.x ^ 0x80808080u, x1 = a.y ^ 0x80808080u;
-            const uint32_t x2 = a.z ^ 0x80808080u, x3 = a.w ^ 0x80808080u;
-            c[0] = int8_pair<0>(x0);
-            c[1] = int8_pair<2>(x0);
-            c[2] = int8_pair<0>(x1);
-            c[3] = int8_pair<2>(x1);
-            c[4] = int8_pair<0>(x2);
-            c[5] = int8_pair<2>(x2);
-            c[6] = int8_pair<0>(x3);
-            c[7] = int8_pair<2>(x3);
-          } else if constexpr (KB == 4) {
-            const uint2 wv = lds64u<OFF>(kw);
-            c[0] = lds64(pair_addr<4, 0, kRS>(wv.x, kbase));
-            c[1] = lds64(pair_addr<4, 1, kRS>(wv.x, kbase));
-            c[2] = lds64(pair_addr<4, 2, kRS>(wv.x, kbase));
-            c[3] = lds64(pair_addr<4, 3, kRS>(wv.x, kbase));
-            c[4] = lds64(pair_addr<4, 0, kRS>(wv.y, kbase));
-            c[5] = lds64(pair_addr<4, 1, kRS>(wv.y, kbase));
-            c[6] = lds64(pair_addr<4, 2, kRS>(wv.y, kbase));
-            c[7] = lds64(pair_addr<4, 3, kRS>(wv.y, kbase));
-          } else if constexpr (KB == 3) {
-            const uint32_t wa = __funnelshift_r(lds32<OFF>(kw), lds32<OFF + 4>(kw), k_sh);
-            const uint32_t wb = __funnelshift_r(lds32<OFF + 24>(kw), lds32<OFF + 28>(kw), k_sh);
-            c[0] = lds64(pair_addr<3, 0, kRS>(wa, kbase));
-            c[1] = lds64(pair_addr<3, 1, kRS>(wa, kbase));
-            c[2] = lds64(pair_addr<3, 2, kRS>(wa, kbase));
-            c[3] = lds64(pair_addr<3, 3, kRS>(wa, kbase));
-            c[4] = lds64(pair_addr<3, 0, kRS>(wb, kbase));
-            c[5] = lds64(pair_addr<3, 1, kRS>(wb, kbase));
-            c[6] = lds64(pair_addr<3, 2, kRS>(wb, kbase));
-            c[7] = lds64(pair_addr<3, 3, kRS>(wb, kbase));
-          } else {
-            const uint32_t wv = lds32<OFF>(kw);
-            c[0] = lds64(pair_addr<2, 0, kRS>(wv, kbase));
-            c[1] = lds64(pair_addr<2, 1, kRS>(wv, kbase));
-            c[2] = lds64(pair_addr<2, 2, kRS>(wv, kbase));
-            c[3] = lds64(pair_addr<2, 3, kRS>(wv, kbase));
-            c[4] = lds64(pair_addr<2, 4, kRS>(wv, kbase));
-            c[5] = lds64(pair_addr<2, 5, kRS>(wv, kbase));
-            c[6] = lds64(pair_addr<2, 6, kRS>(wv, kbase));
-            c[7] = lds64(pair_addr<2, 7, kRS>(wv, kbase));
+      uint32_t stepmask = 0xFFu;  // V steps (2 tokens each) that carry a nonzero weight, warp-uniform
+      if constexpr (C::kMmaK) {
+        // ---- scores on the tensor cores: S = Q K^T, Q the G fp16 query heads (A rows,
+        // zero above G), K the tile's 16 tokens (B columns, two blocks of 8); the
+        // operands are exact in fp16 (fp16 K, or int8 codes) and the products are
+        // summed in float32.  Lane (gq, tq) then holds head gq's raw scores of tokens
+        // 2 tq, 2 tq + 1, 8 + 2 tq, 9 + 2 tq.
+        float sraw[4];
+        const uint32_t kb = tbs + static_cast<uint32_t>(gq * C::kKPitch + (C::kFp16K ? 8 : 4) * tq);
+#pragma unroll
+        for (int nb = 0; nb < 2; ++nb) {
+          float d0 = 0.0f, d1 = 0.0f, d2 = 0.0f, d3 = 0.0f;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint32_t b0, b1;
+            if constexpr (C::kFp16K) {
+              const uint2 w = lds64u<0>(kb + static_cast<uint32_t>(nb * 8 * C::kKPitch + 32 * c));
+              b0 = w.x;
+              b1 = w.y;
+            } else {
+              const uint32_t w = lds32<0>(kb + static_cast<uint32_t>(nb * 8 * C::kKPitch + 16 * c)) ^ 0x80808080u;
+              b0 = int8_half2<0>(w);
+              b1 = int8_half2<2>(w);
+            }
+            mma_16816(d0, d1, d2, d3, qa[c][0], qa[c][1], b0, b1);
           }
-          // heads interleaved: consecutive packed FMAs are independent
-          float2 pa[G];
+          sraw[2 * nb] = d0;
+          sraw[2 * nb + 1] = d1;
+        }
+        // ---- online softmax in that layout (base 2, lazily raised maximum)
+        const bool head_ok = gq < G;
+        const float* kscale = reinterpret_cast<const float*>(tb + C::kKTile);  // int8: the K scales
+        const float* vnorm = reinterpret_cast<const float*>(tb + C::kKTile + C::kKNorm + C::kVTile);
+        const int tk[4] = {2 * tq, 2 * tq + 1, 8 + 2 * tq, 9 + 2 * tq};
+        constexpr float kQs = kLog2e / kSqrtD;
+        float sj[4];
+        bool bump = false;
 #pragma unroll
-          for (int jj = 0; jj < G; ++jj) pa[jj] = mul2(qr[jj][0], c[0]);
+        for (int i = 0; i < 4; ++i) {
+          float s = sraw[i];
+          if constexpr (C::kInt8) s = fmul(s, kscale[tk[i]]);
+          s = fmul(s, kQs);
+          sj[i] = head_ok && tk[i] < n_valid ? s : -INFINITY;  // staged data of masked rows is stale
+          bump |= sj[i] > fadd(m_own[0], kLazy);
+        }
+        if (__any_sync(0xffffffffu, bump)) {
+          float tm = fmaxf(fmaxf(sj[0], sj[1]), fmaxf(sj[2], sj[3]));
+          tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 1));
+          tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 2));
+          const float mn = fmaxf(m_own[0], tm);
+          const float al = mn == -INFINITY ? 1.0f : ex2_approx(fsub(m_own[0], mn));  // 0 for the row's first tile
+          lsum[0] = fmul(lsum[0], al);
+          m_own[0] = mn;
 #pragma unroll
-          for (int pr = 1; pr < 8; ++pr)
+          for (int jj = 0; jj < G; ++jj) {
+            const float aj = __shfl_sync(0xffffffffu, al, 4 * jj);
 #pragma unroll
-            for (int jj = 0; jj < G; ++jj) pa[jj] = fma2(qr[jj][pr], c[pr], pa[jj]);
+            for (int k = 0; k < 4; ++k) acc[jj][k] = mul2(acc[jj][k], make_float2(aj, aj));
+          }
+        }
+        float w4[4];
+        uint32_t bits = 0u;
 #pragma unroll
-          for (int jj = 0; jj < G; ++jj) P[jj] = fadd(pa[jj].x, pa[jj].y);
-        };
-        // stage A of the butterfly: the partner (rr ^ 4) sends what this lane keeps
-        auto stage_a = [&](const float* Pk, const float* Ps, float* A) {
+        for (int i = 0; i < 4; ++i) {
+          const bool live = sj[i] != -INFINITY;
+          float pj = ex2_approx(fsub(sj[i], m_own[0]));
+          pj = live ? pj : 0.0f;  // masked rows (also before any valid token)
+          lsum[0] = fadd(lsum[0], pj);
+          float w = fmul(pj, hot ? 1.0f : vnorm[tk[i]]);
+          w = live ? w : 0.0f;  // the staged norm of a masked row is stale (possibly not a number)
+          if (sparse && pj < p.sparse_tau) w = 0.0f;  // sparse V, as in the other layout
+          w4[i] = w;
+          bits |= (w != 0.0f ? 1u : 0u) << (tk[i] >> 1);
+        }
+        if (head_ok) {  // weights of token tk, head gq: row tk of 4 G bytes
+          float* wf = reinterpret_cast<float*>(wts);
 #pragma unroll
-          for (int jj = 0; jj < G; ++jj) A[jj] = fadd(Pk[jj], __shfl_xor_sync(0xffffffffu, Ps[jj], 4));
-        };
+          for (int i = 0; i < 4; ++i) wf[tk[i] * G + gq] = w4[i];
+        }
+        if (sparse) stepmask = __reduce_or_sync(0xffffffffu, head_ok ? bits : 0u);
+      } else {
+        // ---- K phase: partial scores over the lane's 16 coordinates, 4 tokens per step
+        float Ak[G], As[G];  // after butterfly stage A: the kept step pair and the sent one
         {
-          float Pk[G], Ps[G];
-          k_step(tbs + k_off_kk, Pk);
-          k_step(tbs + k_off_ks, Ps);
-          stage_a(Pk, Ps, Ak);
+          auto k_step = [&](uint32_t kw, float* P) {
+            constexpr int OFF = 0;
+            float2 c[8];
+            if constexpr (C::kFp16K) {
+              const uint4 a = lds128<OFF>(kw), b = lds128<OFF + 128>(kw);
+              c[0] = half2_bits_to_float2(a.x);
+              c[1] = half2_bits_to_float2(a.y);
+              c[2] = half2_bits_to_float2(a.z);
+              c[3] = half2_bits_to_float2(a.w);
+              c[4] = half2_bits_to_float2(b.x);
+              c[5] = half2_bits_to_float2(b.y);
+              c[6] = half2_bits_to_float2(b.z);
+              c[7] = half2_bits_to_float2(b.w);
+            } else if constexpr (C::kInt8) {
+              const uint4 a = lds128<OFF>(kw);
+              const uint32_t x0 = a.x ^ 0x80808080u, x1 = a.y ^ 0x80808080u;
+              const uint32_t x2 = a.z ^ 0x80808080u, x3 = a.w ^ 0x80808080u;
+              c[0] = int8_pair<0>(x0);
+              c[1] = int8_pair<2>(x0);
+              c[2] = int8_pair<0>(x1);
+              c[3] = int8_pair<2>(x1);
+              c[4] = int8_pair<0>(x2);
+              c[5] = int8_pair<2>(x2);
+              c[6] = int8_pair<0>(x3);
+              c[7] = int8_pair<2>(x3);
+            } else if constexpr (KB == 4) {
+              const uint2 wv = lds64u<OFF>(kw);
+              c[0] = lds64(pair_addr<4, 0, kRS>(wv.x, kbase));
+              c[1] = lds64(pair_addr<4, 1, kRS>(wv.x, kbase));
+              c[2] = lds64(pair_addr<4, 2, kRS>(wv.x, kbase));
+              c[3] = lds64(pair_addr<4, 3, kRS>(wv.x, kbase));
+              c[4] = lds64(pair_addr<4, 0, kRS>(wv.y, kbase));
+              c[5] = lds64(pair_addr<4, 1, kRS>(wv.y, kbase));
+              c[6] = lds64(pair_addr<4, 2, kRS>(wv.y, kbase));
+              c[7] = lds64(pair_addr<4, 3, kRS>(wv.y, kbase));
+            } else if constexpr (KB == 3) {
+              const uint32_t wa = __funnelshift_r(lds32<OFF>(kw), lds32<OFF + 4>(kw), k_sh);
+              const uint32_t wb = __funnelshift_r(lds32<OFF + 24>(kw), lds32<OFF + 28>(kw), k_sh);
+              c[0] = lds64(pair_addr<3, 0, kRS>(wa, kbase));
+              c[1] = lds64(pair_addr<3, 1, kRS>(wa, kbase));
+              c[2] = lds64(pair_addr<3, 2, kRS>(wa, kbase));
+              c[3] = lds64(pair_addr<3, 3, kRS>(wa, kbase));
+              c[4] = lds64(pair_addr<3, 0, kRS>(wb, kbase));
+              c[5] = lds64(pair_addr<3, 1, kRS>(wb, kbase));
+              c[6] = lds64(pair_addr<3, 2, kRS>(wb, kbase));
+              c[7] = lds64(pair_addr<3, 3, kRS>(wb, kbase));
+            } else {
+              const uint32_t wv = lds32<OFF>(kw);
+              c[0] = lds64(pair_addr<2, 0, kRS>(wv, kbase));
+              c[1] = lds64(pair_addr<2, 1, kRS>(wv, kbase));
+              c[2] = lds64(pair_addr<2, 2, kRS>(wv, kbase));
+              c[3] = lds64(pair_addr<2, 3, kRS>(wv, kbase));
+              c[4] = lds64(pair_addr<2, 4, kRS>(wv, kbase));
+              c[5] = lds64(pair_addr<2, 5, kRS>(wv, kbase));
+              c[6] = lds64(pair_addr<2, 6, kRS>(wv, kbase));
+              c[7] = lds64(pair_addr<2, 7, kRS>(wv, kbase));
+            }
+            // heads interleaved: consecutive packed FMAs are independent
+            float2 pa[G];
+#pragma unroll
+            for (int jj = 0; jj < G; ++jj) pa[jj] = mul2(qr[jj][0], c[0]);
+#pragma unroll
+            for (int pr = 1; pr < 8; ++pr)
+#pragma unroll
+              for (int jj = 0; jj < G; ++jj) pa[jj] = fma2(qr[jj][pr], c[pr], pa[jj]);
+#pragma unroll
+            for (int jj = 0; jj < G; ++jj) P[jj] = fadd(pa[jj].x, pa[jj].y);
+          };
+          // stage A of the butterfly: the partner (rr ^ 4) sends what this lane keeps
+          auto stage_a = [&](const float* Pk, const float* Ps, float* A) {
+#pragma unroll
+            for (int jj = 0; jj < G; ++jj) A[jj] = fadd(Pk[jj], __shfl_xor_sync(0xffffffffu, Ps[jj], 4));
+          };
+          {
+            float Pk[G], Ps[G];
+            k_step(tbs + k_off_kk, Pk);
+            k_step(tbs + k_off_ks, Ps);
+            stage_a(Pk, Ps, Ak);
+          }
+          {
+            float Pk[G], Ps[G];
+            k_step(tbs + k_off_sk, Pk);
+            k_step(tbs + k_off_ss, Ps);
+            stage_a(Pk, Ps, As);
+          }
         }
+        // ---- stages B (rr ^ 2, step pairs) and C (rr ^ 1, head pairs) of the butterfly
+        float sc[GH];
         {
-          float Pk[G], Ps[G];
-          k_step(tbs + k_off_sk, Pk);
-          k_step(tbs + k_off_ss, Ps);
-          stage_a(Pk, Ps, As);
+          float B[G];
+#pragma unroll
+          for (int jj = 0; jj < G; ++jj) B[jj] = fadd(Ak[jj], __shfl_xor_sync(0xffffffffu, As[jj], 2));
+          if constexpr (G >= 2) {
+#pragma unroll
+            for (int i = 0; i < GH; ++i) sc[i] = fadd(B[i], __shfl_xor_sync(0xffffffffu, B[GH + i], 1));
+          } else {
+            sc[0] = fadd(B[0], __shfl_xor_sync(0xffffffffu, B[0], 1));
+          }
         }
-      }
-      // ---- stages B (rr ^ 2, step pairs) and C (rr ^ 1, head pairs) of the butterfly
-      float sc[GH];
-      {
-        float B[G];
-#pragma unroll
-        for (int jj = 0; jj < G; ++jj) B[jj] = fadd(Ak[jj], __shfl_xor_sync(0xffffffffu, As[jj], 2));
-        if constexpr (G >= 2) {
-#pragma unroll
-          for (int i = 0; i < GH; ++i) sc[i] = fadd(B[i], __shfl_xor_sync(0xffffffffu, B[GH + i], 1));
-        } else {
-          sc[0] = fadd(B[0], __shfl_xor_sync(0xffffffffu, B[0], 1));
-        }
-      }
-      // ---- online softmax over the tile (base 2; log2 e is folded into q').  The
-      // running maximum of a head is raised only when a score exceeds it by more
-      // than kLazy, so most tiles need neither the cross-lane maximum nor a rescale
-      // (weights stay below 2^kLazy).
-      const float nk = C::kFp16K ? 1.0f : reinterpret_cast<const float*>(tb + C::kKTile)[tau_own];
-      const float nv = hot ? 1.0f : reinterpret_cast<const float*>(tb + C::kKTile + C::kKNorm + C::kVTile)[tau_own];
-      const bool full = n_valid == kTile;  // warp-uniform
-      const bool valid = tau_own < n_valid;
-      float sj[GH];
-      bool bump = false;
-#pragma unroll
-      for (int i = 0; i < GH; ++i) {
-        sj[i] = fmul(sc[i], nk);
-        if (!full) sj[i] = valid ? sj[i] : -INFINITY;  // staged data of masked rows is stale
-        bump |= sj[i] > fadd(m_own[i], kLazy);
-      }
-      if (__any_sync(0xffffffffu, bump)) {
-        float alpha[G];
+        // ---- online softmax over the tile (base 2; log2 e is folded into q').  The
+        // running maximum of a head is raised only when a score exceeds it by more
+        // than kLazy, so most tiles need neither the cross-lane maximum nor a rescale
+        // (weights stay below 2^kLazy).
+        const float nk = C::kFp16K ? 1.0f : reinterpret_cast<const float*>(tb + C::kKTile)[tau_own];
+        const float nv = hot ? 1.0f : reinterpret_cast<const float*>(tb + C::kKTile + C::kKNorm + C::kVTile)[tau_own];
+        const bool full = n_valid == kTile;  // warp-uniform
+        const bool valid = tau_own < n_valid;
+        float sj[GH];
+        bool bump = false;
 #pragma unroll
         for (int i = 0; i < GH; ++i) {
-          float tm = sj[i];
-          tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 2));
-          tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 4));
-          tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 8));
-          tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 16));
-          const float mn = fmaxf(m_own[i], tm);  // finite: every staged tile has a valid token
-          const float al = ex2_approx(fsub(m_own[i], mn));  // 0 for the first tile of the row
-          lsum[i] = fmul(lsum[i], al);
-          m_own[i] = mn;
-          if constexpr (G >= 2) {
-            const float oa = __shfl_xor_sync(0xffffffffu, al, 1);  // head (h0 + i) ^ GH
-            const bool hi = (rr & 1) != 0;
-            alpha[i] = hi ? oa : al;
-            alpha[GH + i] = hi ? al : oa;
-          } else {
-            alpha[0] = al;
-          }
+          sj[i] = fmul(sc[i], nk);
+          if (!full) sj[i] = valid ? sj[i] : -INFINITY;  // staged data of masked rows is stale
+          bump |= sj[i] > fadd(m_own[i], kLazy);
         }
+        if (__any_sync(0xffffffffu, bump)) {
+          float alpha[G];
 #pragma unroll
-        for (int jj = 0; jj < G; ++jj)
+          for (int i = 0; i < GH; ++i) {
+            float tm = sj[i];
+            tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 2));
+            tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 4));
+            tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 8));
+            tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 16));
+            const float mn = fmaxf(m_own[i], tm);  // finite: every staged tile has a valid token
+            const float al = ex2_approx(fsub(m_own[i], mn));  // 0 for the first tile of the row
+            lsum[i] = fmul(lsum[i], al);
+            m_own[i] = mn;
+            if constexpr (G >= 2) {
+              const float oa = __shfl_xor_sync(0xffffffffu, al, 1);  // head (h0 + i) ^ GH
+              const bool hi = (rr & 1) != 0;
+              alpha[i] = hi ? oa : al;
+              alpha[GH + i] = hi ? al : oa;
+            } else {
+              alpha[0] = al;
+            }
+          }
 #pragma unroll
-          for (int k = 0; k < 4; ++k) acc[jj][k] = mul2(acc[jj][k], make_float2(alpha[jj], alpha[jj]));
-      }
-      float w_own[GH];
+          for (int jj = 0; jj < G; ++jj)
 #pragma unroll
-      for (int i = 0; i < GH; ++i) {
-        float pj = ex2_approx(fsub(sj[i], m_own[i]));
-        if (!full) pj = valid ? pj : 0.0f;  // masked rows (also before any valid token: -inf - -inf)
-        lsum[i] = fadd(lsum[i], (G >= 2 || owner) ? pj : 0.0f);
-        w_own[i] = fmul(pj, nv);
-        if (!full) w_own[i] = valid ? w_own[i] : 0.0f;
-        // sparse V: a weight below tau relative to the (lazily raised) running
-        // maximum, hence below tau after normalization, contributes no V
-        if (sparse && pj < p.sparse_tau) w_own[i] = 0.0f;
-      }
-      // V steps (2 tokens each) that carry a nonzero weight, warp-uniform
-      uint32_t stepmask = 0xFFu;
-      if (sparse) {
-        bool keep = false;
+            for (int k = 0; k < 4; ++k) acc[jj][k] = mul2(acc[jj][k], make_float2(alpha[jj], alpha[jj]));
+        }
+        float w_own[GH];
 #pragma unroll
-        for (int i = 0; i < GH; ++i) keep |= w_own[i] != 0.0f;
-        stepmask = __reduce_or_sync(0xffffffffu, keep ? 1u << (tau_own >> 1) : 0u);
-      }
-      // weights of token tau_own, heads h0.. : row tau_own of 4 G bytes
-      if constexpr (G == 4) {
-        *reinterpret_cast<float2*>(wts + tau_own * 16 + h0 * 4) = make_float2(w_own[0], w_own[1]);
-      } else if constexpr (G == 2) {
-        *reinterpret_cast<float*>(wts + tau_own * 8 + h0 * 4) = w_own[0];
-      } else {
-        if (owner) *reinterpret_cast<float*>(wts + tau_own * 4) = w_own[0];
+        for (int i = 0; i < GH; ++i) {
+          float pj = ex2_approx(fsub(sj[i], m_own[i]));
+          if (!full) pj = valid ? pj : 0.0f;  // masked rows (also before any valid token: -inf - -inf)
+          lsum[i] = fadd(lsum[i], (G >= 2 || owner) ? pj : 0.0f);
+          w_own[i] = fmul(pj, nv);
+          if (!full) w_own[i] = valid ? w_own[i] : 0.0f;
+          // sparse V: a weight below tau relative to the (lazily raised) running
+          // maximum, hence below tau after normalization, contributes no V
+          if (sparse && pj < p.sparse_tau) w_own[i] = 0.0f;
+        }
+        // V steps (2 tokens each) that carry a nonzero weight, warp-uniform
+        if (sparse) {
+          bool keep = false;
+#pragma unroll
+          for (int i = 0; i < GH; ++i) keep |= w_own[i] != 0.0f;
+          stepmask = __reduce_or_sync(0xffffffffu, keep ? 1u << (tau_own >> 1) : 0u);
+        }
+        // weights of token tau_own, heads h0.. : row tau_own of 4 G bytes
+        if constexpr (G == 4) {
+          *reinterpret_cast<float2*>(wts + tau_own * 16 + h0 * 4) = make_float2(w_own[0], w_own[1]);
+        } else if constexpr (G == 2) {
+          *reinterpret_cast<float*>(wts + tau_own * 8 + h0 * 4) = w_own[0];
+        } else {
+          if (owner) *reinterpret_cast<float*>(wts + tau_own * 4) = w_own[0];
+        }
       }
       __syncwarp();
 
@@ -1020,7 +1178,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
     // ---- leave the row: lanes -> warp -> CTA, one partial per (CTA, row)
     for (int i = tid; i < G * D; i += kThreads) comb[i] = 0.0f;
     float mw[G];  // warp maxima of all heads
-    if constexpr (G >= 2) {
+    if constexpr (C::kMmaK) {  // head jj's maximum is on lanes 4 jj .. 4 jj + 3
+#pragma unroll
+      for (int jj = 0; jj < G; ++jj) mw[jj] = __shfl_sync(0xffffffffu, m_own[0], 4 * jj);
+    } else if constexpr (G >= 2) {
       const bool hi = (rr & 1) != 0;
 #pragma unroll
       for (int i = 0; i < GH; ++i) {
@@ -1042,17 +1203,26 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
       }
     {
       float lw[G];
+      if constexpr (C::kMmaK) {  // head jj's mass: the sum over its 4 lanes
+        float l4 = fadd(lsum[0], __shfl_xor_sync(0xffffffffu, lsum[0], 1));
+        l4 = fadd(l4, __shfl_xor_sync(0xffffffffu, l4, 2));
 #pragma unroll
-      for (int jj = 0; jj < G; ++jj) lw[jj] = 0.0f;
+        for (int jj = 0; jj < G; ++jj) lw[jj] = __shfl_sync(0xffffffffu, l4, 4 * jj);
+      } else {
 #pragma unroll
-      for (int i = 0; i < GH; ++i)
+        for (int jj = 0; jj < G; ++jj) lw[jj] = 0.0f;
+#pragma unroll
+        for (int i = 0; i < GH; ++i)
+#pragma unroll
+          for (int jj = 0; jj < G; ++jj)
+            if (jj == h0 + i) lw[jj] = lsum[i];
 #pragma unroll
         for (int jj = 0; jj < G; ++jj)
-          if (jj == h0 + i) lw[jj] = lsum[i];
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) lw[jj] = fadd(lw[jj], __shfl_xor_sync(0xffffffffu, lw[jj], o));
+      }
 #pragma unroll
       for (int jj = 0; jj < G; ++jj) {
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) lw[jj] = fadd(lw[jj], __shfl_xor_sync(0xffffffffu, lw[jj], o));
         if (lane == 0) {
           wml[(warp * 4 + jj) * 2] = mw[jj];
           wml[(warp * 4 + jj) * 2 + 1] = lw[jj];
