@@ -77,8 +77,6 @@ struct DecodeParams {
 
 namespace {
 
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
 constexpr int kTile = 16;
 constexpr int kCopies = 16;                 // pair-table copies (one per lane of a half-warp)
 constexpr int kSmemBudget = 227 * 1024;
@@ -222,6 +220,11 @@ struct Cfg {
   // the staged K rows are padded so that the MMA operand loads of 4 tokens by 4
   // lanes each fall in distinct banks (288 = 256 + 32, 144 = 128 + 16 bytes)
   static constexpr bool kMmaK = kFp16K || kInt8;
+  // warps per CTA (one CTA per SM): 8 at up to 255 registers; the tensor-core
+  // variants need about 160, so 12 warps fit (int8 0.192 -> 0.174 ms, asym 0.077 ->
+  // 0.073 ms against 8 warps)
+  static constexpr int kWarps = kMmaK ? 12 : 8;
+  static constexpr int kThreads = kWarps * 32;
   static constexpr int kKPitch = kFp16K ? kKRow + 32 : kInt8 ? kKRow + 16 : kKRow;
   static constexpr int kKTile = kTile * kKPitch;
   static constexpr int kKNorm = kFp16K ? 0 : kTile * 4;
@@ -604,7 +607,7 @@ __device__ __forceinline__ int stage_tile(const DecodeParams& p, int b, int h, b
 
 // Split kernel.
 template <int G, int KB, int VB, bool SPARSE, bool PAGED, bool MQ>
-__global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(Cfg<KB, VB>::kThreads, 1) decode_split_kernel(const DecodeParams p) {
   using C = Cfg<KB, VB>;
   constexpr int S = C::kStages;
   constexpr int kRS = C::kRowShift;
@@ -619,11 +622,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
   const uint32_t tab = lay.tab_lo;
   float* qs = reinterpret_cast<float*>(ptr(lay.take(4 * D * 4)));
   float* comb = reinterpret_cast<float*>(ptr(lay.take(4 * D * 4)));
-  float* wml = reinterpret_cast<float*>(ptr(lay.take(kWarps * 4 * 2 * 4)));
-  int4* descs_all = reinterpret_cast<int4*>(ptr(lay.take(kWarps * 8 * 16)));
+  float* wml = reinterpret_cast<float*>(ptr(lay.take(C::kWarps * 4 * 2 * 4)));
+  int4* descs_all = reinterpret_cast<int4*>(ptr(lay.take(C::kWarps * 8 * 16)));
   long long* prefix = reinterpret_cast<long long*>(ptr(lay.take((kMaxDecodeBatch + 1) * 8)));
   long long* scan = reinterpret_cast<long long*>(ptr(lay.take(34 * 8)));
-  uint8_t* wts_all = ptr(lay.take(kWarps * C::kWts));
+  uint8_t* wts_all = ptr(lay.take(C::kWarps * C::kWts));
 
   // the merge grid may be launched now; it waits for this grid's completion
   asm volatile("griddepcontrol.launch_dependents;\n");
@@ -637,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
   // pair tables: entry e = code_a | code_b << bits -> (c[code_a], c[code_b]), 16 copies per row
   if constexpr (!C::kFp16K && !C::kInt8) {
     constexpr int n = (1 << (2 * C::kKBits)) * kCopies;
-    for (int i = tid; i < n; i += kThreads) {
+    for (int i = tid; i < n; i += C::kThreads) {
       const int e = i / kCopies, c = i % kCopies;
       *reinterpret_cast<float2*>(ptr(tab + (e << kRS) + 128 + c * 8)) =
           make_float2(p.k_cent[e & ((1 << C::kKBits) - 1)], p.k_cent[e >> C::kKBits]);
@@ -645,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
   }
   if constexpr (!C::kInt8) {
     constexpr int n = (1 << (2 * VB)) * kCopies;
-    for (int i = tid; i < n; i += kThreads) {
+    for (int i = tid; i < n; i += C::kThreads) {
       const int e = i / kCopies, c = i % kCopies;
       *reinterpret_cast<float2*>(ptr(tab + (e << kRS) + c * 8)) =
           make_float2(p.v_cent[e & ((1 << VB) - 1)], p.v_cent[e >> VB]);
@@ -663,14 +666,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
       }
     }
   }
-  tile_prefix<kThreads, MQ>(p, prefix, scan);  // synchronizes
+  tile_prefix<C::kThreads, MQ>(p, prefix, scan);  // synchronizes
   const long long total = prefix[p.batch];
   const long long t0 = total * blockIdx.x / p.grid, t1 = total * (blockIdx.x + 1) / p.grid;
   if (t0 >= t1) return;
 
   // per-warp staging rings of S buffers, allocated around the table in warp order
   uint32_t ring = 0;
-  for (int w = 0; w < kWarps; ++w) {
+  for (int w = 0; w < C::kWarps; ++w) {
     const uint32_t a = lay.take(S * C::kBuf);
     if (w == warp) ring = a;
   }
@@ -681,7 +684,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
   uint8_t* const wring = ptr(ring);
   uint8_t* wts = wts_all + warp * C::kWts;
   int4* descs = descs_all + warp * 8;
-  const int my_n = static_cast<int>((t1 - t0 - warp + kWarps - 1) / kWarps);  // tiles t0 + warp + kWarps j
+  const int my_n = static_cast<int>((t1 - t0 - warp + C::kWarps - 1) / C::kWarps);  // tiles t0 + warp + C::kWarps j
   int j_issue = 0, j = 0;
   Cursor cur;
   TileBlocks tb{0, 0};  // paged: block-table entries of the tile the cursor points at
@@ -698,7 +701,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
       const int staged = stage_tile<KB, VB, PAGED>(p, cb, cur.h, hot, t_begin, n_valid, tb,
                                                    ring + static_cast<uint32_t>((j_issue % S) * C::kBuf), lane);
       if (lane == 0) descs[j_issue % S] = make_int4(cb, cur.h | (hot << 16), t_begin, staged);
-      cursor_advance<MQ>(p, cur, kWarps);
+      cursor_advance<MQ>(p, cur, C::kWarps);
       if constexpr (PAGED)
         if (j_issue + 1 < my_n) tb = load_tile_blocks(p, cache_seq<MQ>(p, cur.b), cursor_t_begin(cur), cursor_n_valid(cur));
     }
@@ -804,7 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
 #pragma unroll
       for (int k = 0; k < 4; ++k) acc[jj][k] = make_float2(0.0f, 0.0f);
 
-    while (j < my_n && t0 + warp + static_cast<long long>(kWarps) * j < seg_end) {
+    while (j < my_n && t0 + warp + static_cast<long long>(C::kWarps) * j < seg_end) {
       issue();
       cp_async_wait<S - 1>();
       __syncwarp();
@@ -1176,7 +1179,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
     }
 
     // ---- leave the row: lanes -> warp -> CTA, one partial per (CTA, row)
-    for (int i = tid; i < G * D; i += kThreads) comb[i] = 0.0f;
+    for (int i = tid; i < G * D; i += C::kThreads) comb[i] = 0.0f;
     float mw[G];  // warp maxima of all heads
     if constexpr (C::kMmaK) {  // head jj's maximum is on lanes 4 jj .. 4 jj + 3
 #pragma unroll
@@ -1237,10 +1240,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
     for (int jj = 0; jj < G; ++jj) {
       float mm = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) mm = fmaxf(mm, wml[(w * 4 + jj) * 2]);
+      for (int w = 0; w < C::kWarps; ++w) mm = fmaxf(mm, wml[(w * 4 + jj) * 2]);
       sc2[jj] = mw[jj] == -INFINITY ? 0.0f : exp2f(mw[jj] - mm);
     }
-    for (int w = 0; w < kWarps; ++w) {
+    for (int w = 0; w < C::kWarps; ++w) {
       if (warp == w && g == 0) {
 #pragma unroll
         for (int jj = 0; jj < G; ++jj) {
@@ -1256,13 +1259,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
       __syncthreads();
     }
     const long long slot = static_cast<long long>(blockIdx.x) + si.row;
-    for (int i = tid; i < G * D; i += kThreads) p.ws_acc[slot * G * D + i] = comb[i];
+    for (int i = tid; i < G * D; i += C::kThreads) p.ws_acc[slot * G * D + i] = comb[i];
     if (tid < G) {
       float mm = -INFINITY, ll = 0.0f;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) mm = fmaxf(mm, wml[(w * 4 + tid) * 2]);
+      for (int w = 0; w < C::kWarps; ++w) mm = fmaxf(mm, wml[(w * 4 + tid) * 2]);
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
+      for (int w = 0; w < C::kWarps; ++w) {
         const float mwv = wml[(w * 4 + tid) * 2];
         if (mwv != -INFINITY) ll = ffma(wml[(w * 4 + tid) * 2 + 1], exp2f(mwv - mm), ll);
       }
@@ -1289,7 +1292,7 @@ tq_status launch_split(const DecodeParams& p, cudaStream_t stream) {
     return TQ_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.grid);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
