@@ -19,8 +19,10 @@
 // PRMT (4-bit codes) or one shift and one masked OR.  Warp w takes tiles
 // t0 + w, t0 + w + 8, ... of the CTA's range and streams them through a cp.async
 // ring of up to 8 tiles that runs across row boundaries.  Per tile:
-//   scores:  8 lanes share a token, each owning 16 coordinates (8 code pairs,
-//            each looked up at once as (c_a, c_b)); 4 tokens per step, 4 steps.
+//   scores:  packed K: 8 lanes share a token, each owning 16 coordinates (8 code
+//            pairs, each looked up at once as (c_a, c_b)); 4 tokens per step, 4 steps.
+//            fp16 or int8 K: on the tensor cores (mma m16n8k16, exact fp16 operands),
+//            the softmax in the MMA fragment layout.
 //            Partial sums over the lane's coordinates for the G query heads,
 //            then a 3-stage transposing butterfly over the 8 lanes leaves each
 //            lane with the full scores of one token for G/2 heads;
@@ -755,8 +757,8 @@ __global__ void __launch_bounds__(Cfg<KB, VB>::kThreads, 1) decode_split_kernel(
       cur_h = si.h;
     }
     if (!C::kMmaK && (si.b != cur_b || si.h != cur_h)) {
-      // rotated query of the G heads: (log2 e / d) H D q for packed K
-      constexpr bool kRotQ = !C::kFp16K && !C::kInt8;
+      // rotated query of the G heads: (log2 e / d) H D q (packed K)
+      constexpr bool kRotQ = true;
       __syncthreads();
       if (tid < D) {
         const bool neg = kRotQ && sign_negative(p.seed, p.layer, si.h, tid);
@@ -904,29 +906,8 @@ __global__ void __launch_bounds__(Cfg<KB, VB>::kThreads, 1) decode_split_kernel(
           auto k_step = [&](uint32_t kw, float* P) {
             constexpr int OFF = 0;
             float2 c[8];
-            if constexpr (C::kFp16K) {
-              const uint4 a = lds128<OFF>(kw), b = lds128<OFF + 128>(kw);
-              c[0] = half2_bits_to_float2(a.x);
-              c[1] = half2_bits_to_float2(a.y);
-              c[2] = half2_bits_to_float2(a.z);
-              c[3] = half2_bits_to_float2(a.w);
-              c[4] = half2_bits_to_float2(b.x);
-              c[5] = half2_bits_to_float2(b.y);
-              c[6] = half2_bits_to_float2(b.z);
-              c[7] = half2_bits_to_float2(b.w);
-            } else if constexpr (C::kInt8) {
-              const uint4 a = lds128<OFF>(kw);
-              const uint32_t x0 = a.x ^ 0x80808080u, x1 = a.y ^ 0x80808080u;
-              const uint32_t x2 = a.z ^ 0x80808080u, x3 = a.w ^ 0x80808080u;
-              c[0] = int8_pair<0>(x0);
-              c[1] = int8_pair<2>(x0);
-              c[2] = int8_pair<0>(x1);
-              c[3] = int8_pair<2>(x1);
-              c[4] = int8_pair<0>(x2);
-              c[5] = int8_pair<2>(x2);
-              c[6] = int8_pair<0>(x3);
-              c[7] = int8_pair<2>(x3);
-            } else if constexpr (KB == 4) {
+            // packed K only: the fp16 and int8 modes take their scores on the tensor cores
+            if constexpr (KB == 4) {
               const uint2 wv = lds64u<OFF>(kw);
               c[0] = lds64(pair_addr<4, 0, kRS>(wv.x, kbase));
               c[1] = lds64(pair_addr<4, 1, kRS>(wv.x, kbase));
