@@ -361,10 +361,15 @@ TQ_HD void pack_codes32(const float2* z, float inv, const LutEntry* lut, int str
   uint32_t acc[BITS];
 #pragma unroll
   for (int k = 0; k < BITS; ++k) acc[k] = 0u;
+  float2 y2 = make_float2(0.0f, 0.0f), b2 = y2;
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
-    const float y = fmul((i & 1) ? z[i >> 1].y : z[i >> 1].x, inv);
-    const uint32_t raw = fbits(ffma(y, fa, kMagic)) - bias;
+    if ((i & 1) == 0) {  // a pair of coordinates: scaled and bucketed with packed operations
+      y2 = mul2(z[i >> 1], make_float2(inv, inv));
+      b2 = fma2(y2, make_float2(fa, fa), make_float2(kMagic, kMagic));
+    }
+    const float y = (i & 1) ? y2.y : y2.x;
+    const uint32_t raw = fbits((i & 1) ? b2.y : b2.x) - bias;
     const uint32_t idx = raw < last ? raw : last;
     const LutEntry e = lut[idx * stride];
     const uint32_t code = e.base + (y >= e.thr ? 1u : 0u);

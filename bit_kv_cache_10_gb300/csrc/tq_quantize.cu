@@ -28,6 +28,7 @@ constexpr int kRowPitch = kRowBytes + 16;   // padded smem pitch
 constexpr int kTileRows = 16;
 constexpr int kTileBytes = kTileRows * kRowPitch;
 constexpr int kLutCopies = 16;              // one LUT copy per lane of a half-warp
+constexpr int kSignHeads = 16;              // KV heads whose rotation-sign masks a CTA tabulates once
 
 struct QuantParams {
   const uint16_t* k_src;
@@ -116,8 +117,7 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
 
-__device__ __forceinline__ void issue_tile(const QuantParams& p, long long j, uint8_t* tile, int lane) {
-  const Job jb = decode_job(p, j);
+__device__ __forceinline__ void issue_tile(const QuantParams& p, const Job& jb, uint8_t* tile, int lane) {
   if (!jb.valid) return;
 #pragma unroll
   for (int k = 0; k < kTileRows / 2; ++k) {
@@ -242,7 +242,11 @@ __global__ void __launch_bounds__(kWarps * 32, 1) quantize_append_kernel(const Q
   const int lut_v_n = p.v_lut_a ? lut_size(p.v_lut_a) : 0;  // 0: int8 mode
   LutEntry* lut_k = reinterpret_cast<LutEntry*>(smem);
   LutEntry* lut_v = lut_k + lut_k_n * kLutCopies;
-  uint8_t* warp_area = reinterpret_cast<uint8_t*>(lut_v + lut_v_n * kLutCopies);
+  // rotation-sign masks of every KV head (64 words each) when there are at most
+  // kSignHeads heads, else each warp computes its job's head into its own area
+  uint32_t* sign_tab = reinterpret_cast<uint32_t*>(lut_v + lut_v_n * kLutCopies);
+  const bool tab_signs = p.heads <= kSignHeads && p.k_mode != TQ_KV_INT8;
+  uint8_t* warp_area = reinterpret_cast<uint8_t*>(sign_tab + kSignHeads * 64);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int vrow = lane & 7, q = lane >> 3;
   uint8_t* tiles = warp_area + warp * (kTileBytes + 256);
@@ -259,6 +263,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1) quantize_append_kernel(const Q
 #pragma unroll
     for (int c = 0; c < kLutCopies / 2; ++c) dst[c] = two;
   }
+  if (tab_signs)
+    for (int i = threadIdx.x; i < p.heads * 64; i += blockDim.x)
+      sign_tab[i] = sign_mask_pair(p.seed, p.layer, i >> 6, i & 63);
   __syncthreads();
   // launched as a programmatic dependent grid: everything above uses only the
   // parameters; wait here for the preceding grid (it may produce the inputs or
@@ -270,18 +277,23 @@ __global__ void __launch_bounds__(kWarps * 32, 1) quantize_append_kernel(const Q
   // job j goes to CTA j mod grid: small appends put one job per SM
   const long long stride = static_cast<long long>(gridDim.x) * kWarps;
   long long j = static_cast<long long>(warp) * gridDim.x + blockIdx.x;
-  if (j < p.jobs) issue_tile(p, j, tiles, lane);
+  Job next{};  // the job whose tile is in flight, decoded once
+  if (j < p.jobs) {
+    next = decode_job(p, j);
+    issue_tile(p, next, tiles, lane);
+  }
   cp_async_commit();
   for (; j < p.jobs; j += stride) {
     asm volatile("cp.async.wait_all;\n" ::);
     __syncwarp();
 
-    const Job jb = decode_job(p, j);
+    const Job jb = next;
     if (!jb.valid) {
       if (jb.tile == 0 && jb.tensor == (p.evict ? 1 : 0) && jb.h == 0 && lane == 0 && p.status != nullptr)
         atomicOr(p.status, TQ_DEV_ERR_APPEND_RANGE);
     } else {
-      if (p.k_mode != TQ_KV_INT8) {  // rotation-sign masks of this head
+      const uint32_t* msk = tab_signs ? sign_tab + jb.h * 64 : smask;  // rotation-sign masks of this head
+      if (!tab_signs && p.k_mode != TQ_KV_INT8) {
         smask[lane] = sign_mask_pair(p.seed, p.layer, jb.h, lane);
         smask[lane + 32] = sign_mask_pair(p.seed, p.layer, jb.h, lane + 32);
       }
@@ -295,9 +307,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1) quantize_append_kernel(const Q
                               bool store) {
         switch (bits) {
           case 8: quantize_step_int8(rowp, q, dw, dn, store); break;
-          case 2: quantize_step<2>(rowp, q, smask, lut, lut_a, dw, dn, store); break;
-          case 3: quantize_step<3>(rowp, q, smask, lut, lut_a, dw, dn, store); break;
-          default: quantize_step<4>(rowp, q, smask, lut, lut_a, dw, dn, store); break;
+          case 2: quantize_step<2>(rowp, q, msk, lut, lut_a, dw, dn, store); break;
+          case 3: quantize_step<3>(rowp, q, msk, lut, lut_a, dw, dn, store); break;
+          default: quantize_step<4>(rowp, q, msk, lut, lut_a, dw, dn, store); break;
         }
       };
 #pragma unroll 1
@@ -350,7 +362,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1) quantize_append_kernel(const Q
     }
     __syncwarp();
     const long long jn = j + stride;
-    if (jn < p.jobs) issue_tile(p, jn, tiles, lane);
+    if (jn < p.jobs) {
+      next = decode_job(p, jn);
+      issue_tile(p, next, tiles, lane);
+    }
     cp_async_commit();
   }
   asm volatile("cp.async.wait_all;\n" ::);
@@ -560,7 +575,7 @@ tq_status launch_small(const QuantParams& p, cudaStream_t stream) {
 size_t quant_smem_bytes(int k_lut_a, int v_lut_a) {
   const size_t luts = (static_cast<size_t>(k_lut_a ? lut_size(k_lut_a) : 0) + (v_lut_a ? lut_size(v_lut_a) : 0)) *
                       kLutCopies * sizeof(LutEntry);
-  return luts + static_cast<size_t>(kWarps) * (kTileBytes + 256);
+  return luts + kSignHeads * 64 * sizeof(uint32_t) + static_cast<size_t>(kWarps) * (kTileBytes + 256);
 }
 
 int sm_count_q() {
