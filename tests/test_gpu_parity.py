@@ -446,6 +446,29 @@ def test_small_and_bulk_appends_store_the_same_words(bits):
                                       err_msg=name)
 
 
+@pytest.mark.parametrize("hk", [16, 17, 24])
+def test_many_kv_heads_rotation_signs(hk):
+    """The bulk append kernel tabulates the rotation signs of up to 16 KV heads
+    once per CTA and computes them per job beyond that; both must give the
+    oracle's words and norms (seed 3, layer 5), and the same words as the
+    small-append kernel, which computes the signs per vector."""
+    B, T = 2, 40
+    k = synth.kv_fp16(71, 1, B, hk, T, D, synth.channel_scales(71, 4, hk, D))
+    v = synth.kv_fp16(71, 2, B, hk, T, D, synth.channel_scales(71, 5, hk, D))
+    kw = dict(batch=B, num_kv_heads=hk, num_q_heads=hk, capacity=T, bits=(3, 4), seed=3, layer=5)
+    bulk, small = _cache(**kw), _cache(**kw)
+    bulk.append(_dev(k), _dev(v), _dev(np.zeros(B, np.int32)))
+    for c in range(0, T, 16):
+        small.append(_dev(k[:, :, c:c + 16]), _dev(v[:, :, c:c + 16]), _dev(np.full(B, c, np.int32)))
+    assert bulk.device_status() == 0 and small.device_status() == 0
+    for name in ("k_cache", "k_norms", "v_cache", "v_norms"):
+        np.testing.assert_array_equal(getattr(small, name).cpu().numpy(), getattr(bulk, name).cpu().numpy(),
+                                      err_msg=name)
+    lens = np.full(B, T)
+    check_quantized(bulk, k, 0, 3, lens, seed=3, layer=5, what="K, %d KV heads" % hk)
+    check_quantized(bulk, v, 1, 4, lens, seed=3, layer=5, what="V, %d KV heads" % hk)
+
+
 def test_largest_batch_of_ragged_sequences():
     """The largest batch one decode call takes (512 sequences: the per-sequence tile
     prefix is held in shared memory), lengths 0..200 including empty sequences,
