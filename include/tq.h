@@ -280,8 +280,11 @@ tq_status tq_cache_buffer_bytes(const tq_cache_desc *desc, size_t *k_cache_bytes
  * descriptor); no rotation.
  * hot_window W > 0: after the call positions [end - W, end) of V (end =
  * start + n_new) are in the fp16 ring and [0, end - W) are packed; V tokens
- * that leave the ring are quantized before their slot is reused (one extra
- * launch, before the append launch, on the same stream).
+ * that leave the ring are quantized before their slot is reused: inside the
+ * append launch when n_new <= W (each new row takes exactly one slot), else
+ * by one extra launch before the append launch, on the same stream.
+ * Appends of at most 16 tokens per sequence use a one-warp-per-vector kernel
+ * with the same arithmetic (identical words and norms).
  *
  * A start position < 0, a count outside [0, n_new] or start + count >
  * capacity sets TQ_DEV_ERR_APPEND_RANGE in d_status and skips that sequence.
