@@ -15,7 +15,9 @@
  * Ownership.   The caller allocates every device buffer (cache, queries,
  *              outputs, workspace) and keeps it alive while work that uses it
  *              is queued.  The library allocates no device memory, keeps no
- *              global state, and may be called from several host threads.
+ *              global state (the one exception is the fixed scratch array of
+ *              tq_decode_attention_no_alloc, part of the library's device
+ *              image), and may be called from several host threads.
  * Asynchrony.  Functions taking a stream enqueue kernels on it and return at
  *              once; results are ready when the stream is.  A NULL stream is
  *              the legacy default stream.  The host-only helpers are
@@ -316,8 +318,9 @@ size_t tq_decode_workspace_bytes(const tq_cache_desc *desc, int32_t max_seq_len)
  *
  * with k_j, v_j the dequantized tokens n_j R^T c[codes_j] (or the raw fp16 K
  * in TQ_K_FP16 mode, s_j code_j in TQ_KV_INT8 mode, and the raw fp16 V of the
- * hot ring for the newest min(W, L) positions).  The query is rotated once, scores are
- * n_j * sum_i (R q)_i c[code_ji], the softmax runs online over split-K
+ * hot ring for the newest min(W, L) positions).  With packed K the query is
+ * rotated once and scores are n_j * sum_i (R q)_i c[code_ji] (fp16 and int8 K
+ * use the raw query); the softmax runs online over split-K
  * chunks of the context, V is accumulated in the rotated domain and rotated
  * back once per output by a reduction kernel.
  *
