@@ -763,7 +763,8 @@ def run_gpu(args):
         "e2e": {"value": job_throughput(e2e_bytes, e2e_ms, world), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "clocks": clocks,
-        "gpu_launches": args.steps * 4,
+        # per timed step: the one-token append (evict fused), the split-K kernel and the merge
+        "gpu_launches": args.steps * 3,
     }
     if want_cpu:
         line["cpu_baseline"] = cpu_baseline(lens0, synth.queries_fp16(SEED, B, HQ, D), pool, workers)
