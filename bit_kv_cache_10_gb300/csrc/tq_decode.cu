@@ -2,8 +2,6 @@
 // kernel and the dense contiguous split-K instantiations (the split kernel
 // itself is in tq_decode_split.cuh; its sparse-V and paged instantiations are in
 // tq_decode_sparse.cu, tq_decode_paged.cu and tq_decode_paged_sparse.cu).
-#include <mutex>
-
 #include "tq_decode_split.cuh"
 
 namespace tq {
@@ -23,6 +21,10 @@ __global__ void __launch_bounds__(4 * 32) decode_merge_kernel(const DecodeParams
   const int jj = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.x, b = blockIdx.y;
   if (jj >= g) return;
+  // the lengths may be written by a grid before the split kernel and the partials
+  // by the split kernel: wait for the preceding grids before reading either
+  // (programmatic dependent launch lets this grid start while they finish)
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
   float4* out = reinterpret_cast<float4*>(p.out + (static_cast<int64_t>(b) * p.hq + h * g + jj) * D);
   // tiles of the sequences before b, and of all sequences
   long long before = 0, total = 0;
@@ -66,9 +68,6 @@ __global__ void __launch_bounds__(4 * 32) decode_merge_kernel(const DecodeParams
   const int n = n0 + n1;
   const unsigned live32 = __ballot_sync(0xffffffffu, lane < n && live(lane));
   auto is_live = [&](int i) { return i < 32 ? ((live32 >> i) & 1u) != 0 : live(i); };
-  // the partials are written by the split kernel: wait for it (programmatic
-  // dependent launch lets this grid start while the split kernel finishes)
-  asm volatile("griddepcontrol.wait;\n" ::: "memory");
   float mm = -INFINITY, l = 0.0f;
   float y[4] = {0.0f, 0.0f, 0.0f, 0.0f}, hv[4] = {0.0f, 0.0f, 0.0f, 0.0f};
   auto add_partial = [&](int i, float sc, const float4 a) {
@@ -289,24 +288,15 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_no_alloc_scratch[TQ_NO_ALLOC_WORKSPACE_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mutex;
-void* g_scratch_address[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device.  In host code the
-// array's name only stands in for the symbol, so the address is looked up once
-// per device with that device current.
+// Device address of the scratch array in the current context.  In host code the
+// array's name only stands in for the symbol, so the address is looked up with
+// the caller's device current, on every call: the module can be loaded at another
+// address in another context (or after a device reset), so no address is kept
+// between calls.  The lookup is host-side and allocates nothing.
 tq_status no_alloc_scratch(void** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return TQ_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return TQ_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (g_scratch_address[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_no_alloc_scratch) != cudaSuccess || p == nullptr) return TQ_ERR_CUDA;
-    g_scratch_address[dev] = p;
-  }
-  *out = g_scratch_address[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_no_alloc_scratch) != cudaSuccess || p == nullptr) return TQ_ERR_CUDA;
+  *out = p;
   return TQ_OK;
 }
 

@@ -385,9 +385,11 @@ tq_status tq_multi_query_attention(const tq_cache_desc *desc, const void *q, int
  *   Limit      the call needs tq_decode_workspace_bytes(desc, max_seq_len) <=
  *              TQ_NO_ALLOC_WORKSPACE_BYTES; a larger request returns
  *              TQ_ERR_WORKSPACE before any launch.
- *   Device     the current device.  The first call on a device looks up the
- *              scratch array's device address (a runtime call, made once per
- *              device); make that first call before any stream capture.
+ *   Device     the current device.  Every call looks up the scratch array's
+ *              device address in the current context (a host-side runtime
+ *              call that allocates nothing; the first one on a device may
+ *              load the library's device code), so make the first call on a
+ *              device before any stream capture.
  *   Sharing    every call uses the same array and leaves its contents behind;
  *              nothing in it needs to start at zero.  Calls whose kernels can
  *              overlap on the GPU (different streams, no ordering between

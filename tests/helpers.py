@@ -60,3 +60,37 @@ def compare_packed(got_words, ref_words, ref_y, bits, thresholds32, what="", che
     if check_rate:
         assert_code_rate(n, ref_y.size, what)
     return n, ref_y.size
+
+
+class RealBuffers:
+    """Real allocations for the argument-validation tests of the launching entry
+    points.  With a visible GPU they are device buffers of the sizes the call
+    would use, so that a regression in the host-side validation launches on real,
+    large-enough memory instead of a made-up address; without a GPU they are host
+    arrays (no device exists, so no kernel can be launched at all)."""
+
+    def __init__(self):
+        try:
+            import torch
+            self._torch = torch if torch.cuda.is_available() else None
+        except ImportError:
+            self._torch = None
+        self._keep = []
+
+    def alloc(self, nbytes: int) -> int:
+        """Address of a zeroed buffer of at least ``nbytes`` (256-byte aligned)."""
+        nbytes = max(int(nbytes), 256)
+        if self._torch is not None:
+            t = self._torch.zeros((nbytes + 3) // 4, dtype=self._torch.int32, device="cuda")
+            self._keep.append(t)
+            return t.data_ptr()
+        a = np.zeros(nbytes + 256, np.uint8)
+        self._keep.append(a)
+        return (a.ctypes.data + 255) & ~255
+
+    def cache(self, desc) -> None:
+        """Points every cache buffer of ``desc`` at a real allocation of its size."""
+        from bit_kv_cache_10_gb300 import native as N
+        for name, size in N.tq_cache_buffer_bytes(desc).items():
+            if size:
+                setattr(desc, name, self.alloc(size))

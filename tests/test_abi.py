@@ -13,7 +13,7 @@ import oracle
 from bit_kv_cache_10_gb300 import native as N
 from bit_kv_cache_10_gb300 import synth
 
-from helpers import compare_packed
+from helpers import RealBuffers, compare_packed
 
 INCLUDE = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
 
@@ -106,29 +106,40 @@ def test_descriptor_validation():
 
 
 def test_entry_points_reject_bad_arguments_before_launch():
-    d = N.tq_cache_desc_init(1, 8, 32, 128, 64, N.TQ_K_PACKED, 3, 4)
+    B, HK, HQ, CAP = 1, 8, 32, 64
+    d = N.tq_cache_desc_init(B, HK, HQ, 128, CAP, N.TQ_K_PACKED, 3, 4)
     # buffers not set: every launching entry point refuses without touching the GPU
     L = N.lib()
     assert L.tq_quantize_append(d, None, None, 0, 0, 0, 1, None, None, None) == N.TQ_ERR_INVALID_ARG
     assert L.tq_decode_attention(d, None, None, 4, None, None, 0, None) == N.TQ_ERR_INVALID_ARG
     assert L.tq_dequantize(d, 0, 0, 0, 0, 1, None, None) == N.TQ_ERR_INVALID_ARG
-    fake = 1 << 20  # aligned dummy addresses; validation must fail before any use
-    d.k_cache = d.v_cache = d.k_norms = d.v_norms = fake
-    assert L.tq_quantize_append(d, fake, fake, 0, 0, 0, -1, fake, None, None) == N.TQ_ERR_INVALID_ARG
-    assert L.tq_quantize_append(d, fake, fake, 0, 0, 0, 65, fake, None, None) == N.TQ_ERR_CAPACITY
-    assert L.tq_quantize_append(d, fake + 8, fake, 0, 0, 0, 1, fake, None, None) == N.TQ_ERR_INVALID_ARG
-    assert L.tq_quantize_append(d, fake, fake, 0, 0, 3, 1, fake, None, None) == N.TQ_ERR_INVALID_ARG
-    assert L.tq_decode_attention(d, fake, fake, 64, fake, fake, 16, None) == N.TQ_ERR_WORKSPACE
-    assert L.tq_decode_attention(d, fake, fake, 64, fake, None, 1 << 30, None) == N.TQ_ERR_WORKSPACE
-    assert L.tq_dequantize(d, 2, 0, 0, 0, 1, fake, None) == N.TQ_ERR_INVALID_ARG
-    assert L.tq_dequantize(d, 0, 0, 0, 60, 5, fake, None) == N.TQ_ERR_CAPACITY
-    d.k_norms = fake + 4
-    assert L.tq_quantize_append(d, fake, fake, 0, 0, 0, 1, fake, None, None) == N.TQ_ERR_INVALID_ARG
-    d.k_norms = fake
+    # real buffers of the sizes each call would use; validation must refuse before any launch
+    mem = RealBuffers()
+    mem.cache(d)
+    new = mem.alloc(B * HK * (CAP + 1) * 128 * 2)  # fp16 [B, Hkv, 65, d]
+    pos = mem.alloc(4 * B)
+    q = mem.alloc(B * HQ * 128 * 2)
+    lens = mem.alloc(4 * B)
+    out = mem.alloc(B * HQ * 128 * 4)
+    ws_need = N.tq_decode_workspace_bytes(d, CAP)
+    ws = mem.alloc(ws_need)
+    deq = mem.alloc(HK * 5 * 128 * 4)
+    assert L.tq_quantize_append(d, new, new, 0, 0, 0, -1, pos, None, None) == N.TQ_ERR_INVALID_ARG
+    assert L.tq_quantize_append(d, new, new, 0, 0, 0, CAP + 1, pos, None, None) == N.TQ_ERR_CAPACITY
+    assert L.tq_quantize_append(d, new + 8, new, 0, 0, 0, 1, pos, None, None) == N.TQ_ERR_INVALID_ARG
+    assert L.tq_quantize_append(d, new, new, 0, 0, 3, 1, pos, None, None) == N.TQ_ERR_INVALID_ARG
+    assert L.tq_decode_attention(d, q, lens, CAP, out, ws, 16, None) == N.TQ_ERR_WORKSPACE
+    assert L.tq_decode_attention(d, q, lens, CAP, out, None, ws_need, None) == N.TQ_ERR_WORKSPACE
+    assert L.tq_dequantize(d, 2, 0, 0, 0, 1, deq, None) == N.TQ_ERR_INVALID_ARG
+    assert L.tq_dequantize(d, 0, 0, 0, CAP - 4, 5, deq, None) == N.TQ_ERR_CAPACITY
+    k_norms = d.k_norms
+    d.k_norms = k_norms + 4
+    assert L.tq_quantize_append(d, new, new, 0, 0, 0, 1, pos, None, None) == N.TQ_ERR_INVALID_ARG
+    d.k_norms = k_norms
     # the sparse-V threshold must lie in [0, 1] (NaN included in the refusal)
     for tau in (float("nan"), -1e-6, 1.5, float("inf")):
         d.sparse_v_threshold = tau
-        assert L.tq_decode_attention(d, fake, fake, 64, fake, fake, 1 << 30, None) == N.TQ_ERR_INVALID_ARG
+        assert L.tq_decode_attention(d, q, lens, CAP, out, ws, ws_need, None) == N.TQ_ERR_INVALID_ARG
     assert N.tq_cache_desc_init(1, 8, 32, 128, 64, N.TQ_K_PACKED, 3, 4).sparse_v_threshold == 0.0
 
 
@@ -179,23 +190,26 @@ def test_host_quantizer_special_vectors():
 
 def test_paged_layout_validation_and_pool_sizes():
     d = N.tq_cache_desc_init(2, 8, 32, 128, 4096, N.TQ_K_PACKED, 3, 4, hot_window=64)
-    fake = 1 << 20
-    for bs, mb, nb, tab in [(24, 4096 // 24, 10, fake), (8, 512, 10, fake), (8192, 1, 10, fake),
-                            (64, 63, 10, fake), (64, 64, 0, fake), (64, 64, 10, None), (64, 64, 10, fake + 2)]:
+    mem = RealBuffers()
+    tab = mem.alloc(2 * 4096 // 8 * 4)  # the largest table of the cases below
+    for bs, mb, nb, t in [(24, 4096 // 24, 10, tab), (8, 512, 10, tab), (8192, 1, 10, tab),
+                          (64, 63, 10, tab), (64, 64, 0, tab), (64, 64, 10, None), (64, 64, 10, tab + 2)]:
         with pytest.raises(N.TQError) as e:
-            N.tq_cache_desc_set_paged(d, bs, mb, nb, tab)
+            N.tq_cache_desc_set_paged(d, bs, mb, nb, t)
         assert e.value.status == N.TQ_ERR_INVALID_ARG
-    N.tq_cache_desc_set_paged(d, 64, 64, 200, fake)
-    assert (d.block_size, d.max_blocks_per_seq, d.num_blocks, d.block_table) == (64, 64, 200, fake)
+    N.tq_cache_desc_set_paged(d, 64, 64, 200, tab)
+    assert (d.block_size, d.max_blocks_per_seq, d.num_blocks, d.block_table) == (64, 64, 200, tab)
     sizes = N.tq_cache_buffer_bytes(d)
     rows = 200 * 8 * 64  # pools of 200 blocks of 64 tokens per KV head
     assert sizes == {"k_cache": rows * 48, "k_norms": rows * 4, "v_cache": rows * 64, "v_norms": rows * 4,
                      "v_hot": 2 * 8 * 64 * 256}
-    # a corrupted paged descriptor is refused before any launch
+    # a corrupted paged descriptor (no table) is refused before any launch
     L = N.lib()
-    d.k_cache = d.v_cache = d.k_norms = d.v_norms = d.v_hot = fake
+    mem.cache(d)
     d.block_table = None
-    assert L.tq_decode_attention(d, fake, fake, 64, fake, fake, 1 << 30, None) == N.TQ_ERR_INVALID_ARG
+    q, lens, out = mem.alloc(2 * 32 * 128 * 2), mem.alloc(8), mem.alloc(2 * 32 * 128 * 4)
+    need = N.tq_decode_workspace_bytes(d, 64)
+    assert L.tq_decode_attention(d, q, lens, 64, out, mem.alloc(need), need, None) == N.TQ_ERR_INVALID_ARG
 
 
 def test_int8_mode_descriptor_and_sizes():
@@ -222,20 +236,27 @@ def test_multi_query_arguments_and_workspace():
     assert N.tq_multi_query_workspace_bytes(d, 8, 100) == (512 + 2 * 4 * 8 * 8) * per_slot
     assert N.tq_multi_query_workspace_bytes(d, 0, 100) == 0
     L = N.lib()
-    fake = 1 << 20
-    d.k_cache = d.v_cache = d.k_norms = d.v_norms = d.v_hot = fake
-    big = 1 << 30
-    assert L.tq_multi_query_attention(d, fake, 0, fake, 64, fake, fake, big, None) == N.TQ_ERR_INVALID_ARG
-    assert L.tq_multi_query_attention(d, fake, 129, fake, 64, fake, fake, big, None) == N.TQ_ERR_UNSUPPORTED
-    assert L.tq_multi_query_attention(d, fake + 8, 2, fake, 64, fake, fake, big, None) == N.TQ_ERR_INVALID_ARG
+    mem = RealBuffers()
+    mem.cache(d)
+    B, HQ = 4, 32
+    q = mem.alloc(B * 129 * HQ * 128 * 2)  # room for the largest query count of the cases below
+    lens = mem.alloc(4 * B)
+    out = mem.alloc(B * 129 * HQ * 128 * 4)
+    big = N.tq_multi_query_workspace_bytes(d, 129, 64)
+    ws = mem.alloc(big)
+    assert L.tq_multi_query_attention(d, q, 0, lens, 64, out, ws, big, None) == N.TQ_ERR_INVALID_ARG
+    assert L.tq_multi_query_attention(d, q, 129, lens, 64, out, ws, big, None) == N.TQ_ERR_UNSUPPORTED
+    assert L.tq_multi_query_attention(d, q + 8, 2, lens, 64, out, ws, big, None) == N.TQ_ERR_INVALID_ARG
     need = N.tq_multi_query_workspace_bytes(d, 4, 64)
-    assert L.tq_multi_query_attention(d, fake, 4, fake, 64, fake, fake, need - 16, None) == N.TQ_ERR_WORKSPACE
+    assert L.tq_multi_query_attention(d, q, 4, lens, 64, out, ws, need - 16, None) == N.TQ_ERR_WORKSPACE
 
 
 def test_multi_query_refuses_sparse_v():
     d = N.tq_cache_desc_init(2, 8, 32, 128, 4096, N.TQ_K_PACKED, 3, 4)
-    fake = 1 << 20
-    d.k_cache = d.v_cache = d.k_norms = d.v_norms = fake
+    mem = RealBuffers()
+    mem.cache(d)
     d.sparse_v_threshold = 1e-3
+    q, lens, out = mem.alloc(2 * 4 * 32 * 128 * 2), mem.alloc(8), mem.alloc(2 * 4 * 32 * 128 * 4)
+    need = N.tq_multi_query_workspace_bytes(d, 4, 64)
     L = N.lib()
-    assert L.tq_multi_query_attention(d, fake, 4, fake, 64, fake, fake, 1 << 30, None) == N.TQ_ERR_UNSUPPORTED
+    assert L.tq_multi_query_attention(d, q, 4, lens, 64, out, mem.alloc(need), need, None) == N.TQ_ERR_UNSUPPORTED

@@ -243,12 +243,18 @@ def test_long_context_full_size_sampled():
     v_norms = synth.random_norms(5, synth.STREAM_NORMS_V, (B, HK, CAP), median=30.0)
     v_hot = synth.kv_fp16(5, synth.STREAM_V, B, HK, W, D, synth.channel_scales(5, synth.STREAM_SCALE_V, HK, D))
     oc = oracle.PackedCache(0, 0, D, 3, 4, k_words, k_norms, None, v_words, v_norms, W, v_hot)
-    q = synth.queries_fp16(5, B, HQ, D)
     tc = _cache(batch=B, num_kv_heads=HK, num_q_heads=HQ, capacity=CAP, bits=3.5, hot_window=W)
     upload(tc, oc)
-    pairs = [(0, 0), (1, 13), (2, 22), (3, 31), (3, 4), (0, 27)]
-    got, ref = decode_both(tc, oc, q, lens, CAP, pairs)
-    assert_attention_close(got, ref, "long-context decode (sampled heads)")
+    # every query head of the shortest sequence (all 8 KV heads, 32 outputs), and
+    # heads of the other sequences; with the plain queries and with queries scaled
+    # by 2.5, whose softmax concentrates on a few tokens
+    b_all = int(np.argmin(lens))
+    pairs = [(b_all, hq) for hq in range(HQ)] + [(b, hq) for b, hq in ((0, 27), (1, 13), (2, 22), (3, 31), (3, 4))
+                                                 if b != b_all]
+    for scale in (1.0, 2.5):
+        q = (synth.queries_fp16(5, B, HQ, D) * np.float16(scale)).astype(np.float16)
+        got, ref = decode_both(tc, oc, q, lens, CAP, pairs)
+        assert_attention_close(got, ref, "long-context decode, query scale %g" % scale)
     assert tc.device_status() == 0
 
 

@@ -74,9 +74,12 @@ def test_no_alloc_decode_matches_workspace_decode_on_consecutive_calls():
 
 def test_no_alloc_decode_rejects_requests_beyond_its_scratch():
     # 512 sequences x 8 KV heads need more partial slots than the fixed scratch holds: refused before any launch
+    from bit_kv_cache_10_gb300.cache import TurboQuantKVCache
     B, HK, HQ, CAP = 512, 8, 32, 64
-    d = N.tq_cache_desc_init(B, HK, HQ, D, CAP, N.TQ_K_PACKED, 3, 4)
-    assert N.tq_decode_workspace_bytes(d, CAP) > N.TQ_NO_ALLOC_WORKSPACE_BYTES
-    fake = 1 << 20
-    d.k_cache = d.v_cache = d.k_norms = d.v_norms = fake
-    assert N.lib().tq_decode_attention_no_alloc(d, fake, fake, CAP, fake, None) == N.TQ_ERR_WORKSPACE
+    tc = TurboQuantKVCache(B, HK, HQ, CAP, bits=(3, 4))  # real buffers of the request's sizes
+    assert tc.workspace_bytes(CAP) > N.TQ_NO_ALLOC_WORKSPACE_BYTES
+    q = torch.zeros(B, HQ, D, dtype=torch.float16, device="cuda")
+    lens = torch.full((B,), CAP, dtype=torch.int32, device="cuda")
+    out = torch.zeros(B, HQ, D, dtype=torch.float32, device="cuda")
+    assert N.lib().tq_decode_attention_no_alloc(tc.desc, q.data_ptr(), lens.data_ptr(), CAP, out.data_ptr(),
+                                                None) == N.TQ_ERR_WORKSPACE
