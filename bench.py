@@ -216,20 +216,48 @@ def _oracle_task(args):
 def _oracle_quant_task(args):
     """Oracle quantize of n token vectors of K and of V of one (batch, KV head)
     of the quantize workload (N(0,1) x lognormal channel scales) in a worker
-    process: (seconds, token-heads)."""
+    process, K at kb and V at vb bits: (seconds, token-heads)."""
     import oracle
-    b, h, n = args
+    b, h, n = args[:3]
+    kb, vb = args[3:] if len(args) > 3 else (KB, VB)
     rows = []
     for stream, scale_stream in ((synth.STREAM_K, synth.STREAM_SCALE_K), (synth.STREAM_V, synth.STREAM_SCALE_V)):
         s = synth.channel_scales(SEED + 2, scale_stream, HKV, D)[h]
         rows.append((synth.row_rng(SEED + 2, stream, b, h).standard_normal((n, D)) * s).astype(np.float16))
     rot = oracle.rotation(0, 0, h, D)
-    cbs = (oracle.codebook(D, KB), oracle.codebook(D, VB))  # built (or cached) outside the timed part
+    cbs = (oracle.codebook(D, kb), oracle.codebook(D, vb))  # built (or cached) outside the timed part
     t0 = time.perf_counter()
-    for x, bits, cb in zip(rows, (KB, VB), cbs):
+    for x, bits, cb in zip(rows, (kb, vb), cbs):
         codes, _, _ = oracle.quantize_rows(x, rot, cb)
         oracle.pack(codes, bits)
     return time.perf_counter() - t0, n
+
+
+def _oracle_plain_task(args):
+    """Oracle decode of the 4 query heads of one (batch, KV head) row of a
+    plain (no hot window) decode workload of context n: packed K (k_fp16 False)
+    or fp16 K drawn N(0,1) x lognormal channel scales, packed 4-bit V.  Returns
+    (seconds, algorithmic bytes)."""
+    import oracle
+    seed, b, h, n, k_fp16 = args
+    g = HQ // HKV
+    vw, vn = synth.packed_row(seed, synth.STREAM_CODES_V, b, h, n, D * VB // 32, 30.0)
+    if k_fp16:
+        sk = synth.channel_scales(seed, synth.STREAM_SCALE_K, HKV, D)
+        k16 = synth.kv_fp16(seed + b, synth.STREAM_K, 1, HKV, n, D, sk)[:, h:h + 1]
+        c = oracle.PackedCache(0, 0, D, 16, VB, None, None, k16, vw[None, None], vn[None, None], 0, None)
+        k_bytes = n * D * 2
+    else:
+        kw, kn = synth.packed_row(seed, synth.STREAM_CODES_K, b, h, n, D * KB // 32, 12.0)
+        c = oracle.PackedCache(0, 0, D, KB, VB, kw[None, None], kn[None, None], None, vw[None, None],
+                               vn[None, None], 0, None)
+        k_bytes = n * (D * KB // 8 + 4)
+    q16 = synth.queries_fp16(seed, b + 1, HQ, D)[b]
+    t0 = time.perf_counter()
+    k, v = oracle.dequantized_kv(c, 0, 0, n)
+    for j in range(g):
+        oracle.attention_one(q16[h * g + j].astype(np.float64), k, v)
+    return time.perf_counter() - t0, k_bytes + n * (D * VB // 8 + 4) + g * D * 6
 
 
 def oracle_pool():
@@ -262,13 +290,31 @@ def cpu_baseline(lens, q16, pool, workers, rounds=4):
     t0 = time.perf_counter()
     token_heads = sum(n for _, n in pool.map(_oracle_quant_task, qtasks))
     qwall = time.perf_counter() - t0
+    widths = {}
+    for kb, vb in ((3, 3), (4, 4)):
+        wt = [t + (kb, vb) for t in qtasks]
+        t0 = time.perf_counter()
+        th = sum(n for _, n in pool.map(_oracle_quant_task, wt))
+        widths["%d" % kb] = {"value": th / HKV / (time.perf_counter() - t0) / 1e6, "unit": "Mtokens/s"}
+    # the other decode workloads, every (batch, KV head) row of the Llama-like layer
+    # (B1, context 4096) and 2 rows per worker of the asym workload (B8, context 16384)
+    plain = {}
+    for name, seed, batch, ctx, k_fp16, n_rows in (("llama_layer", SEED + 3, 1, 4096, False, HKV),
+                                                   ("asym", SEED + 3, 8, 16384, True, 2 * workers)):
+        ptasks = [(seed, (i // HKV) % batch, i % HKV, ctx, k_fp16) for i in range(n_rows)]
+        t0 = time.perf_counter()
+        pb = sum(nb for _, nb in pool.map(_oracle_plain_task, ptasks))
+        plain[name] = {"value": pb / (time.perf_counter() - t0) / 1e9, "unit": "GB/s",
+                       "sample": "%d (batch, KV head) rows at full context %d" % (n_rows, ctx)}
     return {"value": nbytes / wall / 1e9, "unit": "GB/s", "cores": workers, "kind": "oracle",
+            "llama_layer": plain["llama_layer"], "asym": plain["asym"],
             "sample": "%d (batch, KV head) rows of the workload at full context (%.2f GB of algorithmic bytes) on "
                       "%d worker processes with single-threaded BLAS: numpy float64 dequantize + softmax attention "
                       "for the 4 query heads of each row" % (len(tasks), nbytes / 1e9, workers),
             "quantize": {"value": token_heads / HKV / qwall / 1e6, "unit": "Mtokens/s",
                          "sample": "%d slices of 2048 tokens of one (batch, KV head) of the quantize workload, K 3-bit "
-                                   "and V 4-bit (a token = one position with all 8 KV heads)" % len(qtasks)}}
+                                   "and V 4-bit (a token = one position with all 8 KV heads)" % len(qtasks),
+                         "widths": widths}}
 
 
 def run_reference(args):
@@ -359,9 +405,11 @@ def build_plain_cache(torch, batch, ctx, k_fp16, seed):
     return tc
 
 
-def time_plain_decode(torch, batch, ctx, k_fp16, reps=50):
+def time_plain_decode(torch, batch, ctx, k_fp16, reps=50, flush=False):
     """Mean decode-call time (ms) and algorithmic bytes of one call on a
-    build_plain_cache cache, after 3 untimed calls."""
+    build_plain_cache cache, after 3 untimed calls.  With ``flush`` a 256 MB
+    buffer (twice L2) is written before every call and only the call itself is
+    between the events, so the cache is read from HBM."""
     tc = build_plain_cache(torch, batch, ctx, k_fp16, SEED + 3)
     q = torch.from_numpy(synth.queries_fp16(SEED + 3, batch, HQ, D)).cuda()
     lens = torch.full((batch,), ctx, dtype=torch.int32, device="cuda")
@@ -370,14 +418,27 @@ def time_plain_decode(torch, batch, ctx, k_fp16, reps=50):
     for _ in range(3):
         tc.decode(q, lens, ctx, out=out, workspace=ws)
     st = torch.cuda.current_stream()
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
-    torch.cuda.synchronize()
-    ev[0].record(st)
-    for i in range(reps):
-        tc.decode(q, lens, ctx, out=out, workspace=ws)
-        ev[i + 1].record(st)
-    torch.cuda.synchronize()
-    ms = float(np.mean([ev[i].elapsed_time(ev[i + 1]) for i in range(reps)]))
+    if flush:
+        scrub = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        torch.cuda.synchronize()
+        for e0, e1 in ev:
+            scrub.fill_(1)
+            e0.record(st)
+            tc.decode(q, lens, ctx, out=out, workspace=ws)
+            e1.record(st)
+        torch.cuda.synchronize()
+        ms = float(np.mean([e0.elapsed_time(e1) for e0, e1 in ev]))
+        del scrub
+    else:
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+        torch.cuda.synchronize()
+        ev[0].record(st)
+        for i in range(reps):
+            tc.decode(q, lens, ctx, out=out, workspace=ws)
+            ev[i + 1].record(st)
+        torch.cuda.synchronize()
+        ms = float(np.mean([ev[i].elapsed_time(ev[i + 1]) for i in range(reps)]))
     if tc.device_status() != 0:
         raise RuntimeError("device status set by the decode timing")
     k_tok = D * 2 if k_fp16 else D * KB // 8 + 4
@@ -440,9 +501,7 @@ def time_int8(torch, lens, reps=20):
         raise RuntimeError("device status set by the int8 decode timing")
     dec_bytes = int(np.sum(lens)) * HKV * 2 * (D + 4) + len(lens) * HQ * D * (2 + 4)
     del tc, ws
-    g = synth.rng(SEED + 2, synth.STREAM_K)
-    kq = torch.from_numpy(g.standard_normal((QB, HKV, QT, D), dtype=np.float32).astype(np.float16)).cuda()
-    vq = torch.from_numpy(g.standard_normal((QB, HKV, QT, D), dtype=np.float32).astype(np.float16)).cuda()
+    kq, vq = quantize_inputs(torch)
     qc = TurboQuantKVCache(QB, HKV, HKV * 4, QT, bits="int8")
     zero = torch.zeros(QB, dtype=torch.int32, device="cuda")
     q_ms = timed(lambda: qc.append(kq, vq, zero), 10)
@@ -494,6 +553,46 @@ def paged_decode_ms(torch, tc, lens0, q, seqs, max_len, bs=64, reps=20, permute=
     ms = float(np.mean([ev[i].elapsed_time(ev[i + 1]) for i in range(reps)]))
     del pg
     return ms
+
+
+def quantize_inputs(torch):
+    """The quantize workload's new K and V tokens on the device: fp16 [16, 8, 8192,
+    128], N(0,1) times lognormal(0,1) scales per (KV head, channel), drawn on the
+    host one sequence at a time to bound host memory."""
+    gq = synth.rng(SEED + 2, synth.STREAM_K)
+    qsk = torch.from_numpy(synth.channel_scales(SEED + 2, synth.STREAM_SCALE_K, HKV, D).astype(np.float32)).cuda()
+    qsv = torch.from_numpy(synth.channel_scales(SEED + 2, synth.STREAM_SCALE_V, HKV, D).astype(np.float32)).cuda()
+    kq = torch.empty(QB, HKV, QT, D, dtype=torch.float16, device="cuda")
+    vq = torch.empty_like(kq)
+    for b in range(QB):
+        kq[b].copy_((torch.from_numpy(gq.standard_normal((HKV, QT, D), dtype=np.float32)).cuda()
+                     * qsk[:, None, :]).half())
+        vq[b].copy_((torch.from_numpy(gq.standard_normal((HKV, QT, D), dtype=np.float32)).cuda()
+                     * qsv[:, None, :]).half())
+    return kq, vq
+
+
+def time_quantize(torch, qc, kq, vq, zero, kb, vb, reps=10):
+    """Quantize-append of the whole quantize workload into `qc` (K kb bits, V vb
+    bits): mean time over `reps` calls after 3 untimed ones, Mtokens/s, HBM GB/s."""
+    st = torch.cuda.current_stream()
+    for _ in range(3):
+        qc.append(kq, vq, zero)
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+    ev[0].record(st)
+    for i in range(reps):
+        qc.append(kq, vq, zero)
+        ev[i + 1].record(st)
+    torch.cuda.synchronize()
+    if qc.device_status() != 0:
+        raise RuntimeError("device status set by the quantize benchmark")
+    ms = float(np.mean([ev[i].elapsed_time(ev[i + 1]) for i in range(reps)]))
+    tokens = kq.shape[0] * kq.shape[2]
+    nbytes = 2 * kq.numel() * 2 + kq.shape[0] * HKV * kq.shape[2] * ((D * kb // 8 + 4) + (D * vb // 8 + 4))
+    return {"k_bits": kb, "v_bits": vb, "ms": ms, "value": tokens / (ms * 1e-3) / 1e6, "unit": "Mtokens/s",
+            "token_heads_per_s": tokens * HKV / (ms * 1e-3), "hbm_gbs": nbytes / (ms * 1e-3) / 1e9,
+            "algorithmic_bytes_per_launch": nbytes}
 
 
 def step_inputs(n_steps):
@@ -674,39 +773,19 @@ def run_gpu(args):
 
     # quantize throughput: batch 16 x 8192 new tokens x 8 KV heads at 3.5 bits (K3 / V4)
     del k_dev, v_dev
-    gq = synth.rng(SEED + 2, synth.STREAM_K)
-    qsk = torch.from_numpy(synth.channel_scales(SEED + 2, synth.STREAM_SCALE_K, HKV, D).astype(np.float32)).cuda()
-    qsv = torch.from_numpy(synth.channel_scales(SEED + 2, synth.STREAM_SCALE_V, HKV, D).astype(np.float32)).cuda()
-    kq = torch.empty(QB, HKV, QT, D, dtype=torch.float16, device="cuda")
-    vq = torch.empty_like(kq)
-    for b in range(QB):  # drawn on the host in slices to bound host memory
-        kq[b].copy_((torch.from_numpy(gq.standard_normal((HKV, QT, D), dtype=np.float32)).cuda()
-                     * qsk[:, None, :]).half())
-        vq[b].copy_((torch.from_numpy(gq.standard_normal((HKV, QT, D), dtype=np.float32)).cuda()
-                     * qsv[:, None, :]).half())
-    qc = TurboQuantKVCache(QB, HKV, HKV * 4, QT, bits=(KB, VB))
+    kq, vq = quantize_inputs(torch)
     zero = torch.zeros(QB, dtype=torch.int32, device="cuda")
-    for _ in range(3):
-        qc.append(kq, vq, zero)
-    torch.cuda.synchronize()
-    reps = 10
-    qe = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
-    qe[0].record(stream)
-    for i in range(reps):
-        qc.append(kq, vq, zero)
-        qe[i + 1].record(stream)
-    torch.cuda.synchronize()
-    q_ms = [qe[i].elapsed_time(qe[i + 1]) for i in range(reps)]
-    q_avg = float(np.mean(q_ms))
-    q_tokens = QB * QT
-    q_bytes = 2 * QB * HKV * QT * D * 2 + QB * HKV * QT * ((D * KB // 8 + 4) + (D * VB // 8 + 4))
-    if qc.device_status() != 0:
-        raise RuntimeError("device status set by the quantize benchmark")
-    del kq, vq, qc
+    quant = {}
+    for name, kb, vb in (("3.5", KB, VB), ("3", 3, 3), ("4", 4, 4)):
+        qc = TurboQuantKVCache(QB, HKV, HKV * 4, QT, bits=(kb, vb))
+        quant[name] = time_quantize(torch, qc, kq, vq, zero, kb, vb)
+        del qc
+    del kq, vq
     # the other decode workloads: asym (fp16 K + 4-bit V, B8, context 16384) and the
     # 3.5-bit Llama-3-8B-like layer (B1, context 4096; launch- and L2-bound)
     asym_ms, asym_bytes = time_plain_decode(torch, 8, 16384, True)
     small_ms, small_bytes = time_plain_decode(torch, 1, 4096, False, reps=200)
+    small_cold_ms, _ = time_plain_decode(torch, 1, 4096, False, reps=100, flush=True)
     i8_ms, i8_bytes, i8q_ms, i8q_bytes = time_int8(torch, lens0)
 
     peak, peak_kind = measured_peak()
@@ -728,12 +807,11 @@ def run_gpu(args):
                      "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "algorithmic_bytes_per_launch": dec_bytes, "avg_launch_ms": dec_avg_ms},
-        "quantize": {"value": q_tokens / (q_avg * 1e-3) / 1e6, "unit": "Mtokens/s",
-                     "token": "one (batch, position) with all 8 KV heads, K and V",
-                     "token_heads_per_s": q_tokens * HKV / (q_avg * 1e-3),
-                     "workload": "batch 16 x 8192 new tokens x 8 KV heads, K 3-bit / V 4-bit, lognormal channels",
-                     "ms": q_avg, "hbm_gbs": q_bytes / (q_avg * 1e-3) / 1e9,
-                     "frac": q_bytes / (q_avg * 1e-3) / 1e9 / peak},
+        "quantize": dict(quant["3.5"], frac=quant["3.5"]["hbm_gbs"] / peak,
+                         token="one (batch, position) with all 8 KV heads, K and V",
+                         workload="batch 16 x 8192 new tokens x 8 KV heads, N(0,1) x lognormal(0,1) channel "
+                                  "scales; 3.5 bits = K 3-bit / V 4-bit",
+                         widths={w: dict(quant[w], frac=quant[w]["hbm_gbs"] / peak) for w in ("3", "4", "3.5")}),
         "sparse_v": {"threshold": 1e-3, "ms": sparse_ms, "dense_ms": dec_avg_ms,
                      "value": decode_bytes(lens0 + sv_s + 1) / (sparse_ms * 1e-3) / 1e9, "unit": "GB/s",
                      "note": "same long-context decode call with V skipped for weights below 1e-3 of the running "
@@ -756,10 +834,11 @@ def run_gpu(args):
                              "d128, the long-context lengths",
                  "quantize_mtokens_s": QB * QT / (i8q_ms * 1e-3) / 1e6, "quantize_ms": i8q_ms,
                  "quantize_hbm_gbs": i8q_bytes / (i8q_ms * 1e-3) / 1e9},
-        "llama_layer": {"value": small_bytes / (small_ms * 1e-3) / 1e9, "unit": "GB/s", "ms": small_ms,
-                        "algorithmic_bytes_per_launch": small_bytes,
-                        "workload": "3.5-bit decode: B1, 32q/8kv, d128, context 4096, K3/V4 (launch-bound: "
-                                    "4 MB per call, inside L2)"},
+        "llama_layer": {"value": small_bytes / (small_cold_ms * 1e-3) / 1e9, "unit": "GB/s", "ms": small_cold_ms,
+                        "ms_l2_resident": small_ms, "algorithmic_bytes_per_launch": small_bytes,
+                        "workload": "3.5-bit decode: B1, 32q/8kv, d128, context 4096, K3/V4; ms after a 256 MB "
+                                    "write flushed L2 before each call (ms_l2_resident: back-to-back calls, the "
+                                    "4 MB cache stays in L2)"},
         "e2e": {"value": job_throughput(e2e_bytes, e2e_ms, world), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "clocks": clocks,
