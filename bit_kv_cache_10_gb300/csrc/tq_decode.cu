@@ -2,7 +2,7 @@
 // kernel and the dense contiguous split-K instantiations (the split kernel
 // itself is in tq_decode_split.cuh; its sparse-V and paged instantiations are in
 // tq_decode_sparse.cu, tq_decode_paged.cu and tq_decode_paged_sparse.cu).
-#include "tq_decode_split.cuh"
+#include "tq_decode_dispatch.cuh"
 
 namespace tq {
 namespace {

@@ -1,0 +1,615 @@
+// Split-K decode kernel with the scores and the V sums on the tensor cores,
+// for packed K (2, 3 or 4 bits) and packed 4-bit V.  Work list, staging ring,
+// partial slots and the merge are those of the float32 kernel
+// (tq_decode_split.cuh); only the arithmetic of a tile differs.
+//
+// Exact operands from lookups.  A float32 centroid c is the sum of two fp16
+// numbers, hi = RN16(c) and lo = RN16(c - hi), which together carry 22
+// significant bits; the same holds for the rotated query and for the softmax
+// weights.  Products of fp16 numbers are exact in float32, so
+//   sum_i q_i c_i = sum_i (q_hi + q_lo)_i (c_hi + c_lo)_i
+// is computed by mma.sync (f16 operands, float32 accumulation) to about 2^-21
+// relative, against the 2^-11 of a plain fp16 operand.  Centroids are
+// tabulated times 2^10 so that both halves are normal fp16 numbers.
+//
+// Tables.  Row e (256 bytes) of a shared table holds, for the code pair
+// e = code_a | code_b << bits, the pair (hi_a, hi_b) of fp16 halves 32 times
+// over in bytes [0, 128) and (lo_a, lo_b) 32 times over in bytes [128, 256):
+// lane l reads copy l, so the data-dependent 32-bit loads of a warp fall in 32
+// distinct banks, and the lo half is the same address plus 128.  Each load
+// returns one A-fragment register, so the fragments need no register moves.
+// The V table (256 rows) and the K table (2^(2 bits) rows) start at 64 KB
+// boundaries, so that an entry address is (e << 8) | (table + 4 l).
+//
+// Scores (tokens as M, coordinates as K, 8 columns as N = the G query heads'
+// rotated query in hi and in lo halves).  Lane (g, t) holds tokens g and g + 8
+// and coordinates 32 t .. 32 t + 31; chunk c of the MMA K dimension takes
+// coordinates 32 t + 4 c .. + 3 of every lane t, so each A register is one
+// pair lookup of two adjacent codes of one token.  Two MMAs per chunk (A hi and
+// A lo against [q hi | q lo]) accumulate into one fragment; column h plus
+// column h + 4 is head h's dot product.
+//
+// Softmax.  Lane (g, t) then owns token g + 8 (t >> 1) for heads 2 (t & 1) and
+// 2 (t & 1) + 1.  The V weight of a token is w = 2^(s - m) n_V; the running
+// maximum m of a head is raised (lazily, as in the float32 kernel) against
+// s + e_V + 1, e_V the binary exponent of n_V, so every weight stays below 2^8
+// and its fp16 hi and lo halves are exact.  The mass sums 2^(s - m) alone.
+//
+// V (coordinates as M, tokens as K, N = the weights in hi and lo halves).  Lane
+// (g, t) holds coordinates 16 g .. 16 g + 15 (M block b: rows 16 g + 2 b and
+// 16 g + 2 b + 1) and tokens 2 t, 2 t + 1, 2 t + 8, 2 t + 9; an A register
+// pairs the codes of two tokens at one coordinate, built from two code words
+// by nibble interleaving.  Hot rows read the fp16 ring (exact in fp16: one MMA
+// per block).  The cold sum is tabulated times 2^10, removed at the row exit.
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include "tq_decode_split.cuh"
+
+namespace tq {
+namespace {
+
+constexpr float kCentScale = 1024.0f;       // centroids are tabulated times 2^10
+constexpr float kCentUnscale = 1.0f / 1024.0f;
+
+template <int KB>
+struct MmaCfg {
+  using Stage = Cfg<KB, 4>;                  // K | K norms | V | V norms, with V rows padded:
+  static constexpr int kVPitch = 80;         // 64-byte records 80 bytes apart (conflict-free V code loads)
+  static constexpr int kVTile = kTile * kVPitch;
+  static constexpr int kBuf = Stage::kKTile + Stage::kKNorm + kVTile + kTile * 4;
+  static constexpr int kWarps = 12;
+  static constexpr int kThreads = kWarps * 32;
+  static constexpr int kTabAlign = 65536;
+  static constexpr int kTab = 65536 + (1 << (2 * KB)) * 256;  // V table | K table, rows of 256 bytes
+  static constexpr int kW16 = 2 * 4 * kTile * 2;  // per warp: fp16 weights [hi/lo][head][token]
+  static constexpr int kSmall = kWarps * kW16 + 4 * D * 4 /* rotated query */ + 4 * D * 4 /* combine */ +
+                                kWarps * 4 * 2 * 4 /* warp (m, l) */ + kWarps * 8 * 16 /* tile descriptors */ +
+                                (kMaxDecodeBatch + 1) * 8 + 34 * 8;
+  static constexpr int kWorst(int stages) { return kTab + kSmall + (kWarps + 1) * stages * kBuf + 1024; }
+  // the aligned table can leave a gap of up to kTabAlign - 1024 bytes before it, filled by the other buffers
+  static constexpr int kStages = kWorst(6) <= kSmemBudget ? 6 : kWorst(4) <= kSmemBudget ? 4 : kWorst(3) <= kSmemBudget ? 3 : 2;
+  static constexpr int kSmem = (kWorst(kStages) + 1023) / 1024 * 1024;
+  static_assert(kWorst(kStages) <= kSmemBudget, "shared memory budget");
+};
+
+// D += A B, m16n8k16, f16 operands, float32 accumulators (all four A registers).
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+               "{%0, %1, %2, %3};\n"
+               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+               : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// fp16 hi and lo halves of x (x = hi + lo to 22 significant bits).
+__device__ __forceinline__ void split_f16(float x, uint16_t& hi, uint16_t& lo) {
+  const __half h = __float2half_rn(x);
+  hi = __half_as_ushort(h);
+  lo = __half_as_ushort(__float2half_rn(fsub(x, __half2float(h))));
+}
+// Pair of fp16 halves as one register (a in the low half).
+__device__ __forceinline__ uint32_t pack16(uint16_t a, uint16_t b) {
+  return static_cast<uint32_t>(a) | (static_cast<uint32_t>(b) << 16);
+}
+// Table entry of a code pair: (hi_a, hi_b) in .x, (lo_a, lo_b) in .y (stored 128 bytes apart).
+__device__ __forceinline__ uint2 pair_entry(float ca, float cb) {
+  uint16_t ha, la, hb, lb;
+  split_f16(fmul(ca, kCentScale), ha, la);
+  split_f16(fmul(cb, kCentScale), hb, lb);
+  return make_uint2(pack16(ha, hb), pack16(la, lb));
+}
+
+// hi half (.x) and lo half (.y) of the table entry at addr.
+__device__ __forceinline__ uint2 lds_entry(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(v.x) : "r"(addr));
+  asm volatile("ld.shared.u32 %0, [%1+128];\n" : "=r"(v.y) : "r"(addr));
+  return v;
+}
+
+// Shared address of the K table entry of code pair J (bits 2 KB J .. of the
+// lane's window of 32 coordinates); kbase = K table + 4 lane.
+template <int KB, int J>
+__device__ __forceinline__ uint32_t k_pair_addr(const uint32_t* win, uint32_t kbase) {
+  if constexpr (KB == 4) {
+    return __byte_perm(win[J / 4], kbase, 0x7604 | ((J % 4) << 4));  // byte J of the window into byte 1
+  } else {
+    constexpr int kOff = 2 * KB * J, kW = kOff / 32, kBit = kOff % 32;
+    uint32_t x;
+    if constexpr (kBit + 2 * KB > 32) x = __funnelshift_r(win[kW], win[kW + 1], kBit - 8);
+    else if constexpr (kBit >= 8) x = win[kW] >> (kBit - 8);
+    else x = win[kW] << (8 - kBit);
+    return (x & (((1u << (2 * KB)) - 1u) << 8)) | kbase;
+  }
+}
+
+// Address of the V table entry whose index is byte K of x; vbase = V table + 4 lane.
+template <int K>
+__device__ __forceinline__ uint32_t v_pair_addr(uint32_t x, uint32_t vbase) {
+  return __byte_perm(x, vbase, 0x7604 | (K << 4));
+}
+
+// Nibble interleave of two code words of tokens a and b: byte k of lo_pairs is
+// code_a | code_b << 4 of the even coordinate of byte k, hi_pairs the odd one.
+__device__ __forceinline__ void interleave(uint32_t wa, uint32_t wb, uint32_t& lo_pairs, uint32_t& hi_pairs) {
+  lo_pairs = (wa & 0x0F0F0F0Fu) | ((wb << 4) & 0xF0F0F0F0u);
+  hi_pairs = ((wa >> 4) & 0x0F0F0F0Fu) | (wb & 0xF0F0F0F0u);
+}
+
+template <int G, int KB, bool SPARSE, bool PAGED, bool MQ>
+__global__ void __launch_bounds__(MmaCfg<KB>::kThreads, 1) decode_mma_kernel(const DecodeParams p) {
+  using M = MmaCfg<KB>;
+  using C = Cfg<KB, 4>;
+  constexpr int S = M::kStages;
+  constexpr int NW = M::kWarps;
+  extern __shared__ __align__(16) uint8_t smem[];
+  const uint32_t s0 = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  SmemLayout lay;
+  lay.tab_lo = (s0 + M::kTabAlign - 1) & ~static_cast<uint32_t>(M::kTabAlign - 1);
+  lay.tab_hi = lay.tab_lo + M::kTab;
+  lay.cur = s0;
+  auto ptr = [&](uint32_t addr) { return smem + (addr - s0); };
+  const uint32_t tab = lay.tab_lo;
+  float* qs = reinterpret_cast<float*>(ptr(lay.take(4 * D * 4)));
+  float* comb = reinterpret_cast<float*>(ptr(lay.take(4 * D * 4)));
+  float* wml = reinterpret_cast<float*>(ptr(lay.take(NW * 4 * 2 * 4)));
+  int4* descs_all = reinterpret_cast<int4*>(ptr(lay.take(NW * 8 * 16)));
+  long long* prefix = reinterpret_cast<long long*>(ptr(lay.take((kMaxDecodeBatch + 1) * 8)));
+  long long* scan = reinterpret_cast<long long*>(ptr(lay.take(34 * 8)));
+  const uint32_t w16_all = lay.take(NW * M::kW16);
+
+  asm volatile("griddepcontrol.launch_dependents;\n");
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const uint32_t vbase = tab + 4u * lane;
+  const uint32_t kbase = tab + 65536u + 4u * lane;
+
+  // tables (from the parameters only): entry e, copy c
+  for (int i = tid; i < 256 * 32; i += M::kThreads) {
+    const int e = i >> 5, c = i & 31;
+    uint2 v = pair_entry(p.v_cent[e & 15], p.v_cent[e >> 4]);
+    *reinterpret_cast<uint32_t*>(ptr(tab + (e << 8) + 4 * c)) = v.x;
+    *reinterpret_cast<uint32_t*>(ptr(tab + (e << 8) + 128 + 4 * c)) = v.y;
+    if (e < (1 << (2 * KB))) {
+      v = pair_entry(p.k_cent[e & ((1 << KB) - 1)], p.k_cent[e >> KB]);
+      *reinterpret_cast<uint32_t*>(ptr(tab + 65536 + (e << 8) + 4 * c)) = v.x;
+      *reinterpret_cast<uint32_t*>(ptr(tab + 65536 + (e << 8) + 128 + 4 * c)) = v.y;
+    }
+  }
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  if (blockIdx.x == 0 && tid == 0 && p.status != nullptr) {
+    for (int b = 0; b < p.batch / p.nq; ++b) {
+      const int len = p.seq_lens[b];
+      if (len < 0 || len > p.cap || len > p.max_seq_len) {
+        atomicOr(p.status, TQ_DEV_ERR_SEQ_LEN);
+        break;
+      }
+    }
+  }
+  tile_prefix<M::kThreads, MQ>(p, prefix, scan);  // synchronizes (the tables too)
+  const long long total = prefix[p.batch];
+
+  uint32_t ring = 0;
+  for (int w = 0; w < NW; ++w) {
+    const uint32_t a = lay.take(S * M::kBuf);
+    if (w == warp) ring = a;
+  }
+  if (lay.cur > s0 + static_cast<uint32_t>(M::kSmem)) {  // cannot happen within the static budget
+    if (tid == 0 && p.status != nullptr) atomicOr(p.status, TQ_DEV_ERR_LAYOUT);
+    return;
+  }
+  uint8_t* const wring = ptr(ring);
+  const uint32_t w16 = w16_all + static_cast<uint32_t>(warp * M::kW16);
+  int4* descs = descs_all + warp * 8;
+
+  // softmax role of the lane: token tau, heads h0 and h0 + 1
+  const int tau = g + 8 * (t >> 1);
+  const int h0 = 2 * (t & 1);
+  // K-phase window offset of the lane within a token record, V-phase record offset
+  constexpr int kKRec = KB * 16;
+  const uint32_t k_win = static_cast<uint32_t>(4 * KB * t);  // bytes: 32 coordinates of KB bits
+  const uint32_t v_win = static_cast<uint32_t>(8 * g);
+  uint32_t qb[16];   // B fragments of the scores: [q hi | q lo] of the lane's (head, half), 8 chunks
+  float sc[2];       // log2-domain score scale of heads h0, h0 + 1 (rotation, centroid and query scales)
+  int cur_b = -1, cur_h = -1;
+
+  const long long t0 = total * blockIdx.x / p.grid, t1 = total * (blockIdx.x + 1) / p.grid;
+  if (t0 >= t1) return;
+  const int my_n = static_cast<int>((t1 - t0 - warp + NW - 1) / NW);
+  int j_issue = 0, j = 0;
+  Cursor cur;
+  TileBlocks tb{0, 0};
+  if (my_n > 0) {
+    cur = cursor_at<MQ>(p, prefix, t0 + warp);
+    if constexpr (PAGED) tb = load_tile_blocks(p, cache_seq<MQ>(p, cur.b), cursor_t_begin(cur), cursor_n_valid(cur));
+  }
+  auto issue = [&]() {
+    if (j_issue < my_n) {
+      const bool hot = cur.x >= cur.tc;
+      const int t_begin = cursor_t_begin(cur);
+      const int n_valid = cursor_n_valid(cur);
+      const int cb = cache_seq<MQ>(p, cur.b);
+      const int staged = stage_tile<KB, 4, PAGED, M::kVPitch>(p, cb, cur.h, hot, t_begin, n_valid, tb,
+                                                              ring + static_cast<uint32_t>((j_issue % S) * M::kBuf), lane);
+      if (lane == 0) descs[j_issue % S] = make_int4(cb, cur.h | (hot << 16), t_begin, staged);
+      cursor_advance<MQ>(p, cur, NW);
+      if constexpr (PAGED)
+        if (j_issue + 1 < my_n) tb = load_tile_blocks(p, cache_seq<MQ>(p, cur.b), cursor_t_begin(cur), cursor_n_valid(cur));
+    }
+    cp_async_commit();
+    ++j_issue;
+  };
+#pragma unroll
+  for (int st = 0; st < S - 1; ++st) issue();
+
+  long long seg = t0;
+  while (seg < t1) {
+    const TileInfo si = tile_info<MQ>(p, prefix, seg);
+    const long long seg_end = si.row_end < t1 ? si.row_end : t1;
+    if (si.b != cur_b || si.h != cur_h) {
+      // rotated query of the G heads, H D q (unnormalized), in qs
+      __syncthreads();
+      if (tid < D) {
+        const bool neg = sign_negative(p.seed, p.layer, si.h, tid);
+#pragma unroll
+        for (int jj = 0; jj < G; ++jj) {
+          const float x = half_bits_to_float(p.q[(static_cast<int64_t>(si.b) * p.hq + si.h * G + jj) * D + tid]);
+          qs[jj * D + tid] = neg ? -x : x;
+        }
+      }
+      __syncthreads();
+#pragma unroll
+      for (int st = 1; st < D; st *= 2) {
+        if (tid < D && (tid & st) == 0) {
+#pragma unroll
+          for (int jj = 0; jj < G; ++jj) {
+            const float a = qs[jj * D + tid], c = qs[jj * D + tid + st];
+            qs[jj * D + tid] = fadd(a, c);
+            qs[jj * D + tid + st] = fsub(a, c);
+          }
+        }
+        __syncthreads();
+      }
+      // lane (g, t): head g & 3, half g >> 2, coordinates 32 t .. 32 t + 31, scaled by a
+      // power of two that puts the head's largest |value| in [2^13, 2^14)
+      const int hh = g & 3;
+      float amax = 0.0f;
+      if (hh < G)
+        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(qs[hh * D + 32 * t + i]));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+      const int ex = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);  // biased exponent, 0 for zero
+      const float qscale = ex == 0 ? 1.0f : __uint_as_float(static_cast<uint32_t>(127 + 13 + 127 - ex) << 23);
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+#pragma unroll
+        for (int jp = 0; jp < 2; ++jp) {
+          uint32_t v = 0u;
+          if (hh < G) {
+            const float x0 = fmul(qs[hh * D + 32 * t + 4 * c + 2 * jp], qscale);
+            const float x1 = fmul(qs[hh * D + 32 * t + 4 * c + 2 * jp + 1], qscale);
+            uint16_t a0, l0, a1, l1;
+            split_f16(x0, a0, l0);
+            split_f16(x1, a1, l1);
+            v = (g >> 2) == 0 ? pack16(a0, a1) : pack16(l0, l1);
+          }
+          qb[2 * c + jp] = v;
+        }
+      // the scale of head h sits in lane 4 h (half 0, t = 0)
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const float qsh = __shfl_sync(0xffffffffu, qscale, 4 * ((h0 + i) & 3));
+        sc[i] = kLog2e / static_cast<float>(D) * kCentUnscale / qsh;
+      }
+      cur_b = si.b;
+      cur_h = si.h;
+    }
+
+    float m_own[2] = {-INFINITY, -INFINITY}, lsum[2] = {0.0f, 0.0f};
+    float ms_own[2] = {-INFINITY, -INFINITY};  // sparse V: running maximum of the scores alone
+    float acc[8][4];
+#pragma unroll
+    for (int mb = 0; mb < 8; ++mb)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc[mb][k] = 0.0f;
+
+    while (j < my_n && t0 + warp + static_cast<long long>(NW) * j < seg_end) {
+      issue();
+      cp_async_wait<S - 1>();
+      __syncwarp();
+      const int4 dsc = descs[j % S];
+      const int tb_b = dsc.x, tb_h = dsc.y & 0xFFFF, n_valid = dsc.w, t_begin = dsc.z;
+      const bool hot = (dsc.y >> 16) != 0;
+      const uint8_t* tbp = wring + (j % S) * M::kBuf;
+      const uint32_t tbs = ring + static_cast<uint32_t>((j % S) * M::kBuf);
+
+      // ---- scores on the tensor cores (the A hi and A lo products in two chains)
+      float sacc[4] = {0.0f, 0.0f, 0.0f, 0.0f}, sacl[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      {
+        constexpr int kWords = KB;  // 32 coordinates x KB bits
+        uint32_t wg[kWords + 1], wh[kWords + 1];
+        const uint32_t ag = tbs + static_cast<uint32_t>(g * kKRec) + k_win;
+        const uint32_t ah = ag + static_cast<uint32_t>(8 * kKRec);
+        if constexpr (KB == 4) {  // vector loads sized to the window keep the warp's loads conflict free
+          const uint4 a = lds128<0>(ag), b = lds128<0>(ah);
+          wg[0] = a.x; wg[1] = a.y; wg[2] = a.z; wg[3] = a.w;
+          wh[0] = b.x; wh[1] = b.y; wh[2] = b.z; wh[3] = b.w;
+        } else if constexpr (KB == 2) {
+          const uint2 a = lds64u<0>(ag), b = lds64u<0>(ah);
+          wg[0] = a.x; wg[1] = a.y;
+          wh[0] = b.x; wh[1] = b.y;
+        } else {
+#pragma unroll
+          for (int i = 0; i < kWords; ++i) {
+            wg[i] = lds32<0>(ag + 4u * i);
+            wh[i] = lds32<0>(ah + 4u * i);
+          }
+        }
+        wg[kWords] = 0u;
+        wh[kWords] = 0u;
+        auto chunk = [&](auto C_) {
+          constexpr int c = decltype(C_)::value;
+          const uint2 e0 = lds_entry(k_pair_addr<KB, 2 * c>(wg, kbase));
+          const uint2 e1 = lds_entry(k_pair_addr<KB, 2 * c>(wh, kbase));
+          const uint2 e2 = lds_entry(k_pair_addr<KB, 2 * c + 1>(wg, kbase));
+          const uint2 e3 = lds_entry(k_pair_addr<KB, 2 * c + 1>(wh, kbase));
+          mma_f16(sacc, e0.x, e1.x, e2.x, e3.x, qb[2 * c], qb[2 * c + 1]);
+          mma_f16(sacl, e0.y, e1.y, e2.y, e3.y, qb[2 * c], qb[2 * c + 1]);
+        };
+        chunk(std::integral_constant<int, 0>{});
+        chunk(std::integral_constant<int, 1>{});
+        chunk(std::integral_constant<int, 2>{});
+        chunk(std::integral_constant<int, 3>{});
+        chunk(std::integral_constant<int, 4>{});
+        chunk(std::integral_constant<int, 5>{});
+        chunk(std::integral_constant<int, 6>{});
+        chunk(std::integral_constant<int, 7>{});
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sacc[i] = fadd(sacc[i], sacl[i]);
+      }
+      // hi and lo columns of the lane's token: lanes t < 2 hold the hi columns of
+      // token g, lanes t >= 2 the lo columns of token g + 8; exchange with t ^ 2
+      float dot[2];
+      {
+        const bool lo_lane = (t >> 1) != 0;
+        const float s0v = lo_lane ? sacc[0] : sacc[2], s1v = lo_lane ? sacc[1] : sacc[3];
+        const float r0 = __shfl_xor_sync(0xffffffffu, s0v, 2), r1 = __shfl_xor_sync(0xffffffffu, s1v, 2);
+        dot[0] = fadd(lo_lane ? sacc[2] : sacc[0], r0);
+        dot[1] = fadd(lo_lane ? sacc[3] : sacc[1], r1);
+      }
+
+      // ---- online softmax (base 2); weights below 2^8 (see the header)
+      const float* knorm = reinterpret_cast<const float*>(tbp + C::kKTile);
+      const float* vnorm = reinterpret_cast<const float*>(tbp + C::kKTile + C::kKNorm + M::kVTile);
+      const bool tok_ok = tau < n_valid;
+      const float nk = knorm[tau];
+      const float nv = hot ? 1.0f : vnorm[tau];
+      int ev = static_cast<int>((__float_as_uint(nv) >> 23) & 0xFFu) - 127;
+      ev = ev < -64 ? -64 : ev;
+      const float evf = static_cast<float>(ev + 1);
+      float sj[2];
+      bool ok[2];
+      bool bump = false;
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        ok[i] = tok_ok && h0 + i < G;
+        sj[i] = ok[i] ? fmul(fmul(dot[i], sc[i]), nk) : -INFINITY;  // staged data of masked rows is stale
+        bump |= ok[i] && fadd(sj[i], evf) > fadd(m_own[i], kLazy);
+      }
+      if (__any_sync(0xffffffffu, bump)) {
+        float alpha[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          float tm = ok[i] ? fadd(sj[i], evf) : -INFINITY;
+          tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 2));
+          tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 4));
+          tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 8));
+          tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 16));
+          const float mn = fmaxf(m_own[i], tm);
+          alpha[i] = mn == -INFINITY ? 1.0f : ex2_approx(fsub(m_own[i], mn));  // 0 for the row's first tile
+          lsum[i] = fmul(lsum[i], alpha[i]);
+          m_own[i] = mn;
+        }
+        // accumulator columns 2 t, 2 t + 1 are heads h0, h0 + 1 (hi or lo half)
+#pragma unroll
+        for (int mb = 0; mb < 8; ++mb) {
+          acc[mb][0] = fmul(acc[mb][0], alpha[0]);
+          acc[mb][1] = fmul(acc[mb][1], alpha[1]);
+          acc[mb][2] = fmul(acc[mb][2], alpha[0]);
+          acc[mb][3] = fmul(acc[mb][3], alpha[1]);
+        }
+      }
+      if constexpr (SPARSE) {
+        // a token whose weight relative to the running score maximum is below tau has a
+        // normalized weight below tau: its V is skipped (its weight still counts in the mass)
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          float tm = sj[i];
+          tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 2));
+          tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 4));
+          tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 8));
+          tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 16));
+          ms_own[i] = fmaxf(ms_own[i], tm);
+        }
+      }
+      bool any_w = false;
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        float pj = ok[i] ? ex2_approx(fsub(sj[i], m_own[i])) : 0.0f;
+        lsum[i] = fadd(lsum[i], pj);
+        float w = ok[i] ? fmul(pj, nv) : 0.0f;  // the staged norm of a masked row is stale
+        if (SPARSE && ok[i] && ex2_approx(fsub(sj[i], ms_own[i])) < p.sparse_tau) w = 0.0f;
+        any_w |= w != 0.0f;
+        uint16_t wh16, wl16;
+        split_f16(w, wh16, wl16);
+        const uint32_t o = static_cast<uint32_t>(((h0 + i) * kTile + tau) * 2);
+        asm volatile("st.shared.u16 [%0], %1;\n" ::"r"(w16 + o), "h"(wh16));
+        asm volatile("st.shared.u16 [%0], %1;\n" ::"r"(w16 + 4u * kTile * 2u + o), "h"(wl16));
+      }
+      const bool do_v = SPARSE ? __any_sync(0xffffffffu, any_w) : true;
+      __syncwarp();
+
+      // ---- V on the tensor cores: B = the weights of column g (head g & 3, half g >> 2)
+      if (do_v) {
+        const uint32_t wb = w16 + static_cast<uint32_t>(((g >> 2) * 4 + (g & 3)) * kTile * 2);
+        const uint32_t b0 = lds32<0>(wb + 4u * t), b1 = lds32<0>(wb + 4u * t + 16u);
+        if (!hot) {
+          const uint32_t vt = tbs + static_cast<uint32_t>(C::kKTile + C::kKNorm) + v_win;
+          constexpr int P = M::kVPitch;
+          const uint2 wa = lds64u<0>(vt + static_cast<uint32_t>((2 * t) * P));
+          const uint2 wbw = lds64u<0>(vt + static_cast<uint32_t>((2 * t + 1) * P));
+          const uint2 wc = lds64u<0>(vt + static_cast<uint32_t>((2 * t + 8) * P));
+          const uint2 wd = lds64u<0>(vt + static_cast<uint32_t>((2 * t + 9) * P));
+          uint32_t ab_lo[2], ab_hi[2], cd_lo[2], cd_hi[2];
+          interleave(wa.x, wbw.x, ab_lo[0], ab_hi[0]);
+          interleave(wa.y, wbw.y, ab_lo[1], ab_hi[1]);
+          interleave(wc.x, wd.x, cd_lo[0], cd_hi[0]);
+          interleave(wc.y, wd.y, cd_lo[1], cd_hi[1]);
+          auto vblock = [&](auto B_) {
+            constexpr int mb = decltype(B_)::value, w = mb >> 2, k = mb & 3;
+            const uint2 e0 = lds_entry(v_pair_addr<k>(ab_lo[w], vbase));
+            const uint2 e1 = lds_entry(v_pair_addr<k>(ab_hi[w], vbase));
+            const uint2 e2 = lds_entry(v_pair_addr<k>(cd_lo[w], vbase));
+            const uint2 e3 = lds_entry(v_pair_addr<k>(cd_hi[w], vbase));
+            mma_f16(acc[mb], e0.x, e1.x, e2.x, e3.x, b0, b1);
+            mma_f16(acc[mb], e0.y, e1.y, e2.y, e3.y, b0, b1);
+          };
+          vblock(std::integral_constant<int, 0>{});
+          vblock(std::integral_constant<int, 1>{});
+          vblock(std::integral_constant<int, 2>{});
+          vblock(std::integral_constant<int, 3>{});
+          vblock(std::integral_constant<int, 4>{});
+          vblock(std::integral_constant<int, 5>{});
+          vblock(std::integral_constant<int, 6>{});
+          vblock(std::integral_constant<int, 7>{});
+        } else {
+          // hot row: the fp16 ring (exact operands), coordinates 16 g .. 16 g + 15 of
+          // tokens 2 t, 2 t + 1, 2 t + 8, 2 t + 9 (zeros past the tile's tokens)
+          uint4 x[4][2];
+          const int tk[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            x[u][0] = make_uint4(0u, 0u, 0u, 0u);
+            x[u][1] = make_uint4(0u, 0u, 0u, 0u);
+            if (tk[u] < n_valid) {
+              const int pos = t_begin + tk[u];
+              const uint4* src = reinterpret_cast<const uint4*>(
+                  p.v_ring + ((static_cast<int64_t>(tb_b) * p.hkv + tb_h) * p.hot + pos % p.hot) * D + 16 * g);
+              x[u][0] = src[0];
+              x[u][1] = src[1];
+            }
+          }
+          auto word = [&](int u, int i) {
+            const uint4& q4 = x[u][i >> 2];
+            return (i & 3) == 0 ? q4.x : (i & 3) == 1 ? q4.y : (i & 3) == 2 ? q4.z : q4.w;
+          };
+#pragma unroll
+          for (int mb = 0; mb < 8; ++mb) {
+            const uint32_t a0 = __byte_perm(word(0, mb), word(1, mb), 0x5410);
+            const uint32_t a1 = __byte_perm(word(0, mb), word(1, mb), 0x7632);
+            const uint32_t a2 = __byte_perm(word(2, mb), word(3, mb), 0x5410);
+            const uint32_t a3 = __byte_perm(word(2, mb), word(3, mb), 0x7632);
+            mma_f16(acc[mb], a0, a1, a2, a3, b0, b1);
+          }
+        }
+      }
+      __syncwarp();
+      ++j;
+    }
+
+    // ---- leave the row: hi + lo halves, lanes -> warp -> CTA, one partial per (CTA, row)
+    for (int i = tid; i < G * D; i += M::kThreads) comb[i] = 0.0f;
+    // lanes t < 2 keep head 2 t + (k & 1) at coordinate 16 g + 2 mb + (k >> 1)
+#pragma unroll
+    for (int mb = 0; mb < 8; ++mb)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc[mb][k] = fadd(acc[mb][k], __shfl_xor_sync(0xffffffffu, acc[mb][k], 2));
+    float lw[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      float l = lsum[i];
+      l = fadd(l, __shfl_xor_sync(0xffffffffu, l, 2));
+      l = fadd(l, __shfl_xor_sync(0xffffffffu, l, 4));
+      l = fadd(l, __shfl_xor_sync(0xffffffffu, l, 8));
+      l = fadd(l, __shfl_xor_sync(0xffffffffu, l, 16));
+      lw[i] = l;
+    }
+    if (lane < 2) {  // lane t (g = 0) holds heads 2 t, 2 t + 1
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+        if (h0 + i < G) {
+          wml[(warp * 4 + h0 + i) * 2] = m_own[i];
+          wml[(warp * 4 + h0 + i) * 2 + 1] = lw[i];
+        }
+    }
+    __syncthreads();
+    float sc2[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int hd = (h0 + i) & 3;
+      float mm = -INFINITY;
+      if (hd < G)
+#pragma unroll
+        for (int w = 0; w < NW; ++w) mm = fmaxf(mm, wml[(w * 4 + hd) * 2]);
+      sc2[i] = m_own[i] == -INFINITY ? 0.0f : exp2f(m_own[i] - mm);
+    }
+    for (int w = 0; w < NW; ++w) {
+      if (warp == w && t < 2) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          if (h0 + i >= G || m_own[i] == -INFINITY) continue;
+          float* c2 = comb + (h0 + i) * D + 16 * g;
+#pragma unroll
+          for (int mb = 0; mb < 8; ++mb) {
+            c2[2 * mb] = fadd(c2[2 * mb], fmul(acc[mb][i], sc2[i]));
+            c2[2 * mb + 1] = fadd(c2[2 * mb + 1], fmul(acc[mb][2 + i], sc2[i]));
+          }
+        }
+      }
+      __syncthreads();
+    }
+    const long long slot = static_cast<long long>(blockIdx.x) + si.row;
+    const float unscale = si.hot ? 1.0f : kCentUnscale;  // cold sums carry the table scale
+    for (int i = tid; i < G * D; i += M::kThreads) p.ws_acc[slot * G * D + i] = fmul(comb[i], unscale);
+    if (tid < G) {
+      float mm = -INFINITY, ll = 0.0f;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) mm = fmaxf(mm, wml[(w * 4 + tid) * 2]);
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        const float mwv = wml[(w * 4 + tid) * 2];
+        if (mwv != -INFINITY) ll = ffma(wml[(w * 4 + tid) * 2 + 1], exp2f(mwv - mm), ll);
+      }
+      p.ws_ml[(slot * G + tid) * 2] = mm;
+      p.ws_ml[(slot * G + tid) * 2 + 1] = ll;
+    }
+    __syncthreads();
+    seg = seg_end;
+  }
+  cp_async_wait<0>();
+}
+
+template <int G, int KB, bool SPARSE, bool PAGED, bool MQ>
+tq_status launch_mma(const DecodeParams& p, cudaStream_t stream) {
+  using M = MmaCfg<KB>;
+  auto kern = decode_mma_kernel<G, KB, SPARSE, PAGED, MQ>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, M::kSmem) != cudaSuccess)
+    return TQ_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.grid);
+  cfg.blockDim = dim3(M::kThreads);
+  cfg.dynamicSmemBytes = M::kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return TQ_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace tq

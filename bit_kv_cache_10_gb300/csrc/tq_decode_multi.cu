@@ -1,7 +1,7 @@
 // Instantiations of the split-K kernel for several query tokens per sequence
 // (multi-query attention), contiguous layout, dense V; a translation unit of
 // their own so that the variants compile in parallel.
-#include "tq_decode_split.cuh"
+#include "tq_decode_dispatch.cuh"
 
 namespace tq {
 

@@ -1,6 +1,6 @@
 // Instantiations of the split-K kernel for several query tokens per sequence
 // (multi-query attention), paged layout, dense V.
-#include "tq_decode_split.cuh"
+#include "tq_decode_dispatch.cuh"
 
 namespace tq {
 

@@ -1,7 +1,7 @@
 // Paged-layout (block table) instantiations of the split-K decode kernel with
 // sparse V; a translation unit of their own so that the variants compile in
 // parallel.
-#include "tq_decode_split.cuh"
+#include "tq_decode_dispatch.cuh"
 
 namespace tq {
 

@@ -1,6 +1,6 @@
 // Sparse-V instantiations of the split-K decode kernel (contiguous layout), a
 // translation unit of their own so that the variants compile in parallel.
-#include "tq_decode_split.cuh"
+#include "tq_decode_dispatch.cuh"
 
 namespace tq {
 

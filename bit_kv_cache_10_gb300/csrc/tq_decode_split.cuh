@@ -532,10 +532,11 @@ __device__ __forceinline__ TileBlocks load_tile_blocks(const DecodeParams& p, in
 // (blocks hold at least one tile); a hot tile (K only) that straddles a block
 // boundary is copied token by token.  The common case (a full tile inside one
 // valid block) takes one branch; the others share the second.
-template <int KB, int VB>
+template <int KB, int VB, int VPITCH>
 __device__ __forceinline__ int stage_tile_paged(const DecodeParams& p, int h, bool hot, int t_begin, int n_valid,
                                              TileBlocks tb, uint32_t buf, int lane) {
   using C = Cfg<KB, VB>;
+  constexpr int kVTileP = kTile * VPITCH;
   const int sh = p.map.shift;
   const unsigned nb = static_cast<unsigned>(p.map.num_blocks);
   const bool in_pool = static_cast<unsigned>(tb.first) < nb && static_cast<unsigned>(tb.last) < nb;
@@ -547,7 +548,7 @@ __device__ __forceinline__ int stage_tile_paged(const DecodeParams& p, int h, bo
   long long rn = row0 + (lane & 15);  // norm row of the lane's token
   if (in_pool && one_block && n_valid == kTile) {
     copy_full_pitched<C::kKRow, C::kKPitch>(buf, kbase + row0 * C::kKRow, lane);
-    if (!hot) copy_full<C::kVTile>(vbuf, reinterpret_cast<const uint8_t*>(p.v_words) + row0 * (VB * 16), lane);
+    if (!hot) copy_full_pitched<VB * 16, VPITCH>(vbuf, reinterpret_cast<const uint8_t*>(p.v_words) + row0 * (VB * 16), lane);
   } else {
     if (!in_pool) {  // outside the pool: nothing is staged, the tile is read as empty
       if (lane == 0 && p.status != nullptr) atomicOr(p.status, TQ_DEV_ERR_BLOCK);
@@ -562,7 +563,8 @@ __device__ __forceinline__ int stage_tile_paged(const DecodeParams& p, int h, bo
     }
     if (!hot) {  // cold tiles never straddle
       const uint8_t* vsrc = reinterpret_cast<const uint8_t*>(p.v_words) + row0 * (VB * 16);
-      for (int c = lane; c < n_valid * (C::kVRow / 16); c += 32) cp_async16s(vbuf + 16u * c, vsrc + 16 * c);
+      for (int c = lane; c < n_valid * (C::kVRow / 16); c += 32)
+        cp_async16s(vbuf + k_chunk_dst<VB * 16, VPITCH>(c), vsrc + 16 * c);
     }
     const int tn = t_begin + min(lane & 15, n_valid - 1);
     rn = p.map.in_block((tn >> sh) == blk0 ? tb.first : tb.last, h, tn);
@@ -571,18 +573,20 @@ __device__ __forceinline__ int stage_tile_paged(const DecodeParams& p, int h, bo
   const bool is_k = lane < 16;
   const bool want = nl < n_valid && (is_k ? !C::kFp16K : !hot);
   const float* nsrc = (is_k ? p.k_norms : p.v_norms) + rn;
-  const uint32_t ndst = (is_k ? buf + C::kKTile : vbuf + C::kVTile) + 4u * nl;
+  const uint32_t ndst = (is_k ? buf + C::kKTile : vbuf + kVTileP) + 4u * nl;
   if (want) cp_async4s(ndst, nsrc);
   return n_valid;
 }
 
 // Stages tile [t_begin, t_begin + n_valid) of (b, h) into buf; returns the
 // number of tokens the consumer may read.
-template <int KB, int VB, bool PAGED>
+// V rows are VPITCH bytes apart in the staged tile (VB * 16: contiguous).
+template <int KB, int VB, bool PAGED, int VPITCH = VB * 16>
 __device__ __forceinline__ int stage_tile(const DecodeParams& p, int b, int h, bool hot, int t_begin, int n_valid,
                                           TileBlocks tb, uint32_t buf, int lane) {
   using C = Cfg<KB, VB>;
-  if constexpr (PAGED) return stage_tile_paged<KB, VB>(p, h, hot, t_begin, n_valid, tb, buf, lane);
+  constexpr int kVTileP = kTile * VPITCH;
+  if constexpr (PAGED) return stage_tile_paged<KB, VB, VPITCH>(p, h, hot, t_begin, n_valid, tb, buf, lane);
   const int64_t row0 = (static_cast<int64_t>(b) * p.hkv + h) * p.cap + t_begin;
   const uint8_t* ksrc = C::kFp16K ? reinterpret_cast<const uint8_t*>(p.k_fp16 + row0 * D)
                                   : reinterpret_cast<const uint8_t*>(p.k_words + row0 * (C::kKBits * 4));
@@ -590,19 +594,20 @@ __device__ __forceinline__ int stage_tile(const DecodeParams& p, int b, int h, b
   const uint32_t vbuf = buf + C::kKTile + C::kKNorm;
   if (n_valid == kTile) {
     copy_full_pitched<C::kKRow, C::kKPitch>(buf, ksrc, lane);
-    if (!hot) copy_full<C::kVTile>(vbuf, vsrc, lane);
+    if (!hot) copy_full_pitched<VB * 16, VPITCH>(vbuf, vsrc, lane);
   } else {
     for (int c = lane; c < n_valid * (C::kKRow / 16); c += 32)
       cp_async16s(buf + k_chunk_dst<C::kKRow, C::kKPitch>(c), ksrc + 16 * c);
     if (!hot)
-      for (int c = lane; c < n_valid * (C::kVRow / 16); c += 32) cp_async16s(vbuf + 16u * c, vsrc + 16 * c);
+      for (int c = lane; c < n_valid * (C::kVRow / 16); c += 32)
+        cp_async16s(vbuf + k_chunk_dst<VB * 16, VPITCH>(c), vsrc + 16 * c);
   }
   // norms: lanes 0..15 the K norms, lanes 16..31 the V norms of the tile's tokens
   const int nl = lane & 15;
   const bool is_k = lane < 16;
   const bool want = nl < n_valid && (is_k ? !C::kFp16K : !hot);
   const float* nsrc = (is_k ? p.k_norms : p.v_norms) + row0 + nl;
-  const uint32_t ndst = (is_k ? buf + C::kKTile : vbuf + C::kVTile) + 4u * nl;
+  const uint32_t ndst = (is_k ? buf + C::kKTile : vbuf + kVTileP) + 4u * nl;
   if (want) cp_async4s(ndst, nsrc);
   return n_valid;
 }
@@ -1285,45 +1290,5 @@ tq_status launch_split(const DecodeParams& p, cudaStream_t stream) {
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 
-template <int G, int KB, bool SPARSE, bool PAGED, bool MQ>
-tq_status dispatch_vb(const DecodeParams& p, int vb, cudaStream_t s) {
-  switch (vb) {
-    case 2: return launch_split<G, KB, 2, SPARSE, PAGED, MQ>(p, s);
-    case 3: return launch_split<G, KB, 3, SPARSE, PAGED, MQ>(p, s);
-    default: return launch_split<G, KB, 4, SPARSE, PAGED, MQ>(p, s);
-  }
-}
-
-template <int G, bool SPARSE, bool PAGED, bool MQ>
-tq_status dispatch_kb(const DecodeParams& p, int kb, int vb, cudaStream_t s) {
-  switch (kb) {
-    case 8: return launch_split<G, 8, 8, SPARSE, PAGED, MQ>(p, s);  // int8 mode
-    case 2: return dispatch_vb<G, 2, SPARSE, PAGED, MQ>(p, vb, s);
-    case 3: return dispatch_vb<G, 3, SPARSE, PAGED, MQ>(p, vb, s);
-    case 4: return dispatch_vb<G, 4, SPARSE, PAGED, MQ>(p, vb, s);
-    default: return dispatch_vb<G, 16, SPARSE, PAGED, MQ>(p, vb, s);
-  }
-}
-
-// Split kernels of one variant (dense or sparse V, contiguous or paged, one or
-// several query tokens per sequence) for any group size and widths.
-template <bool SPARSE, bool PAGED, bool MQ = false>
-tq_status dispatch_split_variant(const DecodeParams& p, int g, int kb, int vb, cudaStream_t s) {
-  switch (g) {
-    case 1: return dispatch_kb<1, SPARSE, PAGED, MQ>(p, kb, vb, s);
-    case 2: return dispatch_kb<2, SPARSE, PAGED, MQ>(p, kb, vb, s);
-    default: return dispatch_kb<4, SPARSE, PAGED, MQ>(p, kb, vb, s);
-  }
-}
-
 }  // namespace
-
-// Split-K launches of the other variants, each in a translation unit of its own
-// (the dense contiguous one is in tq_decode.cu).
-tq_status dispatch_split_sparse(const DecodeParams& p, int g, int kb, int vb, cudaStream_t s);
-tq_status dispatch_split_paged(const DecodeParams& p, int g, int kb, int vb, cudaStream_t s);
-tq_status dispatch_split_paged_sparse(const DecodeParams& p, int g, int kb, int vb, cudaStream_t s);
-tq_status dispatch_split_multi(const DecodeParams& p, int g, int kb, int vb, cudaStream_t s);
-tq_status dispatch_split_multi_paged(const DecodeParams& p, int g, int kb, int vb, cudaStream_t s);
-
 }  // namespace tq
