@@ -22,12 +22,14 @@
 // boundaries, so that an entry address is (e << 8) | (table + 4 l).
 //
 // Scores (tokens as M, coordinates as K, 8 columns as N = the G query heads'
-// rotated query in hi and in lo halves).  Lane (g, t) holds tokens g and g + 8
-// and coordinates 32 t .. 32 t + 31; chunk c of the MMA K dimension takes
-// coordinates 32 t + 4 c .. + 3 of every lane t, so each A register is one
-// pair lookup of two adjacent codes of one token.  Two MMAs per chunk (A hi and
-// A lo against [q hi | q lo]) accumulate into one fragment; column h plus
-// column h + 4 is head h's dot product.
+// rotated query in hi and in lo halves).  An MMA covers 8 tokens: row g holds
+// the hi halves of token g's centroids and row g + 8 the lo halves, so that one
+// 64-bit load of a K entry (hi pair, lo pair) fills an aligned register pair of
+// the A fragment; row g plus row g + 8 is the token's dot product.  Lane (g, t)
+// holds coordinates 32 t .. 32 t + 31; chunk c of the MMA K dimension takes
+// coordinates 32 t + 4 c .. + 3 of every lane t.  Column h plus column h + 4
+// is head h.  The K table keeps (hi pair, lo pair) entries 16 times over (one
+// copy per lane of a half-warp, rows of 256 bytes).
 //
 // Softmax.  Lane (g, t) then owns token g + 8 (t >> 1) for heads 2 (t & 1) and
 // 2 (t & 1) + 1.  The V weight of a token is w = 2^(s - m) n_V; the running
@@ -101,6 +103,12 @@ __device__ __forceinline__ uint2 pair_entry(float ca, float cb) {
   return make_uint2(pack16(ha, hb), pack16(la, lb));
 }
 
+__device__ __forceinline__ uint2 lds64a(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];\n" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+
 // hi half (.x) and lo half (.y) of the table entry at addr.
 __device__ __forceinline__ uint2 lds_entry(uint32_t addr) {
   uint2 v;
@@ -110,7 +118,7 @@ __device__ __forceinline__ uint2 lds_entry(uint32_t addr) {
 }
 
 // Shared address of the K table entry of code pair J (bits 2 KB J .. of the
-// lane's window of 32 coordinates); kbase = K table + 4 lane.
+// lane's window of 32 coordinates); kbase = K table + 8 (lane mod 16).
 template <int KB, int J>
 __device__ __forceinline__ uint32_t k_pair_addr(const uint32_t* win, uint32_t kbase) {
   if constexpr (KB == 4) {
@@ -164,7 +172,7 @@ __global__ void __launch_bounds__(MmaCfg<KB>::kThreads, 1) decode_mma_kernel(con
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
   const uint32_t vbase = tab + 4u * lane;
-  const uint32_t kbase = tab + 65536u + 4u * lane;
+  const uint32_t kbase = tab + 65536u + 8u * (lane & 15);
 
   // tables (from the parameters only): entry e, copy c
   for (int i = tid; i < 256 * 32; i += M::kThreads) {
@@ -172,11 +180,9 @@ __global__ void __launch_bounds__(MmaCfg<KB>::kThreads, 1) decode_mma_kernel(con
     uint2 v = pair_entry(p.v_cent[e & 15], p.v_cent[e >> 4]);
     *reinterpret_cast<uint32_t*>(ptr(tab + (e << 8) + 4 * c)) = v.x;
     *reinterpret_cast<uint32_t*>(ptr(tab + (e << 8) + 128 + 4 * c)) = v.y;
-    if (e < (1 << (2 * KB))) {
-      v = pair_entry(p.k_cent[e & ((1 << KB) - 1)], p.k_cent[e >> KB]);
-      *reinterpret_cast<uint32_t*>(ptr(tab + 65536 + (e << 8) + 4 * c)) = v.x;
-      *reinterpret_cast<uint32_t*>(ptr(tab + 65536 + (e << 8) + 128 + 4 * c)) = v.y;
-    }
+    if (e < (1 << (2 * KB)) && c < kCopies)
+      *reinterpret_cast<uint2*>(ptr(tab + 65536 + (e << 8) + 8 * c)) =
+          pair_entry(p.k_cent[e & ((1 << KB) - 1)], p.k_cent[e >> KB]);
   }
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
   if (blockIdx.x == 0 && tid == 0 && p.status != nullptr) {
@@ -325,8 +331,9 @@ __global__ void __launch_bounds__(MmaCfg<KB>::kThreads, 1) decode_mma_kernel(con
       const uint8_t* tbp = wring + (j % S) * M::kBuf;
       const uint32_t tbs = ring + static_cast<uint32_t>((j % S) * M::kBuf);
 
-      // ---- scores on the tensor cores (the A hi and A lo products in two chains)
-      float sacc[4] = {0.0f, 0.0f, 0.0f, 0.0f}, sacl[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      // ---- scores on the tensor cores: tokens 0..7 and 8..15 in two MMA chains,
+      // A row g = hi and row g + 8 = lo halves of the token's centroids
+      float dh[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
       {
         constexpr int kWords = KB;  // 32 coordinates x KB bits
         uint32_t wg[kWords + 1], wh[kWords + 1];
@@ -351,12 +358,12 @@ __global__ void __launch_bounds__(MmaCfg<KB>::kThreads, 1) decode_mma_kernel(con
         wh[kWords] = 0u;
         auto chunk = [&](auto C_) {
           constexpr int c = decltype(C_)::value;
-          const uint2 e0 = lds_entry(k_pair_addr<KB, 2 * c>(wg, kbase));
-          const uint2 e1 = lds_entry(k_pair_addr<KB, 2 * c>(wh, kbase));
-          const uint2 e2 = lds_entry(k_pair_addr<KB, 2 * c + 1>(wg, kbase));
-          const uint2 e3 = lds_entry(k_pair_addr<KB, 2 * c + 1>(wh, kbase));
-          mma_f16(sacc, e0.x, e1.x, e2.x, e3.x, qb[2 * c], qb[2 * c + 1]);
-          mma_f16(sacl, e0.y, e1.y, e2.y, e3.y, qb[2 * c], qb[2 * c + 1]);
+          const uint2 e0 = lds64a(k_pair_addr<KB, 2 * c>(wg, kbase));      // token g: (a0, a1)
+          const uint2 e2 = lds64a(k_pair_addr<KB, 2 * c + 1>(wg, kbase));  // token g: (a2, a3)
+          const uint2 e1 = lds64a(k_pair_addr<KB, 2 * c>(wh, kbase));      // token g + 8
+          const uint2 e3 = lds64a(k_pair_addr<KB, 2 * c + 1>(wh, kbase));
+          mma_f16(dh[0], e0.x, e0.y, e2.x, e2.y, qb[2 * c], qb[2 * c + 1]);
+          mma_f16(dh[1], e1.x, e1.y, e3.x, e3.y, qb[2 * c], qb[2 * c + 1]);
         };
         chunk(std::integral_constant<int, 0>{});
         chunk(std::integral_constant<int, 1>{});
@@ -366,9 +373,13 @@ __global__ void __launch_bounds__(MmaCfg<KB>::kThreads, 1) decode_mma_kernel(con
         chunk(std::integral_constant<int, 5>{});
         chunk(std::integral_constant<int, 6>{});
         chunk(std::integral_constant<int, 7>{});
-#pragma unroll
-        for (int i = 0; i < 4; ++i) sacc[i] = fadd(sacc[i], sacl[i]);
       }
+      // rows g (hi) + g + 8 (lo): columns 2 t, 2 t + 1 of token g (dh[0]) and g + 8 (dh[1])
+      float sacc[4];
+      sacc[0] = fadd(dh[0][0], dh[0][2]);
+      sacc[1] = fadd(dh[0][1], dh[0][3]);
+      sacc[2] = fadd(dh[1][0], dh[1][2]);
+      sacc[3] = fadd(dh[1][1], dh[1][3]);
       // hi and lo columns of the lane's token: lanes t < 2 hold the hi columns of
       // token g, lanes t >= 2 the lo columns of token g + 8; exchange with t ^ 2
       float dot[2];
