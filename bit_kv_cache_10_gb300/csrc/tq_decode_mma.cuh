@@ -66,7 +66,7 @@ struct MmaCfg {
   static constexpr int kTabAlign = 65536;
   static constexpr int kTab = 65536 + (1 << (2 * KB)) * 256;  // V table | K table, rows of 256 bytes
   static constexpr int kW16 = 2 * 4 * kTile * 2;  // per warp: fp16 weights [hi/lo][head][token]
-  static constexpr int kSmall = kWarps * kW16 + 4 * D * 4 /* rotated query */ + 4 * D * 4 /* combine */ +
+  static constexpr int kSmall = kWarps * kW16 + 4 * 132 * 4 /* rotated query */ + 4 * 136 * 4 /* combine */ +
                                 kWarps * 4 * 2 * 4 /* warp (m, l) */ + kWarps * 8 * 16 /* tile descriptors */ +
                                 (kMaxDecodeBatch + 1) * 8 + 34 * 8;
   static constexpr int kWorst(int stages) { return kTab + kSmall + (kWarps + 1) * stages * kBuf + 1024; }
@@ -146,6 +146,12 @@ __device__ __forceinline__ void interleave(uint32_t wa, uint32_t wb, uint32_t& l
   hi_pairs = ((wa >> 4) & 0x0F0F0F0Fu) | (wb & 0xF0F0F0F0u);
 }
 
+// Padded shared layouts: the rotated query with one word after every 32
+// coordinates (the lanes' 32-coordinate windows of the four heads fall in
+// distinct banks), the row combine with one word after every 16 coordinates.
+__device__ __forceinline__ int qs_at(int h, int i) { return h * 132 + i + (i >> 5); }
+__device__ __forceinline__ int comb_at(int h, int i) { return h * 136 + i + (i >> 4); }
+
 template <int G, int KB, bool SPARSE, bool PAGED, bool MQ>
 __global__ void __launch_bounds__(MmaCfg<KB>::kThreads, 1) decode_mma_kernel(const DecodeParams p) {
   using M = MmaCfg<KB>;
@@ -160,8 +166,8 @@ __global__ void __launch_bounds__(MmaCfg<KB>::kThreads, 1) decode_mma_kernel(con
   lay.cur = s0;
   auto ptr = [&](uint32_t addr) { return smem + (addr - s0); };
   const uint32_t tab = lay.tab_lo;
-  float* qs = reinterpret_cast<float*>(ptr(lay.take(4 * D * 4)));
-  float* comb = reinterpret_cast<float*>(ptr(lay.take(4 * D * 4)));
+  float* qs = reinterpret_cast<float*>(ptr(lay.take(4 * 132 * 4)));
+  float* comb = reinterpret_cast<float*>(ptr(lay.take(4 * 136 * 4)));
   float* wml = reinterpret_cast<float*>(ptr(lay.take(NW * 4 * 2 * 4)));
   int4* descs_all = reinterpret_cast<int4*>(ptr(lay.take(NW * 8 * 16)));
   long long* prefix = reinterpret_cast<long long*>(ptr(lay.take((kMaxDecodeBatch + 1) * 8)));
@@ -239,6 +245,11 @@ __global__ void __launch_bounds__(MmaCfg<KB>::kThreads, 1) decode_mma_kernel(con
       const int cb = cache_seq<MQ>(p, cur.b);
       const int staged = stage_tile<KB, 4, PAGED, M::kVPitch>(p, cb, cur.h, hot, t_begin, n_valid, tb,
                                                               ring + static_cast<uint32_t>((j_issue % S) * M::kBuf), lane);
+      if (hot && (lane >> 1) < n_valid) {  // the fp16 ring rows of a hot tile into L1: 128 bytes per lane
+        const int pos = t_begin + (lane >> 1);
+        const uint16_t* row = p.v_ring + ((static_cast<int64_t>(cb) * p.hkv + cur.h) * p.hot + pos % p.hot) * D;
+        asm volatile("prefetch.global.L1 [%0];\n" ::"l"(row + 64 * (lane & 1)));
+      }
       if (lane == 0) descs[j_issue % S] = make_int4(cb, cur.h | (hot << 16), t_begin, staged);
       cursor_advance<MQ>(p, cur, NW);
       if constexpr (PAGED)
@@ -262,7 +273,7 @@ __global__ void __launch_bounds__(MmaCfg<KB>::kThreads, 1) decode_mma_kernel(con
 #pragma unroll
         for (int jj = 0; jj < G; ++jj) {
           const float x = half_bits_to_float(p.q[(static_cast<int64_t>(si.b) * p.hq + si.h * G + jj) * D + tid]);
-          qs[jj * D + tid] = neg ? -x : x;
+          qs[qs_at(jj, tid)] = neg ? -x : x;
         }
       }
       __syncthreads();
@@ -271,9 +282,9 @@ __global__ void __launch_bounds__(MmaCfg<KB>::kThreads, 1) decode_mma_kernel(con
         if (tid < D && (tid & st) == 0) {
 #pragma unroll
           for (int jj = 0; jj < G; ++jj) {
-            const float a = qs[jj * D + tid], c = qs[jj * D + tid + st];
-            qs[jj * D + tid] = fadd(a, c);
-            qs[jj * D + tid + st] = fsub(a, c);
+            const float a = qs[qs_at(jj, tid)], c = qs[qs_at(jj, tid + st)];
+            qs[qs_at(jj, tid)] = fadd(a, c);
+            qs[qs_at(jj, tid + st)] = fsub(a, c);
           }
         }
         __syncthreads();
@@ -283,7 +294,7 @@ __global__ void __launch_bounds__(MmaCfg<KB>::kThreads, 1) decode_mma_kernel(con
       const int hh = g & 3;
       float amax = 0.0f;
       if (hh < G)
-        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(qs[hh * D + 32 * t + i]));
+        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(qs[qs_at(hh, 32 * t + i)]));
       amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
       amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
       const int ex = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);  // biased exponent, 0 for zero
@@ -294,8 +305,8 @@ __global__ void __launch_bounds__(MmaCfg<KB>::kThreads, 1) decode_mma_kernel(con
         for (int jp = 0; jp < 2; ++jp) {
           uint32_t v = 0u;
           if (hh < G) {
-            const float x0 = fmul(qs[hh * D + 32 * t + 4 * c + 2 * jp], qscale);
-            const float x1 = fmul(qs[hh * D + 32 * t + 4 * c + 2 * jp + 1], qscale);
+            const float x0 = fmul(qs[qs_at(hh, 32 * t + 4 * c + 2 * jp)], qscale);
+            const float x1 = fmul(qs[qs_at(hh, 32 * t + 4 * c + 2 * jp + 1)], qscale);
             uint16_t a0, l0, a1, l1;
             split_f16(x0, a0, l0);
             split_f16(x1, a1, l1);
@@ -531,7 +542,7 @@ __global__ void __launch_bounds__(MmaCfg<KB>::kThreads, 1) decode_mma_kernel(con
     }
 
     // ---- leave the row: hi + lo halves, lanes -> warp -> CTA, one partial per (CTA, row)
-    for (int i = tid; i < G * D; i += M::kThreads) comb[i] = 0.0f;
+    for (int i = tid; i < G * D; i += M::kThreads) comb[comb_at(i / D, i % D)] = 0.0f;
     // lanes t < 2 keep head 2 t + (k & 1) at coordinate 16 g + 2 mb + (k >> 1)
 #pragma unroll
     for (int mb = 0; mb < 8; ++mb)
@@ -571,7 +582,7 @@ __global__ void __launch_bounds__(MmaCfg<KB>::kThreads, 1) decode_mma_kernel(con
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
           if (h0 + i >= G || m_own[i] == -INFINITY) continue;
-          float* c2 = comb + (h0 + i) * D + 16 * g;
+          float* c2 = comb + comb_at(h0 + i, 16 * g);  // coordinates 16 g .. 16 g + 15 are contiguous
 #pragma unroll
           for (int mb = 0; mb < 8; ++mb) {
             c2[2 * mb] = fadd(c2[2 * mb], fmul(acc[mb][i], sc2[i]));
@@ -583,7 +594,7 @@ __global__ void __launch_bounds__(MmaCfg<KB>::kThreads, 1) decode_mma_kernel(con
     }
     const long long slot = static_cast<long long>(blockIdx.x) + si.row;
     const float unscale = si.hot ? 1.0f : kCentUnscale;  // cold sums carry the table scale
-    for (int i = tid; i < G * D; i += M::kThreads) p.ws_acc[slot * G * D + i] = fmul(comb[i], unscale);
+    for (int i = tid; i < G * D; i += M::kThreads) p.ws_acc[slot * G * D + i] = fmul(comb[comb_at(i / D, i % D)], unscale);
     if (tid < G) {
       float mm = -INFINITY, ll = 0.0f;
 #pragma unroll
