@@ -374,8 +374,8 @@ TQ_HD void pack_codes32(const float2* z, float inv, const LutEntry* lut, int str
     const LutEntry e = lut[idx * stride];
     const uint32_t code = e.base + (y >= e.thr ? 1u : 0u);
     const int bit = i * BITS, word = bit >> 5, off = bit & 31;
-    acc[word] |= code << off;
-    if (off + BITS > 32) acc[word + 1] |= code >> (32 - off);
+    acc[word] += code * (1u << off);  // disjoint bit fields: one multiply-add inserts the code
+    if (off + BITS > 32) acc[word + 1] += code >> (32 - off);
   }
 #pragma unroll
   for (int k = 0; k < BITS; ++k) words[k] = acc[k];

@@ -153,12 +153,10 @@ __device__ __forceinline__ void quantize_step(const uint8_t* rowp, int q, const 
   const float n = norm_from_sum(h, l, reinterpret_cast<const uint32_t*>(rowp));
   // rotation: in-lane bits 0..4, then bits 5 (q ^ 1) and 6 (q ^ 2) across lanes
   fwht32(v);
-  // pairs are exchanged as 64-bit values, so each lands in a register pair
+  // the two halves of a pair are exchanged as two 32-bit values (no 64-bit packing)
   const float s1 = (q & 1) ? -1.0f : 1.0f, s2 = (q & 2) ? -1.0f : 1.0f;
   auto xchg = [](float2 a, int m) {
-    const unsigned long long u = (static_cast<unsigned long long>(__float_as_uint(a.y)) << 32) | __float_as_uint(a.x);
-    const unsigned long long o = __shfl_xor_sync(0xffffffffu, u, m);
-    return make_float2(__uint_as_float(static_cast<uint32_t>(o)), __uint_as_float(static_cast<uint32_t>(o >> 32)));
+    return make_float2(__shfl_xor_sync(0xffffffffu, a.x, m), __shfl_xor_sync(0xffffffffu, a.y, m));
   };
 #pragma unroll
   for (int j = 0; j < 16; ++j) v[j] = butterfly_pair(v[j], xchg(v[j], 8), make_float2(s1, s1));
