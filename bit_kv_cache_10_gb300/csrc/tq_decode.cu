@@ -92,7 +92,7 @@ __global__ void __launch_bounds__(4 * 32) decode_merge_kernel(const DecodeParams
     l = fmul(ml.y, sc_l);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) l = fadd(l, __shfl_xor_sync(0xffffffffu, l, o));
-#pragma unroll 4
+#pragma unroll 8
     for (int i = 0; i < n; ++i) {
       const float4 a = reinterpret_cast<const float4*>(p.ws_acc + (slot_of(i) * g + jj) * D)[lane];
       const float sc = __shfl_sync(0xffffffffu, sc_l, i);

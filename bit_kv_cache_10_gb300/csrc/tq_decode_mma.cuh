@@ -19,7 +19,7 @@
 // distinct banks, and the lo half is the same address plus 128.  Each load
 // returns one A-fragment register, so the fragments need no register moves.
 // The V table (256 rows) and the K table (2^(2 bits) rows) start at 64 KB
-// boundaries, so that an entry address is (e << 8) | (table + 4 l).
+// boundaries, so that an entry address is (e << 8) | (table + 4 l) (K: (e << 7) | ...).
 //
 // Scores (tokens as M, coordinates as K, 8 columns as N = the G query heads'
 // rotated query in hi and in lo halves).  An MMA covers 8 tokens: row g holds
@@ -29,7 +29,7 @@
 // holds coordinates 32 t .. 32 t + 31; chunk c of the MMA K dimension takes
 // coordinates 32 t + 4 c .. + 3 of every lane t.  Column h plus column h + 4
 // is head h.  The K table keeps (hi pair, lo pair) entries 16 times over (one
-// copy per lane of a half-warp, rows of 256 bytes).
+// copy per lane of a half-warp, rows of 128 bytes).
 //
 // Softmax.  Lane (g, t) then owns token g + 8 (t >> 1) for heads 2 (t & 1) and
 // 2 (t & 1) + 1.  The V weight of a token is w = 2^(s - m) n_V; the running
@@ -64,9 +64,9 @@ struct MmaCfg {
   static constexpr int kWarps = 12;
   static constexpr int kThreads = kWarps * 32;
   static constexpr int kTabAlign = 65536;
-  static constexpr int kTab = 65536 + (1 << (2 * KB)) * 256;  // V table | K table, rows of 256 bytes
+  static constexpr int kTab = 65536 + (1 << (2 * KB)) * 128;  // V table (256-byte rows) | K table (128-byte rows)
   static constexpr int kW16 = 2 * 4 * kTile * 2;  // per warp: fp16 weights [hi/lo][head][token]
-  static constexpr int kSmall = kWarps * kW16 + 4 * 132 * 4 /* rotated query */ + 4 * 136 * 4 /* combine */ +
+  static constexpr int kSmall = kWarps * kW16 + 4 * 132 * 4 /* rotated query */ + kWarps * 4 * 136 * 4 /* combine */ +
                                 kWarps * 4 * 2 * 4 /* warp (m, l) */ + kWarps * 8 * 16 /* tile descriptors */ +
                                 (kMaxDecodeBatch + 1) * 8 + 34 * 8;
   static constexpr int kWorst(int stages) { return kTab + kSmall + (kWarps + 1) * stages * kBuf + 1024; }
@@ -118,18 +118,18 @@ __device__ __forceinline__ uint2 lds_entry(uint32_t addr) {
 }
 
 // Shared address of the K table entry of code pair J (bits 2 KB J .. of the
-// lane's window of 32 coordinates); kbase = K table + 8 (lane mod 16).
+// lane's window of 32 coordinates); kbase = K table + 8 (lane mod 16), rows of 128 bytes.
 template <int KB, int J>
 __device__ __forceinline__ uint32_t k_pair_addr(const uint32_t* win, uint32_t kbase) {
   if constexpr (KB == 4) {
-    return __byte_perm(win[J / 4], kbase, 0x7604 | ((J % 4) << 4));  // byte J of the window into byte 1
+    return (__byte_perm(win[J / 4], 0u, 0x4440 | (J % 4)) << 7) | kbase;  // byte J of the window
   } else {
     constexpr int kOff = 2 * KB * J, kW = kOff / 32, kBit = kOff % 32;
     uint32_t x;
-    if constexpr (kBit + 2 * KB > 32) x = __funnelshift_r(win[kW], win[kW + 1], kBit - 8);
-    else if constexpr (kBit >= 8) x = win[kW] >> (kBit - 8);
-    else x = win[kW] << (8 - kBit);
-    return (x & (((1u << (2 * KB)) - 1u) << 8)) | kbase;
+    if constexpr (kBit + 2 * KB > 32) x = __funnelshift_r(win[kW], win[kW + 1], kBit - 7);
+    else if constexpr (kBit >= 7) x = win[kW] >> (kBit - 7);
+    else x = win[kW] << (7 - kBit);
+    return (x & (((1u << (2 * KB)) - 1u) << 7)) | kbase;
   }
 }
 
@@ -167,7 +167,7 @@ __global__ void __launch_bounds__(MmaCfg<KB>::kThreads, 1) decode_mma_kernel(con
   auto ptr = [&](uint32_t addr) { return smem + (addr - s0); };
   const uint32_t tab = lay.tab_lo;
   float* qs = reinterpret_cast<float*>(ptr(lay.take(4 * 132 * 4)));
-  float* comb = reinterpret_cast<float*>(ptr(lay.take(4 * 136 * 4)));
+  float* comb = reinterpret_cast<float*>(ptr(lay.take(NW * 4 * 136 * 4)));  // one row sum per warp
   float* wml = reinterpret_cast<float*>(ptr(lay.take(NW * 4 * 2 * 4)));
   int4* descs_all = reinterpret_cast<int4*>(ptr(lay.take(NW * 8 * 16)));
   long long* prefix = reinterpret_cast<long long*>(ptr(lay.take((kMaxDecodeBatch + 1) * 8)));
@@ -180,15 +180,27 @@ __global__ void __launch_bounds__(MmaCfg<KB>::kThreads, 1) decode_mma_kernel(con
   const uint32_t vbase = tab + 4u * lane;
   const uint32_t kbase = tab + 65536u + 8u * (lane & 15);
 
-  // tables (from the parameters only): entry e, copy c
-  for (int i = tid; i < 256 * 32; i += M::kThreads) {
-    const int e = i >> 5, c = i & 31;
-    uint2 v = pair_entry(p.v_cent[e & 15], p.v_cent[e >> 4]);
-    *reinterpret_cast<uint32_t*>(ptr(tab + (e << 8) + 4 * c)) = v.x;
-    *reinterpret_cast<uint32_t*>(ptr(tab + (e << 8) + 128 + 4 * c)) = v.y;
-    if (e < (1 << (2 * KB)) && c < kCopies)
-      *reinterpret_cast<uint2*>(ptr(tab + 65536 + (e << 8) + 8 * c)) =
-          pair_entry(p.k_cent[e & ((1 << KB) - 1)], p.k_cent[e >> KB]);
+  // tables (from the parameters only): each lane computes one distinct entry
+  // and writes its copies in an order rotated by the lane, so that the 32 stores
+  // of a warp fall in 32 distinct banks
+  {
+    constexpr int kK = 1 << (2 * KB);
+    for (int e = tid; e < 256 + kK; e += M::kThreads) {
+      if (e < 256) {
+        const uint2 v = pair_entry(p.v_cent[e & 15], p.v_cent[e >> 4]);
+        uint32_t* row = reinterpret_cast<uint32_t*>(ptr(tab + (e << 8)));
+        for (int c0 = 0; c0 < 32; ++c0) {
+          const int c = (c0 + lane) & 31;
+          row[c] = v.x;
+          row[32 + c] = v.y;
+        }
+      } else {
+        const int ek = e - 256;
+        const uint2 v = pair_entry(p.k_cent[ek & ((1 << KB) - 1)], p.k_cent[ek >> KB]);
+        uint2* row = reinterpret_cast<uint2*>(ptr(tab + 65536 + (ek << 7)));
+        for (int c0 = 0; c0 < kCopies; ++c0) row[(c0 + lane) & (kCopies - 1)] = v;
+      }
+    }
   }
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
   if (blockIdx.x == 0 && tid == 0 && p.status != nullptr) {
@@ -266,35 +278,50 @@ __global__ void __launch_bounds__(MmaCfg<KB>::kThreads, 1) decode_mma_kernel(con
     const TileInfo si = tile_info<MQ>(p, prefix, seg);
     const long long seg_end = si.row_end < t1 ? si.row_end : t1;
     if (si.b != cur_b || si.h != cur_h) {
-      // rotated query of the G heads, H D q (unnormalized), in qs
+      // rotated query of the G heads, H D q (unnormalized), in qs: warp jj
+      // transforms head jj, lane l holding coordinates 4 l .. 4 l + 3 (index bits
+      // 0 and 1 in registers, bits 2..6 across lanes, in ascending order)
       __syncthreads();
-      if (tid < D) {
-        const bool neg = sign_negative(p.seed, p.layer, si.h, tid);
+      if (warp < G) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(p.q + (static_cast<int64_t>(si.b) * p.hq + si.h * G + warp) * D +
+                                                          4 * lane);
+        float x[4];
+        const float2 x01 = half2_bits_to_float2(raw.x), x23 = half2_bits_to_float2(raw.y);
+        x[0] = x01.x;
+        x[1] = x01.y;
+        x[2] = x23.x;
+        x[3] = x23.y;
 #pragma unroll
-        for (int jj = 0; jj < G; ++jj) {
-          const float x = half_bits_to_float(p.q[(static_cast<int64_t>(si.b) * p.hq + si.h * G + jj) * D + tid]);
-          qs[qs_at(jj, tid)] = neg ? -x : x;
-        }
-      }
-      __syncthreads();
+        for (int i = 0; i < 4; ++i)
+          if (sign_negative(p.seed, p.layer, si.h, 4 * lane + i)) x[i] = -x[i];
+        float a0 = fadd(x[0], x[1]), a1 = fsub(x[0], x[1]), a2 = fadd(x[2], x[3]), a3 = fsub(x[2], x[3]);  // bit 0
+        x[0] = fadd(a0, a2);  // bit 1
+        x[2] = fsub(a0, a2);
+        x[1] = fadd(a1, a3);
+        x[3] = fsub(a1, a3);
 #pragma unroll
-      for (int st = 1; st < D; st *= 2) {
-        if (tid < D && (tid & st) == 0) {
+        for (int m = 1; m < 32; m <<= 1) {  // bits 2..6
+          const bool upper = (lane & m) != 0;
 #pragma unroll
-          for (int jj = 0; jj < G; ++jj) {
-            const float a = qs[qs_at(jj, tid)], c = qs[qs_at(jj, tid + st)];
-            qs[qs_at(jj, tid)] = fadd(a, c);
-            qs[qs_at(jj, tid + st)] = fsub(a, c);
+          for (int i = 0; i < 4; ++i) {
+            const float o = __shfl_xor_sync(0xffffffffu, x[i], m);
+            x[i] = upper ? fsub(o, x[i]) : fadd(x[i], o);
           }
         }
-        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) qs[qs_at(warp, 4 * lane + i)] = x[i];
       }
+      __syncthreads();
       // lane (g, t): head g & 3, half g >> 2, coordinates 32 t .. 32 t + 31, scaled by a
       // power of two that puts the head's largest |value| in [2^13, 2^14)
       const int hh = g & 3;
       float amax = 0.0f;
-      if (hh < G)
-        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(qs[qs_at(hh, 32 * t + i)]));
+      if (hh < G) {
+        float am[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};  // independent partial maxima
+#pragma unroll
+        for (int i = 0; i < 32; ++i) am[i & 7] = fmaxf(am[i & 7], fabsf(qs[qs_at(hh, 32 * t + i)]));
+        amax = fmaxf(fmaxf(fmaxf(am[0], am[1]), fmaxf(am[2], am[3])), fmaxf(fmaxf(am[4], am[5]), fmaxf(am[6], am[7])));
+      }
       amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
       amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
       const int ex = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);  // biased exponent, 0 for zero
@@ -541,8 +568,9 @@ __global__ void __launch_bounds__(MmaCfg<KB>::kThreads, 1) decode_mma_kernel(con
       ++j;
     }
 
-    // ---- leave the row: hi + lo halves, lanes -> warp -> CTA, one partial per (CTA, row)
-    for (int i = tid; i < G * D; i += M::kThreads) comb[comb_at(i / D, i % D)] = 0.0f;
+    // ---- leave the row: hi + lo halves, lanes -> warp -> CTA, one partial per (CTA, row).
+    // Each warp writes its sum, scaled to the CTA's maximum, to a slot of its own;
+    // the slots are then added in warp order (the result does not depend on timing)
     // lanes t < 2 keep head 2 t + (k & 1) at coordinate 16 g + 2 mb + (k >> 1)
 #pragma unroll
     for (int mb = 0; mb < 8; ++mb)
@@ -567,34 +595,34 @@ __global__ void __launch_bounds__(MmaCfg<KB>::kThreads, 1) decode_mma_kernel(con
         }
     }
     __syncthreads();
-    float sc2[2];
+    if (t < 2) {
+      float* slot_w = comb + warp * 4 * 136;
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const int hd = (h0 + i) & 3;
-      float mm = -INFINITY;
-      if (hd < G)
+      for (int i = 0; i < 2; ++i) {
+        const int hd = h0 + i;
+        if (hd >= G) continue;
+        float mm = -INFINITY;
 #pragma unroll
         for (int w = 0; w < NW; ++w) mm = fmaxf(mm, wml[(w * 4 + hd) * 2]);
-      sc2[i] = m_own[i] == -INFINITY ? 0.0f : exp2f(m_own[i] - mm);
-    }
-    for (int w = 0; w < NW; ++w) {
-      if (warp == w && t < 2) {
+        const float sc2 = m_own[i] == -INFINITY ? 0.0f : exp2f(m_own[i] - mm);  // 0: no token of the head
+        float* c2 = slot_w + comb_at(hd, 16 * g);  // coordinates 16 g .. 16 g + 15 are contiguous
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          if (h0 + i >= G || m_own[i] == -INFINITY) continue;
-          float* c2 = comb + comb_at(h0 + i, 16 * g);  // coordinates 16 g .. 16 g + 15 are contiguous
-#pragma unroll
-          for (int mb = 0; mb < 8; ++mb) {
-            c2[2 * mb] = fadd(c2[2 * mb], fmul(acc[mb][i], sc2[i]));
-            c2[2 * mb + 1] = fadd(c2[2 * mb + 1], fmul(acc[mb][2 + i], sc2[i]));
-          }
+        for (int mb = 0; mb < 8; ++mb) {
+          c2[2 * mb] = fmul(acc[mb][i], sc2);
+          c2[2 * mb + 1] = fmul(acc[mb][2 + i], sc2);
         }
       }
-      __syncthreads();
     }
+    __syncthreads();
     const long long slot = static_cast<long long>(blockIdx.x) + si.row;
     const float unscale = si.hot ? 1.0f : kCentUnscale;  // cold sums carry the table scale
-    for (int i = tid; i < G * D; i += M::kThreads) p.ws_acc[slot * G * D + i] = fmul(comb[comb_at(i / D, i % D)], unscale);
+    for (int i = tid; i < G * D; i += M::kThreads) {
+      const int at = comb_at(i / D, i % D);
+      float sum = 0.0f;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) sum = fadd(sum, comb[w * 4 * 136 + at]);
+      p.ws_acc[slot * G * D + i] = fmul(sum, unscale);
+    }
     if (tid < G) {
       float mm = -INFINITY, ll = 0.0f;
 #pragma unroll
