@@ -89,15 +89,18 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# the sources of the long-context decode call (split kernels, dispatch, merge and entry points)
+DECODE_SOURCES = ("tq_decode_mma.cuh", "tq_decode_split.cuh", "tq_decode_dispatch.cuh", "tq_decode.cu")
+
+
 def profile_traffic():
     """dram bytes per decode launch from the committed ncu summary, if it was
-    taken on the current decode kernel sources (split kernel header + decode
-    translation unit); else None."""
+    taken on the current decode kernel sources (DECODE_SOURCES); else None."""
     path = os.path.join(ROOT, "profiles", "decode_long_context.md")
     csrc = os.path.join(ROOT, "bit_kv_cache_10_gb300", "csrc")
     try:
         text = open(path).read()
-        src = b"".join(open(os.path.join(csrc, f), "rb").read() for f in ("tq_decode_split.cuh", "tq_decode.cu"))
+        src = b"".join(open(os.path.join(csrc, f), "rb").read() for f in DECODE_SOURCES)
         sha = hashlib.sha256(src).hexdigest()[:16]
         m = re.search(r"traffic_bytes_per_step:\s*([0-9]+)", text)
         s = re.search(r"decode_source_sha256_16:\s*([0-9a-f]+)", text)

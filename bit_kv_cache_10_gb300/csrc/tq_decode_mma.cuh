@@ -313,39 +313,59 @@ __global__ void __launch_bounds__(MmaCfg<KB>::kThreads, 1) decode_mma_kernel(con
       }
       __syncthreads();
       // lane (g, t): head g & 3, half g >> 2, coordinates 32 t .. 32 t + 31, scaled by a
-      // power of two that puts the head's largest |value| in [2^13, 2^14)
-      const int hh = g & 3;
-      float amax = 0.0f;
-      if (hh < G) {
-        float am[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};  // independent partial maxima
+      // power of two that puts the head's largest |value| in [2^13, 2^14).  Warp 0
+      // computes the fragments and publishes them (the row-combine buffer is free
+      // here); every warp then loads its lanes' copies.
+      uint32_t* qb_s = reinterpret_cast<uint32_t*>(comb);         // [32 lanes][16]
+      float* qsc_s = comb + 32 * 16;                              // [32 lanes]
+      if (warp == 0) {
+        const int hh = g & 3;
+        float amax = 0.0f;
+        if (hh < G) {
+          float am[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};  // independent partial maxima
 #pragma unroll
-        for (int i = 0; i < 32; ++i) am[i & 7] = fmaxf(am[i & 7], fabsf(qs[qs_at(hh, 32 * t + i)]));
-        amax = fmaxf(fmaxf(fmaxf(am[0], am[1]), fmaxf(am[2], am[3])), fmaxf(fmaxf(am[4], am[5]), fmaxf(am[6], am[7])));
-      }
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-      const int ex = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);  // biased exponent, 0 for zero
-      const float qscale = ex == 0 ? 1.0f : __uint_as_float(static_cast<uint32_t>(127 + 13 + 127 - ex) << 23);
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-#pragma unroll
-        for (int jp = 0; jp < 2; ++jp) {
-          uint32_t v = 0u;
-          if (hh < G) {
-            const float x0 = fmul(qs[qs_at(hh, 32 * t + 4 * c + 2 * jp)], qscale);
-            const float x1 = fmul(qs[qs_at(hh, 32 * t + 4 * c + 2 * jp + 1)], qscale);
-            uint16_t a0, l0, a1, l1;
-            split_f16(x0, a0, l0);
-            split_f16(x1, a1, l1);
-            v = (g >> 2) == 0 ? pack16(a0, a1) : pack16(l0, l1);
-          }
-          qb[2 * c + jp] = v;
+          for (int i = 0; i < 32; ++i) am[i & 7] = fmaxf(am[i & 7], fabsf(qs[qs_at(hh, 32 * t + i)]));
+          amax = fmaxf(fmaxf(fmaxf(am[0], am[1]), fmaxf(am[2], am[3])), fmaxf(fmaxf(am[4], am[5]), fmaxf(am[6], am[7])));
         }
-      // the scale of head h sits in lane 4 h (half 0, t = 0)
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        const int ex = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);  // biased exponent, 0 for zero
+        const float qscale = ex == 0 ? 1.0f : __uint_as_float(static_cast<uint32_t>(127 + 13 + 127 - ex) << 23);
+        uint32_t frag[16];
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const float qsh = __shfl_sync(0xffffffffu, qscale, 4 * ((h0 + i) & 3));
-        sc[i] = kLog2e / static_cast<float>(D) * kCentUnscale / qsh;
+        for (int c = 0; c < 8; ++c)
+#pragma unroll
+          for (int jp = 0; jp < 2; ++jp) {
+            uint32_t v = 0u;
+            if (hh < G) {
+              const float x0 = fmul(qs[qs_at(hh, 32 * t + 4 * c + 2 * jp)], qscale);
+              const float x1 = fmul(qs[qs_at(hh, 32 * t + 4 * c + 2 * jp + 1)], qscale);
+              uint16_t a0, l0, a1, l1;
+              split_f16(x0, a0, l0);
+              split_f16(x1, a1, l1);
+              v = (g >> 2) == 0 ? pack16(a0, a1) : pack16(l0, l1);
+            }
+            frag[2 * c + jp] = v;
+          }
+        uint4* dst = reinterpret_cast<uint4*>(qb_s + 16 * lane);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) dst[k] = make_uint4(frag[4 * k], frag[4 * k + 1], frag[4 * k + 2], frag[4 * k + 3]);
+        qsc_s[lane] = qscale;
+      }
+      __syncthreads();
+      {
+        const uint4* src = reinterpret_cast<const uint4*>(qb_s + 16 * lane);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint4 v = src[k];
+          qb[4 * k] = v.x;
+          qb[4 * k + 1] = v.y;
+          qb[4 * k + 2] = v.z;
+          qb[4 * k + 3] = v.w;
+        }
+        // the scale of head h was computed by lane 4 h (half 0, t = 0)
+#pragma unroll
+        for (int i = 0; i < 2; ++i) sc[i] = kLog2e / static_cast<float>(D) * kCentUnscale / qsc_s[4 * ((h0 + i) & 3)];
       }
       cur_b = si.b;
       cur_h = si.h;

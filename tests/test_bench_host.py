@@ -37,7 +37,7 @@ def _copy_tree(tmp_path):
     csrc = root / "bit_kv_cache_10_gb300" / "csrc"
     csrc.mkdir(parents=True)
     shutil.copy(os.path.join(bench.ROOT, "profiles", "decode_long_context.md"), root / "profiles")
-    for f in ("tq_decode_split.cuh", "tq_decode.cu"):
+    for f in bench.DECODE_SOURCES:
         shutil.copy(os.path.join(bench.ROOT, "bit_kv_cache_10_gb300", "csrc", f), csrc / f)
     return root
 
@@ -47,7 +47,7 @@ def test_traffic_follows_the_source_hash(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "ROOT", str(root))
     text = (root / "profiles" / "decode_long_context.md").read_text()
     csrc = root / "bit_kv_cache_10_gb300" / "csrc"
-    src = (csrc / "tq_decode_split.cuh").read_bytes() + (csrc / "tq_decode.cu").read_bytes()
+    src = b"".join((csrc / f).read_bytes() for f in bench.DECODE_SOURCES)
     sha = hashlib.sha256(src).hexdigest()[:16]
     # a summary that names the current hash gives its traffic figure
     stamped = "traffic_bytes_per_step: 123456789\ndecode_source_sha256_16: %s\n" % sha
