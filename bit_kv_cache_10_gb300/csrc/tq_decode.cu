@@ -21,6 +21,11 @@ __global__ void __launch_bounds__(4 * 32) decode_merge_kernel(const DecodeParams
   const int jj = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.x, b = blockIdx.y;
   if (jj >= g) return;
+  // rotation signs of the lane's coordinates 4 lane .. 4 lane + 3 (parameters only)
+  unsigned neg4 = 0u;
+  if (p.rotated)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) neg4 |= sign_negative(p.seed, p.layer, h, 4 * lane + i) ? 1u << i : 0u;
   // the lengths may be written by a grid before the split kernel and the partials
   // by the split kernel: wait for the preceding grids before reading either
   // (programmatic dependent launch lets this grid start while they finish)
@@ -62,8 +67,7 @@ __global__ void __launch_bounds__(4 * 32) decode_merge_kernel(const DecodeParams
     return i < n0 ? static_cast<long long>(c0 + i) + row0 : static_cast<long long>(c1 + i - n0) + row0 + 1;
   };
   auto live = [&](int i) {  // a CTA with an empty range wrote no partial
-    const int c = i < n0 ? c0 + i : c1 + i - n0;
-    return cta_start(c, total, p.grid) != cta_start(c + 1, total, p.grid);
+    return cta_live(i < n0 ? c0 + i : c1 + i - n0, total, p.grid);
   };
   const int n = n0 + n1;
   const unsigned live32 = __ballot_sync(0xffffffffu, lane < n && live(lane));
@@ -78,13 +82,18 @@ __global__ void __launch_bounds__(4 * 32) decode_merge_kernel(const DecodeParams
       else y[k] = ffma(av[k], sc, y[k]);
     }
   };
-  if (n <= 32) {
-    // one partial per lane: its (max, mass) read once, its scale shared by shuffles;
-    // the accumulator loads do not wait on the scales (a partial that was not
+  if (n <= 16) {
+    // one partial per lane: its (max, mass) read once, its scale shared by
+    // shuffles; every accumulator load is issued before the scales are known, so
+    // the whole merge waits for one round of loads (a partial that was not
     // written has scale 0 and its loaded values are not used)
     float2 ml = make_float2(-INFINITY, 0.0f);
     if (lane < n && ((live32 >> lane) & 1u))
       ml = reinterpret_cast<const float2*>(p.ws_ml)[slot_of(lane) * g + jj];
+    float4 a[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      if (i < n) a[i] = reinterpret_cast<const float4*>(p.ws_acc + (slot_of(i) * g + jj) * D)[lane];
     mm = ml.x;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
@@ -92,11 +101,40 @@ __global__ void __launch_bounds__(4 * 32) decode_merge_kernel(const DecodeParams
     l = fmul(ml.y, sc_l);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) l = fadd(l, __shfl_xor_sync(0xffffffffu, l, o));
-#pragma unroll 8
-    for (int i = 0; i < n; ++i) {
-      const float4 a = reinterpret_cast<const float4*>(p.ws_acc + (slot_of(i) * g + jj) * D)[lane];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if (i >= n) break;
       const float sc = __shfl_sync(0xffffffffu, sc_l, i);
-      if (sc != 0.0f) add_partial(i, sc, a);
+      if (sc != 0.0f) add_partial(i, sc, a[i]);
+    }
+  } else if (n <= 32) {
+    // as above with the loads in two rounds of 16
+    float2 ml = make_float2(-INFINITY, 0.0f);
+    if (lane < n && ((live32 >> lane) & 1u))
+      ml = reinterpret_cast<const float2*>(p.ws_ml)[slot_of(lane) * g + jj];
+    float4 a[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) a[i] = reinterpret_cast<const float4*>(p.ws_acc + (slot_of(i) * g + jj) * D)[lane];
+    mm = ml.x;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
+    const float sc_l = ml.x == -INFINITY ? 0.0f : exp2f(ml.x - mm);
+    l = fmul(ml.y, sc_l);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) l = fadd(l, __shfl_xor_sync(0xffffffffu, l, o));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float sc = __shfl_sync(0xffffffffu, sc_l, i);
+      const float4 nxt = 16 + i < n ? reinterpret_cast<const float4*>(p.ws_acc + (slot_of(16 + i) * g + jj) * D)[lane]
+                                    : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      if (sc != 0.0f) add_partial(i, sc, a[i]);
+      a[i] = nxt;
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if (16 + i >= n) break;
+      const float sc = __shfl_sync(0xffffffffu, sc_l, 16 + i);
+      if (sc != 0.0f) add_partial(16 + i, sc, a[i]);
     }
   } else {
     // (max, mass) of the partials, several per lane, then across the warp
@@ -147,7 +185,7 @@ __global__ void __launch_bounds__(4 * 32) decode_merge_kernel(const DecodeParams
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     float v = fmul(y[i], 1.0f / kSqrtD);
-    if (sign_negative(p.seed, p.layer, h, 4 * lane + i)) v = -v;
+    if ((neg4 >> i) & 1u) v = -v;
     r[i] = l > 0.0f ? fadd(v, hv[i]) / l : 0.0f;  // no token read (every block outside the pool): zero
   }
   out[lane] = make_float4(r[0], r[1], r[2], r[3]);

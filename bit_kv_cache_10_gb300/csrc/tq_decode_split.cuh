@@ -1264,11 +1264,26 @@ __global__ void __launch_bounds__(Cfg<KB, VB>::kThreads, 1) decode_split_kernel(
   cp_async_wait<0>();
 }
 
-// CTA of the split kernel that processes tile t (the last one whose range starts at or before t).
+// CTA of the split kernel that processes tile t (the last one whose range starts
+// at or before t): floor(((t + 1) grid - 1) / total), a value below grid.  A float
+// estimate of the quotient is off by at most one (its relative error is a few
+// 2^-24 and the quotient is below 2^10); exact 64-bit products correct it, so no
+// 64-bit division is needed.
 __device__ __forceinline__ int cta_of(long long t, long long total, int grid) {
-  return static_cast<int>(((t + 1) * grid - 1) / total);
+  const long long num = (t + 1) * grid - 1;
+  int c = static_cast<int>(static_cast<float>(num) * (1.0f / static_cast<float>(total)));
+  c = c < 0 ? 0 : (c > grid - 1 ? grid - 1 : c);
+  if (static_cast<long long>(c) * total > num) --c;
+  if (static_cast<long long>(c + 1) * total <= num) ++c;
+  return c;
 }
-__device__ __forceinline__ long long cta_start(int c, long long total, int grid) { return total * c / grid; }
+// Whether CTA c of the split kernel has a non-empty range: always when there are
+// at least as many tiles as CTAs (then total / grid >= 1 separates the starts).
+__device__ __forceinline__ bool cta_live(int c, long long total, int grid) {
+  if (total >= grid) return true;
+  const int t32 = static_cast<int>(total);
+  return t32 * c / grid != t32 * (c + 1) / grid;
+}
 
 template <int G, int KB, int VB, bool SPARSE, bool PAGED, bool MQ>
 tq_status launch_split(const DecodeParams& p, cudaStream_t stream) {
