@@ -909,6 +909,16 @@ def run_profile(args):
             tc.decode(q, sl, cap, out=out, workspace=ws)
         torch.cuda.synchronize()
         print(json.dumps({"profile": "int8", "steps": total, "status": tc.device_status()}))
+    elif args.profile == "llama":
+        tc = build_plain_cache(torch, 1, 4096, False, SEED + 3)
+        q = torch.from_numpy(synth.queries_fp16(SEED + 3, 1, HQ, D)).cuda()
+        lens = torch.full((1,), 4096, dtype=torch.int32, device="cuda")
+        out = torch.empty(1, HQ, D, dtype=torch.float32, device="cuda")
+        ws = torch.empty(tc.workspace_bytes(4096), dtype=torch.uint8, device="cuda")
+        for s in range(total):
+            tc.decode(q, lens, 4096, out=out, workspace=ws)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile": "llama", "steps": total, "status": tc.device_status()}))
     elif args.profile == "asym":
         tc = build_plain_cache(torch, 8, 16384, True, SEED + 3)
         q = torch.from_numpy(synth.queries_fp16(SEED + 3, 8, HQ, D)).cuda()
@@ -940,7 +950,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle timing")
-    ap.add_argument("--profile", choices=["decode", "quantize", "asym", "int8", "paged"],
+    ap.add_argument("--profile", choices=["decode", "quantize", "asym", "int8", "paged", "llama"],
                     help="run only warm-up + timed steps of one part (for ncu captures); prints a short line")
     ap.add_argument("--profile-batch", type=int, default=4, help="batch of the quantize part in --profile mode")
     args = ap.parse_args()

@@ -20,7 +20,7 @@ OBJDIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtq.so")
 
 SOURCES = ["tq_host.cpp", "tq_quantize.cu", "tq_decode.cu", "tq_decode_sparse.cu", "tq_decode_paged.cu",
-           "tq_decode_paged_sparse.cu", "tq_decode_multi.cu", "tq_decode_multi_paged.cu", "tq_dequantize.cu"]
+           "tq_decode_paged_sparse.cu", "tq_decode_multi.cu", "tq_decode_multi_paged.cu", "tq_decode_cluster.cu", "tq_dequantize.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-ffp-contract=off", "-I", INCLUDE]
 

@@ -2,7 +2,10 @@
 // kernel and the dense contiguous split-K instantiations (the split kernel
 // itself is in tq_decode_split.cuh; its sparse-V and paged instantiations are in
 // tq_decode_sparse.cu, tq_decode_paged.cu and tq_decode_paged_sparse.cu).
+#include <atomic>
+
 #include "tq_decode_dispatch.cuh"
+#include "tq_debug.h"
 
 namespace tq {
 namespace {
@@ -157,38 +160,7 @@ __global__ void __launch_bounds__(4 * 32) decode_merge_kernel(const DecodeParams
       add_partial(i, exp2f(ms - mm), reinterpret_cast<const float4*>(p.ws_acc + (slot * g + jj) * D)[lane]);
     }
   }
-  // inverse rotation of the cold sum: D_h H y / sqrt(d), index t = 4 lane + i (the
-  // int8 mode sums V unrotated)
-  if (!p.rotated) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) y[i] = l > 0.0f ? fadd(y[i], hv[i]) / l : 0.0f;
-    out[lane] = make_float4(y[0], y[1], y[2], y[3]);
-    return;
-  }
-  {
-    float a0 = fadd(y[0], y[1]), a1 = fsub(y[0], y[1]), a2 = fadd(y[2], y[3]), a3 = fsub(y[2], y[3]);  // bit 0
-    y[0] = fadd(a0, a2);  // bit 1
-    y[2] = fsub(a0, a2);
-    y[1] = fadd(a1, a3);
-    y[3] = fsub(a1, a3);
-  }
-#pragma unroll
-  for (int m = 1; m < 32; m <<= 1) {  // bits 2..6
-    const bool upper = (lane & m) != 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float o = __shfl_xor_sync(0xffffffffu, y[i], m);
-      y[i] = upper ? fsub(o, y[i]) : fadd(y[i], o);
-    }
-  }
-  float r[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    float v = fmul(y[i], 1.0f / kSqrtD);
-    if ((neg4 >> i) & 1u) v = -v;
-    r[i] = l > 0.0f ? fadd(v, hv[i]) / l : 0.0f;  // no token read (every block outside the pool): zero
-  }
-  out[lane] = make_float4(r[0], r[1], r[2], r[3]);
+  merge_finish(y, hv, l, neg4, p.rotated, p.out + (static_cast<int64_t>(b) * p.hq + h * g + jj) * D, lane);
 }
 
 int sm_count() {
@@ -203,6 +175,13 @@ int sm_count() {
 
 namespace tq {
 namespace {
+
+// Decode path selection for tests: 0 automatic, 1 always the persistent split
+// kernel and the merge kernel, 2 the cluster variant wherever the mode allows it.
+std::atomic<int> g_decode_path{0};
+// Longest context the automatic selection sends to the cluster variant: about
+// four 16-token tiles per warp of a row's kClusterCtas CTAs.
+constexpr int kClusterMaxLen = kClusterCtas * 12 * 4 * kTile;
 
 // Split-K attention of nq query tokens per sequence (the newest nq positions,
 // causal; nq = 1 is decode) over the cache: the work list holds B nq
@@ -257,6 +236,14 @@ tq_status run_attention(const tq_cache_desc* d, const void* q, int nq, const int
   const int kb = d->k_mode == TQ_K_FP16 ? 16 : d->k_bits;
   tq_status st;
   const bool sparse = p.sparse_tau > 0.0f, paged = d->block_size > 0;
+  // small work (rows of at most kClusterMaxLen positions, every row's cluster
+  // resident at once): one thread-block cluster per (b, h) row, no merge launch
+  const int path = g_decode_path.load(std::memory_order_relaxed);
+  if (nq == 1 && !paged && !sparse && d->k_mode == TQ_K_PACKED && kb >= 2 && kb <= 4 && d->v_bits == 4 && path != 1 &&
+      (path == 2 || max_seq_len <= kClusterMaxLen)) {
+    st = dispatch_cluster(p, g, kb, s);
+    if (st != TQ_ERR_UNSUPPORTED) return st;
+  }
   if (nq > 1) {
     st = paged ? dispatch_split_multi_paged(p, g, kb, d->v_bits, s) : dispatch_split_multi(p, g, kb, d->v_bits, s);
   } else if (paged) {
@@ -350,4 +337,8 @@ extern "C" tq_status tq_decode_attention_no_alloc(const tq_cache_desc* d, const 
   const tq_status st = no_alloc_scratch(&scratch);
   if (st != TQ_OK) return st;
   return tq_decode_attention(d, q, d_seq_lens, max_seq_len, out, scratch, TQ_NO_ALLOC_WORKSPACE_BYTES, stream);
+}
+
+extern "C" void tq_debug_set_decode_path(int32_t path) {
+  tq::g_decode_path.store(path == 1 || path == 2 ? path : 0, std::memory_order_relaxed);
 }

@@ -55,7 +55,9 @@ namespace {
 constexpr float kCentScale = 1024.0f;       // centroids are tabulated times 2^10
 constexpr float kCentUnscale = 1.0f / 1024.0f;
 
-template <int KB>
+constexpr int kClusterCtas = 8;  // CTAs of a (b, h) row in the cluster variant (the portable cluster size)
+
+template <int KB, bool CL = false>
 struct MmaCfg {
   using Stage = Cfg<KB, 4>;                  // K | K norms | V | V norms, with V rows padded:
   static constexpr int kVPitch = 80;         // 64-byte records 80 bytes apart (conflict-free V code loads)
@@ -66,9 +68,11 @@ struct MmaCfg {
   static constexpr int kTabAlign = 65536;
   static constexpr int kTab = 65536 + (1 << (2 * KB)) * 128;  // V table (256-byte rows) | K table (128-byte rows)
   static constexpr int kW16 = 2 * 4 * kTile * 2;  // per warp: fp16 weights [hi/lo][head][token]
+  // cluster variant: the CTA's cold and hot partials, acc [part][4][D] then (m, l) [part][4]
+  static constexpr int kPart = CL ? 2 * 4 * (D + 2) * 4 : 0;
   static constexpr int kSmall = kWarps * kW16 + 4 * 132 * 4 /* rotated query */ + kWarps * 4 * 136 * 4 /* combine */ +
                                 kWarps * 4 * 2 * 4 /* warp (m, l) */ + kWarps * 8 * 16 /* tile descriptors */ +
-                                (kMaxDecodeBatch + 1) * 8 + 34 * 8;
+                                (kMaxDecodeBatch + 1) * 8 + 34 * 8 + kPart;
   static constexpr int kWorst(int stages) { return kTab + kSmall + (kWarps + 1) * stages * kBuf + 1024; }
   // the aligned table can leave a gap of up to kTabAlign - 1024 bytes before it, filled by the other buffers
   static constexpr int kStages = kWorst(6) <= kSmemBudget ? 6 : kWorst(4) <= kSmemBudget ? 4 : kWorst(3) <= kSmemBudget ? 3 : 2;
@@ -150,11 +154,36 @@ __device__ __forceinline__ void interleave(uint32_t wa, uint32_t wb, uint32_t& l
 // coordinates (the lanes' 32-coordinate windows of the four heads fall in
 // distinct banks), the row combine with one word after every 16 coordinates.
 __device__ __forceinline__ int qs_at(int h, int i) { return h * 132 + i + (i >> 5); }
+
+// Thread-block cluster: barrier of every thread of the cluster (release /
+// acquire: shared-memory writes before it are seen by the cluster's reads after
+// it), the address of the same shared variable in CTA `rank`, and loads from it.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ uint32_t map_cluster(uint32_t addr, int rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float2 ld_cluster_f2(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];\n" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];\n"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
 __device__ __forceinline__ int comb_at(int h, int i) { return h * 136 + i + (i >> 4); }
 
-template <int G, int KB, bool SPARSE, bool PAGED, bool MQ>
-__global__ void __launch_bounds__(MmaCfg<KB>::kThreads, 1) decode_mma_kernel(const DecodeParams p) {
-  using M = MmaCfg<KB>;
+template <int G, int KB, bool SPARSE, bool PAGED, bool MQ, bool CL = false>
+__global__ void __launch_bounds__(MmaCfg<KB, CL>::kThreads, 1) decode_mma_kernel(const DecodeParams p) {
+  using M = MmaCfg<KB, CL>;
   using C = Cfg<KB, 4>;
   constexpr int S = M::kStages;
   constexpr int NW = M::kWarps;
@@ -173,6 +202,8 @@ __global__ void __launch_bounds__(MmaCfg<KB>::kThreads, 1) decode_mma_kernel(con
   long long* prefix = reinterpret_cast<long long*>(ptr(lay.take((kMaxDecodeBatch + 1) * 8)));
   long long* scan = reinterpret_cast<long long*>(ptr(lay.take(34 * 8)));
   const uint32_t w16_all = lay.take(NW * M::kW16);
+  float* cpart = nullptr;
+  if constexpr (CL) cpart = reinterpret_cast<float*>(ptr(lay.take(M::kPart)));
 
   asm volatile("griddepcontrol.launch_dependents;\n");
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -239,8 +270,27 @@ __global__ void __launch_bounds__(MmaCfg<KB>::kThreads, 1) decode_mma_kernel(con
   float sc[2];       // log2-domain score scale of heads h0, h0 + 1 (rotation, centroid and query scales)
   int cur_b = -1, cur_h = -1;
 
-  const long long t0 = total * blockIdx.x / p.grid, t1 = total * (blockIdx.x + 1) / p.grid;
-  if (t0 >= t1) return;
+  long long t0, t1;
+  if constexpr (CL) {
+    // one cluster of kClusterCtas CTAs per (b, h) row, CTA rank r taking the r-th
+    // equal part of the row's tiles (cold, then hot); a CTA with no tile still
+    // takes part in the cluster barriers of the merge
+    const int crow = blockIdx.x / kClusterCtas, rank = blockIdx.x % kClusterCtas;
+    const int rb = crow / p.hkv, rh = crow % p.hkv;
+    const SeqTiles sq = seq_tiles<MQ>(p, rb);
+    const long long per_h = sq.tc + sq.th;
+    const long long hb = prefix[rb] + rh * per_h;
+    t0 = hb + per_h * rank / kClusterCtas;
+    t1 = hb + per_h * (rank + 1) / kClusterCtas;
+    if (tid < 2 * 4) {  // no partial yet: (m, l) = (-inf, 0) for both parts of every head slot
+      cpart[2 * 4 * D + 2 * tid] = -INFINITY;
+      cpart[2 * 4 * D + 2 * tid + 1] = 0.0f;
+    }
+  } else {
+    t0 = total * blockIdx.x / p.grid;
+    t1 = total * (blockIdx.x + 1) / p.grid;
+    if (t0 >= t1) return;
+  }
   const int my_n = static_cast<int>((t1 - t0 - warp + NW - 1) / NW);
   int j_issue = 0, j = 0;
   Cursor cur;
@@ -634,31 +684,99 @@ __global__ void __launch_bounds__(MmaCfg<KB>::kThreads, 1) decode_mma_kernel(con
       }
     }
     __syncthreads();
-    const long long slot = static_cast<long long>(blockIdx.x) + si.row;
     const float unscale = si.hot ? 1.0f : kCentUnscale;  // cold sums carry the table scale
-    for (int i = tid; i < G * D; i += M::kThreads) {
-      const int at = comb_at(i / D, i % D);
-      float sum = 0.0f;
+    if constexpr (CL) {
+      // the partial stays in this CTA's shared memory, part 0 cold and part 1 hot
+      float* pa = cpart + si.hot * 4 * D;
+      for (int i = tid; i < G * D; i += M::kThreads) {
+        const int at = comb_at(i / D, i % D);
+        float sum = 0.0f;
 #pragma unroll
-      for (int w = 0; w < NW; ++w) sum = fadd(sum, comb[w * 4 * 136 + at]);
-      p.ws_acc[slot * G * D + i] = fmul(sum, unscale);
-    }
-    if (tid < G) {
-      float mm = -INFINITY, ll = 0.0f;
-#pragma unroll
-      for (int w = 0; w < NW; ++w) mm = fmaxf(mm, wml[(w * 4 + tid) * 2]);
-#pragma unroll
-      for (int w = 0; w < NW; ++w) {
-        const float mwv = wml[(w * 4 + tid) * 2];
-        if (mwv != -INFINITY) ll = ffma(wml[(w * 4 + tid) * 2 + 1], exp2f(mwv - mm), ll);
+        for (int w = 0; w < NW; ++w) sum = fadd(sum, comb[w * 4 * 136 + at]);
+        pa[i] = fmul(sum, unscale);
       }
-      p.ws_ml[(slot * G + tid) * 2] = mm;
-      p.ws_ml[(slot * G + tid) * 2 + 1] = ll;
+      if (tid < G) {
+        float mm = -INFINITY, ll = 0.0f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) mm = fmaxf(mm, wml[(w * 4 + tid) * 2]);
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+          const float mwv = wml[(w * 4 + tid) * 2];
+          if (mwv != -INFINITY) ll = ffma(wml[(w * 4 + tid) * 2 + 1], exp2f(mwv - mm), ll);
+        }
+        cpart[2 * 4 * D + (si.hot * 4 + tid) * 2] = mm;
+        cpart[2 * 4 * D + (si.hot * 4 + tid) * 2 + 1] = ll;
+      }
+    } else {
+      const long long slot = static_cast<long long>(blockIdx.x) + si.row;
+      for (int i = tid; i < G * D; i += M::kThreads) {
+        const int at = comb_at(i / D, i % D);
+        float sum = 0.0f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) sum = fadd(sum, comb[w * 4 * 136 + at]);
+        p.ws_acc[slot * G * D + i] = fmul(sum, unscale);
+      }
+      if (tid < G) {
+        float mm = -INFINITY, ll = 0.0f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) mm = fmaxf(mm, wml[(w * 4 + tid) * 2]);
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+          const float mwv = wml[(w * 4 + tid) * 2];
+          if (mwv != -INFINITY) ll = ffma(wml[(w * 4 + tid) * 2 + 1], exp2f(mwv - mm), ll);
+        }
+        p.ws_ml[(slot * G + tid) * 2] = mm;
+        p.ws_ml[(slot * G + tid) * 2 + 1] = ll;
+      }
     }
     __syncthreads();
     seg = seg_end;
   }
   cp_async_wait<0>();
+  if constexpr (CL) {
+    // merge of the row's partials through distributed shared memory: CTA rank
+    // hd < G combines query head hd of every CTA of the cluster (one warp, lane l
+    // holding coordinates 4 l .. 4 l + 3) and writes the output; the second
+    // barrier keeps every CTA's shared memory alive until the reads are done
+    cluster_sync_all();
+    const int rank = blockIdx.x % kClusterCtas, crow = blockIdx.x / kClusterCtas;
+    if (rank < G && warp == 0) {
+      const int hd = rank, rb = crow / p.hkv, rh = crow % p.hkv;
+      const uint32_t base = static_cast<uint32_t>(__cvta_generic_to_shared(cpart));
+      float2 ml[2 * kClusterCtas];
+      float4 av[2 * kClusterCtas];
+#pragma unroll
+      for (int r = 0; r < kClusterCtas; ++r) {
+        const uint32_t rbase = map_cluster(base, r);
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+          ml[2 * r + part] = ld_cluster_f2(rbase + 4u * (2 * 4 * D + (part * 4 + hd) * 2));
+          av[2 * r + part] = ld_cluster_f4(rbase + 4u * ((part * 4 + hd) * D + 4 * lane));
+        }
+      }
+      float mm = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 2 * kClusterCtas; ++i) mm = fmaxf(mm, ml[i].x);
+      float l = 0.0f, y[4] = {0.0f, 0.0f, 0.0f, 0.0f}, hv[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int i = 0; i < 2 * kClusterCtas; ++i) {
+        if (ml[i].x == -INFINITY) continue;  // a CTA without tiles of this part
+        const float sc = exp2f(ml[i].x - mm);
+        l = ffma(ml[i].y, sc, l);
+        const float a[4] = {av[i].x, av[i].y, av[i].z, av[i].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          if (i & 1) hv[k] = ffma(a[k], sc, hv[k]);
+          else y[k] = ffma(a[k], sc, y[k]);
+        }
+      }
+      unsigned neg4 = 0u;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) neg4 |= sign_negative(p.seed, p.layer, rh, 4 * lane + i) ? 1u << i : 0u;
+      merge_finish(y, hv, l, neg4, true, p.out + (static_cast<int64_t>(rb) * p.hq + rh * G + hd) * D, lane);
+    }
+    cluster_sync_all();
+  }
 }
 
 template <int G, int KB, bool SPARSE, bool PAGED, bool MQ>
@@ -677,6 +795,38 @@ tq_status launch_mma(const DecodeParams& p, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return TQ_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+// Cluster variant (one cluster of kClusterCtas CTAs per (b, h) row, partials
+// merged through distributed shared memory, no merge launch).  Returns
+// TQ_ERR_UNSUPPORTED without launching when the rows do not fit in one wave of
+// clusters on this GPU (the caller then runs the persistent split kernel).
+template <int G, int KB>
+tq_status launch_mma_cluster(const DecodeParams& p, cudaStream_t stream) {
+  using M = MmaCfg<KB, true>;
+  auto kern = decode_mma_kernel<G, KB, false, false, false, true>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, M::kSmem) != cudaSuccess)
+    return TQ_ERR_CUDA;
+  const long long rows = static_cast<long long>(p.batch) * p.hkv;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(rows * kClusterCtas));
+  cfg.blockDim = dim3(M::kThreads);
+  cfg.dynamicSmemBytes = M::kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kClusterCtas;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  int fit = 0;  // clusters resident at once (a property of the device and the kernel)
+  if (cudaOccupancyMaxActiveClusters(&fit, kern, &cfg) != cudaSuccess) return TQ_ERR_CUDA;
+  if (rows > fit) return TQ_ERR_UNSUPPORTED;
   if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return TQ_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }

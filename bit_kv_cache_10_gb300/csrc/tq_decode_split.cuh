@@ -1264,6 +1264,47 @@ __global__ void __launch_bounds__(Cfg<KB, VB>::kThreads, 1) decode_split_kernel(
   cp_async_wait<0>();
 }
 
+// Output of one (b, query head) row from its merged sums, by a full warp (lane
+// l holds coordinates 4 l .. 4 l + 3): the cold sum y is rotated back, D_h H y /
+// sqrt(d) (sign flips neg4, a Hadamard transform over index bits 0..1 in
+// registers and 2..6 across lanes; not in the int8 mode, whose V is summed
+// unrotated), the hot sum hv is added and the softmax mass l divided out (a row
+// that read no token gives zeros).
+__device__ __forceinline__ void merge_finish(float (&y)[4], const float (&hv)[4], float l, unsigned neg4, bool rotated,
+                                             float* out_row, int lane) {
+  float4* out = reinterpret_cast<float4*>(out_row);
+  if (!rotated) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) y[i] = l > 0.0f ? fadd(y[i], hv[i]) / l : 0.0f;
+    out[lane] = make_float4(y[0], y[1], y[2], y[3]);
+    return;
+  }
+  {
+    float a0 = fadd(y[0], y[1]), a1 = fsub(y[0], y[1]), a2 = fadd(y[2], y[3]), a3 = fsub(y[2], y[3]);  // bit 0
+    y[0] = fadd(a0, a2);  // bit 1
+    y[2] = fsub(a0, a2);
+    y[1] = fadd(a1, a3);
+    y[3] = fsub(a1, a3);
+  }
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {  // bits 2..6
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float o = __shfl_xor_sync(0xffffffffu, y[i], m);
+      y[i] = upper ? fsub(o, y[i]) : fadd(y[i], o);
+    }
+  }
+  float r[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float v = fmul(y[i], 1.0f / kSqrtD);
+    if ((neg4 >> i) & 1u) v = -v;
+    r[i] = l > 0.0f ? fadd(v, hv[i]) / l : 0.0f;
+  }
+  out[lane] = make_float4(r[0], r[1], r[2], r[3]);
+}
+
 // CTA of the split kernel that processes tile t (the last one whose range starts
 // at or before t): floor(((t + 1) grid - 1) / total), a value below grid.  A float
 // estimate of the quotient is off by at most one (its relative error is a few

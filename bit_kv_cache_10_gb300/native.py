@@ -33,6 +33,7 @@ EXPORTED = (
     "tq_cache_desc_init", "tq_cache_buffer_bytes", "tq_quantize_append", "tq_decode_workspace_bytes",
     "tq_decode_attention", "tq_dequantize", "tq_debug_quantize_rows_host", "tq_decode_attention_no_alloc",
     "tq_cache_desc_set_paged", "tq_multi_query_workspace_bytes", "tq_multi_query_attention",
+    "tq_debug_set_decode_path",
 )
 TQ_DEV_ERR_APPEND_RANGE, TQ_DEV_ERR_SEQ_LEN, TQ_DEV_ERR_LAYOUT, TQ_DEV_ERR_BLOCK = 0x1, 0x2, 0x4, 0x8
 TQ_NO_ALLOC_WORKSPACE_BYTES = 16 << 20
@@ -111,6 +112,8 @@ def lib() -> ctypes.CDLL:
         L.tq_dequantize.restype = c_int32
         L.tq_dequantize.argtypes = [POINTER(TQCacheDesc), c_int32, c_int32, c_int32, c_int32, c_int32, c_void_p,
                                     c_void_p]
+        L.tq_debug_set_decode_path.restype = None
+        L.tq_debug_set_decode_path.argtypes = [c_int32]
         L.tq_debug_quantize_rows_host.restype = c_int32
         L.tq_debug_quantize_rows_host.argtypes = [POINTER(TQCodebook), c_uint64, c_int32, c_int32, POINTER(c_uint16),
                                                   c_int32, POINTER(c_uint32), POINTER(c_float)]
@@ -218,3 +221,9 @@ def tq_debug_quantize_rows_host(cb: TQCodebook, seed: int, layer: int, head: int
         ctypes.byref(cb), seed, layer, head, rows.view(np.uint16).ctypes.data_as(POINTER(c_uint16)), n,
         words.ctypes.data_as(POINTER(c_uint32)), norms.ctypes.data_as(POINTER(c_float))), "tq_debug_quantize_rows_host")
     return words, norms
+
+
+def tq_debug_set_decode_path(path: int) -> None:
+    """Decode path for tests (process-wide): 0 automatic, 1 persistent split-K
+    kernel + merge kernel, 2 the thread-block-cluster variant where allowed."""
+    lib().tq_debug_set_decode_path(int(path))

@@ -26,6 +26,17 @@ extern "C" {
 tq_status tq_debug_quantize_rows_host(const tq_codebook *cb, uint64_t seed, int32_t layer, int32_t head,
                                       const uint16_t *rows, int32_t n_rows, uint32_t *words, float *norms);
 
+/*
+ * Decode path for tests of tq_decode_attention (process-wide, not thread
+ * safe against concurrent calls): 0 selects automatically (the default), 1
+ * always runs the persistent split-K kernel followed by the merge kernel, 2
+ * runs the cluster variant (one thread-block cluster per (sequence, KV head)
+ * row, merged in distributed shared memory) wherever the mode allows it:
+ * packed K of 2..4 bits with 4-bit V, dense V, contiguous layout, and every
+ * row's cluster resident on the GPU at once.  Any other value means 0.
+ */
+void tq_debug_set_decode_path(int32_t path);
+
 #ifdef __cplusplus
 }
 #endif

@@ -78,7 +78,14 @@ def test_paged_equals_contiguous(hot, k_fp16):
     # decode and dequantize
     q = _dev(synth.queries_fp16(17, B, HQ, D))
     sl = _dev(lens)
-    np.testing.assert_array_equal(paged.decode(q, sl, cap).cpu().numpy(), flat.decode(q, sl, cap).cpu().numpy())
+    # the paged layout always runs the persistent split kernel: the contiguous
+    # decode it must equal bit for bit is taken through the same kernel
+    N.tq_debug_set_decode_path(1)
+    try:
+        ref = flat.decode(q, sl, cap).cpu().numpy()
+    finally:
+        N.tq_debug_set_decode_path(0)
+    np.testing.assert_array_equal(paged.decode(q, sl, cap).cpu().numpy(), ref)
     for which in (0, 1):
         for b in range(B):
             L = int(lens[b])
@@ -100,7 +107,11 @@ def test_block_outside_the_pool_is_flagged_and_skipped():
     out = paged.decode(q, _dev(lens), cap).cpu().numpy()
     assert paged.device_status() & N.TQ_DEV_ERR_BLOCK
     assert np.all(np.isfinite(out))
-    ref = flat.decode(q, _dev(lens), cap).cpu().numpy()
+    N.tq_debug_set_decode_path(1)  # the persistent split kernel, as for the paged layout
+    try:
+        ref = flat.decode(q, _dev(lens), cap).cpu().numpy()
+    finally:
+        N.tq_debug_set_decode_path(0)
     np.testing.assert_array_equal(out[0], ref[0])  # sequence 0 does not use the bad block
 
 
