@@ -219,21 +219,55 @@ __global__ void __launch_bounds__(MmaCfg<KB, CL>::kThreads, 1) decode_mma_kernel
     for (int e = tid; e < 256 + kK; e += M::kThreads) {
       if (e < 256) {
         const uint2 v = pair_entry(p.v_cent[e & 15], p.v_cent[e >> 4]);
-        uint32_t* row = reinterpret_cast<uint32_t*>(ptr(tab + (e << 8)));
-        for (int c0 = 0; c0 < 32; ++c0) {
-          const int c = (c0 + lane) & 31;
-          row[c] = v.x;
-          row[32 + c] = v.y;
+        if constexpr (CL) {  // latency first: 16-byte stores, the 8 lanes of a store phase in 8 distinct chunks
+          uint4* row = reinterpret_cast<uint4*>(ptr(tab + (e << 8)));
+          const uint4 hi4 = make_uint4(v.x, v.x, v.x, v.x), lo4 = make_uint4(v.y, v.y, v.y, v.y);
+#pragma unroll
+          for (int c0 = 0; c0 < 8; ++c0) {
+            row[(c0 + lane) & 7] = hi4;
+            row[8 + ((c0 + lane) & 7)] = lo4;
+          }
+        } else {
+          uint32_t* row = reinterpret_cast<uint32_t*>(ptr(tab + (e << 8)));
+          for (int c0 = 0; c0 < 32; ++c0) {
+            const int c = (c0 + lane) & 31;
+            row[c] = v.x;
+            row[32 + c] = v.y;
+          }
         }
       } else {
         const int ek = e - 256;
         const uint2 v = pair_entry(p.k_cent[ek & ((1 << KB) - 1)], p.k_cent[ek >> KB]);
-        uint2* row = reinterpret_cast<uint2*>(ptr(tab + 65536 + (ek << 7)));
-        for (int c0 = 0; c0 < kCopies; ++c0) row[(c0 + lane) & (kCopies - 1)] = v;
+        if constexpr (CL) {
+          uint4* row = reinterpret_cast<uint4*>(ptr(tab + 65536 + (ek << 7)));
+          const uint4 v4 = make_uint4(v.x, v.y, v.x, v.y);
+#pragma unroll
+          for (int c0 = 0; c0 < kCopies / 2; ++c0) row[(c0 + lane) & (kCopies / 2 - 1)] = v4;
+        } else {
+          uint2* row = reinterpret_cast<uint2*>(ptr(tab + 65536 + (ek << 7)));
+          for (int c0 = 0; c0 < kCopies; ++c0) row[(c0 + lane) & (kCopies - 1)] = v;
+        }
       }
     }
   }
+  // cluster variant: the CTA's row is known from its index, so the rotation
+  // signs of the query (parameters only) are computed before the wait and the
+  // query itself is loaded right after it, alongside the sequence lengths
+  unsigned cl_neg = 0u;
+  uint2 cl_q = make_uint2(0u, 0u);
+  if constexpr (CL) {
+    const int crow = blockIdx.x / kClusterCtas;
+    if (warp < G)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) cl_neg |= sign_negative(p.seed, p.layer, crow % p.hkv, 4 * lane + i) ? 1u << i : 0u;
+  }
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  if constexpr (CL) {
+    const int crow = blockIdx.x / kClusterCtas;
+    if (warp < G)
+      cl_q = *reinterpret_cast<const uint2*>(p.q + (static_cast<int64_t>(crow / p.hkv) * p.hq + (crow % p.hkv) * G + warp) * D +
+                                             4 * lane);
+  }
   if (blockIdx.x == 0 && tid == 0 && p.status != nullptr) {
     for (int b = 0; b < p.batch / p.nq; ++b) {
       const int len = p.seq_lens[b];
@@ -320,8 +354,13 @@ __global__ void __launch_bounds__(MmaCfg<KB, CL>::kThreads, 1) decode_mma_kernel
     cp_async_commit();
     ++j_issue;
   };
+  if constexpr (CL) {
+#pragma unroll 1
+    for (int st = 0; st < S - 1; ++st) issue();  // one copy of the code: it runs once per CTA here
+  } else {
 #pragma unroll
-  for (int st = 0; st < S - 1; ++st) issue();
+    for (int st = 0; st < S - 1; ++st) issue();
+  }
 
   long long seg = t0;
   while (seg < t1) {
@@ -333,8 +372,9 @@ __global__ void __launch_bounds__(MmaCfg<KB, CL>::kThreads, 1) decode_mma_kernel
       // 0 and 1 in registers, bits 2..6 across lanes, in ascending order)
       __syncthreads();
       if (warp < G) {
-        const uint2 raw = *reinterpret_cast<const uint2*>(p.q + (static_cast<int64_t>(si.b) * p.hq + si.h * G + warp) * D +
-                                                          4 * lane);
+        uint2 raw;
+        if constexpr (CL) raw = cl_q;  // the cluster variant's one row, loaded after the wait
+        else raw = *reinterpret_cast<const uint2*>(p.q + (static_cast<int64_t>(si.b) * p.hq + si.h * G + warp) * D + 4 * lane);
         float x[4];
         const float2 x01 = half2_bits_to_float2(raw.x), x23 = half2_bits_to_float2(raw.y);
         x[0] = x01.x;
@@ -343,7 +383,7 @@ __global__ void __launch_bounds__(MmaCfg<KB, CL>::kThreads, 1) decode_mma_kernel
         x[3] = x23.y;
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-          if (sign_negative(p.seed, p.layer, si.h, 4 * lane + i)) x[i] = -x[i];
+          if (CL ? ((cl_neg >> i) & 1u) != 0 : sign_negative(p.seed, p.layer, si.h, 4 * lane + i)) x[i] = -x[i];
         float a0 = fadd(x[0], x[1]), a1 = fsub(x[0], x[1]), a2 = fadd(x[2], x[3]), a3 = fsub(x[2], x[3]);  // bit 0
         x[0] = fadd(a0, a2);  // bit 1
         x[2] = fsub(a0, a2);
