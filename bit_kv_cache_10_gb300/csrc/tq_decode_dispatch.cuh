@@ -2,8 +2,8 @@
 // translation units (each instantiates one variant: dense or sparse V,
 // contiguous or paged layout, one or several query tokens per sequence).
 //
-// Packed K of 2..4 bits with packed 4-bit V runs the tensor-core kernel
-// (tq_decode_mma.cuh); fp16 K, the int8 mode and the other V widths run the
+// Packed K of 2..4 bits or fp16 K, with packed 4-bit V, runs the tensor-core
+// kernel (tq_decode_mma.cuh); the int8 mode and V of 2 or 3 bits run the
 // float32 kernel (tq_decode_split.cuh), whose fp16 and int8 scores are on the
 // tensor cores too.
 #pragma once
@@ -20,7 +20,7 @@ tq_status dispatch_vb(const DecodeParams& p, int vb, cudaStream_t s) {
     case 2: return launch_split<G, KB, 2, SPARSE, PAGED, MQ>(p, s);
     case 3: return launch_split<G, KB, 3, SPARSE, PAGED, MQ>(p, s);
     default:
-      if constexpr (KB >= 2 && KB <= 4) return launch_mma<G, KB, SPARSE, PAGED, MQ>(p, s);
+      if constexpr ((KB >= 2 && KB <= 4) || KB == 16) return launch_mma<G, KB, SPARSE, PAGED, MQ>(p, s);
       else return launch_split<G, KB, 4, SPARSE, PAGED, MQ>(p, s);
   }
 }

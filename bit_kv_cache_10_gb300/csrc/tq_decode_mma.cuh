@@ -60,13 +60,20 @@ constexpr int kClusterCtas = 8;  // CTAs of a (b, h) row in the cluster variant 
 template <int KB, bool CL = false>
 struct MmaCfg {
   using Stage = Cfg<KB, 4>;                  // K | K norms | V | V norms, with V rows padded:
+  static constexpr bool kF16K = KB == 16;    // fp16 K (asym): K tiles read with ldmatrix, no K table
+  // fp16 K rows 256 + 16 bytes apart (the 8 rows of an ldmatrix phase hit distinct banks)
+  static constexpr int kKPitch = kF16K ? 272 : Stage::kKPitch;
+  static constexpr int kKTile = kTile * kKPitch;
+  static constexpr int kKNorm = Stage::kKNorm;
   static constexpr int kVPitch = 80;         // 64-byte records 80 bytes apart (conflict-free V code loads)
   static constexpr int kVTile = kTile * kVPitch;
-  static constexpr int kBuf = Stage::kKTile + Stage::kKNorm + kVTile + kTile * 4;
-  static constexpr int kWarps = 12;
+  static constexpr int kBuf = kKTile + kKNorm + kVTile + kTile * 4;
+  // fp16 K tiles are 2.7 times larger: 10 warps keep two stages each within the budget
+  static constexpr int kWarps = kF16K ? 10 : 12;
   static constexpr int kThreads = kWarps * 32;
   static constexpr int kTabAlign = 65536;
-  static constexpr int kTab = 65536 + (1 << (2 * KB)) * 128;  // V table (256-byte rows) | K table (128-byte rows)
+  static constexpr int kKTabRows = kF16K ? 0 : 1 << (2 * (kF16K ? 2 : KB));
+  static constexpr int kTab = 65536 + kKTabRows * 128;  // V table (256-byte rows) | K table (128-byte rows)
   static constexpr int kW16 = 2 * 4 * kTile * 2;  // per warp: fp16 weights [hi/lo][head][token]
   // cluster variant: the CTA's cold and hot partials, acc [part][4][D] then (m, l) [part][4]
   static constexpr int kPart = CL ? 2 * 4 * (D + 2) * 4 : 0;
@@ -105,6 +112,13 @@ __device__ __forceinline__ uint2 pair_entry(float ca, float cb) {
   split_f16(fmul(ca, kCentScale), ha, la);
   split_f16(fmul(cb, kCentScale), hb, lb);
   return make_uint2(pack16(ha, hb), pack16(la, lb));
+}
+
+// Four 8x8 fp16 matrices from shared memory in the mma.sync A-fragment layout.
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& a0, uint32_t& a1, uint32_t& a2, uint32_t& a3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];\n"
+               : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+               : "r"(addr));
 }
 
 __device__ __forceinline__ uint2 lds64a(uint32_t addr) {
@@ -215,7 +229,7 @@ __global__ void __launch_bounds__(MmaCfg<KB, CL>::kThreads, 1) decode_mma_kernel
   // and writes its copies in an order rotated by the lane, so that the 32 stores
   // of a warp fall in 32 distinct banks
   {
-    constexpr int kK = 1 << (2 * KB);
+    constexpr int kK = M::kKTabRows;
     for (int e = tid; e < 256 + kK; e += M::kThreads) {
       if (e < 256) {
         const uint2 v = pair_entry(p.v_cent[e & 15], p.v_cent[e >> 4]);
@@ -237,7 +251,8 @@ __global__ void __launch_bounds__(MmaCfg<KB, CL>::kThreads, 1) decode_mma_kernel
         }
       } else {
         const int ek = e - 256;
-        const uint2 v = pair_entry(p.k_cent[ek & ((1 << KB) - 1)], p.k_cent[ek >> KB]);
+        constexpr int kb = M::kF16K ? 2 : KB;  // (no K table for fp16 K)
+        const uint2 v = pair_entry(p.k_cent[ek & ((1 << kb) - 1)], p.k_cent[ek >> kb]);
         if constexpr (CL) {
           uint4* row = reinterpret_cast<uint4*>(ptr(tab + 65536 + (ek << 7)));
           const uint4 v4 = make_uint4(v.x, v.y, v.x, v.y);
@@ -339,7 +354,7 @@ __global__ void __launch_bounds__(MmaCfg<KB, CL>::kThreads, 1) decode_mma_kernel
       const int t_begin = cursor_t_begin(cur);
       const int n_valid = cursor_n_valid(cur);
       const int cb = cache_seq<MQ>(p, cur.b);
-      const int staged = stage_tile<KB, 4, PAGED, M::kVPitch>(p, cb, cur.h, hot, t_begin, n_valid, tb,
+      const int staged = stage_tile<KB, 4, PAGED, M::kVPitch, M::kKPitch>(p, cb, cur.h, hot, t_begin, n_valid, tb,
                                                               ring + static_cast<uint32_t>((j_issue % S) * M::kBuf), lane);
       if (hot && (lane >> 1) < n_valid) {  // the fp16 ring rows of a hot tile into L1: 128 bytes per lane
         const int pos = t_begin + (lane >> 1);
@@ -367,6 +382,20 @@ __global__ void __launch_bounds__(MmaCfg<KB, CL>::kThreads, 1) decode_mma_kernel
     const TileInfo si = tile_info<MQ>(p, prefix, seg);
     const long long seg_end = si.row_end < t1 ? si.row_end : t1;
     if (si.b != cur_b || si.h != cur_h) {
+      if constexpr (M::kF16K) {
+        // fp16 K: the scores are q . k / sqrt(d) with the raw fp16 query, exact
+        // operands.  Lane (g, t) holds column g (query head g of the group, zero
+        // for g >= G) of every chunk's B fragment: coordinates 16 c + 2 t, + 1
+        // and 16 c + 2 t + 8, + 9 (two 32-bit words of the query row).
+        const uint32_t* q32 =
+            reinterpret_cast<const uint32_t*>(p.q + (static_cast<int64_t>(si.b) * p.hq + si.h * G + (g < G ? g : 0)) * D);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          qb[2 * c] = g < G ? q32[8 * c + t] : 0u;
+          qb[2 * c + 1] = g < G ? q32[8 * c + t + 4] : 0u;
+        }
+        sc[0] = sc[1] = kLog2e / kSqrtD;
+      } else {
       // rotated query of the G heads, H D q (unnormalized), in qs: warp jj
       // transforms head jj, lane l holding coordinates 4 l .. 4 l + 3 (index bits
       // 0 and 1 in registers, bits 2..6 across lanes, in ascending order)
@@ -457,6 +486,7 @@ __global__ void __launch_bounds__(MmaCfg<KB, CL>::kThreads, 1) decode_mma_kernel
 #pragma unroll
         for (int i = 0; i < 2; ++i) sc[i] = kLog2e / static_cast<float>(D) * kCentUnscale / qsc_s[4 * ((h0 + i) & 3)];
       }
+      }
       cur_b = si.b;
       cur_h = si.h;
     }
@@ -481,6 +511,27 @@ __global__ void __launch_bounds__(MmaCfg<KB, CL>::kThreads, 1) decode_mma_kernel
 
       // ---- scores on the tensor cores: tokens 0..7 and 8..15 in two MMA chains,
       // A row g = hi and row g + 8 = lo halves of the token's centroids
+      float sacc[4];
+      if constexpr (M::kF16K) {
+        // tokens as M (rows g and g + 8 of an MMA are tokens g and g + 8), chunk c =
+        // coordinates 16 c .. 16 c + 15 as K, the query heads as N; ldmatrix reads
+        // the A fragment from the staged fp16 rows (lane l addresses row l mod 16,
+        // coordinate half l / 16)
+        float dk[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        const uint32_t arow = tbs + static_cast<uint32_t>((lane & 15) * M::kKPitch + (lane >> 4) * 16);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(arow + 32u * c, a0, a1, a2, a3);
+          mma_f16(dk, a0, a1, a2, a3, qb[2 * c], qb[2 * c + 1]);
+        }
+        // columns 2 t, 2 t + 1 of tokens g and g + 8 (columns >= 4 are zero), laid out
+        // as the hi / lo sums below so that the same exchange gives every lane its dot
+        sacc[0] = dk[0];
+        sacc[1] = dk[1];
+        sacc[2] = dk[2];
+        sacc[3] = dk[3];
+      } else {
       float dh[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
       {
         constexpr int kWords = KB;  // 32 coordinates x KB bits
@@ -523,11 +574,11 @@ __global__ void __launch_bounds__(MmaCfg<KB, CL>::kThreads, 1) decode_mma_kernel
         chunk(std::integral_constant<int, 7>{});
       }
       // rows g (hi) + g + 8 (lo): columns 2 t, 2 t + 1 of token g (dh[0]) and g + 8 (dh[1])
-      float sacc[4];
       sacc[0] = fadd(dh[0][0], dh[0][2]);
       sacc[1] = fadd(dh[0][1], dh[0][3]);
       sacc[2] = fadd(dh[1][0], dh[1][2]);
       sacc[3] = fadd(dh[1][1], dh[1][3]);
+      }
       // hi and lo columns of the lane's token: lanes t < 2 hold the hi columns of
       // token g, lanes t >= 2 the lo columns of token g + 8; exchange with t ^ 2
       float dot[2];
@@ -540,10 +591,10 @@ __global__ void __launch_bounds__(MmaCfg<KB, CL>::kThreads, 1) decode_mma_kernel
       }
 
       // ---- online softmax (base 2); weights below 2^8 (see the header)
-      const float* knorm = reinterpret_cast<const float*>(tbp + C::kKTile);
-      const float* vnorm = reinterpret_cast<const float*>(tbp + C::kKTile + C::kKNorm + M::kVTile);
+      const float* knorm = reinterpret_cast<const float*>(tbp + M::kKTile);
+      const float* vnorm = reinterpret_cast<const float*>(tbp + M::kKTile + M::kKNorm + M::kVTile);
       const bool tok_ok = tau < n_valid;
-      const float nk = knorm[tau];
+      const float nk = M::kF16K ? 1.0f : knorm[tau];  // fp16 K: the dot product is the score
       const float nv = hot ? 1.0f : vnorm[tau];
       int ev = static_cast<int>((__float_as_uint(nv) >> 23) & 0xFFu) - 127;
       ev = ev < -64 ? -64 : ev;
@@ -615,7 +666,7 @@ __global__ void __launch_bounds__(MmaCfg<KB, CL>::kThreads, 1) decode_mma_kernel
         const uint32_t wb = w16 + static_cast<uint32_t>(((g >> 2) * 4 + (g & 3)) * kTile * 2);
         const uint32_t b0 = lds32<0>(wb + 4u * t), b1 = lds32<0>(wb + 4u * t + 16u);
         if (!hot) {
-          const uint32_t vt = tbs + static_cast<uint32_t>(C::kKTile + C::kKNorm) + v_win;
+          const uint32_t vt = tbs + static_cast<uint32_t>(M::kKTile + M::kKNorm) + v_win;
           constexpr int P = M::kVPitch;
           const uint2 wa = lds64u<0>(vt + static_cast<uint32_t>((2 * t) * P));
           const uint2 wbw = lds64u<0>(vt + static_cast<uint32_t>((2 * t + 1) * P));

@@ -532,11 +532,12 @@ __device__ __forceinline__ TileBlocks load_tile_blocks(const DecodeParams& p, in
 // (blocks hold at least one tile); a hot tile (K only) that straddles a block
 // boundary is copied token by token.  The common case (a full tile inside one
 // valid block) takes one branch; the others share the second.
-template <int KB, int VB, int VPITCH>
+template <int KB, int VB, int VPITCH, int KPITCH>
 __device__ __forceinline__ int stage_tile_paged(const DecodeParams& p, int h, bool hot, int t_begin, int n_valid,
                                              TileBlocks tb, uint32_t buf, int lane) {
   using C = Cfg<KB, VB>;
   constexpr int kVTileP = kTile * VPITCH;
+  constexpr int kKP = KPITCH ? KPITCH : C::kKPitch, kKTileP = kTile * kKP;
   const int sh = p.map.shift;
   const unsigned nb = static_cast<unsigned>(p.map.num_blocks);
   const bool in_pool = static_cast<unsigned>(tb.first) < nb && static_cast<unsigned>(tb.last) < nb;
@@ -544,10 +545,10 @@ __device__ __forceinline__ int stage_tile_paged(const DecodeParams& p, int h, bo
   const long long row0 = ((static_cast<long long>(tb.first) * p.map.hkv + h) << sh) + (t_begin & ((1 << sh) - 1));
   const uint8_t* kbase = C::kFp16K ? reinterpret_cast<const uint8_t*>(p.k_fp16)
                                    : reinterpret_cast<const uint8_t*>(p.k_words);
-  const uint32_t vbuf = buf + C::kKTile + C::kKNorm;
+  const uint32_t vbuf = buf + kKTileP + C::kKNorm;
   long long rn = row0 + (lane & 15);  // norm row of the lane's token
   if (in_pool && one_block && n_valid == kTile) {
-    copy_full_pitched<C::kKRow, C::kKPitch>(buf, kbase + row0 * C::kKRow, lane);
+    copy_full_pitched<C::kKRow, kKP>(buf, kbase + row0 * C::kKRow, lane);
     if (!hot) copy_full_pitched<VB * 16, VPITCH>(vbuf, reinterpret_cast<const uint8_t*>(p.v_words) + row0 * (VB * 16), lane);
   } else {
     if (!in_pool) {  // outside the pool: nothing is staged, the tile is read as empty
@@ -559,7 +560,7 @@ __device__ __forceinline__ int stage_tile_paged(const DecodeParams& p, int h, bo
     for (int c = lane; c < n_valid * kPer; c += 32) {  // K token by token (a partial or a straddling tile)
       const int t = t_begin + c / kPer;
       const long long r = p.map.in_block((t >> sh) == blk0 ? tb.first : tb.last, h, t);
-      cp_async16s(buf + k_chunk_dst<C::kKRow, C::kKPitch>(c), kbase + r * C::kKRow + (c % kPer) * 16);
+      cp_async16s(buf + k_chunk_dst<C::kKRow, kKP>(c), kbase + r * C::kKRow + (c % kPer) * 16);
     }
     if (!hot) {  // cold tiles never straddle
       const uint8_t* vsrc = reinterpret_cast<const uint8_t*>(p.v_words) + row0 * (VB * 16);
@@ -573,7 +574,7 @@ __device__ __forceinline__ int stage_tile_paged(const DecodeParams& p, int h, bo
   const bool is_k = lane < 16;
   const bool want = nl < n_valid && (is_k ? !C::kFp16K : !hot);
   const float* nsrc = (is_k ? p.k_norms : p.v_norms) + rn;
-  const uint32_t ndst = (is_k ? buf + C::kKTile : vbuf + kVTileP) + 4u * nl;
+  const uint32_t ndst = (is_k ? buf + kKTileP : vbuf + kVTileP) + 4u * nl;
   if (want) cp_async4s(ndst, nsrc);
   return n_valid;
 }
@@ -581,23 +582,25 @@ __device__ __forceinline__ int stage_tile_paged(const DecodeParams& p, int h, bo
 // Stages tile [t_begin, t_begin + n_valid) of (b, h) into buf; returns the
 // number of tokens the consumer may read.
 // V rows are VPITCH bytes apart in the staged tile (VB * 16: contiguous).
-template <int KB, int VB, bool PAGED, int VPITCH = VB * 16>
+// KPITCH: pitch of the staged K rows (0: the split kernel's Cfg::kKPitch).
+template <int KB, int VB, bool PAGED, int VPITCH = VB * 16, int KPITCH = 0>
 __device__ __forceinline__ int stage_tile(const DecodeParams& p, int b, int h, bool hot, int t_begin, int n_valid,
                                           TileBlocks tb, uint32_t buf, int lane) {
   using C = Cfg<KB, VB>;
   constexpr int kVTileP = kTile * VPITCH;
-  if constexpr (PAGED) return stage_tile_paged<KB, VB, VPITCH>(p, h, hot, t_begin, n_valid, tb, buf, lane);
+  constexpr int kKP = KPITCH ? KPITCH : C::kKPitch, kKTileP = kTile * kKP;
+  if constexpr (PAGED) return stage_tile_paged<KB, VB, VPITCH, KPITCH>(p, h, hot, t_begin, n_valid, tb, buf, lane);
   const int64_t row0 = (static_cast<int64_t>(b) * p.hkv + h) * p.cap + t_begin;
   const uint8_t* ksrc = C::kFp16K ? reinterpret_cast<const uint8_t*>(p.k_fp16 + row0 * D)
                                   : reinterpret_cast<const uint8_t*>(p.k_words + row0 * (C::kKBits * 4));
   const uint8_t* vsrc = reinterpret_cast<const uint8_t*>(p.v_words + row0 * (VB * 4));
-  const uint32_t vbuf = buf + C::kKTile + C::kKNorm;
+  const uint32_t vbuf = buf + kKTileP + C::kKNorm;
   if (n_valid == kTile) {
-    copy_full_pitched<C::kKRow, C::kKPitch>(buf, ksrc, lane);
+    copy_full_pitched<C::kKRow, kKP>(buf, ksrc, lane);
     if (!hot) copy_full_pitched<VB * 16, VPITCH>(vbuf, vsrc, lane);
   } else {
     for (int c = lane; c < n_valid * (C::kKRow / 16); c += 32)
-      cp_async16s(buf + k_chunk_dst<C::kKRow, C::kKPitch>(c), ksrc + 16 * c);
+      cp_async16s(buf + k_chunk_dst<C::kKRow, kKP>(c), ksrc + 16 * c);
     if (!hot)
       for (int c = lane; c < n_valid * (C::kVRow / 16); c += 32)
         cp_async16s(vbuf + k_chunk_dst<VB * 16, VPITCH>(c), vsrc + 16 * c);
@@ -607,7 +610,7 @@ __device__ __forceinline__ int stage_tile(const DecodeParams& p, int b, int h, b
   const bool is_k = lane < 16;
   const bool want = nl < n_valid && (is_k ? !C::kFp16K : !hot);
   const float* nsrc = (is_k ? p.k_norms : p.v_norms) + row0 + nl;
-  const uint32_t ndst = (is_k ? buf + C::kKTile : vbuf + kVTileP) + 4u * nl;
+  const uint32_t ndst = (is_k ? buf + kKTileP : vbuf + kVTileP) + 4u * nl;
   if (want) cp_async4s(ndst, nsrc);
   return n_valid;
 }
