@@ -2,10 +2,9 @@
 // translation units (each instantiates one variant: dense or sparse V,
 // contiguous or paged layout, one or several query tokens per sequence).
 //
-// Packed K of 2..4 bits or fp16 K, with packed 4-bit V, runs the tensor-core
-// kernel (tq_decode_mma.cuh); the int8 mode and V of 2 or 3 bits run the
-// float32 kernel (tq_decode_split.cuh), whose fp16 and int8 scores are on the
-// tensor cores too.
+// Packed K of 2..4 bits or fp16 K with packed 4-bit V, and the int8 mode, run
+// the tensor-core kernel (tq_decode_mma.cuh); V of 2 or 3 bits runs the float32
+// kernel (tq_decode_split.cuh), whose fp16-K scores are on the tensor cores too.
 #pragma once
 
 #include "tq_decode_mma.cuh"
@@ -28,7 +27,7 @@ tq_status dispatch_vb(const DecodeParams& p, int vb, cudaStream_t s) {
 template <int G, bool SPARSE, bool PAGED, bool MQ>
 tq_status dispatch_kb(const DecodeParams& p, int kb, int vb, cudaStream_t s) {
   switch (kb) {
-    case 8: return launch_split<G, 8, 8, SPARSE, PAGED, MQ>(p, s);  // int8 mode
+    case 8: return launch_mma<G, 8, SPARSE, PAGED, MQ>(p, s);  // int8 mode
     case 2: return dispatch_vb<G, 2, SPARSE, PAGED, MQ>(p, vb, s);
     case 3: return dispatch_vb<G, 3, SPARSE, PAGED, MQ>(p, vb, s);
     case 4: return dispatch_vb<G, 4, SPARSE, PAGED, MQ>(p, vb, s);

@@ -59,21 +59,26 @@ constexpr int kClusterCtas = 8;  // CTAs of a (b, h) row in the cluster variant 
 
 template <int KB, bool CL = false>
 struct MmaCfg {
-  using Stage = Cfg<KB, 4>;                  // K | K norms | V | V norms, with V rows padded:
   static constexpr bool kF16K = KB == 16;    // fp16 K (asym): K tiles read with ldmatrix, no K table
+  static constexpr bool kI8 = KB == 8;       // int8 mode: int8 K and V codes, exact in fp16, no tables
+  static constexpr int kVB = kI8 ? 8 : 4;
+  using Stage = Cfg<KB, kVB>;                // K | K norms | V | V norms, with V rows padded:
   // fp16 K rows 256 + 16 bytes apart (the 8 rows of an ldmatrix phase hit distinct banks)
   static constexpr int kKPitch = kF16K ? 272 : Stage::kKPitch;
   static constexpr int kKTile = kTile * kKPitch;
   static constexpr int kKNorm = Stage::kKNorm;
-  static constexpr int kVPitch = 80;         // 64-byte records 80 bytes apart (conflict-free V code loads)
+  // 64-byte records 80 bytes apart (conflict-free V code loads); int8: 128-byte records 144 apart
+  static constexpr int kVPitch = kI8 ? 144 : 80;
   static constexpr int kVTile = kTile * kVPitch;
   static constexpr int kBuf = kKTile + kKNorm + kVTile + kTile * 4;
   // fp16 K tiles are 2.7 times larger: 10 warps keep two stages each within the budget
   static constexpr int kWarps = kF16K ? 10 : 12;
   static constexpr int kThreads = kWarps * 32;
-  static constexpr int kTabAlign = 65536;
-  static constexpr int kKTabRows = kF16K ? 0 : 1 << (2 * (kF16K ? 2 : KB));
-  static constexpr int kTab = 65536 + kKTabRows * 128;  // V table (256-byte rows) | K table (128-byte rows)
+  static constexpr int kTabAlign = kI8 ? 1024 : 65536;
+  static constexpr int kKTabRows = (kF16K || kI8) ? 0 : 1 << (2 * ((kF16K || kI8) ? 2 : KB));
+  static constexpr int kVTabRows = kI8 ? 0 : 256;
+  // V table (256-byte rows) | K table (128-byte rows); int8: a 1 KB placeholder
+  static constexpr int kTab = (kI8 ? 1024 : 65536) + kKTabRows * 128;
   static constexpr int kW16 = 2 * 4 * kTile * 2;  // per warp: fp16 weights [hi/lo][head][token]
   // cluster variant: the CTA's cold and hot partials, acc [part][4][D] then (m, l) [part][4]
   static constexpr int kPart = CL ? 2 * 4 * (D + 2) * 4 : 0;
@@ -198,7 +203,7 @@ __device__ __forceinline__ int comb_at(int h, int i) { return h * 136 + i + (i >
 template <int G, int KB, bool SPARSE, bool PAGED, bool MQ, bool CL = false>
 __global__ void __launch_bounds__(MmaCfg<KB, CL>::kThreads, 1) decode_mma_kernel(const DecodeParams p) {
   using M = MmaCfg<KB, CL>;
-  using C = Cfg<KB, 4>;
+  using C = Cfg<KB, M::kVB>;
   constexpr int S = M::kStages;
   constexpr int NW = M::kWarps;
   extern __shared__ __align__(16) uint8_t smem[];
@@ -229,9 +234,9 @@ __global__ void __launch_bounds__(MmaCfg<KB, CL>::kThreads, 1) decode_mma_kernel
   // and writes its copies in an order rotated by the lane, so that the 32 stores
   // of a warp fall in 32 distinct banks
   {
-    constexpr int kK = M::kKTabRows;
-    for (int e = tid; e < 256 + kK; e += M::kThreads) {
-      if (e < 256) {
+    constexpr int kK = M::kKTabRows, kV = M::kVTabRows;
+    for (int e = tid; e < kV + kK; e += M::kThreads) {
+      if (e < kV) {
         const uint2 v = pair_entry(p.v_cent[e & 15], p.v_cent[e >> 4]);
         if constexpr (CL) {  // latency first: 16-byte stores, the 8 lanes of a store phase in 8 distinct chunks
           uint4* row = reinterpret_cast<uint4*>(ptr(tab + (e << 8)));
@@ -250,7 +255,7 @@ __global__ void __launch_bounds__(MmaCfg<KB, CL>::kThreads, 1) decode_mma_kernel
           }
         }
       } else {
-        const int ek = e - 256;
+        const int ek = e - kV;
         constexpr int kb = M::kF16K ? 2 : KB;  // (no K table for fp16 K)
         const uint2 v = pair_entry(p.k_cent[ek & ((1 << kb) - 1)], p.k_cent[ek >> kb]);
         if constexpr (CL) {
@@ -354,7 +359,7 @@ __global__ void __launch_bounds__(MmaCfg<KB, CL>::kThreads, 1) decode_mma_kernel
       const int t_begin = cursor_t_begin(cur);
       const int n_valid = cursor_n_valid(cur);
       const int cb = cache_seq<MQ>(p, cur.b);
-      const int staged = stage_tile<KB, 4, PAGED, M::kVPitch, M::kKPitch>(p, cb, cur.h, hot, t_begin, n_valid, tb,
+      const int staged = stage_tile<KB, M::kVB, PAGED, M::kVPitch, M::kKPitch>(p, cb, cur.h, hot, t_begin, n_valid, tb,
                                                               ring + static_cast<uint32_t>((j_issue % S) * M::kBuf), lane);
       if (hot && (lane >> 1) < n_valid) {  // the fp16 ring rows of a hot tile into L1: 128 bytes per lane
         const int pos = t_begin + (lane >> 1);
@@ -382,17 +387,19 @@ __global__ void __launch_bounds__(MmaCfg<KB, CL>::kThreads, 1) decode_mma_kernel
     const TileInfo si = tile_info<MQ>(p, prefix, seg);
     const long long seg_end = si.row_end < t1 ? si.row_end : t1;
     if (si.b != cur_b || si.h != cur_h) {
-      if constexpr (M::kF16K) {
-        // fp16 K: the scores are q . k / sqrt(d) with the raw fp16 query, exact
-        // operands.  Lane (g, t) holds column g (query head g of the group, zero
-        // for g >= G) of every chunk's B fragment: coordinates 16 c + 2 t, + 1
-        // and 16 c + 2 t + 8, + 9 (two 32-bit words of the query row).
+      if constexpr (M::kF16K || M::kI8) {
+        // fp16 K and the int8 mode: the scores are q . k / sqrt(d) (times the K
+        // scale in the int8 mode) with the raw fp16 query, exact operands.  Lane
+        // (g, t) holds column g (query head g of the group, zero for g >= G) of
+        // every chunk's B fragment: for fp16 K coordinates 16 c + 2 t, + 1 and
+        // 16 c + 2 t + 8, + 9; for int8 K, whose chunk rows are permuted so that a
+        // lane's four codes are one word, coordinates 16 c + 4 t .. 16 c + 4 t + 3.
         const uint32_t* q32 =
             reinterpret_cast<const uint32_t*>(p.q + (static_cast<int64_t>(si.b) * p.hq + si.h * G + (g < G ? g : 0)) * D);
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          qb[2 * c] = g < G ? q32[8 * c + t] : 0u;
-          qb[2 * c + 1] = g < G ? q32[8 * c + t + 4] : 0u;
+          qb[2 * c] = g < G ? q32[M::kI8 ? 8 * c + 2 * t : 8 * c + t] : 0u;
+          qb[2 * c + 1] = g < G ? q32[M::kI8 ? 8 * c + 2 * t + 1 : 8 * c + t + 4] : 0u;
         }
         sc[0] = sc[1] = kLog2e / kSqrtD;
       } else {
@@ -512,7 +519,24 @@ __global__ void __launch_bounds__(MmaCfg<KB, CL>::kThreads, 1) decode_mma_kernel
       // ---- scores on the tensor cores: tokens 0..7 and 8..15 in two MMA chains,
       // A row g = hi and row g + 8 = lo halves of the token's centroids
       float sacc[4];
-      if constexpr (M::kF16K) {
+      if constexpr (M::kI8) {
+        // int8 K: tokens as M (rows g and g + 8), chunk c as K with k = 2 t, 2 t + 1 ->
+        // coordinates 16 c + 4 t, + 1 and k = 2 t + 8, 2 t + 9 -> 16 c + 4 t + 2, + 3:
+        // one 32-bit load per token and chunk, its codes made exact fp16 pairs
+        float dk[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        const uint32_t ka = tbs + static_cast<uint32_t>(g * M::kKPitch + 4 * t);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint32_t wg = lds32<0>(ka + 16u * c) ^ 0x80808080u;
+          const uint32_t wh = lds32<0>(ka + static_cast<uint32_t>(8 * M::kKPitch) + 16u * c) ^ 0x80808080u;
+          mma_f16(dk, int8_half2<0>(wg), int8_half2<0>(wh), int8_half2<2>(wg), int8_half2<2>(wh), qb[2 * c],
+                  qb[2 * c + 1]);
+        }
+        sacc[0] = dk[0];
+        sacc[1] = dk[1];
+        sacc[2] = dk[2];
+        sacc[3] = dk[3];
+      } else if constexpr (M::kF16K) {
         // tokens as M (rows g and g + 8 of an MMA are tokens g and g + 8), chunk c =
         // coordinates 16 c .. 16 c + 15 as K, the query heads as N; ldmatrix reads
         // the A fragment from the staged fp16 rows (lane l addresses row l mod 16,
@@ -665,7 +689,27 @@ __global__ void __launch_bounds__(MmaCfg<KB, CL>::kThreads, 1) decode_mma_kernel
       if (do_v) {
         const uint32_t wb = w16 + static_cast<uint32_t>(((g >> 2) * 4 + (g & 3)) * kTile * 2);
         const uint32_t b0 = lds32<0>(wb + 4u * t), b1 = lds32<0>(wb + 4u * t + 16u);
-        if (!hot) {
+        if (M::kI8 && !hot) {
+          // int8 V codes (exact fp16) in the layout of the hot rows: lane (g, t) holds
+          // coordinates 16 g .. 16 g + 15 of tokens 2 t, 2 t + 1, 2 t + 8, 2 t + 9 (one
+          // 16-byte load each); M block b pairs the bytes of coordinates 16 g + 2 b, + 1
+          const uint32_t vt = tbs + static_cast<uint32_t>(M::kKTile + M::kKNorm + 16 * g);
+          constexpr int P = M::kVPitch;
+          const uint4 xa = lds128<0>(vt + static_cast<uint32_t>((2 * t) * P));
+          const uint4 xb = lds128<0>(vt + static_cast<uint32_t>((2 * t + 1) * P));
+          const uint4 xc = lds128<0>(vt + static_cast<uint32_t>((2 * t + 8) * P));
+          const uint4 xd = lds128<0>(vt + static_cast<uint32_t>((2 * t + 9) * P));
+          auto w4 = [](const uint4& v, int i) { return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w; };
+#pragma unroll
+          for (int mb = 0; mb < 8; ++mb) {
+            const int wi = mb >> 1, c0 = 2 * (mb & 1);
+            const uint32_t sel = static_cast<uint32_t>(c0 | (4 + c0) << 4 | (c0 + 1) << 8 | (5 + c0) << 12);
+            // bytes (a, b) of coordinate 16 g + 2 mb, then of + 1, biased to code + 128
+            const uint32_t ab = __byte_perm(w4(xa, wi), w4(xb, wi), sel) ^ 0x80808080u;
+            const uint32_t cd = __byte_perm(w4(xc, wi), w4(xd, wi), sel) ^ 0x80808080u;
+            mma_f16(acc[mb], int8_half2<0>(ab), int8_half2<2>(ab), int8_half2<0>(cd), int8_half2<2>(cd), b0, b1);
+          }
+        } else if (!hot) {
           const uint32_t vt = tbs + static_cast<uint32_t>(M::kKTile + M::kKNorm) + v_win;
           constexpr int P = M::kVPitch;
           const uint2 wa = lds64u<0>(vt + static_cast<uint32_t>((2 * t) * P));
@@ -775,7 +819,7 @@ __global__ void __launch_bounds__(MmaCfg<KB, CL>::kThreads, 1) decode_mma_kernel
       }
     }
     __syncthreads();
-    const float unscale = si.hot ? 1.0f : kCentUnscale;  // cold sums carry the table scale
+    const float unscale = (si.hot || M::kI8) ? 1.0f : kCentUnscale;  // cold packed sums carry the table scale
     if constexpr (CL) {
       // the partial stays in this CTA's shared memory, part 0 cold and part 1 hot
       float* pa = cpart + si.hot * 4 * D;

@@ -70,7 +70,7 @@ def test_multi_query_matches_oracle(bits, hq, hot, nq):
         oc = oracle.build_cache(k, v, lens, CAP, 8, 8, hot_window=hot, codec="int8")
     else:
         oc = oracle.build_cache(k, v, lens, CAP, 16 if k_fp16 else bits[0], bits[1], hot_window=hot, k_fp16=k_fp16)
-        # decode parity is judged on the oracle's own cache (a counted code flip may differ)
+        # decode parity is checked on the oracle's own cache (a counted code flip may differ)
         upload(tc, oc)
     q = _queries(31, B, nq, hq)
     got = tc.multi_query(_dev(q), _dev(lens), CAP).cpu().numpy()
