@@ -12,6 +12,10 @@
 // own, whose length is its causal prefix; its tiles are read from the cache
 // rows of the sequence it belongs to.
 //
+// This float32 kernel serves V of 2 or 3 bits (packed or fp16 K); packed K of
+// 2..4 bits or fp16 K with 4-bit V and the int8 mode run the tensor-core kernel
+// (tq_decode_mma.cuh), which shares the work list, the staging and the merge.
+//
 // Split kernel: one CTA of 8 warps per SM (up to 255 registers per thread).  The
 // codebook pair tables are built once per CTA in shared memory (16 copies, one
 // per lane of a half-warp, so the data-dependent lookups are bank-conflict
@@ -21,7 +25,7 @@
 // ring of up to 8 tiles that runs across row boundaries.  Per tile:
 //   scores:  packed K: 8 lanes share a token, each owning 16 coordinates (8 code
 //            pairs, each looked up at once as (c_a, c_b)); 4 tokens per step, 4 steps.
-//            fp16 or int8 K: on the tensor cores (mma m16n8k16, exact fp16 operands),
+//            fp16 K: on the tensor cores (mma m16n8k16, exact fp16 operands),
 //            the softmax in the MMA fragment layout.
 //            Partial sums over the lane's coordinates for the G query heads,
 //            then a 3-stage transposing butterfly over the 8 lanes leaves each
@@ -218,7 +222,8 @@ struct Cfg {
   static constexpr int kKBits = kFp16K ? 2 : KB;       // placeholder width when K is fp16
   static constexpr int kKRow = kFp16K ? 256 : KB * 16;  // bytes of one K token
   static constexpr int kVRow = VB * 16;
-  // fp16 and int8 K: scores on the tensor cores (their values are exact in fp16);
+  // fp16 and int8 K: scores on the tensor cores (their values are exact in fp16; the
+  // int8 staging layout also serves the tensor-core kernel, which runs that mode);
   // the staged K rows are padded so that the MMA operand loads of 4 tokens by 4
   // lanes each fall in distinct banks (288 = 256 + 32, 144 = 128 + 16 bytes)
   static constexpr bool kMmaK = kFp16K || kInt8;
@@ -351,16 +356,6 @@ __device__ __forceinline__ uint32_t int8_half2(uint32_t xw) {
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 
-// Two int8 codes (bytes K and K + 1 of a word) as exact floats: the biased
-// byte u = code + 128 goes into the low mantissa byte of 2^23, and one packed
-// subtraction of 2^23 + 128 leaves the code.  `xw` is the word with every byte
-// already biased (w ^ 0x80808080).
-template <int K>
-__device__ __forceinline__ float2 int8_pair(uint32_t xw) {
-  const float a = __uint_as_float(__byte_perm(xw, 0x4B000000u, 0x7440 | K));
-  const float b = __uint_as_float(__byte_perm(xw, 0x4B000000u, 0x7440 | (K + 1)));
-  return add2(make_float2(a, b), make_float2(-8388736.0f, -8388736.0f));
-}
 // Shared loads at a register base plus a compile-time byte offset (no address arithmetic).
 template <int OFF>
 __device__ __forceinline__ uint32_t lds32(uint32_t base) {
@@ -619,6 +614,7 @@ __device__ __forceinline__ int stage_tile(const DecodeParams& p, int b, int h, b
 template <int G, int KB, int VB, bool SPARSE, bool PAGED, bool MQ>
 __global__ void __launch_bounds__(Cfg<KB, VB>::kThreads, 1) decode_split_kernel(const DecodeParams p) {
   using C = Cfg<KB, VB>;
+  static_assert(!C::kInt8, "the int8 mode runs the tensor-core kernel");
   constexpr int S = C::kStages;
   constexpr int kRS = C::kRowShift;
   constexpr int GH = G >= 2 ? G / 2 : 1;  // heads whose scores a K-phase lane owns after the butterfly
@@ -858,7 +854,6 @@ __global__ void __launch_bounds__(Cfg<KB, VB>::kThreads, 1) decode_split_kernel(
         }
         // ---- online softmax in that layout (base 2, lazily raised maximum)
         const bool head_ok = gq < G;
-        const float* kscale = reinterpret_cast<const float*>(tb + C::kKTile);  // int8: the K scales
         const float* vnorm = reinterpret_cast<const float*>(tb + C::kKTile + C::kKNorm + C::kVTile);
         const int tk[4] = {2 * tq, 2 * tq + 1, 8 + 2 * tq, 9 + 2 * tq};
         constexpr float kQs = kLog2e / kSqrtD;
@@ -867,7 +862,6 @@ __global__ void __launch_bounds__(Cfg<KB, VB>::kThreads, 1) decode_split_kernel(
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           float s = sraw[i];
-          if constexpr (C::kInt8) s = fmul(s, kscale[tk[i]]);
           s = fmul(s, kQs);
           sj[i] = head_ok && tk[i] < n_valid ? s : -INFINITY;  // staged data of masked rows is stale
           bump |= sj[i] > fadd(m_own[0], kLazy);
@@ -1087,19 +1081,7 @@ __global__ void __launch_bounds__(Cfg<KB, VB>::kThreads, 1) decode_split_kernel(
         constexpr int kVRec = VB * 16;
         float2 w2[G];
         load_w(U_, w2);
-        if constexpr (VB == 8) {  // int8 mode: codes of coordinates 8 r .. 8 r + 7, no table
-          const uint2 wv = lds64u<U * 2 * kVRec>(vw);
-          const uint32_t x0 = wv.x ^ 0x80808080u, x1 = wv.y ^ 0x80808080u;
-          const float2 c0 = int8_pair<0>(x0), c1 = int8_pair<2>(x0);
-          const float2 c2 = int8_pair<0>(x1), c3 = int8_pair<2>(x1);
-#pragma unroll
-          for (int jj = 0; jj < G; ++jj) {
-            acc[jj][0] = fma2(w2[jj], c0, acc[jj][0]);
-            acc[jj][1] = fma2(w2[jj], c1, acc[jj][1]);
-            acc[jj][2] = fma2(w2[jj], c2, acc[jj][2]);
-            acc[jj][3] = fma2(w2[jj], c3, acc[jj][3]);
-          }
-        } else {  // packed codes: one pair-table lookup per two coordinates
+        {  // packed codes: one pair-table lookup per two coordinates
           uint32_t win;
           if constexpr (VB == 4) win = lds32<U * 2 * kVRec>(vw);
           else if constexpr (VB == 2) win = lds32<U * 2 * kVRec>(vw) >> v_sh;
