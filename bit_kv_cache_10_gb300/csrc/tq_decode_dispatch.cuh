@@ -16,11 +16,9 @@ namespace {
 template <int G, int KB, bool SPARSE, bool PAGED, bool MQ>
 tq_status dispatch_vb(const DecodeParams& p, int vb, cudaStream_t s) {
   switch (vb) {
-    case 2: return launch_split<G, KB, 2, SPARSE, PAGED, MQ>(p, s);
-    case 3: return launch_split<G, KB, 3, SPARSE, PAGED, MQ>(p, s);
-    default:
-      if constexpr ((KB >= 2 && KB <= 4) || KB == 16) return launch_mma<G, KB, SPARSE, PAGED, MQ>(p, s);
-      else return launch_split<G, KB, 4, SPARSE, PAGED, MQ>(p, s);
+    case 2: return launch_mma<G, KB, SPARSE, PAGED, MQ, 2>(p, s);
+    case 3: return launch_mma<G, KB, SPARSE, PAGED, MQ, 3>(p, s);
+    default: return launch_mma<G, KB, SPARSE, PAGED, MQ, 4>(p, s);
   }
 }
 

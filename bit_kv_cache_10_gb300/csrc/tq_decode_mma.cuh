@@ -57,17 +57,18 @@ constexpr float kCentUnscale = 1.0f / 1024.0f;
 
 constexpr int kClusterCtas = 8;  // CTAs of a (b, h) row in the cluster variant (the portable cluster size)
 
-template <int KB, bool CL = false>
+template <int KB, bool CL = false, int VB = 4>
 struct MmaCfg {
   static constexpr bool kF16K = KB == 16;    // fp16 K (asym): K tiles read with ldmatrix, no K table
   static constexpr bool kI8 = KB == 8;       // int8 mode: int8 K and V codes, exact in fp16, no tables
-  static constexpr int kVB = kI8 ? 8 : 4;
+  static constexpr int kVB = kI8 ? 8 : VB;  // V of 2 or 3 bits: codes expanded to nibbles, 4-bit path
   using Stage = Cfg<KB, kVB>;                // K | K norms | V | V norms, with V rows padded:
   // fp16 K rows 256 + 16 bytes apart (the 8 rows of an ldmatrix phase hit distinct banks)
   static constexpr int kKPitch = kF16K ? 272 : Stage::kKPitch;
   static constexpr int kKTile = kTile * kKPitch;
   static constexpr int kKNorm = Stage::kKNorm;
-  // 64-byte records 80 bytes apart (conflict-free V code loads); int8: 128-byte records 144 apart
+  // 64-byte records 80 bytes apart (conflict-free V code loads; 32- and 48-byte records
+  // use the same pitch); int8: 128-byte records 144 apart
   static constexpr int kVPitch = kI8 ? 144 : 80;
   static constexpr int kVTile = kTile * kVPitch;
   static constexpr int kBuf = kKTile + kKNorm + kVTile + kTile * 4;
@@ -162,6 +163,41 @@ __device__ __forceinline__ uint32_t v_pair_addr(uint32_t x, uint32_t vbase) {
   return __byte_perm(x, vbase, 0x7604 | (K << 4));
 }
 
+// Codes of 8 coordinates (3 or 2 bits each, LSB-first) spread to one nibble each.
+__device__ __forceinline__ uint32_t spread3(uint32_t v) {  // 24 bits -> 8 nibbles
+  v = (v & 0x00000FFFu) | ((v & 0x00FFF000u) << 4);       // 12-bit groups at bits 0, 16
+  v = (v & 0x003F003Fu) | ((v & 0x0FC00FC0u) << 2);       // 6-bit groups at bytes 0..3
+  return (v & 0x07070707u) | ((v & 0x38383838u) << 1);    // 3-bit codes at nibbles
+}
+__device__ __forceinline__ uint32_t spread2(uint32_t v) {  // 16 bits -> 8 nibbles
+  v = (v & 0x000000FFu) | ((v & 0x0000FF00u) << 8);       // bytes at bits 0, 16
+  v = (v & 0x000F000Fu) | ((v & 0x00F000F0u) << 4);       // nibbles at bytes 0..3
+  return (v & 0x03030303u) | ((v & 0x0C0C0C0Cu) << 2);    // 2-bit codes at nibbles
+}
+// The lane's 16 V codes of one token (coordinates 16 g .. 16 g + 15, at shared
+// address `addr`) as two words of nibbles, codes 0..7 and 8..15: the 4-bit record
+// as it is, narrower codes spread.  A 3-bit window (6 bytes at 6 g) starts on a
+// 4-byte boundary or 2 bytes after one.
+template <int VB>
+__device__ __forceinline__ uint2 v_nibbles(uint32_t addr) {
+  if constexpr (VB == 4) {
+    uint2 v;
+    asm("ld.shared.v2.u32 {%0, %1}, [%2];\n" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+    return v;
+  } else if constexpr (VB == 2) {
+    uint32_t w;
+    asm("ld.shared.u32 %0, [%1];\n" : "=r"(w) : "r"(addr));
+    return make_uint2(spread2(w & 0xFFFFu), spread2(w >> 16));
+  } else {
+    const uint32_t base = addr & ~3u, sh = (addr & 3u) * 8u;
+    uint32_t w0, w1;
+    asm("ld.shared.u32 %0, [%1];\n" : "=r"(w0) : "r"(base));
+    asm("ld.shared.u32 %0, [%1+4];\n" : "=r"(w1) : "r"(base));
+    const uint32_t x = __funnelshift_r(w0, w1, sh), y = w1 >> sh;  // window bits 0..31 and 32..47
+    return make_uint2(spread3(x & 0x00FFFFFFu), spread3((x >> 24) | (y << 8)));
+  }
+}
+
 // Nibble interleave of two code words of tokens a and b: byte k of lo_pairs is
 // code_a | code_b << 4 of the even coordinate of byte k, hi_pairs the odd one.
 __device__ __forceinline__ void interleave(uint32_t wa, uint32_t wb, uint32_t& lo_pairs, uint32_t& hi_pairs) {
@@ -200,9 +236,9 @@ __device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr) {
 }
 __device__ __forceinline__ int comb_at(int h, int i) { return h * 136 + i + (i >> 4); }
 
-template <int G, int KB, bool SPARSE, bool PAGED, bool MQ, bool CL = false>
-__global__ void __launch_bounds__(MmaCfg<KB, CL>::kThreads, 1) decode_mma_kernel(const DecodeParams p) {
-  using M = MmaCfg<KB, CL>;
+template <int G, int KB, bool SPARSE, bool PAGED, bool MQ, bool CL = false, int VB = 4>
+__global__ void __launch_bounds__(MmaCfg<KB, CL, VB>::kThreads, 1) decode_mma_kernel(const DecodeParams p) {
+  using M = MmaCfg<KB, CL, VB>;
   using C = Cfg<KB, M::kVB>;
   constexpr int S = M::kStages;
   constexpr int NW = M::kWarps;
@@ -319,7 +355,7 @@ __global__ void __launch_bounds__(MmaCfg<KB, CL>::kThreads, 1) decode_mma_kernel
   // K-phase window offset of the lane within a token record, V-phase record offset
   constexpr int kKRec = KB * 16;
   const uint32_t k_win = static_cast<uint32_t>(4 * KB * t);  // bytes: 32 coordinates of KB bits
-  const uint32_t v_win = static_cast<uint32_t>(8 * g);
+  const uint32_t v_win = static_cast<uint32_t>(2 * M::kVB * g);  // byte offset of coordinates 16 g .. 16 g + 15
   uint32_t qb[16];   // B fragments of the scores: [q hi | q lo] of the lane's (head, half), 8 chunks
   float sc[2];       // log2-domain score scale of heads h0, h0 + 1 (rotation, centroid and query scales)
   int cur_b = -1, cur_h = -1;
@@ -712,10 +748,10 @@ __global__ void __launch_bounds__(MmaCfg<KB, CL>::kThreads, 1) decode_mma_kernel
         } else if (!hot) {
           const uint32_t vt = tbs + static_cast<uint32_t>(M::kKTile + M::kKNorm) + v_win;
           constexpr int P = M::kVPitch;
-          const uint2 wa = lds64u<0>(vt + static_cast<uint32_t>((2 * t) * P));
-          const uint2 wbw = lds64u<0>(vt + static_cast<uint32_t>((2 * t + 1) * P));
-          const uint2 wc = lds64u<0>(vt + static_cast<uint32_t>((2 * t + 8) * P));
-          const uint2 wd = lds64u<0>(vt + static_cast<uint32_t>((2 * t + 9) * P));
+          const uint2 wa = v_nibbles<M::kVB>(vt + static_cast<uint32_t>((2 * t) * P));
+          const uint2 wbw = v_nibbles<M::kVB>(vt + static_cast<uint32_t>((2 * t + 1) * P));
+          const uint2 wc = v_nibbles<M::kVB>(vt + static_cast<uint32_t>((2 * t + 8) * P));
+          const uint2 wd = v_nibbles<M::kVB>(vt + static_cast<uint32_t>((2 * t + 9) * P));
           uint32_t ab_lo[2], ab_hi[2], cd_lo[2], cd_hi[2];
           interleave(wa.x, wbw.x, ab_lo[0], ab_hi[0]);
           interleave(wa.y, wbw.y, ab_lo[1], ab_hi[1]);
@@ -914,10 +950,10 @@ __global__ void __launch_bounds__(MmaCfg<KB, CL>::kThreads, 1) decode_mma_kernel
   }
 }
 
-template <int G, int KB, bool SPARSE, bool PAGED, bool MQ>
+template <int G, int KB, bool SPARSE, bool PAGED, bool MQ, int VB = 4>
 tq_status launch_mma(const DecodeParams& p, cudaStream_t stream) {
-  using M = MmaCfg<KB>;
-  auto kern = decode_mma_kernel<G, KB, SPARSE, PAGED, MQ>;
+  using M = MmaCfg<KB, false, VB>;
+  auto kern = decode_mma_kernel<G, KB, SPARSE, PAGED, MQ, false, VB>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, M::kSmem) != cudaSuccess)
     return TQ_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
