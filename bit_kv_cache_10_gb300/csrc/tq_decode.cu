@@ -239,9 +239,8 @@ tq_status run_attention(const tq_cache_desc* d, const void* q, int nq, const int
   // small work (rows of at most kClusterMaxLen positions, every row's cluster
   // resident at once): one thread-block cluster per (b, h) row, no merge launch
   const int path = g_decode_path.load(std::memory_order_relaxed);
-  if (nq == 1 && !paged && !sparse && d->k_mode == TQ_K_PACKED && kb >= 2 && kb <= 4 && d->v_bits == 4 && path != 1 &&
-      (path == 2 || max_seq_len <= kClusterMaxLen)) {
-    st = dispatch_cluster(p, g, kb, s);
+  if (nq == 1 && !paged && !sparse && path != 1 && (path == 2 || max_seq_len <= kClusterMaxLen)) {
+    st = dispatch_cluster(p, g, kb, d->v_bits, s);
     if (st != TQ_ERR_UNSUPPORTED) return st;
   }
   if (nq > 1) {

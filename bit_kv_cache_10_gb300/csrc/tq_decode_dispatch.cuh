@@ -53,9 +53,9 @@ tq_status dispatch_split_paged(const DecodeParams& p, int g, int kb, int vb, cud
 tq_status dispatch_split_paged_sparse(const DecodeParams& p, int g, int kb, int vb, cudaStream_t s);
 tq_status dispatch_split_multi(const DecodeParams& p, int g, int kb, int vb, cudaStream_t s);
 tq_status dispatch_split_multi_paged(const DecodeParams& p, int g, int kb, int vb, cudaStream_t s);
-// Cluster variant (packed K of kb = 2..4 bits, 4-bit V, dense, contiguous, one
-// query token): TQ_ERR_UNSUPPORTED without a launch when the rows do not fit
-// in one wave of clusters.
-tq_status dispatch_cluster(const DecodeParams& p, int g, int kb, cudaStream_t s);
+// Cluster variant (any K and V width, dense V, contiguous layout, one query
+// token): TQ_ERR_UNSUPPORTED without a launch when the rows do not fit in one
+// wave of clusters.
+tq_status dispatch_cluster(const DecodeParams& p, int g, int kb, int vb, cudaStream_t s);
 
 }  // namespace tq

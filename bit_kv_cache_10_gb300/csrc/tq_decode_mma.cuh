@@ -944,7 +944,7 @@ __global__ void __launch_bounds__(MmaCfg<KB, CL, VB>::kThreads, 1) decode_mma_ke
       unsigned neg4 = 0u;
 #pragma unroll
       for (int i = 0; i < 4; ++i) neg4 |= sign_negative(p.seed, p.layer, rh, 4 * lane + i) ? 1u << i : 0u;
-      merge_finish(y, hv, l, neg4, true, p.out + (static_cast<int64_t>(rb) * p.hq + rh * G + hd) * D, lane);
+      merge_finish(y, hv, l, neg4, !M::kI8, p.out + (static_cast<int64_t>(rb) * p.hq + rh * G + hd) * D, lane);
     }
     cluster_sync_all();
   }
@@ -974,10 +974,10 @@ tq_status launch_mma(const DecodeParams& p, cudaStream_t stream) {
 // merged through distributed shared memory, no merge launch).  Returns
 // TQ_ERR_UNSUPPORTED without launching when the rows do not fit in one wave of
 // clusters on this GPU (the caller then runs the persistent split kernel).
-template <int G, int KB>
+template <int G, int KB, int VB>
 tq_status launch_mma_cluster(const DecodeParams& p, cudaStream_t stream) {
-  using M = MmaCfg<KB, true>;
-  auto kern = decode_mma_kernel<G, KB, false, false, false, true>;
+  using M = MmaCfg<KB, true, VB>;
+  auto kern = decode_mma_kernel<G, KB, false, false, false, true, VB>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, M::kSmem) != cudaSuccess)
     return TQ_ERR_CUDA;
   const long long rows = static_cast<long long>(p.batch) * p.hkv;

@@ -220,10 +220,16 @@ def test_int8_paged_sparse_and_reproducible():
     for tc in (flat, paged):
         tc.append(_dev(k), _dev(v), _dev(np.zeros(B, np.int32)), sl)
     assert flat.device_status() == 0 and paged.device_status() == 0
-    ref = flat.decode(q, sl, cap).cpu().numpy()
-    np.testing.assert_array_equal(paged.decode(q, sl, cap).cpu().numpy(), ref)
-    np.testing.assert_array_equal(flat.decode(q, sl, cap).cpu().numpy(), ref)
-    flat.desc.sparse_v_threshold = 1e-30
-    np.testing.assert_array_equal(flat.decode(q, sl, cap).cpu().numpy(), ref)
+    # the paged layout and sparse V run the persistent kernel: the contiguous dense
+    # decode they must equal bit for bit is taken through the same kernel
+    N.tq_debug_set_decode_path(1)
+    try:
+        ref = flat.decode(q, sl, cap).cpu().numpy()
+        np.testing.assert_array_equal(paged.decode(q, sl, cap).cpu().numpy(), ref)
+        np.testing.assert_array_equal(flat.decode(q, sl, cap).cpu().numpy(), ref)
+        flat.desc.sparse_v_threshold = 1e-30
+        np.testing.assert_array_equal(flat.decode(q, sl, cap).cpu().numpy(), ref)
+    finally:
+        N.tq_debug_set_decode_path(0)
     oc = oracle.build_cache(k, v, lens, cap, 8, 8, hot_window=32, codec="int8")
     assert_attention_close(ref, oracle.decode_attention(oc, synth.queries_fp16(16, B, HQ, D), lens), "int8 paged")
