@@ -181,7 +181,7 @@ TQ_HD float2 half2_bits_to_float2(uint32_t w) {
 // Sum of x^2 in units of 2^-48 (every fp16 square is a multiple of it): exact.
 TQ_HD unsigned __int128 exact_sum_squares(const uint32_t* w) {
   unsigned __int128 s = 0;
-#pragma unroll
+#pragma unroll 1
   for (int j = 0; j < 2 * 64; ++j) {
     const uint32_t h = (j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xFFFFu);
     const uint32_t e = (h >> 10) & 31u, m = h & 1023u;
@@ -252,16 +252,24 @@ TQ_HD void twosum_merge(float& h, float& l, float h2, float l2) {
 // n = sqrt(RN(h + l)) is within one ulp of the answer; the residual
 // r = (h + l) - n^2 (n^2 split exactly with an FMA) decides between n and its
 // neighbours by comparison with the rounding midpoints.  When r is within
-// 2^-30 S of a midpoint the exact integer sum decides (ties to even).
+// 2^-37 S of a midpoint the exact integer sum decides (ties to even).
+//
+// Why 2^-37 S suffices (u = 2^-24, every square exact in float32, all terms
+// positive).  One TwoSum accumulator of 16 squares of total T: each step's
+// error term e_j is exact and |e_j| <= u T, the float sum of the e_j adds at
+// most u |lo_j| <= j u^2 T per step, 136 u^2 T in all.  The two accumulators of
+// a lane merged (one TwoSum, two roundings of the low parts): 32 u^2 T more;
+// each of the two merges across lanes: at most 80 u^2 S.  So h + l = S + E with
+// |E| <= 328 u^2 S < 2^-39.6 S.  In r, h - p is exact (Sterbenz: p = RN(n^2) is
+// within a factor 2 of h), l - pe and the final addition round at most 2 u^2 S
+// and 2^-46 S, and t_up, t_dn round at most 2^-47 S: the float decision is
+// wrong only if the exact r is within 2^-39.4 S of a midpoint, a quarter of the
+// margin.  (A margin of 2^-30 S sent 3 % of the vectors to the exact sum.)
 // Rare path of norm_from_sum (the float residual cannot tell n from a
 // neighbour): compare the exact integer sum of squares with the squared
-// midpoints.  Kept out of line so that the per-token loops stay small.
-#ifdef __CUDACC__
-static __host__ __device__ __noinline__
-#else
-static inline
-#endif
-float norm_near_midpoint(float n, const uint32_t* row) {
+// midpoints.  Its loop is not unrolled and it runs after the vector's
+// arithmetic (see norm_decided), so that it costs the per-token code nothing.
+TQ_HD float norm_near_midpoint(float n, const uint32_t* row) {
   const float n_up = bitsf(fbits(n) + 1u), n_dn = bitsf(fbits(n) - 1u);
   const float u_up = fsub(n_up, n), u_dn = fsub(n, n_dn);
   const unsigned __int128 se = exact_sum_squares(row);
@@ -272,7 +280,15 @@ float norm_near_midpoint(float n, const uint32_t* row) {
   return n;
 }
 
-TQ_HD float norm_from_sum(float h, float l, const uint32_t* row) {
+// The float32 norm as far as the float residual decides it: the correctly
+// rounded result, or, when r lies within the margin of a rounding midpoint, the
+// candidate n with `exact` set — the caller then takes norm_near_midpoint(n,
+// row).  The quantizers use the candidate for the codes (it is within one ulp
+// of the norm, so a code can differ only for a coordinate within a few ulps of
+// a threshold) and settle the stored norm after the vector's arithmetic, where
+// the integer path's registers meet no live vector registers.
+TQ_HD float norm_decided(float h, float l, bool& exact) {
+  exact = false;
   const float s_approx = fadd(h, l);
   if (!(s_approx > 0.0f)) return 0.0f;  // all zero (squares are >= 0)
   const float n = fsqrt(s_approx);
@@ -283,7 +299,7 @@ TQ_HD float norm_from_sum(float h, float l, const uint32_t* row) {
   const float u_up = fsub(n_up, n), u_dn = fsub(n, n_dn);
   const float t_up = ffma(n, u_up, fmul(fmul(u_up, u_up), 0.25f));   // (n + u/2)^2 - n^2
   const float t_dn = ffma(n, u_dn, -fmul(fmul(u_dn, u_dn), 0.25f));  // n^2 - (n - u/2)^2
-  const float margin = fmul(s_approx, 9.313225746154785e-10f);       // 2^-30 S
+  const float margin = fmul(s_approx, 7.275957614183426e-12f);       // 2^-37 S
   const bool near_up = fabsf(fsub(r, t_up)) <= margin;
   const bool near_dn = fabsf(fadd(r, t_dn)) <= margin;
   if (!near_up && !near_dn) {
@@ -291,7 +307,14 @@ TQ_HD float norm_from_sum(float h, float l, const uint32_t* row) {
     if (r < -t_dn) return n_dn;
     return n;
   }
-  return norm_near_midpoint(n, row);
+  exact = true;
+  return n;
+}
+
+TQ_HD float norm_from_sum(float h, float l, const uint32_t* row) {
+  bool exact;
+  const float n = norm_decided(h, l, exact);
+  return exact ? norm_near_midpoint(n, row) : n;
 }
 
 // ---------------------------------------------------------------------------

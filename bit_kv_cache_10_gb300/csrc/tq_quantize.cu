@@ -150,7 +150,8 @@ __device__ __forceinline__ void quantize_step(const uint8_t* rowp, int q, const 
   norm_partial<16>(v, h, l);  // squares of the sign-flipped values
   twosum_merge(h, l, __shfl_xor_sync(0xffffffffu, h, 8), __shfl_xor_sync(0xffffffffu, l, 8));
   twosum_merge(h, l, __shfl_xor_sync(0xffffffffu, h, 16), __shfl_xor_sync(0xffffffffu, l, 16));
-  const float n = norm_from_sum(h, l, reinterpret_cast<const uint32_t*>(rowp));
+  bool exact;  // the rare exact norm is settled after the vector's arithmetic (see norm_decided)
+  const float n = norm_decided(h, l, exact);
   // rotation: in-lane bits 0..4, then bits 5 (q ^ 1) and 6 (q ^ 2) across lanes
   fwht32(v);
   // the two halves of a pair are exchanged as two 32-bit values (no 64-bit packing)
@@ -175,8 +176,8 @@ __device__ __forceinline__ void quantize_step(const uint8_t* rowp, int q, const 
 #pragma unroll
       for (int k = 0; k < BITS; ++k) d[k] = words[k];
     }
-    if (q == 0) *dst_norm = n;
   }
+  if (store && q == 0) *dst_norm = exact ? norm_near_midpoint(n, reinterpret_cast<const uint32_t*>(rowp)) : n;
 }
 
 // Code of x in the int8 mode for a scale s > 0: the float32 quotient x / s
@@ -425,7 +426,8 @@ __device__ __forceinline__ void quantize_vector_warp(const uint16_t* row, uint2 
 #pragma unroll
   for (int m = 1; m < 32; m <<= 1)
     twosum_merge(h, l, __shfl_xor_sync(0xffffffffu, h, m), __shfl_xor_sync(0xffffffffu, l, m));
-  const float n = norm_from_sum(h, l, reinterpret_cast<const uint32_t*>(row));
+  bool exact;  // the rare exact norm is settled after the vector's arithmetic (see norm_decided)
+  const float n = norm_decided(h, l, exact);
   // FWHT: index bits 0 and 1 inside the lane, bits 2..6 across lanes (lane bit k - 2)
   float z[4];
   {
@@ -450,7 +452,7 @@ __device__ __forceinline__ void quantize_vector_warp(const uint16_t* row, uint2 
 #pragma unroll
   for (int k = 0; k < 4; ++k) val |= threshold_code<BITS>(fmul(z[k], inv), thr) << (BITS * k);
   store_codes_warp<BITS>(val, lane, dst_words, store);
-  if (store && lane == 0) *dst_norm = n;
+  if (store && lane == 0) *dst_norm = exact ? norm_near_midpoint(n, reinterpret_cast<const uint32_t*>(row)) : n;
 }
 
 // The int8 mode for one token vector per warp (arithmetic of quantize_step_int8).
@@ -723,7 +725,8 @@ extern "C" tq_status tq_debug_quantize_rows_host(const tq_codebook* cb, uint64_t
     }
     float hs = h1[0], ls = l1[0];
     twosum_merge(hs, ls, h1[2], l1[2]);
-    const float n = norm_from_sum(hs, ls, w);
+    bool exact;  // as the kernels: codes from the candidate, the stored norm settled afterwards
+    const float n = norm_decided(hs, ls, exact);
     for (int stage = 1; stage <= 2; stage *= 2) {  // index bit 5 (q ^ 1), then bit 6 (q ^ 2)
       float2 prev[4][16];
       std::memcpy(prev, v, sizeof(prev));
@@ -742,7 +745,7 @@ extern "C" tq_status tq_debug_quantize_rows_host(const tq_codebook* cb, uint64_t
         default: pack_codes32<4>(v[q], inv, lut, 1, a, out + 4 * q); break;
       }
     }
-    norms[r] = n;
+    norms[r] = exact ? norm_near_midpoint(n, w) : n;
   }
   return TQ_OK;
 }
