@@ -1,7 +1,9 @@
 // Decode attention over the packed cache: the host entry points, the merge
-// kernel and the dense contiguous split-K instantiations (the split kernel
-// itself is in tq_decode_split.cuh; its sparse-V and paged instantiations are in
-// tq_decode_sparse.cu, tq_decode_paged.cu and tq_decode_paged_sparse.cu).
+// kernel and the dense contiguous instantiations of the split-K kernel (the
+// kernel itself is in tq_decode_mma.cuh; its sparse-V, paged and multi-token
+// instantiations are in tq_decode_sparse.cu, tq_decode_paged.cu,
+// tq_decode_paged_sparse.cu, tq_decode_multi.cu and tq_decode_multi_paged.cu,
+// the cluster variant's in tq_decode_cluster.cu).
 #include <atomic>
 
 #include "tq_decode_dispatch.cuh"

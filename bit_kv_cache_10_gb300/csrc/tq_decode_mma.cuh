@@ -1,7 +1,9 @@
-// Split-K decode kernel with the scores and the V sums on the tensor cores,
-// for packed K (2, 3 or 4 bits) and packed 4-bit V.  Work list, staging ring,
-// partial slots and the merge are those of the float32 kernel
-// (tq_decode_split.cuh); only the arithmetic of a tile differs.
+// Split-K decode kernel with the scores and the V sums on the tensor cores, for
+// every mode: packed K of 2, 3 or 4 bits or fp16 K, with packed V of 2, 3 or 4
+// bits (narrower codes spread to nibbles), and the int8 mode.  The work list,
+// the tile staging, the partial slots and the merge output are in
+// tq_decode_split.cuh; the persistent variant covers an equal tile range per
+// CTA, the cluster variant (CL) one (b, h) row per 8-CTA cluster.
 //
 // Exact operands from lookups.  A float32 centroid c is the sum of two fp16
 // numbers, hi = RN16(c) and lo = RN16(c - hi), which together carry 22
@@ -33,7 +35,7 @@
 //
 // Softmax.  Lane (g, t) then owns token g + 8 (t >> 1) for heads 2 (t & 1) and
 // 2 (t & 1) + 1.  The V weight of a token is w = 2^(s - m) n_V; the running
-// maximum m of a head is raised (lazily, as in the float32 kernel) against
+// maximum m of a head is raised lazily (only when a score exceeds it by 2^8) against
 // s + e_V + 1, e_V the binary exponent of n_V, so every weight stays below 2^8
 // and its fp16 hi and lo halves are exact.  The mass sums 2^(s - m) alone.
 //
@@ -973,7 +975,7 @@ tq_status launch_mma(const DecodeParams& p, cudaStream_t stream) {
 // Cluster variant (one cluster of kClusterCtas CTAs per (b, h) row, partials
 // merged through distributed shared memory, no merge launch).  Returns
 // TQ_ERR_UNSUPPORTED without launching when the rows do not fit in one wave of
-// clusters on this GPU (the caller then runs the persistent split kernel).
+// clusters on this GPU (the caller then runs the persistent kernel).
 template <int G, int KB, int VB>
 tq_status launch_mma_cluster(const DecodeParams& p, cudaStream_t stream) {
   using M = MmaCfg<KB, true, VB>;

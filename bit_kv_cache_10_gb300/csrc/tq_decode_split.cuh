@@ -441,7 +441,7 @@ __device__ __forceinline__ int stage_tile_paged(const DecodeParams& p, int h, bo
 // Stages tile [t_begin, t_begin + n_valid) of (b, h) into buf; returns the
 // number of tokens the consumer may read.
 // V rows are VPITCH bytes apart in the staged tile (VB * 16: contiguous).
-// KPITCH: pitch of the staged K rows (0: the split kernel's Cfg::kKPitch).
+// KPITCH: pitch of the staged K rows (0: Cfg::kKPitch).
 template <int KB, int VB, bool PAGED, int VPITCH = VB * 16, int KPITCH = 0>
 __device__ __forceinline__ int stage_tile(const DecodeParams& p, int b, int h, bool hot, int t_begin, int n_valid,
                                           TileBlocks tb, uint32_t buf, int lane) {
