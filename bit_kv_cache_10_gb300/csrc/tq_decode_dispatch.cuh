@@ -2,9 +2,9 @@
 // translation units (each instantiates one variant: dense or sparse V,
 // contiguous or paged layout, one or several query tokens per sequence).
 //
-// Packed K of 2..4 bits or fp16 K with packed 4-bit V, and the int8 mode, run
-// the tensor-core kernel (tq_decode_mma.cuh); V of 2 or 3 bits runs the float32
-// kernel (tq_decode_split.cuh), whose fp16-K scores are on the tensor cores too.
+// Every mode runs the tensor-core kernel (tq_decode_mma.cuh): packed K of 2..4
+// bits or fp16 K with packed V of 2..4 bits, and the int8 mode.  The tile list,
+// staging and merge helpers it uses are in tq_decode_split.cuh.
 #pragma once
 
 #include "tq_decode_mma.cuh"

@@ -1,8 +1,8 @@
 """GPU parity of the asym mode (fp16 K, packed V) against the oracle.
 
-fp16 K with 4-bit V runs the tensor-core kernel (scores from ldmatrix fragments
-of the staged fp16 rows against the raw fp16 query); fp16 K with 3-bit V runs the
-float32 kernel.  Cases: empty rows, rows shorter than a tile, partial last tiles,
+fp16 K runs the tensor-core kernel (scores from ldmatrix fragments of the staged
+fp16 rows against the raw fp16 query) with packed V of 4 bits, or of 3 bits spread
+to nibbles.  Cases: empty rows, rows shorter than a tile, partial last tiles,
 hot windows longer and shorter than the rows, group sizes 1, 2 and 4, peaked
 softmax, and sparse V within the oracle's exact deviation bound.
 """
