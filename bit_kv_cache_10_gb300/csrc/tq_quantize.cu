@@ -67,18 +67,8 @@ struct Job {
   int count;           // rows this sequence appends
 };
 
-__device__ __forceinline__ Job decode_job(const QuantParams& p, long long jl) {
-  // 32-bit index arithmetic: the host keeps the job count below 2^31
-  const int j = static_cast<int>(jl);
-  Job jb;
-  // tensor-major order: at any moment nearly all warps run the same code width
-  const int per_tensor = static_cast<int>(p.jobs) / p.tensors;
-  jb.tensor = j >= per_tensor ? 1 : 0;
-  int r = j - jb.tensor * per_tensor;
-  const int rt = r / p.tiles_per_row;
-  jb.tile = r - rt * p.tiles_per_row;
-  jb.b = rt / p.heads;
-  jb.h = rt - jb.b * p.heads;
+// Sequence fields of a job from its sequence b: append range or evict range.
+__device__ __forceinline__ void job_sequence(const QuantParams& p, Job& jb) {
   const int s = p.start_pos[jb.b];
   const int cnt = p.num_new != nullptr ? p.num_new[jb.b] : p.n_new;
   jb.valid = s >= 0 && cnt >= 0 && cnt <= p.n_new && static_cast<long long>(s) + cnt <= p.cap;
@@ -92,23 +82,45 @@ __device__ __forceinline__ Job decode_job(const QuantParams& p, long long jl) {
     jb.end = min(s, end - p.hot);
     if (jb.end < jb.start) jb.end = jb.start;
   }
-  if (p.evict) jb.tensor = 1;  // 0 = K, 1 = V
+}
+
+// Mixed-radix digits (tensor, b, h, tile) of a job index: tile fastest, then
+// head, then sequence, then tensor, so that at any moment nearly all warps run
+// the same code width.  (The evict pass has one tensor digit, 0, and
+// quantizes V: the walk keeps the digit and the loop sets jb.tensor = 1.)
+__device__ __forceinline__ Job job_digits(const QuantParams& p, long long jl) {
+  const int j = static_cast<int>(jl);  // the host keeps the job count below 2^31
+  Job jb;
+  const int rt = j / p.tiles_per_row;
+  jb.tile = j - rt * p.tiles_per_row;
+  const int bt = rt / p.heads;
+  jb.h = rt - bt * p.heads;
+  jb.tensor = bt / p.batch;
+  jb.b = bt - jb.tensor * p.batch;
   return jb;
 }
 
-// Global address of the fp16 source row for tile row `row` of a job, or null.
-__device__ __forceinline__ const uint16_t* src_row(const QuantParams& p, const Job& jb, int row, int* pos_out) {
+// jb + d in the mixed radix (every digit of d below its radix): at most one
+// carry per digit.
+__device__ __forceinline__ void job_advance(const QuantParams& p, Job& jb, const Job& d) {
+  jb.tile += d.tile;
+  int c = jb.tile >= p.tiles_per_row;
+  if (c) jb.tile -= p.tiles_per_row;
+  jb.h += d.h + c;
+  c = jb.h >= p.heads;
+  if (c) jb.h -= p.heads;
+  jb.b += d.b + c;
+  c = jb.b >= p.batch;
+  if (c) jb.b -= p.batch;
+  jb.tensor += d.tensor + c;
+}
+
+// Whether tile row `row` of a job holds a token (its cache position in *pos_out).
+__device__ __forceinline__ bool row_present(const QuantParams& p, const Job& jb, int row, int* pos_out) {
   const int t = jb.tile * kTileRows + row;
-  if (!p.evict) {
-    if (t >= jb.count) return nullptr;
-    *pos_out = jb.start + t;
-    const uint16_t* base = jb.tensor == 0 ? p.k_src : p.v_src;
-    return base + jb.b * p.stride_b + jb.h * p.stride_h + t * p.stride_t;
-  }
   const int pos = jb.start + t;
-  if (pos >= jb.end) return nullptr;
   *pos_out = pos;
-  return p.v_ring + ((static_cast<int64_t>(jb.b) * p.heads + jb.h) * p.hot + pos % p.hot) * D;
+  return p.evict ? pos < jb.end : t < jb.count;
 }
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
@@ -119,12 +131,24 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 
 __device__ __forceinline__ void issue_tile(const QuantParams& p, const Job& jb, uint8_t* tile, int lane) {
   if (!jb.valid) return;
+  const int row0 = lane >> 4, col = lane & 15;
+  uint8_t* dst = tile + row0 * kRowPitch + col * 16;
+  if (!p.evict) {
+    // rows t = 16 tile + 2k + row0 of the source, 2 stride_t apart
+    const int t0 = jb.tile * kTileRows + row0;
+    const uint16_t* src = (jb.tensor == 0 ? p.k_src : p.v_src) + jb.b * p.stride_b + jb.h * p.stride_h +
+                          static_cast<int64_t>(t0) * p.stride_t + col * 8;
+    const int64_t step = 2 * p.stride_t;
+#pragma unroll
+    for (int k = 0; k < kTileRows / 2; ++k)
+      if (t0 + 2 * k < jb.count) cp_async16(dst + 2 * k * kRowPitch, src + k * step);
+    return;
+  }
+  const uint16_t* ring = p.v_ring + (static_cast<int64_t>(jb.b) * p.heads + jb.h) * p.hot * D + col * 8;
 #pragma unroll
   for (int k = 0; k < kTileRows / 2; ++k) {
-    const int row = 2 * k + (lane >> 4), col = lane & 15;
-    int pos = 0;
-    const uint16_t* src = src_row(p, jb, row, &pos);
-    if (src != nullptr) cp_async16(tile + row * kRowPitch + col * 16, src + col * 8);
+    const int pos = jb.start + jb.tile * kTileRows + 2 * k + row0;
+    if (pos < jb.end) cp_async16(dst + 2 * k * kRowPitch, ring + (pos % p.hot) * D);
   }
 }
 
@@ -273,20 +297,28 @@ __global__ void __launch_bounds__(kWarps * 32, 1) quantize_append_kernel(const Q
   const LutEntry* my_lut_k = lut_k + (lane & (kLutCopies - 1));
   const LutEntry* my_lut_v = lut_v + (lane & (kLutCopies - 1));
 
-  // job j goes to CTA j mod grid: small appends put one job per SM
+  // job j goes to CTA j mod grid: small appends put one job per SM.  The
+  // warp's jobs are stride apart, walked in the mixed radix of job_digits
   const long long stride = static_cast<long long>(gridDim.x) * kWarps;
+  const Job dstep = job_digits(p, stride < p.jobs ? stride : 0);
   long long j = static_cast<long long>(warp) * gridDim.x + blockIdx.x;
-  Job next{};  // the job whose tile is in flight, decoded once
+  Job next{};  // the job whose tile is in flight
   if (j < p.jobs) {
-    next = decode_job(p, j);
+    next = job_digits(p, j);
+    const int digit = next.tensor;
+    if (p.evict) next.tensor = 1;
+    job_sequence(p, next);
     issue_tile(p, next, tiles, lane);
+    next.tensor = digit;
   }
   cp_async_commit();
   for (; j < p.jobs; j += stride) {
     asm volatile("cp.async.wait_all;\n" ::);
     __syncwarp();
 
-    const Job jb = next;
+    Job jb = next;
+    const int digit = jb.tensor;
+    if (p.evict) jb.tensor = 1;  // 0 = K, 1 = V
     if (!jb.valid) {
       if (jb.tile == 0 && jb.tensor == (p.evict ? 1 : 0) && jb.h == 0 && lane == 0 && p.status != nullptr)
         atomicOr(p.status, TQ_DEV_ERR_APPEND_RANGE);
@@ -315,13 +347,15 @@ __global__ void __launch_bounds__(kWarps * 32, 1) quantize_append_kernel(const Q
       for (int step = 0; step < kTileRows / 8; ++step) {
         const int row = 8 * step + vrow;
         int pos = 0;
-        const bool have = src_row(p, jb, row, &pos) != nullptr;
+        const bool have = row_present(p, jb, row, &pos);
         if (!__any_sync(0xffffffffu, have)) break;  // rows are filled in order: no later step has one
         long long ridx = (static_cast<long long>(jb.b) * p.heads + jb.h) * p.cap + pos;  // cache row
         if constexpr (PAGED) ridx = have ? p.map.row(jb.b, jb.h, pos) : 0;  // through the block table
         const bool to_copy = copy_k || (!k_tensor && pos >= cold_end);
         const bool to_ring = !copy_k && to_copy;  // hot V goes to the per-sequence ring, not the pool
-        if (have && ridx < 0 && !to_ring && p.status != nullptr) atomicOr(p.status, TQ_DEV_ERR_BLOCK);
+        if constexpr (PAGED)
+          if (have && ridx < 0 && !to_ring && p.status != nullptr) atomicOr(p.status, TQ_DEV_ERR_BLOCK);
+        const bool in_pool = !PAGED || ridx >= 0;  // contiguous rows always are
         const int64_t slot = (static_cast<int64_t>(jb.b) * p.heads + jb.h) * p.hot + (p.hot > 0 ? pos % p.hot : 0);
         if (FUSE && !k_tensor) {
           // appends of at most W tokens: the ring slot this row takes holds
@@ -339,7 +373,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) quantize_append_kernel(const Q
           }
           __syncwarp();
         }
-        if (to_copy && have && (to_ring || ridx >= 0)) {
+        if (to_copy && have && (to_ring || in_pool)) {
           // fp16 copy of the row (asym K, or V going to the hot ring): 4 x 16 bytes per lane
           uint4* dst = copy_k ? reinterpret_cast<uint4*>(p.k_fp16 + ridx * D)
                               : reinterpret_cast<uint4*>(p.v_ring + slot * D);
@@ -351,7 +385,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) quantize_append_kernel(const Q
         // every lane takes part in the shuffles of quantize_step; rows that are
         // absent or go to the ring are computed but not stored (a step with no
         // stored row is skipped)
-        const bool store = have && !to_copy && ridx >= 0;
+        const bool store = have && !to_copy && in_pool;
         if (!__any_sync(0xffffffffu, store)) continue;
         const int bits = k_tensor ? p.k_bits : p.v_bits;
         quantize_row(tile + row * kRowPitch, bits, k_tensor ? my_lut_k : my_lut_v, k_tensor ? p.k_lut_a : p.v_lut_a,
@@ -360,10 +394,15 @@ __global__ void __launch_bounds__(kWarps * 32, 1) quantize_append_kernel(const Q
       }
     }
     __syncwarp();
-    const long long jn = j + stride;
-    if (jn < p.jobs) {
-      next = decode_job(p, jn);
+    if (j + stride < p.jobs) {
+      next = jb;
+      next.tensor = digit;
+      job_advance(p, next, dstep);
+      const int nd = next.tensor;
+      if (p.evict) next.tensor = 1;
+      if (next.b != jb.b || next.tensor != jb.tensor) job_sequence(p, next);
       issue_tile(p, next, tiles, lane);
+      next.tensor = nd;
     }
     cp_async_commit();
   }
