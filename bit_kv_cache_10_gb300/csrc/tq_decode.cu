@@ -5,6 +5,8 @@
 // tq_decode_paged_sparse.cu, tq_decode_multi.cu and tq_decode_multi_paged.cu,
 // the cluster variant's in tq_decode_cluster.cu).
 #include <atomic>
+#include <cstring>
+#include <vector>
 
 #include "tq_decode_dispatch.cuh"
 #include "tq_debug.h"
@@ -56,23 +58,28 @@ __global__ void __launch_bounds__(4 * 32) decode_merge_kernel(const DecodeParams
   }
   const int per_h = st.tc + st.th;
   const long long hbase = before + static_cast<long long>(h) * per_h;
-  // rows of this (b, h): cold [hbase, hbase + tc), hot [hbase + tc, hbase + per_h);
-  // partial i < n0 comes from cold CTA c0 + i, partial n0 + i from hot CTA c1 + i
+  // rows of this (b, h): cold [hbase, hbase + tc), hot [hbase + tc, hbase + per_h),
+  // at the costs of the split kernel's weighted split (tq_split_plan.h); partial
+  // i < n0 comes from cold CTA c0 + i, partial n0 + i from hot CTA c1 + i
+  const long long r = static_cast<long long>(b) * p.hkv + h;
+  const long long cost_all = split_total_cost(total, static_cast<long long>(p.batch) * p.hkv, p.price);
+  const long long a0 = split_cold_cost(hbase, r, p.price), e0 = a0 + st.tc - 1;        // cold costs [a0, e0]
+  const long long a1 = split_hot_cost(hbase, st.tc, r, p.price), e1 = a1 + st.th - 1;  // hot costs [a1, e1]
   int c0 = 0, n0 = 0, c1 = 0, n1 = 0;
   if (st.tc > 0) {
-    c0 = cta_of(hbase, total, p.grid);
-    n0 = cta_of(hbase + st.tc - 1, total, p.grid) - c0 + 1;
+    c0 = split_cta(a0, cost_all, p.grid);
+    n0 = split_cta(e0, cost_all, p.grid) - c0 + 1;
   }
   if (st.th > 0) {
-    c1 = cta_of(hbase + st.tc, total, p.grid);
-    n1 = cta_of(hbase + per_h - 1, total, p.grid) - c1 + 1;
+    c1 = split_cta(a1, cost_all, p.grid);
+    n1 = split_cta(e1, cost_all, p.grid) - c1 + 1;
   }
   const int row0 = (b * p.hkv + h) * 2;
   auto slot_of = [&](int i) {
     return i < n0 ? static_cast<long long>(c0 + i) + row0 : static_cast<long long>(c1 + i - n0) + row0 + 1;
   };
-  auto live = [&](int i) {  // a CTA with an empty range wrote no partial
-    return cta_live(i < n0 ? c0 + i : c1 + i - n0, total, p.grid);
+  auto live = [&](int i) {  // a CTA that took no tile of the segment wrote no partial for it
+    return i < n0 ? split_cta_hits(c0 + i, a0, e0, cost_all, p.grid) : split_cta_hits(c1 + i - n0, a1, e1, cost_all, p.grid);
   };
   const int n = n0 + n1;
   const unsigned live32 = __ballot_sync(0xffffffffu, lane < n && live(lane));
@@ -185,6 +192,16 @@ std::atomic<int> g_decode_path{0};
 // four 16-token tiles per warp of a row's kClusterCtas CTAs.
 constexpr int kClusterMaxLen = kClusterCtas * 12 * 4 * kTile;
 
+// Segment start prices of the weighted split (tq_split_plan.h), in tiles,
+// chosen by timing the decode calls over a sweep of prices on GB300 (the
+// optimum is broad): 56 per segment with a hot window (long-context 3.5-bit
+// decode, 159 -> 152 us), 32 per row without one (the hot parts are empty; fp16
+// K with 4-bit V at context 16384: 69.7 -> 68.2 us; the int8 mode within 1 %).
+SplitPrice split_price(const tq_cache_desc* d, int nq) {
+  (void)nq;  // the multi-token work list has rows of the same tiles
+  return d->hot_window > 0 ? SplitPrice{56, 56} : SplitPrice{32, 0};
+}
+
 // Split-K attention of nq query tokens per sequence (the newest nq positions,
 // causal; nq = 1 is decode) over the cache: the work list holds B nq
 // sequences, sequence b nq + i being query token i of cache sequence b.
@@ -231,6 +248,7 @@ tq_status run_attention(const tq_cache_desc* d, const void* q, int nq, const int
   p.ws_acc = static_cast<float*>(workspace);
   p.ws_ml = p.ws_acc + slots * g * D;
   p.grid = sms < kMaxDecodeCtas ? sms : kMaxDecodeCtas;
+  p.price = split_price(d, nq);
   p.sparse_tau = d->sparse_v_threshold;
   p.rotated = d->k_mode != TQ_KV_INT8;
   p.out = out;
@@ -342,4 +360,52 @@ extern "C" tq_status tq_decode_attention_no_alloc(const tq_cache_desc* d, const 
 
 extern "C" void tq_debug_set_decode_path(int32_t path) {
   tq::g_decode_path.store(path == 1 || path == 2 ? path : 0, std::memory_order_relaxed);
+}
+
+extern "C" tq_status tq_debug_split_plan(const int32_t* tiles_cold, const int32_t* tiles_hot, int32_t nv, int32_t hkv,
+                                         int32_t grid, int32_t price_cold, int32_t price_hot, int64_t* starts,
+                                         uint8_t* seg_ctas) {
+  using namespace tq;
+  if (tiles_cold == nullptr || tiles_hot == nullptr || starts == nullptr || nv < 1 || hkv < 1 || grid < 1 ||
+      price_cold < 0 || price_hot < 0)
+    return TQ_ERR_INVALID_ARG;
+  const SplitPrice price{price_cold, price_hot};
+  std::vector<long long> prefix(static_cast<size_t>(nv) + 1, 0);
+  for (int v = 0; v < nv; ++v) {
+    if (tiles_cold[v] < 0 || tiles_hot[v] < 0) return TQ_ERR_INVALID_ARG;
+    prefix[v + 1] = prefix[v] + static_cast<long long>(hkv) * (tiles_cold[v] + tiles_hot[v]);
+    if (prefix[v + 1] >= (1ll << 40)) return TQ_ERR_INVALID_ARG;
+  }
+  const long long total = prefix[nv], rows = static_cast<long long>(nv) * hkv;
+  const long long cost_all = split_total_cost(total, rows, price);
+  // the split kernel's ranges (its start_of)
+  for (int c = 0; c <= grid; ++c) {
+    if (c == grid) {
+      starts[c] = total;
+      continue;
+    }
+    const long long tau = split_cost_at(cost_all, grid, c);
+    const int v = split_find_seq(prefix.data(), nv, hkv, price, tau);
+    starts[c] = v < 0 ? 0 : split_tile_in_seq(prefix.data(), v, hkv, tiles_cold[v], price, tau);
+  }
+  if (seg_ctas == nullptr) return TQ_OK;
+  // the merge kernel's choice of partials per row
+  std::memset(seg_ctas, 0, static_cast<size_t>(2 * rows) * grid);
+  for (int v = 0; v < nv; ++v) {
+    const int tc = tiles_cold[v], th = tiles_hot[v];
+    for (int h = 0; h < hkv; ++h) {
+      const long long r = static_cast<long long>(v) * hkv + h;
+      const long long hbase = prefix[v] + static_cast<long long>(h) * (tc + th);
+      const long long a[2] = {split_cold_cost(hbase, r, price), split_hot_cost(hbase, tc, r, price)};
+      const int n_t[2] = {tc, th};
+      for (int part = 0; part < 2; ++part) {
+        if (n_t[part] == 0) continue;
+        const long long e = a[part] + n_t[part] - 1;
+        const int c_first = split_cta(a[part], cost_all, grid), c_last = split_cta(e, cost_all, grid);
+        for (int c = c_first; c <= c_last; ++c)
+          if (split_cta_hits(c, a[part], e, cost_all, grid)) seg_ctas[(2 * r + part) * grid + c] = 1;
+      }
+    }
+  }
+  return TQ_OK;
 }

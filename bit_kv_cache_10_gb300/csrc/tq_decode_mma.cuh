@@ -379,8 +379,17 @@ __global__ void __launch_bounds__(MmaCfg<KB, CL, VB>::kThreads, 1) decode_mma_ke
       cpart[2 * 4 * D + 2 * tid + 1] = 0.0f;
     }
   } else {
-    t0 = total * blockIdx.x / p.grid;
-    t1 = total * (blockIdx.x + 1) / p.grid;
+    // the CTA's range of the weighted split (tq_split_plan.h): tiles plus a
+    // price for every segment start, in equal shares
+    const long long cost_all = split_total_cost(total, static_cast<long long>(p.batch) * p.hkv, p.price);
+    auto start_of = [&](int c) -> long long {
+      if (c >= p.grid) return total;
+      const long long tau = split_cost_at(cost_all, p.grid, c);
+      const int v = split_find_seq(prefix, p.batch, p.hkv, p.price, tau);
+      return v < 0 ? 0 : split_tile_in_seq(prefix, v, p.hkv, seq_tiles<MQ>(p, v).tc, p.price, tau);
+    };
+    t0 = start_of(blockIdx.x);
+    t1 = start_of(blockIdx.x + 1);
     if (t0 >= t1) return;
   }
   const int my_n = static_cast<int>((t1 - t0 - warp + NW - 1) / NW);

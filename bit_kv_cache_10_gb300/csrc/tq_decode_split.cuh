@@ -28,6 +28,7 @@
 
 #include "tq_device.cuh"
 #include "tq_internal.h"
+#include "tq_split_plan.h"
 
 namespace tq {
 
@@ -54,6 +55,7 @@ struct DecodeParams {
   float sparse_tau;  // sparse-V threshold (0: dense)
   int rotated;    // 1: V is summed in the rotated domain (packed modes); 0: int8 mode
   int grid;       // CTAs of the split kernel
+  SplitPrice price;  // segment start prices of the weighted split (tq_split_plan.h)
   float* out;     // [B, Hq, D]
 };
 
@@ -63,8 +65,6 @@ constexpr int kTile = 16;
 constexpr int kCopies = 16;                 // pair-table copies (one per lane of a half-warp)
 constexpr int kSmemBudget = 227 * 1024;
 constexpr float kLazy = 8.0f;               // log2 headroom of the lazily raised softmax maximum
-
-
 
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
 template <int N>
@@ -513,27 +513,6 @@ __device__ __forceinline__ void merge_finish(float (&y)[4], const float (&hv)[4]
     r[i] = l > 0.0f ? fadd(v, hv[i]) / l : 0.0f;
   }
   out[lane] = make_float4(r[0], r[1], r[2], r[3]);
-}
-
-// CTA of the split kernel that processes tile t (the last one whose range starts
-// at or before t): floor(((t + 1) grid - 1) / total), a value below grid.  A float
-// estimate of the quotient is off by at most one (its relative error is a few
-// 2^-24 and the quotient is below 2^10); exact 64-bit products correct it, so no
-// 64-bit division is needed.
-__device__ __forceinline__ int cta_of(long long t, long long total, int grid) {
-  const long long num = (t + 1) * grid - 1;
-  int c = static_cast<int>(static_cast<float>(num) * (1.0f / static_cast<float>(total)));
-  c = c < 0 ? 0 : (c > grid - 1 ? grid - 1 : c);
-  if (static_cast<long long>(c) * total > num) --c;
-  if (static_cast<long long>(c + 1) * total <= num) ++c;
-  return c;
-}
-// Whether CTA c of the split kernel has a non-empty range: always when there are
-// at least as many tiles as CTAs (then total / grid >= 1 separates the starts).
-__device__ __forceinline__ bool cta_live(int c, long long total, int grid) {
-  if (total >= grid) return true;
-  const int t32 = static_cast<int>(total);
-  return t32 * c / grid != t32 * (c + 1) / grid;
 }
 
 }  // namespace

@@ -9,7 +9,8 @@ from __future__ import annotations
 
 import ctypes
 import os
-from ctypes import POINTER, c_double, c_float, c_int8, c_int32, c_int64, c_size_t, c_uint16, c_uint32, c_uint64, c_void_p
+from ctypes import (POINTER, c_double, c_float, c_int8, c_int32, c_int64, c_size_t, c_uint8, c_uint16, c_uint32, c_uint64,
+                    c_void_p)
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libtq.so")
@@ -33,7 +34,7 @@ EXPORTED = (
     "tq_cache_desc_init", "tq_cache_buffer_bytes", "tq_quantize_append", "tq_decode_workspace_bytes",
     "tq_decode_attention", "tq_dequantize", "tq_debug_quantize_rows_host", "tq_decode_attention_no_alloc",
     "tq_cache_desc_set_paged", "tq_multi_query_workspace_bytes", "tq_multi_query_attention",
-    "tq_debug_set_decode_path",
+    "tq_debug_set_decode_path", "tq_debug_split_plan",
 )
 TQ_DEV_ERR_APPEND_RANGE, TQ_DEV_ERR_SEQ_LEN, TQ_DEV_ERR_LAYOUT, TQ_DEV_ERR_BLOCK = 0x1, 0x2, 0x4, 0x8
 TQ_NO_ALLOC_WORKSPACE_BYTES = 16 << 20
@@ -114,6 +115,9 @@ def lib() -> ctypes.CDLL:
                                     c_void_p]
         L.tq_debug_set_decode_path.restype = None
         L.tq_debug_set_decode_path.argtypes = [c_int32]
+        L.tq_debug_split_plan.restype = c_int32
+        L.tq_debug_split_plan.argtypes = [POINTER(c_int32), POINTER(c_int32), c_int32, c_int32, c_int32, c_int32,
+                                          c_int32, POINTER(c_int64), POINTER(c_uint8)]
         L.tq_debug_quantize_rows_host.restype = c_int32
         L.tq_debug_quantize_rows_host.argtypes = [POINTER(TQCodebook), c_uint64, c_int32, c_int32, POINTER(c_uint16),
                                                   c_int32, POINTER(c_uint32), POINTER(c_float)]
@@ -227,3 +231,25 @@ def tq_debug_set_decode_path(path: int) -> None:
     """Decode path for tests (process-wide): 0 automatic, 1 persistent split-K
     kernel + merge kernel, 2 the thread-block-cluster variant where allowed."""
     lib().tq_debug_set_decode_path(int(path))
+
+
+def tq_debug_split_plan(tiles_cold, tiles_hot, hkv: int, grid: int, price_cold: int, price_hot: int,
+                        with_segments: bool = True):
+    """Host computation of the persistent decode path's split (verification only).
+    ``tiles_cold`` / ``tiles_hot``: per work-list sequence, the cold and hot tiles
+    of each of its hkv rows; ``price_cold`` / ``price_hot``: tiles' worth of a
+    cold / hot segment start.  Returns (starts int64 [grid + 1], seg_ctas uint8
+    [2 nv hkv, grid] or None): CTA c takes tiles [starts[c], starts[c + 1]);
+    seg_ctas[2 r + part, c] = 1 when the merge reads CTA c for that row part."""
+    import numpy as np
+
+    tc = np.ascontiguousarray(tiles_cold, dtype=np.int32)
+    th = np.ascontiguousarray(tiles_hot, dtype=np.int32)
+    nv = tc.shape[0]
+    starts = np.zeros(grid + 1, np.int64)
+    seg = np.zeros((2 * nv * hkv, grid), np.uint8) if with_segments else None
+    _check(lib().tq_debug_split_plan(
+        tc.ctypes.data_as(POINTER(c_int32)), th.ctypes.data_as(POINTER(c_int32)), nv, hkv, grid, price_cold, price_hot,
+        starts.ctypes.data_as(POINTER(c_int64)),
+        seg.ctypes.data_as(POINTER(c_uint8)) if seg is not None else None), "tq_debug_split_plan")
+    return starts, seg

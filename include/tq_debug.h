@@ -37,6 +37,25 @@ tq_status tq_debug_quantize_rows_host(const tq_codebook *cb, uint64_t seed, int3
  */
 void tq_debug_set_decode_path(int32_t path);
 
+/*
+ * Split plan of the persistent decode path, computed on the host by the same
+ * functions the kernels use (tq_split_plan.h): the work list has nv sequences
+ * of hkv rows each, a row of sequence v being tiles_cold[v] cold 16-token tiles
+ * followed by tiles_hot[v] hot ones (host arrays, each entry >= 0), and a
+ * CTA's share is counted in tiles plus price_cold (price_hot) tiles for every
+ * cold (hot) segment it starts, a segment being the cold or the hot tiles of
+ * one row.  Writes
+ * starts[0 .. grid] (host, grid + 1 entries): CTA c of the split kernel takes
+ * the tiles [starts[c], starts[c + 1]) of the list.  If seg_ctas is not null
+ * it receives 2 nv hkv rows of grid bytes (host): byte (2 r + part) grid + c is
+ * 1 when the merge kernel reads CTA c's partial for part 0 (cold) or 1 (hot)
+ * of row r, else 0.  TQ_ERR_INVALID_ARG for null arrays, nv < 1, hkv < 1,
+ * grid < 1, a negative count or price, or a list of 2^40 tiles or more.
+ */
+tq_status tq_debug_split_plan(const int32_t *tiles_cold, const int32_t *tiles_hot, int32_t nv, int32_t hkv,
+                              int32_t grid, int32_t price_cold, int32_t price_hot, int64_t *starts,
+                              uint8_t *seg_ctas);
+
 #ifdef __cplusplus
 }
 #endif
