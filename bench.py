@@ -90,7 +90,7 @@ def measured_peak():
 
 
 # the sources of the long-context decode call (split kernels, dispatch, merge and entry points)
-DECODE_SOURCES = ("tq_decode_mma.cuh", "tq_decode_split.cuh", "tq_decode_dispatch.cuh", "tq_decode.cu")
+DECODE_SOURCES = ("tq_decode_mma.cuh", "tq_decode_split.cuh", "tq_split_plan.h", "tq_decode_dispatch.cuh", "tq_decode.cu")
 
 
 def profile_traffic():
