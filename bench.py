@@ -737,23 +737,26 @@ def run_gpu(args):
     paged_ms = paged_decode_ms(torch, tc, lens0, q_dev[sv_s], seqs[sv_s], max_len)
     paged_inorder_ms = paged_decode_ms(torch, tc, lens0, q_dev[sv_s], seqs[sv_s], max_len, permute=False)
 
-    # end to end through the public API with host buffers
-    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
-    h_k, h_v, h_q = pin(kn), pin(vn), pin(qn)
-    h_start = pin((lens0[None, :] + np.arange(total_steps)[:, None]).astype(np.int32))
+    # end to end through the public API with host buffers: each step's new K and V
+    # tokens, queries, start positions and lengths packed in one pinned host record
+    # (one host-to-device copy per step; every part 16-byte aligned), the output
+    # read back into pinned host memory
+    starts_h = (lens0[None, :] + np.arange(total_steps)[:, None]).astype(np.int32)
+    parts = [kn.reshape(total_steps, -1).view(np.uint8), vn.reshape(total_steps, -1).view(np.uint8),
+             qn.reshape(total_steps, -1).view(np.uint8), starts_h.view(np.uint8), (starts_h + 1).view(np.uint8)]
+    offs = np.cumsum([0] + [pt.shape[1] for pt in parts])
+    assert all(o % 16 == 0 for o in offs[:-1])
+    h_rec = torch.from_numpy(np.ascontiguousarray(np.concatenate(parts, axis=1))).pin_memory()
     h_out = torch.empty(B, HQ, D, dtype=torch.float32).pin_memory()
-    d_k = torch.empty_like(k_dev[0])
-    d_v = torch.empty_like(v_dev[0])
-    d_q = torch.empty_like(q_dev[0])
-    d_start = torch.empty(B, dtype=torch.int32, device="cuda")
-    d_seq = torch.empty(B, dtype=torch.int32, device="cuda")
+    d_rec = torch.empty(h_rec.shape[1], dtype=torch.uint8, device="cuda")
+    d_k = d_rec[offs[0]:offs[1]].view(torch.float16).view(k_dev[0].shape)
+    d_v = d_rec[offs[1]:offs[2]].view(torch.float16).view(v_dev[0].shape)
+    d_q = d_rec[offs[2]:offs[3]].view(torch.float16).view(q_dev[0].shape)
+    d_start = d_rec[offs[3]:offs[4]].view(torch.int32)
+    d_seq = d_rec[offs[4]:offs[5]].view(torch.int32)
 
     def e2e_step(s):
-        d_k.copy_(h_k[s], non_blocking=True)
-        d_v.copy_(h_v[s], non_blocking=True)
-        d_q.copy_(h_q[s], non_blocking=True)
-        d_start.copy_(h_start[s], non_blocking=True)
-        torch.add(d_start, 1, out=d_seq)
+        d_rec.copy_(h_rec[s], non_blocking=True)
         tc.append(d_k, d_v, d_start)
         tc.decode(d_q, d_seq, max_len, out=out, workspace=ws)
         h_out.copy_(out, non_blocking=True)
@@ -771,7 +774,7 @@ def run_gpu(args):
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dist, "cuda")
     e2e_bytes = sum(decode_bytes(lens0 + s0 + e2e_warm + i + 1) for i in range(e2e_steps))
-    h2d = kn[0].nbytes + vn[0].nbytes + qn[0].nbytes + B * 4
+    h2d = int(h_rec.shape[1])  # K, V, q, start positions and lengths of one step
     d2h = B * HQ * D * 4
 
     # quantize throughput: batch 16 x 8192 new tokens x 8 KV heads at 3.5 bits (K3 / V4)
