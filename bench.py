@@ -740,26 +740,47 @@ def run_gpu(args):
     # end to end through the public API with host buffers: each step's new K and V
     # tokens, queries, start positions and lengths packed in one pinned host record
     # (one host-to-device copy per step; every part 16-byte aligned), the output
-    # read back into pinned host memory
+    # read back into pinned host memory.  Copies run on their own streams into
+    # double buffers, ordered by events: the record of step s + 1 uploads while
+    # step s computes, and the output of step s downloads while step s + 1 computes
     starts_h = (lens0[None, :] + np.arange(total_steps)[:, None]).astype(np.int32)
     parts = [kn.reshape(total_steps, -1).view(np.uint8), vn.reshape(total_steps, -1).view(np.uint8),
              qn.reshape(total_steps, -1).view(np.uint8), starts_h.view(np.uint8), (starts_h + 1).view(np.uint8)]
     offs = np.cumsum([0] + [pt.shape[1] for pt in parts])
     assert all(o % 16 == 0 for o in offs[:-1])
     h_rec = torch.from_numpy(np.ascontiguousarray(np.concatenate(parts, axis=1))).pin_memory()
-    h_out = torch.empty(B, HQ, D, dtype=torch.float32).pin_memory()
-    d_rec = torch.empty(h_rec.shape[1], dtype=torch.uint8, device="cuda")
-    d_k = d_rec[offs[0]:offs[1]].view(torch.float16).view(k_dev[0].shape)
-    d_v = d_rec[offs[1]:offs[2]].view(torch.float16).view(v_dev[0].shape)
-    d_q = d_rec[offs[2]:offs[3]].view(torch.float16).view(q_dev[0].shape)
-    d_start = d_rec[offs[3]:offs[4]].view(torch.int32)
-    d_seq = d_rec[offs[4]:offs[5]].view(torch.int32)
+    h_outs = [torch.empty(B, HQ, D, dtype=torch.float32).pin_memory() for _ in range(2)]
+    d_recs = [torch.empty(h_rec.shape[1], dtype=torch.uint8, device="cuda") for _ in range(2)]
+    d_outs = [torch.empty(B, HQ, D, dtype=torch.float32, device="cuda") for _ in range(2)]
+
+    def rec_views(d_rec):  # (k, v, q, start positions, lengths) of a device record
+        return (d_rec[offs[0]:offs[1]].view(torch.float16).view(k_dev[0].shape),
+                d_rec[offs[1]:offs[2]].view(torch.float16).view(v_dev[0].shape),
+                d_rec[offs[2]:offs[3]].view(torch.float16).view(q_dev[0].shape),
+                d_rec[offs[3]:offs[4]].view(torch.int32), d_rec[offs[4]:offs[5]].view(torch.int32))
+
+    views = [rec_views(d) for d in d_recs]
+    h2d_stream, d2h_stream = torch.cuda.Stream(), torch.cuda.Stream()
+    in_ready = [torch.cuda.Event() for _ in range(2)]  # record i uploaded
+    done = [torch.cuda.Event() for _ in range(2)]      # the step that used record / output i computed
+    out_read = [torch.cuda.Event() for _ in range(2)]  # output i downloaded
 
     def e2e_step(s):
-        d_rec.copy_(h_rec[s], non_blocking=True)
+        i = s % 2
+        d_k, d_v, d_q, d_start, d_seq = views[i]
+        h2d_stream.wait_event(done[i])  # the step two back has read this record
+        with torch.cuda.stream(h2d_stream):
+            d_recs[i].copy_(h_rec[s], non_blocking=True)
+        in_ready[i].record(h2d_stream)
+        stream.wait_event(in_ready[i])
+        stream.wait_event(out_read[i])  # the output two steps back has been read
         tc.append(d_k, d_v, d_start)
-        tc.decode(d_q, d_seq, max_len, out=out, workspace=ws)
-        h_out.copy_(out, non_blocking=True)
+        tc.decode(d_q, d_seq, max_len, out=d_outs[i], workspace=ws)
+        done[i].record(stream)
+        d2h_stream.wait_event(done[i])
+        with torch.cuda.stream(d2h_stream):
+            h_outs[i].copy_(d_outs[i], non_blocking=True)
+        out_read[i].record(d2h_stream)
 
     for i in range(e2e_warm):
         e2e_step(s0 + i)
@@ -768,14 +789,19 @@ def run_gpu(args):
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
+    h2d_stream.wait_event(e0)  # no copy of the timed steps starts before the first event
     for i in range(e2e_steps):
         e2e_step(s0 + e2e_warm + i)
+    last = (s0 + e2e_warm + e2e_steps - 1) % 2
+    stream.wait_event(out_read[last])  # the last output is on the host inside the timed region
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dist, "cuda")
     e2e_bytes = sum(decode_bytes(lens0 + s0 + e2e_warm + i + 1) for i in range(e2e_steps))
     h2d = int(h_rec.shape[1])  # K, V, q, start positions and lengths of one step
     d2h = B * HQ * D * 4
+    if tc.device_status() != 0:
+        raise RuntimeError("device status set by the end-to-end steps")
 
     # quantize throughput: batch 16 x 8192 new tokens x 8 KV heads at 3.5 bits (K3 / V4)
     del k_dev, v_dev
@@ -846,7 +872,9 @@ def run_gpu(args):
                                     "write flushed L2 before each call (ms_l2_resident: back-to-back calls, the "
                                     "4 MB cache stays in L2)"},
         "e2e": {"value": job_throughput(e2e_bytes, e2e_ms, world), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "copies": "pinned host record uploaded and output downloaded every step on two copy streams "
+                          "into double buffers, overlapping the previous and next step's kernels"},
         "clocks": clocks,
         # per timed step: the one-token append (evict fused), the split-K kernel and the merge
         "gpu_launches": args.steps * 3,
