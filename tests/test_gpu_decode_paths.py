@@ -39,6 +39,10 @@ CASES = {
     "asym_v3_hot": ([100, 1500], 2, 8, 16, 3, 64, 1.0),
     "int8_b1": ([4096], 8, 32, 8, 8, 0, 1.0),
     "int8_hot_ragged": ([0, 15, 700, 2049], 2, 4, 8, 8, 48, 2.0),
+    # one or two long rows: the persistent kernel spreads each row over more than 32
+    # CTAs, so the merge takes its general path (partials read in rounds of 32)
+    "one_long_row_hot": ([20000], 1, 4, 3, 4, 256, 1.0),
+    "two_long_rows_g1": ([9000, 12001], 1, 1, 4, 4, 0, 2.0),
 }
 
 
