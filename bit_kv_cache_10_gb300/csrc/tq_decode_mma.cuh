@@ -2,8 +2,9 @@
 // every mode: packed K of 2, 3 or 4 bits or fp16 K, with packed V of 2, 3 or 4
 // bits (narrower codes spread to nibbles), and the int8 mode.  The work list,
 // the tile staging, the partial slots and the merge output are in
-// tq_decode_split.cuh; the persistent variant covers an equal tile range per
-// CTA, the cluster variant (CL) one (b, h) row per 8-CTA cluster.
+// tq_decode_split.cuh; the persistent variant covers one contiguous tile range
+// per CTA (the weighted split of tq_split_plan.h), the cluster variant (CL) one
+// (b, h) row per 8-CTA cluster.
 //
 // Exact operands from lookups.  A float32 centroid c is the sum of two fp16
 // numbers, hi = RN16(c) and lo = RN16(c - hi), which together carry 22

@@ -6,8 +6,9 @@
 // positions [0, L - min(W, L))) and, with a hot window, a hot row (the newest
 // min(W, L) positions, whose V is read from the fp16 ring).  Rows are cut into
 // 16-token tiles and listed in (b, h, cold/hot) order; the list is split into
-// one contiguous, equal range per CTA, so that every SM gets the same number
-// of tiles whatever the lengths are.  For attention of nq query tokens per
+// one contiguous range per CTA, equal in tiles plus a price for every row part
+// a CTA starts (tq_split_plan.h), so that every SM gets the same work whatever
+// the lengths are.  For attention of nq query tokens per
 // sequence (MQ variants) every query token is a sequence of the list of its
 // own, whose length is its causal prefix; its tiles are read from the cache
 // rows of the sequence it belongs to.
