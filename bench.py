@@ -90,6 +90,7 @@ def measured_peak():
 
 
 # the sources of the long-context decode call (split kernels, dispatch, merge and entry points)
+DECODE_SAMPLE = 8  # one timed step in DECODE_SAMPLE has its decode call bracketed by events
 DECODE_SOURCES = ("tq_decode_mma.cuh", "tq_decode_split.cuh", "tq_split_plan.h", "tq_decode_dispatch.cuh", "tq_decode.cu")
 
 
@@ -660,20 +661,26 @@ def run_gpu(args):
     sampler = ClockSampler(torch.cuda.current_device())
     sampler.start()
     time.sleep(0.15)
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps + 2)]
+    # the decode call of every DECODE_SAMPLE-th step is bracketed by a pair of events
+    # (its duration, for the roofline); the other steps run without events between
+    # their kernels, as an application's loop would
+    sampled = list(range(0, args.steps, DECODE_SAMPLE))
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * len(sampled) + 2)]
     torch.cuda.synchronize()
     ev[0].record(stream)
     for i in range(args.steps):
         s = args.warmup + i
         tc.append(k_dev[s], v_dev[s], starts[s])
-        ev[2 * i + 1].record(stream)
+        if i % DECODE_SAMPLE == 0:
+            ev[2 * (i // DECODE_SAMPLE) + 1].record(stream)
         tc.decode(q_dev[s], seqs[s], max_len, out=out, workspace=ws)
-        ev[2 * i + 2].record(stream)
+        if i % DECODE_SAMPLE == 0:
+            ev[2 * (i // DECODE_SAMPLE) + 2].record(stream)
     ev[-1].record(stream)
     torch.cuda.synchronize()
     clock_rows = sampler.stop()
     total_ms = ev[0].elapsed_time(ev[-1])
-    decode_ms = [ev[2 * i + 1].elapsed_time(ev[2 * i + 2]) for i in range(args.steps)]
+    decode_ms = [ev[2 * k + 1].elapsed_time(ev[2 * k + 2]) for k in range(len(sampled))]
     status = tc.device_status()
     if status != 0:
         raise RuntimeError("device status %#x during the benchmark" % status)
@@ -822,7 +829,7 @@ def run_gpu(args):
 
     peak, peak_kind = measured_peak()
     dec_avg_ms = float(np.mean(decode_ms))
-    dec_bytes = float(np.mean(step_bytes))
+    dec_bytes = float(np.mean([step_bytes[i] for i in sampled]))  # the bracketed calls
     achieved = dec_bytes / (dec_avg_ms * 1e-3) / 1e9
     traffic = profile_traffic()
     line = {

@@ -271,8 +271,9 @@ tq_status run_attention(const tq_cache_desc* d, const void* q, int nq, const int
     st = sparse ? dispatch_split_sparse(p, g, kb, d->v_bits, s) : dispatch_split_variant<false, false>(p, g, kb, d->v_bits, s);
   }
   if (st != TQ_OK) return st;
-  // programmatic dependent launch: the merge grid is scheduled as the split
-  // kernel's CTAs retire and waits (griddepcontrol.wait) for its completion
+  // with programmatic dependent launch (kProgrammaticLaunch) the merge grid would be
+  // scheduled as the split kernel's CTAs retire and wait (griddepcontrol.wait) for
+  // its completion; without it, it starts after the split kernel
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(d->num_kv_heads, p.batch);
   cfg.blockDim = dim3(4 * 32);
@@ -280,7 +281,7 @@ tq_status run_attention(const tq_cache_desc* d, const void* q, int nq, const int
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[0].val.programmaticStreamSerializationAllowed = kProgrammaticLaunch;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (cudaLaunchKernelEx(&cfg, decode_merge_kernel, p) != cudaSuccess) return TQ_ERR_CUDA;

@@ -14,6 +14,13 @@ constexpr int kMaxBits = 4;       // "What bit widths does TurboQuant support?")
 constexpr int kMaxGroup = 4;      // query heads per KV head handled by the decode kernels
 constexpr int kMaxDecodeCtas = 512;   // largest split-K grid (one CTA per SM)
 constexpr int kMaxDecodeBatch = 512;  // sequences per decode call (per-sequence tile prefix in shared memory)
+// Programmatic dependent launch of the append, split and merge kernels (each
+// kernel's parameter-only prologue overlapping the grid before it).  Off: on
+// GB300 the decode step (one-token append, split kernel, merge kernel) ran
+// 0.1563 ms without it and 0.1688 ms with it on all three launches, the split
+// kernel's early launch costing the most.  The kernels keep their
+// griddepcontrol instructions, which do nothing in a launch without it.
+constexpr int kProgrammaticLaunch = 0;
 
 // Words of one packed token vector.
 inline int words_per_token(int head_dim, int bits) { return head_dim * bits / 32; }
