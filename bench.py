@@ -634,8 +634,9 @@ def run_gpu(args):
     native.lib()
 
     e2e_steps, e2e_warm = max(3, min(args.steps, 500)), 3
+    graph_steps = max(3, min(args.steps, 300))
     probe_steps = 10000
-    total_steps = args.warmup + args.steps + e2e_warm + e2e_steps + probe_steps
+    total_steps = args.warmup + args.steps + e2e_warm + e2e_steps + 1 + graph_steps + probe_steps
     cap = HI + total_steps + 64
     tc, lens0 = build_decode_cache(torch, cap)
     kn, vn, qn = step_inputs(total_steps)
@@ -656,31 +657,39 @@ def run_gpu(args):
     for s in range(args.warmup):
         step(s)
     torch.cuda.synchronize()
+    # the timed steps, captured as one CUDA graph (the kernels of K steps in order,
+    # without launch gaps between them) and replayed once; the decode call of every
+    # DECODE_SAMPLE-th step is bracketed by two events that are nodes of the graph
+    # (its duration, for the roofline).  Capturing runs nothing: the steps run in
+    # the replay.
+    sampled = list(range(0, args.steps, DECODE_SAMPLE))
+    dev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2 * len(sampled))]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(args.steps):
+            s = args.warmup + i
+            tc.append(k_dev[s], v_dev[s], starts[s])
+            if i % DECODE_SAMPLE == 0:
+                dev[2 * (i // DECODE_SAMPLE)].record()
+            tc.decode(q_dev[s], seqs[s], max_len, out=out, workspace=ws)
+            if i % DECODE_SAMPLE == 0:
+                dev[2 * (i // DECODE_SAMPLE) + 1].record()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     sampler = ClockSampler(torch.cuda.current_device())
     sampler.start()
     time.sleep(0.15)
-    # the decode call of every DECODE_SAMPLE-th step is bracketed by a pair of events
-    # (its duration, for the roofline); the other steps run without events between
-    # their kernels, as an application's loop would
-    sampled = list(range(0, args.steps, DECODE_SAMPLE))
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * len(sampled) + 2)]
     torch.cuda.synchronize()
     ev[0].record(stream)
-    for i in range(args.steps):
-        s = args.warmup + i
-        tc.append(k_dev[s], v_dev[s], starts[s])
-        if i % DECODE_SAMPLE == 0:
-            ev[2 * (i // DECODE_SAMPLE) + 1].record(stream)
-        tc.decode(q_dev[s], seqs[s], max_len, out=out, workspace=ws)
-        if i % DECODE_SAMPLE == 0:
-            ev[2 * (i // DECODE_SAMPLE) + 2].record(stream)
-    ev[-1].record(stream)
+    graph.replay()
+    ev[1].record(stream)
     torch.cuda.synchronize()
     clock_rows = sampler.stop()
-    total_ms = ev[0].elapsed_time(ev[-1])
-    decode_ms = [ev[2 * k + 1].elapsed_time(ev[2 * k + 2]) for k in range(len(sampled))]
+    total_ms = ev[0].elapsed_time(ev[1])
+    decode_ms = [dev[2 * k].elapsed_time(dev[2 * k + 1]) for k in range(len(sampled))]
+    del graph
     status = tc.device_status()
     if status != 0:
         raise RuntimeError("device status %#x during the benchmark" % status)
@@ -810,6 +819,21 @@ def run_gpu(args):
     if tc.device_status() != 0:
         raise RuntimeError("device status set by the end-to-end steps")
 
+    # the same step launched on the stream, one call after the other (no graph)
+    sg0 = s0 + e2e_warm + e2e_steps
+    step(sg0)
+    se0, se1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    se0.record(stream)
+    for i in range(graph_steps):
+        step(sg0 + 1 + i)
+    se1.record(stream)
+    torch.cuda.synchronize()
+    stream_ms = max_over_ranks(se0.elapsed_time(se1), world, dist, "cuda")
+    stream_bytes = sum(decode_bytes(lens0 + sg0 + 1 + i + 1) for i in range(graph_steps))
+    if tc.device_status() != 0:
+        raise RuntimeError("device status set by the stream-launched steps")
+
     # quantize throughput: batch 16 x 8192 new tokens x 8 KV heads at 3.5 bits (K3 / V4)
     del k_dev, v_dev
     kq, vq = quantize_inputs(torch)
@@ -882,6 +906,11 @@ def run_gpu(args):
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "copies": "pinned host record uploaded and output downloaded every step on two copy streams "
                           "into double buffers, overlapping the previous and next step's kernels"},
+        "launch": "the timed steps captured as one CUDA graph (each step's kernels in order) and replayed once",
+        "stream_launched": {"value": job_throughput(stream_bytes, stream_ms, world), "unit": "GB/s",
+                            "ms_per_step": stream_ms / graph_steps, "steps": graph_steps,
+                            "note": "the same step launched call by call on the stream instead of replayed as a "
+                                    "CUDA graph"},
         "clocks": clocks,
         # per timed step: the one-token append (evict fused), the split-K kernel and the merge
         "gpu_launches": args.steps * 3,
