@@ -409,11 +409,33 @@ def build_plain_cache(torch, batch, ctx, k_fp16, seed):
     return tc
 
 
+def graph_call_ms(torch, fn, n):
+    """Mean time (ms) of fn over n back-to-back calls captured as one CUDA graph
+    and replayed once between two events (after 3 calls on the stream)."""
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(n):
+            fn()
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(st)
+    graph.replay()
+    e1.record(st)
+    torch.cuda.synchronize()
+    del graph
+    return e0.elapsed_time(e1) / n
+
+
 def time_plain_decode(torch, batch, ctx, k_fp16, reps=50, flush=False):
     """Mean decode-call time (ms) and algorithmic bytes of one call on a
     build_plain_cache cache, after 3 untimed calls.  With ``flush`` a 256 MB
     buffer (twice L2) is written before every call and only the call itself is
-    between the events, so the cache is read from HBM."""
+    between the events, so the cache is read from HBM; without it the calls run
+    back to back, replayed as one CUDA graph."""
     tc = build_plain_cache(torch, batch, ctx, k_fp16, SEED + 3)
     q = torch.from_numpy(synth.queries_fp16(SEED + 3, batch, HQ, D)).cuda()
     lens = torch.full((batch,), ctx, dtype=torch.int32, device="cuda")
@@ -434,15 +456,8 @@ def time_plain_decode(torch, batch, ctx, k_fp16, reps=50, flush=False):
         torch.cuda.synchronize()
         ms = float(np.mean([e0.elapsed_time(e1) for e0, e1 in ev]))
         del scrub
-    else:
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
-        torch.cuda.synchronize()
-        ev[0].record(st)
-        for i in range(reps):
-            tc.decode(q, lens, ctx, out=out, workspace=ws)
-            ev[i + 1].record(st)
-        torch.cuda.synchronize()
-        ms = float(np.mean([ev[i].elapsed_time(ev[i + 1]) for i in range(reps)]))
+    else:  # back-to-back calls, replayed as a CUDA graph
+        ms = graph_call_ms(torch, lambda: tc.decode(q, lens, ctx, out=out, workspace=ws), reps)
     if tc.device_status() != 0:
         raise RuntimeError("device status set by the decode timing")
     k_tok = D * 2 if k_fp16 else D * KB // 8 + 4
@@ -500,7 +515,7 @@ def time_int8(torch, lens, reps=20):
         torch.cuda.synchronize()
         return float(np.mean([ev[i].elapsed_time(ev[i + 1]) for i in range(n)]))
 
-    dec_ms = timed(lambda: tc.decode(q, sl, cap, out=out, workspace=ws), reps)
+    dec_ms = graph_call_ms(torch, lambda: tc.decode(q, sl, cap, out=out, workspace=ws), reps)
     if tc.device_status() != 0:
         raise RuntimeError("device status set by the int8 decode timing")
     dec_bytes = int(np.sum(lens)) * HKV * 2 * (D + 4) + len(lens) * HQ * D * (2 + 4)
@@ -538,23 +553,14 @@ def paged_copy(torch, tc, bs=64, permute=True):
 
 
 def paged_decode_ms(torch, tc, lens0, q, seqs, max_len, bs=64, reps=20, permute=True):
-    """Mean decode-call time of a paged copy of `tc`, after 3 untimed calls."""
+    """Mean decode-call time of a paged copy of `tc` (back-to-back calls replayed as
+    one CUDA graph, after 3 calls on the stream)."""
     pg = paged_copy(torch, tc, bs, permute)
     out = torch.empty(B, HQ, D, dtype=torch.float32, device="cuda")
     ws = torch.empty(pg.workspace_bytes(max_len), dtype=torch.uint8, device="cuda")
-    for _ in range(3):
-        pg.decode(q, seqs, max_len, out=out, workspace=ws)
-    st = torch.cuda.current_stream()
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
-    torch.cuda.synchronize()
-    ev[0].record(st)
-    for i in range(reps):
-        pg.decode(q, seqs, max_len, out=out, workspace=ws)
-        ev[i + 1].record(st)
-    torch.cuda.synchronize()
+    ms = graph_call_ms(torch, lambda: pg.decode(q, seqs, max_len, out=out, workspace=ws), reps)
     if pg.device_status() != 0:
         raise RuntimeError("device status set by the paged decode")
-    ms = float(np.mean([ev[i].elapsed_time(ev[i + 1]) for i in range(reps)]))
     del pg
     return ms
 
@@ -713,16 +719,7 @@ def run_gpu(args):
     # sparse-V decode on the same cache (threshold 1e-3; the dense call above is the headline)
     tc.desc.sparse_v_threshold = 1e-3
     sv_s = args.warmup + args.steps
-    for _ in range(3):
-        tc.decode(q_dev[sv_s], seqs[sv_s], max_len, out=out, workspace=ws)
-    sev = [torch.cuda.Event(enable_timing=True) for _ in range(21)]
-    torch.cuda.synchronize()
-    sev[0].record(stream)
-    for i in range(20):
-        tc.decode(q_dev[sv_s], seqs[sv_s], max_len, out=out, workspace=ws)
-        sev[i + 1].record(stream)
-    torch.cuda.synchronize()
-    sparse_ms = float(np.mean([sev[i].elapsed_time(sev[i + 1]) for i in range(20)]))
+    sparse_ms = graph_call_ms(torch, lambda: tc.decode(q_dev[sv_s], seqs[sv_s], max_len, out=out, workspace=ws), 20)
     tc.desc.sparse_v_threshold = 0.0
     if tc.device_status() != 0:
         raise RuntimeError("device status set by the sparse-V decode")
@@ -733,16 +730,7 @@ def run_gpu(args):
     mq_out = torch.empty(B, mq_n, HQ, D, dtype=torch.float32, device="cuda")
     mq_ws = torch.empty(native.tq_multi_query_workspace_bytes(tc.desc, mq_n, max_len), dtype=torch.uint8,
                         device="cuda")
-    for _ in range(3):
-        tc.multi_query(mq_q, seqs[sv_s], max_len, out=mq_out, workspace=mq_ws)
-    mev = [torch.cuda.Event(enable_timing=True) for _ in range(11)]
-    torch.cuda.synchronize()
-    mev[0].record(stream)
-    for i in range(10):
-        tc.multi_query(mq_q, seqs[sv_s], max_len, out=mq_out, workspace=mq_ws)
-        mev[i + 1].record(stream)
-    torch.cuda.synchronize()
-    mq_ms = float(np.mean([mev[i].elapsed_time(mev[i + 1]) for i in range(10)]))
+    mq_ms = graph_call_ms(torch, lambda: tc.multi_query(mq_q, seqs[sv_s], max_len, out=mq_out, workspace=mq_ws), 10)
     if tc.device_status() != 0:
         raise RuntimeError("device status set by the multi-query attention")
     mq_lens = lens0 + sv_s + 1
@@ -878,30 +866,33 @@ def run_gpu(args):
         "sparse_v": {"threshold": 1e-3, "ms": sparse_ms, "dense_ms": dec_avg_ms,
                      "value": decode_bytes(lens0 + sv_s + 1) / (sparse_ms * 1e-3) / 1e9, "unit": "GB/s",
                      "note": "same long-context decode call with V skipped for weights below 1e-3 of the running "
-                             "maximum (random synthetic codes: diffuse attention, few skips)"},
+                             "maximum (random synthetic codes: diffuse attention, few skips); back-to-back calls "
+                             "replayed as one CUDA graph"},
         "paged": {"block_size": 64, "ms": paged_ms, "ms_blocks_in_order": paged_inorder_ms,
                   "value": decode_bytes(lens0 + sv_s + 1) / (paged_ms * 1e-3) / 1e9, "unit": "GB/s",
                   "note": "same long-context decode call on a block-table copy of the cache (64-token blocks, "
-                          "permuted pool)"},
+                          "permuted pool); back-to-back calls replayed as one CUDA graph"},
         "multi_query": {"n_query": mq_n, "ms": mq_ms, "value": mq_fma / (mq_ms * 1e-3) / 1e12, "unit": "T FMA/s",
                         "frac": mq_fma / (mq_ms * 1e-3) / FP32_FMA_PEAK, "bound": "alu",
                         "peak": FP32_FMA_PEAK / 1e12, "cache_gbs": decode_bytes(mq_lens) / (mq_ms * 1e-3) / 1e9,
                         "workload": "speculative verification: the 8 newest tokens of each long-context sequence, "
-                                    "causal, B4, 32q/8kv, K3/V4 + 256 fp16 hot V"},
+                                    "causal, B4, 32q/8kv, K3/V4 + 256 fp16 hot V; back-to-back calls replayed as "
+                                    "one CUDA graph"},
         "asym": {"value": asym_bytes / (asym_ms * 1e-3) / 1e9, "unit": "GB/s", "ms": asym_ms,
                  "frac": asym_bytes / (asym_ms * 1e-3) / 1e9 / peak, "algorithmic_bytes_per_launch": asym_bytes,
-                 "workload": "asym decode: fp16 K + 4-bit V, B8, 32q/8kv, d128, context 16384, no hot window"},
+                 "workload": "asym decode: fp16 K + 4-bit V, B8, 32q/8kv, d128, context 16384, no hot window; "
+                             "back-to-back calls replayed as one CUDA graph"},
         "int8": {"value": i8_bytes / (i8_ms * 1e-3) / 1e9, "unit": "GB/s", "ms": i8_ms,
                  "frac": i8_bytes / (i8_ms * 1e-3) / 1e9 / peak, "algorithmic_bytes_per_launch": i8_bytes,
                  "workload": "int8-mode decode (per-token INT8 absmax K and V, no hot window): B4, 32q/8kv, "
-                             "d128, the long-context lengths",
+                             "d128, the long-context lengths; back-to-back calls replayed as one CUDA graph",
                  "quantize_mtokens_s": QB * QT / (i8q_ms * 1e-3) / 1e6, "quantize_ms": i8q_ms,
                  "quantize_hbm_gbs": i8q_bytes / (i8q_ms * 1e-3) / 1e9},
         "llama_layer": {"value": small_bytes / (small_cold_ms * 1e-3) / 1e9, "unit": "GB/s", "ms": small_cold_ms,
                         "ms_l2_resident": small_ms, "algorithmic_bytes_per_launch": small_bytes,
                         "workload": "3.5-bit decode: B1, 32q/8kv, d128, context 4096, K3/V4; ms after a 256 MB "
-                                    "write flushed L2 before each call (ms_l2_resident: back-to-back calls, the "
-                                    "4 MB cache stays in L2)"},
+                                    "write flushed L2 before each call (ms_l2_resident: back-to-back calls "
+                                    "replayed as one CUDA graph, the 4 MB cache stays in L2)"},
         "e2e": {"value": job_throughput(e2e_bytes, e2e_ms, world), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "copies": "pinned host record uploaded and output downloaded every step on two copy streams "
