@@ -21,7 +21,13 @@
  * Asynchrony.  Functions taking a stream enqueue kernels on it and return at
  *              once; results are ready when the stream is.  A NULL stream is
  *              the legacy default stream.  The host-only helpers are
- *              synchronous and need no GPU.
+ *              synchronous and need no GPU.  The stream functions only
+ *              launch kernels (no allocation, no synchronisation, no reads of
+ *              device data on the host), so a sequence of appends and decodes
+ *              may be captured into a CUDA graph and replayed; the captured
+ *              kernels keep the arguments of the capture (pointers, sizes,
+ *              max_seq_len), while device-side inputs such as start
+ *              positions and lengths are read when the graph runs.
  * Errors.      Argument errors are found on the host and returned before any
  *              launch (nothing is enqueued).  A failed launch returns
  *              TQ_ERR_CUDA.  Errors that only the device can see (a start
