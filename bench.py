@@ -769,37 +769,55 @@ def run_gpu(args):
     done = [torch.cuda.Event() for _ in range(2)]      # the step that used record / output i computed
     out_read = [torch.cuda.Event() for _ in range(2)]  # output i downloaded
 
-    def e2e_step(s):
+    first_use = [True, True]  # no earlier step has used record / output i yet
+
+    def e2e_step(s, cs):
+        """Step s on compute stream cs: upload, append + decode, download."""
         i = s % 2
         d_k, d_v, d_q, d_start, d_seq = views[i]
-        h2d_stream.wait_event(done[i])  # the step two back has read this record
+        if not first_use[i]:
+            h2d_stream.wait_event(done[i])  # the step two back has read this record
         with torch.cuda.stream(h2d_stream):
             d_recs[i].copy_(h_rec[s], non_blocking=True)
         in_ready[i].record(h2d_stream)
-        stream.wait_event(in_ready[i])
-        stream.wait_event(out_read[i])  # the output two steps back has been read
-        tc.append(d_k, d_v, d_start)
-        tc.decode(d_q, d_seq, max_len, out=d_outs[i], workspace=ws)
-        done[i].record(stream)
+        cs.wait_event(in_ready[i])
+        if not first_use[i]:
+            cs.wait_event(out_read[i])  # the output two steps back has been read
+        with torch.cuda.stream(cs):
+            tc.append(d_k, d_v, d_start)
+            tc.decode(d_q, d_seq, max_len, out=d_outs[i], workspace=ws)
+        done[i].record(cs)
         d2h_stream.wait_event(done[i])
         with torch.cuda.stream(d2h_stream):
             h_outs[i].copy_(d_outs[i], non_blocking=True)
         out_read[i].record(d2h_stream)
+        first_use[i] = False
 
     for i in range(e2e_warm):
-        e2e_step(s0 + i)
+        e2e_step(s0 + i, stream)
+    torch.cuda.synchronize()
+    # the timed steps (uploads, kernels, downloads and the events that order them)
+    # captured as one CUDA graph, the copy streams forked from and joined to the
+    # capture; the replay is the timed region
+    graph = torch.cuda.CUDAGraph()
+    first_use[:] = [True, True]
+    with torch.cuda.graph(graph):
+        cap = torch.cuda.current_stream()
+        h2d_stream.wait_stream(cap)
+        d2h_stream.wait_stream(cap)
+        for i in range(e2e_steps):
+            e2e_step(s0 + e2e_warm + i, cap)
+        cap.wait_stream(h2d_stream)
+        cap.wait_stream(d2h_stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    h2d_stream.wait_event(e0)  # no copy of the timed steps starts before the first event
-    for i in range(e2e_steps):
-        e2e_step(s0 + e2e_warm + i)
-    last = (s0 + e2e_warm + e2e_steps - 1) % 2
-    stream.wait_event(out_read[last])  # the last output is on the host inside the timed region
+    graph.replay()  # ends after the last output is on the host
     e1.record(stream)
     torch.cuda.synchronize()
+    del graph
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dist, "cuda")
     e2e_bytes = sum(decode_bytes(lens0 + s0 + e2e_warm + i + 1) for i in range(e2e_steps))
     h2d = int(h_rec.shape[1])  # K, V, q, start positions and lengths of one step
@@ -896,7 +914,8 @@ def run_gpu(args):
         "e2e": {"value": job_throughput(e2e_bytes, e2e_ms, world), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "copies": "pinned host record uploaded and output downloaded every step on two copy streams "
-                          "into double buffers, overlapping the previous and next step's kernels"},
+                          "into double buffers, overlapping the previous and next step's kernels; the steps "
+                          "captured as one CUDA graph with the copies and replayed"},
         "launch": "the timed steps captured as one CUDA graph (each step's kernels in order) and replayed once",
         "stream_launched": {"value": job_throughput(stream_bytes, stream_ms, world), "unit": "GB/s",
                             "ms_per_step": stream_ms / graph_steps, "steps": graph_steps,
