@@ -257,7 +257,9 @@ __device__ __forceinline__ void quantize_step_int8(const uint8_t* rowp, int q, u
   }
 }
 
-template <bool PAGED, bool FUSE>
+// PLAIN: contiguous layout, no hot window, packed or int8 K, append pass: no row
+// goes to the ring or to an fp16 copy, so the step needs neither test.
+template <bool PAGED, bool FUSE, bool PLAIN = false>
 __global__ void __launch_bounds__(kWarps * 32, 1) quantize_append_kernel(const QuantParams p) {
   asm volatile("griddepcontrol.launch_dependents;\n");  // the next grid may start its prologue
   extern __shared__ __align__(16) uint8_t smem[];
@@ -331,9 +333,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1) quantize_append_kernel(const Q
       __syncwarp();
       const uint8_t* tile = tiles;
       const bool k_tensor = jb.tensor == 0;
-      const bool copy_k = k_tensor && p.k_mode == TQ_K_FP16;
+      const bool copy_k = !PLAIN && k_tensor && p.k_mode == TQ_K_FP16;
       int cold_end = 1 << 30;
-      if (!k_tensor && p.hot > 0 && !p.evict) cold_end = jb.end - min(p.hot, jb.end);
+      if (!PLAIN && !k_tensor && p.hot > 0 && !p.evict) cold_end = jb.end - min(p.hot, jb.end);
       auto quantize_row = [&](const uint8_t* rowp, int bits, const LutEntry* lut, int lut_a, uint32_t* dw, float* dn,
                               bool store) {
         switch (bits) {
@@ -347,11 +349,17 @@ __global__ void __launch_bounds__(kWarps * 32, 1) quantize_append_kernel(const Q
       for (int step = 0; step < kTileRows / 8; ++step) {
         const int row = 8 * step + vrow;
         int pos = 0;
-        const bool have = row_present(p, jb, row, &pos);
+        bool have;
+        if constexpr (PLAIN) {
+          pos = jb.start + jb.tile * kTileRows + row;
+          have = jb.tile * kTileRows + row < jb.count;
+        } else {
+          have = row_present(p, jb, row, &pos);
+        }
         if (!__any_sync(0xffffffffu, have)) break;  // rows are filled in order: no later step has one
         long long ridx = (static_cast<long long>(jb.b) * p.heads + jb.h) * p.cap + pos;  // cache row
         if constexpr (PAGED) ridx = have ? p.map.row(jb.b, jb.h, pos) : 0;  // through the block table
-        const bool to_copy = copy_k || (!k_tensor && pos >= cold_end);
+        const bool to_copy = !PLAIN && (copy_k || (!k_tensor && pos >= cold_end));
         const bool to_ring = !copy_k && to_copy;  // hot V goes to the per-sequence ring, not the pool
         if constexpr (PAGED)
           if (have && ridx < 0 && !to_ring && p.status != nullptr) atomicOr(p.status, TQ_DEV_ERR_BLOCK);
@@ -628,8 +636,10 @@ tq_status launch_quantize(QuantParams& p, cudaStream_t stream) {
   if (p.jobs <= 0) return TQ_OK;
   const size_t smem = quant_smem_bytes(p.k_lut_a, p.v_lut_a);
   const bool paged = p.map.table != nullptr;
+  const bool plain = !paged && !p.fuse_evict && p.hot == 0 && !p.evict && p.k_mode != TQ_K_FP16;
   auto kern = paged ? (p.fuse_evict ? quantize_append_kernel<true, true> : quantize_append_kernel<true, false>)
-                    : (p.fuse_evict ? quantize_append_kernel<false, true> : quantize_append_kernel<false, false>);
+                    : (p.fuse_evict ? quantize_append_kernel<false, true>
+                                    : (plain ? quantize_append_kernel<false, false, true> : quantize_append_kernel<false, false>));
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
     return TQ_ERR_CUDA;
   const int sms = sm_count_q();
