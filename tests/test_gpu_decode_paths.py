@@ -43,6 +43,10 @@ CASES = {
     # CTAs, so the merge takes its general path (partials read in rounds of 32)
     "one_long_row_hot": ([20000], 1, 4, 3, 4, 256, 1.0),
     "two_long_rows_g1": ([9000, 12001], 1, 1, 4, 4, 0, 2.0),
+    # a single short row: fewer price units of the weighted split than CTAs, so the
+    # merge must skip candidate CTAs that took no tile of the row
+    "one_short_row": ([40], 1, 4, 3, 4, 0, 1.0),
+    "one_short_row_hot": ([40], 1, 4, 3, 4, 16, 1.0),
 }
 
 
