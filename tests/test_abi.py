@@ -66,6 +66,21 @@ def test_codebook_argument_errors():
     assert N.lib().tq_build_codebook(128, 3, None) == N.TQ_ERR_INVALID_ARG
 
 
+def test_status_strings():
+    """Every status code has its own name; any other value maps to one fallback
+    name (never NULL), and an error raised by the binding carries the name."""
+    codes = [N.TQ_OK, N.TQ_ERR_INVALID_ARG, N.TQ_ERR_UNSUPPORTED, N.TQ_ERR_CAPACITY, N.TQ_ERR_WORKSPACE,
+             N.TQ_ERR_CUDA, N.TQ_ERR_DEVICE]
+    names = [N.tq_status_string(c) for c in codes]
+    assert names[0] == "TQ_OK" and len(set(names)) == len(codes)
+    assert all(n.startswith("TQ_") for n in names)
+    assert N.tq_status_string(42) == N.tq_status_string(-99) == "TQ_ERR_UNKNOWN"
+    assert "TQ_ERR_UNKNOWN" not in names
+    with pytest.raises(N.TQError) as e:
+        N.tq_build_codebook(2, 3)
+    assert "TQ_ERR_UNSUPPORTED" in str(e.value)
+
+
 @pytest.mark.parametrize("seed,layer,head", [(0, 0, 0), (0, 0, 7), (123456789, 3, 2), (2**63 + 5, 31, 65535)])
 def test_rotation_signs_match_oracle(seed, layer, head):
     np.testing.assert_array_equal(np.array(N.tq_rotation_signs(seed, layer, head, 128)),
