@@ -13,7 +13,15 @@ import torch
 from . import native as N
 
 
+# Raw handle of a device's current stream without building a Stream object (a
+# tenth of the host time of torch.cuda.current_stream); the public call where
+# this torch build lacks it.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream_handle(device) -> int:
+    if _raw_stream is not None and device.index is not None:
+        return _raw_stream(device.index)
     return torch.cuda.current_stream(device).cuda_stream
 
 
@@ -126,8 +134,8 @@ class TurboQuantKVCache:
             raise ValueError("seq_lens must be a contiguous int32 tensor on the cache device")
         if out is None:
             out = torch.empty(self.batch, self.num_q_heads, self.head_dim, dtype=torch.float32, device=self.device)
-        need = self.workspace_bytes(max_seq_len)
-        if workspace is None:
+        if workspace is None:  # (a caller's workspace is sized by the library's own check)
+            need = self.workspace_bytes(max_seq_len)
             if self._workspace is None or self._workspace.numel() < need:
                 self._workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=self.device)
             workspace = self._workspace
@@ -150,8 +158,8 @@ class TurboQuantKVCache:
         if out is None:
             out = torch.empty(self.batch, nq, self.num_q_heads, self.head_dim, dtype=torch.float32,
                               device=self.device)
-        need = N.tq_multi_query_workspace_bytes(self.desc, nq, max_seq_len)
         if workspace is None:
+            need = N.tq_multi_query_workspace_bytes(self.desc, nq, max_seq_len)
             if self._workspace is None or self._workspace.numel() < need:
                 self._workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=self.device)
             workspace = self._workspace

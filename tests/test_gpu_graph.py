@@ -73,3 +73,15 @@ def test_graph_replay_equals_stream(lens):
         assert torch.equal(outs[0][s], outs[1][s]), "step %d output" % s
     for name in ("k_cache", "k_norms", "v_cache", "v_norms", "v_hot"):
         assert torch.equal(getattr(caches[0], name), getattr(caches[1], name)), name
+
+
+def test_stream_handle_follows_the_current_stream():
+    """The binding launches on the caller's current stream: the handle it passes
+    is torch's current stream of the cache's device, on a side stream too."""
+    from bit_kv_cache_10_gb300.cache import _stream_handle
+    dev = torch.device("cuda", torch.cuda.current_device())
+    assert _stream_handle(dev) == torch.cuda.current_stream(dev).cuda_stream
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        assert _stream_handle(dev) == side.cuda_stream
+    assert _stream_handle(dev) == torch.cuda.current_stream(dev).cuda_stream
