@@ -51,6 +51,7 @@
 #include <cuda_fp16.h>
 
 #include "tq_decode_split.cuh"
+#include "tq_launch.cuh"
 
 namespace tq {
 namespace {
@@ -966,8 +967,7 @@ template <int G, int KB, bool SPARSE, bool PAGED, bool MQ, int VB = 4>
 tq_status launch_mma(const DecodeParams& p, cudaStream_t stream) {
   using M = MmaCfg<KB, false, VB>;
   auto kern = decode_mma_kernel<G, KB, SPARSE, PAGED, MQ, false, VB>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, M::kSmem) != cudaSuccess)
-    return TQ_ERR_CUDA;
+  static KernelMemo memo;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.grid);
   cfg.blockDim = dim3(M::kThreads);
@@ -978,7 +978,7 @@ tq_status launch_mma(const DecodeParams& p, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = kProgrammaticLaunch;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return TQ_ERR_CUDA;
+  if (launch_with_limit(kern, M::kSmem, memo, current_device(), cfg, p) != cudaSuccess) return TQ_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 
@@ -990,8 +990,9 @@ template <int G, int KB, int VB>
 tq_status launch_mma_cluster(const DecodeParams& p, cudaStream_t stream) {
   using M = MmaCfg<KB, true, VB>;
   auto kern = decode_mma_kernel<G, KB, false, false, false, true, VB>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, M::kSmem) != cudaSuccess)
-    return TQ_ERR_CUDA;
+  static KernelMemo memo;
+  const int dev = current_device();
+  if (!ensure_smem_limit(kern, M::kSmem, memo, dev)) return TQ_ERR_CUDA;
   const long long rows = static_cast<long long>(p.batch) * p.hkv;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(rows * kClusterCtas));
@@ -1007,10 +1008,10 @@ tq_status launch_mma_cluster(const DecodeParams& p, cudaStream_t stream) {
   attr[1].val.programmaticStreamSerializationAllowed = kProgrammaticLaunch;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  int fit = 0;  // clusters resident at once (a property of the device and the kernel)
-  if (cudaOccupancyMaxActiveClusters(&fit, kern, &cfg) != cudaSuccess) return TQ_ERR_CUDA;
+  const int fit = cluster_fit(kern, cfg, memo, dev);  // clusters resident at once (device and kernel)
+  if (fit < 0) return TQ_ERR_CUDA;
   if (rows > fit) return TQ_ERR_UNSUPPORTED;
-  if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return TQ_ERR_CUDA;
+  if (launch_with_limit(kern, M::kSmem, memo, dev, cfg, p) != cudaSuccess) return TQ_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 

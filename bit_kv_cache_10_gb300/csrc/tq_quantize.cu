@@ -16,6 +16,7 @@
 #include <cstring>
 
 #include "tq_device.cuh"
+#include "tq_launch.cuh"
 #include "tq_internal.h"
 #include "tq_debug.h"
 
@@ -640,8 +641,10 @@ tq_status launch_quantize(QuantParams& p, cudaStream_t stream) {
   auto kern = paged ? (p.fuse_evict ? quantize_append_kernel<true, true> : quantize_append_kernel<true, false>)
                     : (p.fuse_evict ? quantize_append_kernel<false, true>
                                     : (plain ? quantize_append_kernel<false, false, true> : quantize_append_kernel<false, false>));
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
-    return TQ_ERR_CUDA;
+  // one memo per kernel above; a launch that needs more shared memory than the
+  // limit set so far is refused once and retried with the limit raised
+  static KernelMemo memos[5];
+  KernelMemo& memo = memos[paged ? (p.fuse_evict ? 0 : 1) : (p.fuse_evict ? 2 : (plain ? 3 : 4))];
   const int sms = sm_count_q();
   if (sms <= 0) return TQ_ERR_CUDA;
   const int grid = static_cast<int>(p.jobs < sms ? p.jobs : sms);
@@ -655,7 +658,8 @@ tq_status launch_quantize(QuantParams& p, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = kProgrammaticLaunch;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return TQ_ERR_CUDA;
+  if (launch_with_limit(kern, static_cast<int>(smem), memo, current_device(), cfg, p) != cudaSuccess)
+    return TQ_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 
